@@ -1,0 +1,178 @@
+"""CPU oracle for the tree speculative decoding hot path.
+
+TEST INFRASTRUCTURE ONLY: tests/, ``__graft_entry__.smoke()`` and the CPU
+baseline leg of ``bench.py`` may import this package; the product library
+never does.  It wraps ``jt_oracle.c`` (plain C, fp64 loops) through ctypes and
+shares no code with the CUDA path.
+
+Functions return numpy arrays.  See ``jt_oracle.c`` for the definition each
+one follows and the passage of the pages it cites.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "jt_oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_jt_oracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile jt_oracle.c into a shared library next to it (gcc, -O2)."""
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-ffp-contract=off",
+               "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            P = ctypes.c_void_p
+            i32, i64, dbl = ctypes.c_int, ctypes.c_int64, ctypes.c_double
+            lib.jto_topw_lse.argtypes = [P, i64, i64, i32, P, P, P]
+            lib.jto_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, P, P, P, P, P, P]
+            lib.jto_tree_build.argtypes = [P, P, P, i32, i32, i32, i64, P, P, P, P, P, P, P, P, P]
+            lib.jto_tree_attn.argtypes = [P, P, P, i32, P, i32, P, P, P, i32, i32, i32, i32, i32,
+                                          dbl, P, i64, P, P]
+            lib.jto_verify_accept.argtypes = [P, P, P, P, i32, i32, i64, i32, dbl, P, P, P]
+            for f in (lib.jto_topw_lse, lib.jto_tree_expand, lib.jto_tree_build,
+                      lib.jto_tree_attn, lib.jto_verify_accept):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    return None if a is None else ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise OracleError(f"{what}: invalid arguments (status {rc})")
+
+
+def topw_lse(z, W):
+    """Per row of z [..., V] fp32: top-W ids, their log-probs and lse (fp64)."""
+    z = _c(z, np.float32)
+    V = z.shape[-1]
+    rows = int(np.prod(z.shape[:-1]))
+    tok = np.empty(z.shape[:-1] + (W,), np.int32)
+    lp = np.empty(z.shape[:-1] + (W,), np.float64)
+    lse = np.empty(z.shape[:-1], np.float64)
+    _check(_load().jto_topw_lse(_ptr(z), rows, V, W, _ptr(tok), _ptr(lp), _ptr(lse)), "topw_lse")
+    return tok, lp, lse
+
+
+def _tree_outputs(total):
+    return (np.empty(total, np.int32), np.empty(total, np.int32), np.empty(total, np.int32),
+            np.empty((total, 8), np.uint32), np.empty(total, np.float64))
+
+
+def tree_expand(tok, lp, root_token, tree_off, N, W):
+    """Best-first expansion from per-depth tables tok/lp [nseq, N, W].
+
+    Returns dict(parent, token, depth, anc, score, gap)."""
+    tok, lp = _c(tok, np.int32), _c(lp, np.float64)
+    root_token, tree_off = _c(root_token, np.int32), _c(tree_off, np.int32)
+    nseq = len(root_token)
+    total = int(tree_off[-1])
+    parent, token, depth, anc, score = _tree_outputs(total)
+    gap = np.empty(nseq, np.float64)
+    _check(_load().jto_tree_expand(_ptr(tok), _ptr(lp), _ptr(root_token), _ptr(tree_off), nseq,
+                                   N, W, _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc),
+                                   _ptr(score), _ptr(gap)), "tree_expand")
+    return dict(parent=parent, token=token, depth=depth, anc=anc, score=score, gap=gap)
+
+
+def tree_build(draft_logits, root_token, tree_off, W):
+    """Full tree build from per-depth draft logits [nseq, N, V] fp32.
+
+    Returns dict(parent, token, depth, anc, score, gap, tok, lp, lse)."""
+    z = _c(draft_logits, np.float32)
+    nseq, N, V = z.shape
+    root_token, tree_off = _c(root_token, np.int32), _c(tree_off, np.int32)
+    total = int(tree_off[-1])
+    parent, token, depth, anc, score = _tree_outputs(total)
+    gap = np.empty(nseq, np.float64)
+    tok = np.empty((nseq, N, W), np.int32)
+    lp = np.empty((nseq, N, W), np.float64)
+    lse = np.empty((nseq, N), np.float64)
+    _check(_load().jto_tree_build(_ptr(z), _ptr(root_token), _ptr(tree_off), nseq, N, W, V,
+                                  _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc), _ptr(score),
+                                  _ptr(gap), _ptr(tok), _ptr(lp), _ptr(lse)), "tree_build")
+    return dict(parent=parent, token=token, depth=depth, anc=anc, score=score, gap=gap,
+                tok=tok, lp=lp, lse=lse)
+
+
+def tree_attn(q, k_cache, v_cache, block_table, prefix_len, tree_off, parent, scale, rows=None):
+    """Tree-causal paged attention in fp64.
+
+    q [total, Hq, D], k/v [pages, page_size, Hkv, D] given as numpy float32
+    arrays (dtype 0) or uint16 bf16 bit patterns (dtype 1).  Returns
+    (out [n, Hq, D] float64, lse [n, Hq] float64) for the nodes in ``rows``
+    (global indices; default all)."""
+    if q.dtype == np.uint16:
+        dtype = 1
+    elif q.dtype == np.float32:
+        dtype = 0
+    else:
+        raise TypeError("q/k/v must be float32 or uint16 (bf16 bits)")
+    q, k_cache, v_cache = (np.ascontiguousarray(a) for a in (q, k_cache, v_cache))
+    assert k_cache.dtype == q.dtype and v_cache.dtype == q.dtype
+    block_table = _c(block_table, np.int32)
+    prefix_len, tree_off, parent = (_c(a, np.int32) for a in (prefix_len, tree_off, parent))
+    total, Hq, D = q.shape
+    _, page_size, Hkv, _ = k_cache.shape
+    nseq, max_pages = block_table.shape
+    if rows is None:
+        n = total
+        rows_p = None
+    else:
+        rows = _c(rows, np.int32)
+        n = len(rows)
+        rows_p = _ptr(rows)
+    out = np.empty((n, Hq, D), np.float64)
+    lse = np.empty((n, Hq), np.float64)
+    _check(_load().jto_tree_attn(_ptr(q), _ptr(k_cache), _ptr(v_cache), dtype, _ptr(block_table),
+                                 max_pages, _ptr(prefix_len), _ptr(tree_off), _ptr(parent), nseq,
+                                 Hq, Hkv, D, page_size, float(scale), rows_p, n, _ptr(out),
+                                 _ptr(lse)), "tree_attn")
+    return out, lse
+
+
+def verify_accept(target_logits, parent, token, tree_off, N, rule, log_t=0.0):
+    """Tree acceptance; rule 0 = greedy, 1 = margin (log_t = log(t)).
+
+    Returns (accept_len [nseq], path [nseq, N+1], bonus [nseq])."""
+    z = _c(target_logits, np.float32)
+    V = z.shape[-1]
+    parent, token, tree_off = (_c(a, np.int32) for a in (parent, token, tree_off))
+    nseq = len(tree_off) - 1
+    acc = np.empty(nseq, np.int32)
+    path = np.empty((nseq, N + 1), np.int32)
+    bonus = np.empty(nseq, np.int32)
+    _check(_load().jto_verify_accept(_ptr(z), _ptr(parent), _ptr(token), _ptr(tree_off), nseq, N,
+                                     V, rule, float(log_t), _ptr(acc), _ptr(path), _ptr(bonus)),
+           "verify_accept")
+    return acc, path, bonus
