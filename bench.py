@@ -1,0 +1,434 @@
+"""Benchmark of one tree speculative decoding verify step on GB300.
+
+A step is one pass of the whole hot path over one batch of seeded synthetic
+input: jt_tree_build (top-W per depth + best-first expansion), then
+jt_tree_attn_paged (tree-causal attention over the paged bf16 KV cache, fed
+by the build's ancestor sets), then jt_verify_accept with the greedy rule
+and with the margin rule (t = 0.8).  Metric: tree-node tokens per second.
+
+Default workload: a Qwen3-8B-shaped attention layer (32 query / 8 KV heads,
+head dim 128, bf16), batch 1, prefix 4096, tree budget 256 (N=16, W=4),
+vocab 151936; pages randomly permuted in the pool.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
+
+Rank 0 prints one JSON line.  With torchrun (N > 1) every rank runs an
+independent replica on its own GPU (the path has no cross-GPU exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from tree_speculative_decoding_jt_gb300 import workloads as wk  # noqa: E402
+
+METRIC = "tree-verify attention tree-node-tokens/sec and % of roofline (HBM GB/s) at 1 GB300"
+UNIT = "tree-node tokens/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def attn_algorithmic(wl, depth):
+    """Algorithmic bytes and FLOPs of one attention call: K and V of the
+    prefix + tree slots once, q and o once; 4*D flops per (query head,
+    visible key) for QK^T and PV, visible keys = prefix + ancestors."""
+    c = wl.cfg
+    Hq, Hkv, D = c["Hq"], c["Hkv"], c["D"]
+    esz = 2 if c["dtype"] == "bf16" else 4
+    B = np.diff(wl.tree_off)
+    slots = int(np.sum(wl.prefix_len.astype(np.int64) + B))
+    kv_bytes = slots * Hkv * D * 2 * esz
+    qo_bytes = 2 * wl.total * Hq * D * esz
+    flops = 0
+    for b in range(wl.nseq):
+        o, e = int(wl.tree_off[b]), int(wl.tree_off[b + 1])
+        flops += int(np.sum(int(wl.prefix_len[b]) + depth[o:e].astype(np.int64) + 1)) * 4 * Hq * D
+    return kv_bytes + qo_bytes, flops
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        h.update(open(os.path.join(ROOT, p), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_file):
+    """DRAM bytes per attention call from the committed ncu summary, or None
+    when absent or taken on a different version of the kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        if d.get("source_hash") != source_hash([kernel_file]):
+            return None
+        return d.get("attn_dram_bytes_per_call")
+    except (ValueError, OSError):
+        return None
+
+
+# --------------------------------------------------------------------------
+# CPU baseline: the oracle, as it stands, on a bounded sample
+# --------------------------------------------------------------------------
+def cpu_oracle_sample(wl, tree_parent, tree_token, target, attn_nodes):
+    import oracle
+
+    c = wl.cfg
+    t0 = time.perf_counter()
+    tr = oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, c["W"])
+    t1 = time.perf_counter()
+    oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len, wl.tree_off,
+                     tr["parent"], wl.scale, rows=attn_nodes)
+    t2 = time.perf_counter()
+    oracle.verify_accept(target, tree_parent, tree_token, wl.tree_off, c["N"], 0)
+    oracle.verify_accept(target, tree_parent, tree_token, wl.tree_off, c["N"], 1, math.log(c["t"]))
+    t3 = time.perf_counter()
+    # per-node cost of the whole step: build and accept per node of the
+    # batch, attention per sampled node
+    per_node = (t1 - t0) / wl.total + (t2 - t1) / len(attn_nodes) + (t3 - t2) / wl.total
+    return 1.0 / per_node, t3 - t0
+
+
+def attn_sample_nodes(wl, k):
+    step = max(1, wl.total // k)
+    return np.arange(0, wl.total, step, dtype=np.int32)[:k]
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    wl = wk.make(args.config)
+    import oracle
+    tr = oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"])
+    target = wk.target_logits(wl, tr["parent"], tr["token"])
+    nodes = attn_sample_nodes(wl, args.cpu_attn_nodes)
+    vals = []
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        cpu_oracle_sample(wl, tr["parent"], tr["token"], target, nodes[:2])
+    t_start = time.perf_counter()
+    for _ in range(args.steps):
+        v, _ = cpu_oracle_sample(wl, tr["parent"], tr["token"], target, nodes)
+        vals.append(v)
+    wall = time.perf_counter() - t_start
+    value = statistics.mean(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.total / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": wl.cfg["name"], "sample": "see cpu_baseline"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"full tree build and both acceptance rules over all {wl.total} "
+                                   f"nodes, attention for {len(nodes)} of {wl.total} nodes; "
+                                   f"single-threaded C, fp64; {wall:.1f} s for {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------------
+# GPU arm
+# --------------------------------------------------------------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-attn-nodes", type=int, default=48)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--flush-mb", type=int, default=512)
+    args = ap.parse_args()
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import torch.distributed as dist
+    import tree_speculative_decoding_jt_gb300 as jt
+
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    cfg = args.config
+    wl = wk.make(cfg)
+    c = wl.cfg
+    dev = torch.device("cuda", local_rank)
+
+    def to_dev(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    h = {  # host copies (pinned) of every per-step input, for the end-to-end leg
+        "draft": torch.from_numpy(wl.draft_logits),
+        "root": torch.from_numpy(wl.root_token),
+        "off": torch.from_numpy(wl.tree_off),
+        "plen": torch.from_numpy(wl.prefix_len),
+        "bt": torch.from_numpy(wl.block_table),
+        "q": torch.from_numpy(wl.q.view(np.int16)).view(torch.bfloat16) if wl.q.dtype == np.uint16 else torch.from_numpy(wl.q),
+        "k": torch.from_numpy(wl.k_cache.view(np.int16)).view(torch.bfloat16) if wl.k_cache.dtype == np.uint16 else torch.from_numpy(wl.k_cache),
+        "v": torch.from_numpy(wl.v_cache.view(np.int16)).view(torch.bfloat16) if wl.v_cache.dtype == np.uint16 else torch.from_numpy(wl.v_cache),
+    }
+    d = {k: v.to(dev) for k, v in h.items()}
+    total, nseq, N, W = wl.total, wl.nseq, c["N"], c["W"]
+    max_tree = int(np.diff(wl.tree_off).max())
+    Hq, Hkv, D = c["Hq"], c["Hkv"], c["D"]
+    max_pages = wl.block_table.shape[1]
+    log_t = math.log(c["t"])
+
+    # outputs and workspaces, allocated once
+    parent = torch.empty(total, dtype=torch.int32, device=dev)
+    token = torch.empty_like(parent)
+    depth = torch.empty_like(parent)
+    anc = torch.empty((total, 8), dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((total, Hq), dtype=torch.float32, device=dev)
+    acc = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(2)]
+    path = [torch.empty((nseq, N + 1), dtype=torch.int32, device=dev) for _ in range(2)]
+    bonus = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(2)]
+    ws_b = jt.workspace(jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, nseq, N, W, c["V"]), dev)
+    ws_a = jt.workspace(jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq, Hkv, D,
+                                             max_pages, max_tree), dev)
+    ws_v = [jt.workspace(jt.jt_workspace_size(jt.JT_OP_VERIFY_ACCEPT, nseq, 0, 0, 0, total), dev)
+            for _ in range(2)]
+
+    # target logits need the drafted tokens: build the tree once, then draw
+    jt.jt_tree_build(d["draft"], d["root"], d["off"], W, total_nodes=total,
+                     out=(parent, token, depth, anc), ws=ws_b)
+    jt.jt_check(ws_b)
+    par_h, tok_h, dep_h = parent.cpu().numpy(), token.cpu().numpy(), depth.cpu().numpy()
+    target_np = wk.target_logits(wl, par_h, tok_h)
+    h["target"] = torch.from_numpy(target_np)
+    d["target"] = h["target"].to(dev)
+
+    stream = torch.cuda.current_stream()
+    attn_ev = []
+
+    def step(inp, record_attn=False):
+        jt.jt_tree_build(inp["draft"], inp["root"], inp["off"], W, total_nodes=total,
+                         out=(parent, token, depth, anc), ws=ws_b)
+        if record_attn:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], inp["off"], anc,
+                              scale=wl.scale, max_tree=max_tree, out=out, lse=lse, ws=ws_a)
+        if record_attn:
+            e1.record(stream)
+            attn_ev.append((e0, e1))
+        for i, rule in enumerate((jt.JT_RULE_GREEDY, jt.JT_RULE_MARGIN)):
+            jt.jt_verify_accept(inp["target"], parent, token, inp["off"], N, rule=rule, log_t=log_t,
+                                out=(acc[i], path[i], bonus[i]), ws=ws_v[i])
+
+    flush = torch.empty(args.flush_mb * (1 << 20), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(d)
+    torch.cuda.synchronize()
+    for ws in (ws_b, ws_a, *ws_v):
+        jt.jt_check(ws)
+
+    # ---- timed region (inputs resident in HBM; L2 flushed before each step)
+    evs = []
+    with ClockSampler(local_rank) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        t_wall0 = time.perf_counter()
+        for _ in range(args.steps):
+            flush.zero_()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            step(d, record_attn=True)
+            e1.record(stream)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - t_wall0
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    ms = statistics.mean(step_ms)
+    attn_mean = statistics.mean(attn_ms)
+    if world > 1:
+        t = torch.tensor([ms, attn_mean], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, attn_mean = float(t[0]), float(t[1])
+    value = world * total / (ms * 1e-3)
+
+    # ---- end to end: pinned host inputs -> C-ABI calls -> host results
+    e2e = None
+    if args.e2e_steps > 0:
+        hp = {k: v.pin_memory() for k, v in h.items()}
+        res_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in
+                 (parent, token, out, acc[0], path[0], bonus[0], acc[1], path[1], bonus[1])]
+        h2d = sum(v.numel() * v.element_size() for v in hp.values())
+        d2h = sum(v.numel() * v.element_size() for v in res_h)
+        dd = {k: torch.empty_like(v) for k, v in d.items()}
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            for k in hp:
+                dd[k].copy_(hp[k], non_blocking=True)
+            step(dd)
+            for dst, src in zip(res_h, (parent, token, out, acc[0], path[0], bonus[0], acc[1],
+                                        path[1], bonus[1])):
+                dst.copy_(src, non_blocking=True)
+            torch.cuda.synchronize()
+        e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+        if world > 1:
+            t = torch.tensor([e2e_s], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_s = float(t[0])
+        e2e = {"value": world * total / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+
+    # ---- roofline of the dominant kernel (the attention call)
+    peaks, peak_src = load_peaks()
+    bytes_a, flops_a = attn_algorithmic(wl, dep_h)
+    t_hbm = bytes_a / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops_a / (peaks["bf16_tflops"] * 1e12)
+    if t_tc >= t_hbm:
+        roof = {"bound": "tensor", "achieved": flops_a / (attn_mean * 1e-3) / 1e12,
+                "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": bytes_a / (attn_mean * 1e-3) / 1e9,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu")
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
+    roof["kernel"] = "jt_tree_attn_paged (tree_attn_tc_kernel + combine)"
+    roof["algorithmic_bytes"] = int(bytes_a)
+    roof["algorithmic_flops"] = int(flops_a)
+    roof["attn_ms"] = attn_mean
+    roof["attn_tokens_per_s"] = total / (attn_mean * 1e-3)
+
+    # ---- CPU baseline (rank 0, N = 1)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        nodes = attn_sample_nodes(wl, args.cpu_attn_nodes)
+        v, secs = cpu_oracle_sample(wl, par_h, tok_h, target_np, nodes)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"full tree build and both acceptance rules over all {total} nodes, "
+                         f"attention for {len(nodes)} of {total} nodes ({secs:.1f} s, "
+                         f"single-threaded C, fp64)"}
+
+    launches_per_step = 2 + (2 if jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq,
+                                                       Hkv, D, max_pages, max_tree) > 256 else 1) + 2
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": c["name"], "nseq": nseq, "tree_nodes": total,
+                       "prefix_len": [int(x) for x in wl.prefix_len[:4]] + (["..."] if nseq > 4 else []),
+                       "Hq": Hq, "Hkv": Hkv, "head_dim": D, "N": N, "W": W, "V": c["V"],
+                       "step": "tree_build + tree_attn_paged + verify_accept(greedy) + verify_accept(margin t=0.8)",
+                       "l2": f"flushed before every step ({args.flush_mb} MiB write)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks.summary(),
+            "wall_s_timed_region": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

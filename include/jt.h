@@ -1,0 +1,212 @@
+/*
+ * jt.h -- C ABI of libjt, the GB300 (sm_103a) hot path of JetSpec-style tree
+ * speculative decoding: draft-tree build, tree-causal paged attention and
+ * tree acceptance.
+ *
+ * Conventions shared by every entry point
+ *  - Array arguments are DEVICE pointers owned by the caller, unless a
+ *    comment says "host".  The library allocates no memory and keeps no
+ *    state besides a per-device cache of device properties.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *    default stream).  Outputs are valid once the stream reaches the call.
+ *  - Arguments checkable on the host (null pointers, sizes, limits, the
+ *    workspace size) are checked before anything is enqueued; on failure the
+ *    call returns JT_ERR_INVALID / JT_ERR_UNSUPPORTED / JT_ERR_WORKSPACE and
+ *    writes nothing.
+ *  - Contents of device arrays (tree offsets, prefix lengths, tree
+ *    structure) are checked on the device; an offending sequence is skipped
+ *    (its outputs are left untouched) and a flag is raised in the first
+ *    word of the workspace.  jt_check() synchronises the stream and turns
+ *    that flag into a status.  Device-side waits are bounded in time; a wait
+ *    that runs out raises JT_ERR_TIMEOUT the same way.
+ *  - Every call needs a caller-allocated device workspace of at least
+ *    jt_workspace_size(...) bytes, 256-byte aligned.  Calls that share one
+ *    workspace must not overlap on the device.
+ *
+ * Tree layout shared by the three steps
+ *  - nseq sequences; sequence b owns global node indices
+ *    tree_off[b] .. tree_off[b+1]-1 (tree_off: int32 [nseq+1], tree_off[0]=0),
+ *    so its budget is B_b = tree_off[b+1] - tree_off[b], 1 <= B_b <= 256.
+ *  - Within a sequence, nodes are numbered 0..B_b-1 in the order the
+ *    best-first expansion pops them; node 0 is the root (the last verified
+ *    token); parent[] holds LOCAL indices (root: -1) and parent < child.
+ *  - anc: uint32 [total_nodes, 8], a 256-bit ancestor-or-self set per node:
+ *    bit j of word w is set when local node 32*w + j is the node itself or
+ *    one of its ancestors.
+ *
+ * Sources (prose pages; no code is printed there):
+ *  [JS-news] JetSpec news summary (mlqm.cn/news/158889): tree-causal
+ *      attention mask; building the candidate tree from one forward's
+ *      per-depth logits, top-W per depth, cumulative draft log-prob, greedy
+ *      fill to the budget B, depth at most N; longest consistent prefix.
+ *  [JS-art] "加速AI思考：UC San Diego等机构研究出让大模型“一心多用”的推测解码新方法":
+ *      section 三 (mask, one-forward verification), section 五 (best-first
+ *      expansion with a priority queue), section 七 (paged tree attention
+ *      without a dense mask).
+ *  [AS] "AdaptiveSpec：免训练推测解码方案提速56%的技术解析", section
+ *      "逐步Margin规则": accept when p(draft)/p(top1) >= t.
+ */
+#ifndef JT_H
+#define JT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t; declared here so that users need no CUDA
+ * header to include this file. */
+typedef struct CUstream_st* jt_stream_t;
+
+typedef enum {
+    JT_OK = 0,
+    JT_ERR_INVALID = -1,      /* bad argument, or bad device-side array contents */
+    JT_ERR_UNSUPPORTED = -2,  /* valid but outside this build's limits (dtype, D, G, GPU) */
+    JT_ERR_CUDA = -3,         /* a CUDA runtime call failed */
+    JT_ERR_TIMEOUT = -4,      /* a bounded device-side wait ran out */
+    JT_ERR_WORKSPACE = -5     /* workspace missing, misaligned or too small */
+} jt_status;
+
+typedef enum { JT_DTYPE_F32 = 0, JT_DTYPE_BF16 = 1 } jt_dtype;
+typedef enum { JT_RULE_GREEDY = 0, JT_RULE_MARGIN = 1 } jt_rule;
+typedef enum { JT_OP_TREE_BUILD = 0, JT_OP_TREE_ATTN = 1, JT_OP_VERIFY_ACCEPT = 2,
+               JT_OP_TREE_TOPW = 3 } jt_op;
+
+/* Limits of this build. */
+#define JT_MAX_TREE 256   /* B_b (bitset width) */
+#define JT_MAX_W 8        /* draft width W */
+#define JT_MAX_N 64       /* draft depth N */
+#define JT_PAGE_SIZE 16   /* KV page size in tokens */
+
+/*
+ * Workspace bytes needed by one call of `op` with these sizes (arguments an
+ * op does not use are ignored; pass 0).  Depends on the current device's SM
+ * count for JT_OP_TREE_ATTN.  Returns 0 for invalid sizes.
+ *   TREE_BUILD:    nseq, N, W, V
+ *   TREE_TOPW:     nseq*N rows given as nseq (N=1), W, V
+ *   TREE_ATTN:     nseq, total_nodes, Hq, Hkv, D, max_pages, max_tree
+ *   VERIFY_ACCEPT: nseq, total_nodes
+ */
+size_t jt_workspace_size(int op, int nseq, int N, int W, int64_t V, int total_nodes,
+                         int Hq, int Hkv, int D, int max_pages, int max_tree);
+
+/*
+ * jt_tree_build -- draft-tree construction ([JS-news] tree construction;
+ * [JS-art] section 五).
+ *   draft_logits: fp32 [nseq, N, V]; row (b, d) is the draft distribution
+ *                 for depth d+1 of sequence b (shared by every node of that
+ *                 depth).
+ *   root_token:   int32 [nseq], token of each root.
+ *   tree_off:     int32 [nseq+1], budgets B_b as described above; the full
+ *                 W-ary tree of depth N must hold at least B_b nodes.
+ *   total_nodes:  tree_off[nseq] (host value; sizes the outputs).
+ * Step 1 takes, per row, the top-W tokens (logit descending, token id
+ * ascending) and lse = log sum exp(z).  Step 2 runs best-first expansion:
+ * a queue of candidate nodes keyed by (cumulative log-prob descending, depth
+ * ascending, token ascending, parent index ascending); the best candidate is
+ * popped and becomes the next node; its W children (depth < N) are pushed;
+ * stop at B_b nodes.  Log-probs and scores are fp64.
+ * Outputs (global node index): parent (local), token, depth (int32
+ * [total_nodes]) and anc (uint32 [total_nodes, 8]).
+ */
+jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
+                        const int32_t* tree_off, int nseq, int N, int W, int64_t V,
+                        int total_nodes, int32_t* parent, int32_t* token, int32_t* depth,
+                        uint32_t* anc, void* ws, size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_tree_topw -- step 1 of jt_tree_build alone, on `rows` rows of V fp32
+ * logits: tok int32 [rows, W], lp fp64 [rows, W] (= z[tok] - lse), lse fp64
+ * [rows].  Same kernels as jt_tree_build.
+ */
+jt_status jt_tree_topw(const float* logits, int64_t rows, int64_t V, int W, int32_t* tok,
+                       double* lp, double* lse, void* ws, size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_tree_expand -- step 2 of jt_tree_build alone, from given per-depth
+ * tables tok int32 [nseq, N, W] and lp fp64 [nseq, N, W] (row d = candidates
+ * of depth d+1, best first).  Same outputs as jt_tree_build.  Needs a
+ * workspace of jt_workspace_size(JT_OP_VERIFY_ACCEPT, nseq, ...) or more
+ * (only its error word is used).
+ */
+jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
+                         const int32_t* tree_off, int nseq, int N, int W, int total_nodes,
+                         int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc,
+                         void* ws, size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_tree_attn_paged -- tree-causal attention over a paged KV cache
+ * ([JS-news] tree-causal attention mask; [JS-art] sections 三 and 七).
+ *   q:        [total_nodes, Hq, D] (dtype), the tree nodes' queries.
+ *   k_cache, v_cache: [num_pages, page_size, Hkv, D] (dtype).
+ *   dtype:    JT_DTYPE_BF16 (tensor-core path: D in {64,128},
+ *             Hq/Hkv in {1,2,4,8,16}) or JT_DTYPE_F32 (D in {32,64,96,128}).
+ *   block_table: int32 [nseq, max_pages]; logical page p of sequence b is
+ *             physical page block_table[b*max_pages + p].  Entries past the
+ *             pages a sequence uses are never read.
+ *   prefix_len: int32 [nseq], L_b cached tokens in logical slots 0..L_b-1.
+ *             Tree node i of sequence b has its K/V (written by the caller)
+ *             in logical slot L_b + i; L_b + B_b <= max_pages*page_size.
+ *   anc:      the ancestor-or-self sets of the tree (see above).
+ *   max_tree: max_b B_b (host value; sizes the grid).
+ *   page_size: must be JT_PAGE_SIZE.  scale: softmax scale (e.g. 1/sqrt(D)).
+ * Node n of sequence b, query head h (KV head h / (Hq/Hkv)) attends to
+ * slots 0..L_b-1 and to slot L_b + j for every j in anc(n): never to a
+ * sibling or a descendant.  No dense mask is formed.
+ *   out:      [total_nodes, Hq, D] (bf16 for the bf16 path, fp32 for fp32):
+ *             softmax(scale * q.K^T) V, fp32 accumulation, one rounding.
+ *   lse:      fp32 [total_nodes, Hq] or NULL: natural-log sum of
+ *             exp(scale * q.k) over the visible keys.
+ */
+jt_status jt_tree_attn_paged(const void* q, const void* k_cache, const void* v_cache, int dtype,
+                             const int32_t* block_table, int max_pages, int num_pages,
+                             const int32_t* prefix_len, const int32_t* tree_off,
+                             const uint32_t* anc, int nseq, int total_nodes, int max_tree,
+                             int Hq, int Hkv, int D, int page_size, float scale, void* out,
+                             float* lse, void* ws, size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_verify_accept -- tree acceptance ([JS-art] section 三; [AS] margin rule).
+ *   target_logits: fp32 [total_nodes, V]; row u = the target's logits
+ *             after node u (it verifies u's children and gives u's bonus).
+ *   parent, token: the tree (local parent indices, topological order).
+ *   N:        maximum depth (width of `path` is N+1).
+ *   rule:     JT_RULE_GREEDY: child c of an accepted node u is accepted
+ *             when token[c] == argmax(row u) (lowest id on ties; first such
+ *             child in node order).
+ *             JT_RULE_MARGIN: child c of u passes when
+ *             (double)row_u[token c] - (double)max(row u) >= log_t, i.e.
+ *             p(draft)/p(top1) >= t; a node is reached when every edge of
+ *             its root path passes; the result is the deepest reached node
+ *             (lowest index on ties).
+ *   log_t:    log(t) in fp64, t in (0, 1] (margin rule only).
+ * Outputs per sequence: accept_len int32 [nseq] (accepted draft tokens =
+ * depth of the final node), path int32 [nseq, N+1] (local node at each depth
+ * of the accepted path, root first, -1 after the end), bonus int32 [nseq]
+ * (argmax of the final node's row).  Only rows on reached nodes are read.
+ */
+jt_status jt_verify_accept(const float* target_logits, const int32_t* parent,
+                           const int32_t* token, const int32_t* tree_off, int nseq, int N,
+                           int64_t V, int total_nodes, int rule, double log_t,
+                           int32_t* accept_len, int32_t* path, int32_t* bonus, void* ws,
+                           size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_check -- synchronise `stream`, read the device-side error flag of a
+ * workspace used by an earlier call, clear it, and return the matching
+ * status (JT_OK, JT_ERR_INVALID, JT_ERR_TIMEOUT or JT_ERR_CUDA).
+ */
+jt_status jt_check(void* ws, jt_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* jt_status_str(jt_status status);
+
+/* Library ABI version (major*10000 + minor*100 + patch). */
+int jt_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* JT_H */

@@ -1,0 +1,269 @@
+"""Thin ctypes binding of libjt (include/jt.h) for torch tensors.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Each function takes CUDA tensors, passes their device pointers and the
+current torch stream to the C entry point of the same name, and raises
+``JtError`` on a non-OK status.  Workspaces and outputs are allocated with
+torch when the caller does not pass them.  There is no CPU path: without a
+GPU or without the built library the calls fail.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+JT_OK, JT_ERR_INVALID, JT_ERR_UNSUPPORTED, JT_ERR_CUDA, JT_ERR_TIMEOUT, JT_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
+JT_DTYPE_F32, JT_DTYPE_BF16 = 0, 1
+JT_RULE_GREEDY, JT_RULE_MARGIN = 0, 1
+JT_OP_TREE_BUILD, JT_OP_TREE_ATTN, JT_OP_VERIFY_ACCEPT, JT_OP_TREE_TOPW = 0, 1, 2, 3
+JT_MAX_TREE, JT_MAX_W, JT_MAX_N, JT_PAGE_SIZE = 256, 8, 64, 16
+
+# every symbol include/jt.h declares
+EXPORTS = ("jt_workspace_size", "jt_tree_build", "jt_tree_topw", "jt_tree_expand",
+           "jt_tree_attn_paged", "jt_verify_accept", "jt_check", "jt_status_str", "jt_version")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class JtError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {jt_status_str(status)}")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load libjt.so (building it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_missing else _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libjt.so not found at {path}; run tree_speculative_decoding_jt_gb300.build")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, f32, f64, sz = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                                     ctypes.c_double, ctypes.c_size_t)
+        lib.jt_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, i32, i32, i32]
+        lib.jt_workspace_size.restype = sz
+        lib.jt_tree_build.argtypes = [P, P, P, i32, i32, i32, i64, i32, P, P, P, P, P, sz, P]
+        lib.jt_tree_topw.argtypes = [P, i64, i64, i32, P, P, P, P, sz, P]
+        lib.jt_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz, P]
+        lib.jt_tree_attn_paged.argtypes = [P, P, P, i32, P, i32, i32, P, P, P, i32, i32, i32, i32,
+                                           i32, i32, i32, f32, P, P, P, sz, P]
+        lib.jt_verify_accept.argtypes = [P, P, P, P, i32, i32, i64, i32, i32, f64, P, P, P, P, sz, P]
+        lib.jt_check.argtypes = [P, P]
+        lib.jt_status_str.argtypes = [i32]
+        lib.jt_status_str.restype = ctypes.c_char_p
+        lib.jt_version.argtypes = []
+        for name in ("jt_tree_build", "jt_tree_topw", "jt_tree_expand", "jt_tree_attn_paged",
+                     "jt_verify_accept", "jt_check", "jt_version"):
+            getattr(lib, name).restype = i32
+        _lib = lib
+        return lib
+
+
+def jt_status_str(status: int) -> str:
+    return load().jt_status_str(int(status)).decode()
+
+
+def jt_version() -> int:
+    return int(load().jt_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t, name, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (libjt has no CPU path)")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _check(rc, where):
+    if rc != JT_OK:
+        raise JtError(rc, where)
+
+
+def jt_workspace_size(op, nseq=0, N=0, W=0, V=0, total_nodes=0, Hq=0, Hkv=0, D=0, max_pages=0,
+                      max_tree=0) -> int:
+    return int(load().jt_workspace_size(op, nseq, N, W, V, total_nodes, Hq, Hkv, D, max_pages,
+                                        max_tree))
+
+
+def workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A device buffer usable as a libjt workspace (torch allocations are
+    256-byte aligned)."""
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def jt_check(ws: torch.Tensor, stream=None) -> None:
+    """Synchronise and raise if a kernel flagged a device-side error in ws."""
+    _check(load().jt_check(_ptr(ws), _stream(stream)), "jt_check")
+
+
+def jt_tree_build(draft_logits, root_token, tree_off, W, total_nodes=None, out=None, ws=None,
+                  stream=None):
+    """Best-first draft tree from per-depth draft logits [nseq, N, V] (fp32).
+
+    Returns (parent, token, depth, anc) on the device."""
+    lib = load()
+    _need(draft_logits, "draft_logits", torch.float32)
+    _need(root_token, "root_token", torch.int32)
+    _need(tree_off, "tree_off", torch.int32)
+    nseq, N, V = draft_logits.shape
+    if total_nodes is None:
+        total_nodes = int(tree_off[-1].item())
+    dev = draft_logits.device
+    if out is None:
+        out = (torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty((total_nodes, 8), dtype=torch.int32, device=dev))
+    parent, token, depth, anc = out
+    if ws is None:
+        ws = workspace(jt_workspace_size(JT_OP_TREE_BUILD, nseq, N, W, V), dev)
+    rc = lib.jt_tree_build(_ptr(draft_logits), _ptr(root_token), _ptr(tree_off), nseq, N, W, V,
+                           total_nodes, _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc),
+                           _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jt_tree_build")
+    return parent, token, depth, anc
+
+
+def jt_tree_topw(logits, W, ws=None, stream=None):
+    """Top-W ids (int32), log-probs and lse (fp64) of every row of [..., V] fp32."""
+    lib = load()
+    _need(logits, "logits", torch.float32)
+    V = logits.shape[-1]
+    rows = logits.numel() // V
+    dev = logits.device
+    tok = torch.empty(logits.shape[:-1] + (W,), dtype=torch.int32, device=dev)
+    lp = torch.empty(logits.shape[:-1] + (W,), dtype=torch.float64, device=dev)
+    lse = torch.empty(logits.shape[:-1], dtype=torch.float64, device=dev)
+    if ws is None:
+        ws = workspace(jt_workspace_size(JT_OP_TREE_TOPW, rows, 1, W, V), dev)
+    rc = lib.jt_tree_topw(_ptr(logits), rows, V, W, _ptr(tok), _ptr(lp), _ptr(lse), _ptr(ws),
+                          ws.numel(), _stream(stream))
+    _check(rc, "jt_tree_topw")
+    return tok, lp, lse
+
+
+def jt_tree_expand(tok, lp, root_token, tree_off, total_nodes=None, ws=None, stream=None):
+    """Best-first expansion from given tables tok [nseq,N,W] int32, lp fp64."""
+    lib = load()
+    _need(tok, "tok", torch.int32)
+    _need(lp, "lp", torch.float64)
+    _need(root_token, "root_token", torch.int32)
+    _need(tree_off, "tree_off", torch.int32)
+    nseq, N, W = tok.shape
+    if total_nodes is None:
+        total_nodes = int(tree_off[-1].item())
+    dev = tok.device
+    parent = torch.empty(total_nodes, dtype=torch.int32, device=dev)
+    token = torch.empty_like(parent)
+    depth = torch.empty_like(parent)
+    anc = torch.empty((total_nodes, 8), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(256, dev)
+    rc = lib.jt_tree_expand(_ptr(tok), _ptr(lp), _ptr(root_token), _ptr(tree_off), nseq, N, W,
+                            total_nodes, _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc),
+                            _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jt_tree_expand")
+    return parent, token, depth, anc
+
+
+def jt_tree_attn_paged(q, k_cache, v_cache, block_table, prefix_len, tree_off, anc, scale=None,
+                       max_tree=None, out=None, lse=None, ws=None, stream=None, with_lse=True):
+    """Tree-causal attention over a paged KV cache.
+
+    q [total, Hq, D]; k/v [pages, 16, Hkv, D] (both bf16, or both fp32);
+    block_table [nseq, max_pages] int32; prefix_len [nseq] int32;
+    tree_off [nseq+1] int32; anc [total, 8] int32/uint32 ancestor sets.
+    Returns (out, lse)."""
+    lib = load()
+    if q.dtype == torch.bfloat16:
+        dtype = JT_DTYPE_BF16
+    elif q.dtype == torch.float32:
+        dtype = JT_DTYPE_F32
+    else:
+        raise TypeError("q must be bf16 or fp32")
+    _need(q, "q", None)
+    _need(k_cache, "k_cache", q.dtype)
+    _need(v_cache, "v_cache", q.dtype)
+    _need(block_table, "block_table", torch.int32)
+    _need(prefix_len, "prefix_len", torch.int32)
+    _need(tree_off, "tree_off", torch.int32)
+    _need(anc, "anc", None)
+    total, Hq, D = q.shape
+    num_pages, page, Hkv, D2 = k_cache.shape
+    if D2 != D:
+        raise ValueError("q and k_cache head dims differ")
+    nseq, max_pages = block_table.shape
+    if max_tree is None:
+        max_tree = int((tree_off[1:] - tree_off[:-1]).max().item())
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and with_lse:
+        lse = torch.empty((total, Hq), dtype=torch.float32, device=q.device)
+    if ws is None:
+        ws = workspace(jt_workspace_size(JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq, Hkv, D,
+                                         max_pages, max_tree), q.device)
+    rc = lib.jt_tree_attn_paged(_ptr(q), _ptr(k_cache), _ptr(v_cache), dtype, _ptr(block_table),
+                                max_pages, num_pages, _ptr(prefix_len), _ptr(tree_off), _ptr(anc),
+                                nseq, total, max_tree, Hq, Hkv, D, page, float(scale), _ptr(out),
+                                _ptr(lse), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jt_tree_attn_paged")
+    return out, lse
+
+
+def jt_verify_accept(target_logits, parent, token, tree_off, N, rule=JT_RULE_GREEDY, t=None,
+                     log_t=None, out=None, ws=None, stream=None):
+    """Tree acceptance: returns (accept_len [nseq], path [nseq, N+1], bonus [nseq])."""
+    lib = load()
+    _need(target_logits, "target_logits", torch.float32)
+    _need(parent, "parent", torch.int32)
+    _need(token, "token", torch.int32)
+    _need(tree_off, "tree_off", torch.int32)
+    total, V = target_logits.shape
+    nseq = tree_off.numel() - 1
+    if isinstance(rule, str):
+        rule = {"greedy": JT_RULE_GREEDY, "margin": JT_RULE_MARGIN}[rule]
+    if log_t is None:
+        log_t = math.log(t) if t is not None else 0.0
+    dev = target_logits.device
+    if out is None:
+        out = (torch.empty(nseq, dtype=torch.int32, device=dev),
+               torch.empty((nseq, N + 1), dtype=torch.int32, device=dev),
+               torch.empty(nseq, dtype=torch.int32, device=dev))
+    acc, path, bonus = out
+    if ws is None:
+        ws = workspace(jt_workspace_size(JT_OP_VERIFY_ACCEPT, nseq, 0, 0, 0, total), dev)
+    rc = lib.jt_verify_accept(_ptr(target_logits), _ptr(parent), _ptr(token), _ptr(tree_off), nseq,
+                              N, V, total, rule, float(log_t), _ptr(acc), _ptr(path), _ptr(bonus),
+                              _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jt_verify_accept")
+    return acc, path, bonus

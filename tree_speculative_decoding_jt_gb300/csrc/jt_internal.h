@@ -1,0 +1,67 @@
+// jt_internal.h -- declarations shared between the host API (jt_api.cu) and
+// the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace jt {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t n) { return (n + kAlign - 1) / kAlign * kAlign; }
+
+// Workspace header (first kAlign bytes of every workspace).
+struct WsHeader {
+    uint32_t err;       // device error flags (DEVERR_*)
+    uint32_t bar_count; // grid barrier arrivals
+    uint32_t bar_gen;   // grid barrier generation
+    uint32_t active[2]; // accept: sequences still walking, per level parity
+    uint32_t pad[3];
+};
+constexpr size_t kWsHeader = kAlign;
+
+// tree_build.cu
+size_t topw_workspace_bytes(long long rows, long long V, int W);
+cudaError_t tree_topw_launch(const float* z, long long rows, long long V, int W, int32_t* tok,
+                             double* lp, double* lse, char* ws_parts, cudaStream_t st);
+cudaError_t tree_build_launch(const float* z, const int32_t* root_token, const int32_t* tree_off,
+                              int nseq, int N, int W, long long V, int32_t* parent, int32_t* token,
+                              int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
+                              cudaStream_t st);
+cudaError_t tree_expand_launch(const int32_t* tok, const double* lp, const int32_t* root_token,
+                               const int32_t* tree_off, int nseq, int N, int W, int32_t* parent,
+                               int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
+                               cudaStream_t st);
+
+// verify_accept.cu
+size_t accept_workspace_bytes(int nseq, int total_nodes);
+cudaError_t verify_accept_launch(const float* z, const int32_t* parent, const int32_t* token,
+                                 const int32_t* tree_off, int nseq, int N, long long V,
+                                 int total_nodes, int rule, double log_t, int32_t* accept_len,
+                                 int32_t* path, int32_t* bonus, char* ws, cudaStream_t st);
+
+// tree_attn.cu / tree_attn_f32.cu
+struct AttnPlan {
+    int splits;      // KV splits per (sequence, kv head, row tile)
+    int mtiles;      // row tiles per (sequence, kv head) at max_tree
+    int rows_per_tile_nodes;  // tree nodes per 128-row tile (128 / G)
+};
+AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int dtype);
+size_t attn_workspace_bytes(const AttnPlan& p, int total_nodes, int Hq, int D);
+cudaError_t tree_attn_bf16_launch(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, int max_pages, int num_pages,
+                                  const int32_t* prefix_len, const int32_t* tree_off,
+                                  const uint32_t* anc, int nseq, int total_nodes, int Hq, int Hkv,
+                                  int D, float scale, void* out, float* lse, const AttnPlan& plan,
+                                  char* ws_parts, uint32_t* err, cudaStream_t st);
+cudaError_t tree_attn_f32_launch(const float* q, const float* k_cache, const float* v_cache,
+                                 const int32_t* block_table, int max_pages,
+                                 const int32_t* prefix_len, const int32_t* tree_off,
+                                 const uint32_t* anc, int nseq, int total_nodes, int Hq, int Hkv,
+                                 int D, float scale, float* out, float* lse, uint32_t* err,
+                                 cudaStream_t st);
+
+int device_sm_count();
+
+}  // namespace jt

@@ -1,0 +1,621 @@
+// tree_attn.cu -- tree-causal attention over a paged bf16 KV cache on the
+// sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Semantics (JetSpec news summary, tree-causal attention mask; "加速AI思考…
+// 推测解码新方法" sections 三 and 七): tree node n of sequence b attends to
+// every prefix slot 0..L_b-1 and to the tree slot L_b+j of each node j in
+// its ancestor-or-self set, never to a sibling or a descendant; the mask is
+// read from 256-bit ancestor sets, never expanded into a dense matrix.  The
+// pages' own kernel (SM90, CuTe DSL, shared-memory mask staging) is prior
+// art; this is a Blackwell design.
+//
+// Work unit (one CTA): sequence b, KV head g, a 128-row tile of query rows
+// = 128/G tree nodes x G query heads of that KV head (GQA heads share the
+// K/V tile because they are stacked in the M dimension), and a contiguous
+// range of 128-key tiles of the logical key sequence (prefix + tree tail).
+// Keys past the last node of the row tile are never loaded (ancestors have
+// smaller indices).  Several ranges of one row tile (KV split) are merged by
+// tree_attn_combine_kernel.
+//
+// Warp roles (192 threads):
+//   warps 0-3  softmax + epilogue, one query row per thread (TMEM lane);
+//   warp 4     TMA producer: Q tile once, then per KV tile one 16-row box
+//              per 16-token page for K and for V (128-byte swizzle), page ids
+//              from the block table; zero-fills V rows past the last needed
+//              slot of the final tile;
+//   warp 5     TMEM allocator and single-thread MMA issuer.
+// TMEM (512 columns): S[2] (128 fp32 cols each), O (D fp32 cols),
+// P[2] (64 cols each: 128 bf16 probabilities packed in pairs).
+// Per KV tile j: S[j%2] = Q K^T (SS MMA, K-major operands, M=128, N=128,
+// K=D), softmax reads S, writes P in TMEM, O += P V (TS MMA: A = P from
+// TMEM, B = V MN-major, N=D).  QK^T of tile j+1 is issued before PV of tile
+// j so the tensor core overlaps the softmax.  Online softmax in the log2
+// domain with lazy rescaling of O (only when the running max grows by more
+// than 2^8).  All waits are bounded in time.
+#include "jt_common.cuh"
+#include "jt_internal.h"
+
+namespace jt {
+
+constexpr int kAttnThreads = 192;
+constexpr int kStages = 2;
+constexpr int kTileN = 128;  // keys per KV tile
+constexpr int kTileM = 128;  // query rows per tile
+constexpr float kRescaleLog2 = 8.0f;
+constexpr int kMaxSplits = 32;
+
+struct AttnParams {
+    const int32_t* block_table;
+    const int32_t* prefix_len;
+    const int32_t* tree_off;
+    const uint32_t* anc;
+    __nv_bfloat16* out;
+    float* lse;
+    float* part_o;   // [total*Hq*splits, D] when splits > 1
+    float2* part_ml; // [total*Hq*splits]: running max (log2 units), sum
+    uint32_t* err;
+    int max_pages, nseq, Hq, G, npt, splits;
+    float scale_log2;
+};
+
+template <int D>
+struct SmemLayout {
+    static constexpr int kChunks = D / 64;            // 64-element (128-byte) column blocks
+    static constexpr int kChunkBytes = kTileM * 128;  // 128 rows x 128 bytes
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kChunks * kChunkBytes;
+    static constexpr int kV = kK + kStages * kChunks * kChunkBytes;
+    static constexpr int kBar = kV + kStages * kChunks * kChunkBytes;
+    static constexpr int kBytes = kBar + 256;
+    static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
+};
+
+struct Bars {
+    uint64_t q_full;
+    uint64_t k_full[kStages];
+    uint64_t v_full[kStages];
+    uint64_t kv_empty[kStages];
+    uint64_t s_full[2];
+    uint64_t s_free[2];
+    uint64_t p_full[2];
+    uint64_t pv_done[2];
+    uint64_t v_last;
+    uint64_t mma_final;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Tile range [t0, t1) of split sp for a unit whose needed keys end at
+// valid_end; returns the count.
+__device__ __forceinline__ int split_range(int valid_end, int splits, int sp, int& t0) {
+    const int T = (valid_end + kTileN - 1) / kTileN;
+    const int tps = (T + splits - 1) / splits;
+    t0 = sp * tps;
+    const int t1 = min(T, t0 + tps);
+    return max(0, t1 - t0);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
+                        const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+    using SL = SmemLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Bars* bars = reinterpret_cast<Bars*>(smem + SL::kBar);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int b = blockIdx.z, g = blockIdx.y;
+    const int m = blockIdx.x / p.splits, sp = blockIdx.x % p.splits;
+    const int off = p.tree_off[b];
+    const int B = p.tree_off[b + 1] - off;
+    const int L = p.prefix_len[b];
+    if (m * p.npt >= B) return;  // row tile past this sequence's tree
+    if (B > JT_MAX_TREE || L < 0 || static_cast<long long>(L) + B >
+                                        static_cast<long long>(p.max_pages) * JT_PAGE_SIZE) {
+        if (tid == 0) raise_error(p.err, DEVERR_INVALID);
+        return;
+    }
+    const int n_end = min(B, (m + 1) * p.npt);
+    const int valid_end = L + n_end;
+    int t0;
+    const int nt = split_range(valid_end, p.splits, sp, t0);
+    if (nt == 0) return;  // empty split (the combine skips it too)
+
+    if (tid == 0) {
+        mbar_init(&bars->q_full, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->s_full[s], 1);
+            mbar_init(&bars->s_free[s], 128);
+            mbar_init(&bars->p_full[s], 128);
+            mbar_init(&bars->pv_done[s], 1);
+        }
+        mbar_init(&bars->v_last, 1);
+        mbar_init(&bars->mma_final, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) tmem_alloc(&bars->tmem_base, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tS0 = tmem, tO = tmem + 256, tP0 = tmem + 384;
+    volatile int* abort = &bars->abort;
+
+    uint8_t* sQ = smem + SL::kQ;
+    uint8_t* sK = smem + SL::kK;
+    uint8_t* sV = smem + SL::kV;
+    constexpr int kTileBytes = SL::kChunks * SL::kChunkBytes;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            mbar_arrive_expect_tx(&bars->q_full, kTileBytes);
+            for (int c = 0; c < SL::kChunks; ++c)
+                tma_load_3d(sQ + c * SL::kChunkBytes, &tm_q, &bars->q_full, c * 64, g * p.G,
+                            off + m * p.npt);
+        }
+        int issued = 0;
+        for (int j = 0; j < nt; ++j) {
+            const int st = j % kStages;
+            if (j >= kStages &&
+                !mbar_wait_warp(&bars->kv_empty[st], ((j / kStages) & 1) ^ 1, p.err, abort))
+                break;
+            const int slot0 = (t0 + j) * kTileN;
+            const int nvalid = min(kTileN, valid_end - slot0);
+            const int npg = (nvalid + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
+            const int pid = (lane < npg)
+                                ? p.block_table[static_cast<long long>(b) * p.max_pages +
+                                                slot0 / JT_PAGE_SIZE + lane]
+                                : 0;
+            if (lane == 0) {
+                const uint32_t bytes = npg * SL::kChunks * (JT_PAGE_SIZE * 128);
+                mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+                mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+            }
+            __syncwarp();
+            if (lane < npg) {
+                for (int c = 0; c < SL::kChunks; ++c) {
+                    const int dst = st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128);
+                    tma_load_4d(sK + dst, &tm_k, &bars->k_full[st], c * 64, g, 0, pid);
+                    tma_load_4d(sV + dst, &tm_v, &bars->v_full[st], c * 64, g, 0, pid);
+                }
+            }
+            issued = j + 1;
+            if (j == nt - 1) {
+                // final tile: once its V has landed, zero rows past the last
+                // needed slot (stale or foreign data; P is 0 there but
+                // 0 * NaN would not be), then release it to the MMA warp
+                if (!mbar_wait_warp(&bars->v_full[st], (j / kStages) & 1, p.err, abort)) break;
+                uint8_t* vt = sV + st * kTileBytes;
+                const int n16 = (kTileN - nvalid) * 8;  // 16-byte pieces per column block
+                for (int c = 0; c < SL::kChunks; ++c)
+                    for (int idx = lane; idx < n16; idx += 32)
+                        reinterpret_cast<uint4*>(vt + c * SL::kChunkBytes + (nvalid + (idx >> 3)) * 128)[idx & 7] =
+                            make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->v_last);
+            }
+        }
+        // on abort: let copies already in flight land before the CTA exits
+        if (*abort) {
+            for (int j = max(0, issued - kStages); j < issued; ++j) {
+                mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, p.err, nullptr);
+                mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, p.err, nullptr);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, true);
+            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+            auto issue_pv = [&](int i) -> bool {
+                const int st = i % kStages, pb = i & 1;
+                if (!mbar_wait(&bars->p_full[pb], (i >> 1) & 1, p.err, abort)) return false;
+                if (i == nt - 1) {
+                    if (!mbar_wait(&bars->v_last, 0, p.err, abort)) return false;
+                } else if (!mbar_wait(&bars->v_full[st], (i / kStages) & 1, p.err, abort)) {
+                    return false;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kTileN / 16; ++kk) {
+                    const uint64_t bdesc = smem_desc_sw128(aV + st * kTileBytes + kk * 16 * 128,
+                                                           SL::kChunkBytes, 1024);
+                    mma_ts(tO, tP0 + pb * 64 + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                }
+                mma_commit(&bars->kv_empty[st]);
+                mma_commit(&bars->pv_done[pb]);
+                return true;
+            };
+            bool ok = mbar_wait(&bars->q_full, 0, p.err, abort);
+            for (int j = 0; ok && j < nt; ++j) {
+                const int st = j % kStages, sb = j & 1;
+                ok = mbar_wait(&bars->k_full[st], (j / kStages) & 1, p.err, abort);
+                if (ok && j >= 2) ok = mbar_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1, p.err, abort);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t koff = (kk >> 2) * SL::kChunkBytes + (kk & 3) * 32;
+                    const uint64_t adesc = smem_desc_sw128(aQ + koff, 16, 1024);
+                    const uint64_t bdesc = smem_desc_sw128(aK + st * kTileBytes + koff, 16, 1024);
+                    mma_ss(tS0 + sb * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
+                }
+                mma_commit(&bars->s_full[sb]);
+                if (j >= 1) ok = issue_pv(j - 1);
+            }
+            if (ok) issue_pv(nt - 1);
+            // every MMA issued above completes before TMEM is released
+            mma_commit(&bars->mma_final);
+            mbar_wait(&bars->mma_final, 0, p.err, nullptr);
+        }
+    } else {
+        // ------------------------------------------------------- softmax
+        const int r = tid;  // query row = TMEM lane
+        const int node = m * p.npt + r / p.G;
+        const int head = g * p.G + r % p.G;
+        const bool valid_row = node < n_end;
+        uint32_t a[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w)
+            a[w] = valid_row ? p.anc[static_cast<long long>(off + node) * 8 + w] : 0u;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const float sl2 = p.scale_log2;
+        float m_run = -INFINITY, l_run = 0.0f;
+        bool ok = true;
+        for (int j = 0; j < nt && ok; ++j) {
+            const int sb = j & 1;
+            if (!mbar_wait_warp(&bars->s_full[sb], (j >> 1) & 1, p.err, abort)) { ok = false; break; }
+            tc_fence_after();
+            float s[kTileN];
+#pragma unroll
+            for (int q = 0; q < kTileN / 32; ++q) {
+                uint32_t v[32];
+                tmem_ld32(tS0 + sb * 128 + lane_off + q * 32, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) s[q * 32 + c] = __uint_as_float(v[c]);
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->s_free[sb]);
+
+            const int slot0 = (t0 + j) * kTileN;
+            if (slot0 + kTileN > L) {  // tile reaches the tree tail: ancestor mask
+#pragma unroll
+                for (int c = 0; c < kTileN; ++c) {
+                    const int rel = slot0 + c - L;
+                    bool vis = rel < 0;
+                    if (rel >= 0 && rel < JT_MAX_TREE) {
+                        uint32_t word = 0;
+#pragma unroll
+                        for (int w = 0; w < 8; ++w)
+                            if (w == (rel >> 5)) word = a[w];
+                        vis = (word >> (rel & 31)) & 1u;
+                    }
+                    if (!vis) s[c] = -INFINITY;
+                }
+            }
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < kTileN; ++c) mx = fmaxf(mx, s[c]);
+            const float mx_s = mx * sl2;
+            bool resc = false;
+            float factor = 1.0f;
+            if (mx_s > m_run + kRescaleLog2 || m_run == -INFINITY) {
+                const float m_new = fmaxf(m_run, mx_s);
+                if (m_run != -INFINITY) {
+                    factor = ex2_approx(m_run - m_new);
+                    resc = j > 0;
+                } else {
+                    factor = 0.0f;
+                }
+                l_run *= factor;
+                m_run = m_new;
+            }
+            if (__any_sync(0xFFFFFFFFu, resc)) {
+                // O must hold PV(j-1) before it is rescaled
+                if (!mbar_wait_warp(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t v[32];
+                    tmem_ld32(tO + lane_off + q * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c)
+                        v[c] = __float_as_uint(__uint_as_float(v[c]) * (resc ? factor : 1.0f));
+                    tmem_st32(tO + lane_off + q * 32, v);
+                }
+                tmem_wait_st();
+            }
+            // P buffer sb is free once PV(j-2) has completed
+            if (j >= 2 && !mbar_wait_warp(&bars->pv_done[sb], ((j - 2) >> 1) & 1, p.err, abort)) {
+                ok = false;
+                break;
+            }
+            const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pr[32];
+#pragma unroll
+                for (int c2 = 0; c2 < 32; ++c2) {
+                    const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * c2], sl2, -m_use));
+                    const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * c2 + 1], sl2, -m_use));
+                    l_run += p0 + p1;
+                    pr[c2] = pack_bf16x2(p0, p1);
+                }
+                tmem_st32(tP0 + sb * 64 + lane_off + h * 32, pr);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[sb]);
+        }
+        // epilogue
+        if (ok && mbar_wait_warp(&bars->pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, p.err, abort)) {
+            tc_fence_after();
+            const long long rowid = static_cast<long long>(off + node) * p.Hq + head;
+            const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t v[32];
+                tmem_ld32(tO + lane_off + q * 32, v);
+                tmem_wait_ld();
+                if (valid_row) {
+                    if (p.splits == 1) {
+                        uint4* dst = reinterpret_cast<uint4*>(p.out + rowid * D + q * 32);
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            dst[c] = make_uint4(
+                                pack_bf16x2(__uint_as_float(v[8 * c + 0]) * inv, __uint_as_float(v[8 * c + 1]) * inv),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 2]) * inv, __uint_as_float(v[8 * c + 3]) * inv),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 4]) * inv, __uint_as_float(v[8 * c + 5]) * inv),
+                                pack_bf16x2(__uint_as_float(v[8 * c + 6]) * inv, __uint_as_float(v[8 * c + 7]) * inv));
+                    } else {
+                        float4* dst = reinterpret_cast<float4*>(
+                            p.part_o + (rowid * p.splits + sp) * D + q * 32);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            dst[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
+                                                 __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+                    }
+                }
+            }
+            if (valid_row) {
+                if (p.splits == 1) {
+                    if (p.lse) p.lse[rowid] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+                } else {
+                    p.part_ml[rowid * p.splits + sp] = make_float2(m_run, l_run);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// Merge the KV-split partials of every (node, head) row.  One warp per row.
+template <int D>
+__global__ void __launch_bounds__(128)
+    tree_attn_combine_kernel(const AttnParams p, int total_nodes) {
+    const int lane = threadIdx.x & 31;
+    const int n = blockIdx.x;
+    const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
+    if (n >= total_nodes || h >= p.Hq) return;
+    int lo = 0, hi = p.nseq;  // sequence of node n
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (p.tree_off[mid] <= n) lo = mid; else hi = mid;
+    }
+    const int b = lo, off = p.tree_off[b];
+    const int B = p.tree_off[b + 1] - off;
+    const int L = p.prefix_len[b];
+    if (B > JT_MAX_TREE || L < 0 ||
+        static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE)
+        return;  // reported by the main kernel
+    const int node = n - off;
+    const int m = node / p.npt;
+    const int valid_end = L + min(B, (m + 1) * p.npt);
+    const long long rowid = static_cast<long long>(n) * p.Hq + h;
+    float M = -INFINITY;
+    int ns = 0;
+    for (int s = 0; s < p.splits; ++s) {
+        int t0;
+        if (split_range(valid_end, p.splits, s, t0) == 0) break;
+        M = fmaxf(M, p.part_ml[rowid * p.splits + s].x);
+        ns = s + 1;
+    }
+    float acc[D / 32];
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
+    float lsum = 0.0f;
+    for (int s = 0; s < ns; ++s) {
+        const float2 ml = p.part_ml[rowid * p.splits + s];
+        const float wgt = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - M);
+        lsum += wgt * ml.y;
+        const float* po = p.part_o + (rowid * p.splits + s) * D;
+#pragma unroll
+        for (int k = 0; k < D / 32; ++k) acc[k] += wgt * po[lane + 32 * k];
+    }
+    const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) p.out[rowid * D + lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+    if (lane == 0 && p.lse) p.lse[rowid] = (M + log2f(lsum)) * 0.6931471805599453f;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*PFN_encodeTiled_t)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                      const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                      const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                      CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static PFN_encodeTiled_t get_encode_fn() {
+    static PFN_encodeTiled_t fn = nullptr;
+    if (!fn) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_encodeTiled_t>(ptr);
+    }
+    return fn;
+}
+
+AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int dtype) {
+    AttnPlan pl;
+    const int G = Hq / Hkv;
+    pl.rows_per_tile_nodes = kTileM / G;
+    pl.mtiles = (max_tree + pl.rows_per_tile_nodes - 1) / pl.rows_per_tile_nodes;
+    pl.splits = 1;
+    if (dtype == JT_DTYPE_BF16) {
+        const long long units = static_cast<long long>(nseq) * Hkv * pl.mtiles;
+        const int sms = device_sm_count();
+        const int tmax = (max_pages * JT_PAGE_SIZE + kTileN - 1) / kTileN;
+        if (units > 0 && units < sms) {
+            int s = static_cast<int>(sms / units);
+            s = min(s, max(1, tmax / 2));
+            pl.splits = max(1, min(s, kMaxSplits));
+        }
+    }
+    return pl;
+}
+
+size_t attn_workspace_bytes(const AttnPlan& p, int total_nodes, int Hq, int D) {
+    size_t b = kWsHeader;
+    if (p.splits > 1) {
+        const size_t rows = static_cast<size_t>(total_nodes) * Hq * p.splits;
+        b += align_up(rows * D * sizeof(float));
+        b += align_up(rows * sizeof(float2));
+    }
+    return b;
+}
+
+template <int D>
+static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v_cache,
+                               const int32_t* block_table, int max_pages, int num_pages,
+                               const int32_t* prefix_len, const int32_t* tree_off,
+                               const uint32_t* anc, int nseq, int total_nodes, int Hq, int Hkv,
+                               float scale, void* out, float* lse, const AttnPlan& plan,
+                               char* ws_parts, uint32_t* err, cudaStream_t st) {
+    PFN_encodeTiled_t enc = get_encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    const int G = Hq / Hkv;
+    CUtensorMap tq, tk, tv;
+    {
+        const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hq),
+                                    static_cast<cuuint64_t>(total_nodes)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                       static_cast<cuuint64_t>(Hq) * D * 2};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G),
+                                   static_cast<cuuint32_t>(plan.rows_per_tile_nodes)};
+        const cuuint32_t es[3] = {1, 1, 1};
+        if (enc(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides, box,
+                es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(Hkv),
+                                    JT_PAGE_SIZE, static_cast<cuuint64_t>(num_pages)};
+        const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                       static_cast<cuuint64_t>(Hkv) * D * 2,
+                                       static_cast<cuuint64_t>(JT_PAGE_SIZE) * Hkv * D * 2};
+        const cuuint32_t box[4] = {64, 1, JT_PAGE_SIZE, 1};
+        const cuuint32_t es[4] = {1, 1, 1, 1};
+        if (enc(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(k_cache), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+        if (enc(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v_cache), dims, strides,
+                box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    AttnParams prm;
+    prm.block_table = block_table;
+    prm.prefix_len = prefix_len;
+    prm.tree_off = tree_off;
+    prm.anc = anc;
+    prm.out = static_cast<__nv_bfloat16*>(out);
+    prm.lse = lse;
+    prm.part_o = nullptr;
+    prm.part_ml = nullptr;
+    if (plan.splits > 1) {
+        const size_t rows = static_cast<size_t>(total_nodes) * Hq * plan.splits;
+        prm.part_o = reinterpret_cast<float*>(ws_parts);
+        prm.part_ml = reinterpret_cast<float2*>(ws_parts + align_up(rows * D * sizeof(float)));
+    }
+    prm.err = err;
+    prm.max_pages = max_pages;
+    prm.nseq = nseq;
+    prm.Hq = Hq;
+    prm.G = G;
+    prm.npt = plan.rows_per_tile_nodes;
+    prm.splits = plan.splits;
+    prm.scale_log2 = scale * 1.4426950408889634f;
+
+    using SL = SmemLayout<D>;
+    static bool attr_done = false;
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    dim3 grid(plan.mtiles * plan.splits, Hkv, nseq);
+    tree_attn_tc_kernel<D><<<grid, kAttnThreads, SL::kAlloc, st>>>(tq, tk, tv, prm);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || plan.splits == 1) return e;
+    dim3 cgrid(total_nodes, (Hq + 3) / 4);
+    tree_attn_combine_kernel<D><<<cgrid, 128, 0, st>>>(prm, total_nodes);
+    return cudaGetLastError();
+}
+
+cudaError_t tree_attn_bf16_launch(const void* q, const void* k_cache, const void* v_cache,
+                                  const int32_t* block_table, int max_pages, int num_pages,
+                                  const int32_t* prefix_len, const int32_t* tree_off,
+                                  const uint32_t* anc, int nseq, int total_nodes, int Hq, int Hkv,
+                                  int D, float scale, void* out, float* lse, const AttnPlan& plan,
+                                  char* ws_parts, uint32_t* err, cudaStream_t st) {
+    if (D == 128)
+        return launch_bf16<128>(q, k_cache, v_cache, block_table, max_pages, num_pages, prefix_len,
+                                tree_off, anc, nseq, total_nodes, Hq, Hkv, scale, out, lse, plan,
+                                ws_parts, err, st);
+    if (D == 64)
+        return launch_bf16<64>(q, k_cache, v_cache, block_table, max_pages, num_pages, prefix_len,
+                               tree_off, anc, nseq, total_nodes, Hq, Hkv, scale, out, lse, plan,
+                               ws_parts, err, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace jt

@@ -1,0 +1,662 @@
+// tree_build.cu -- draft-tree construction on CUDA cores.
+//
+// Follows the JetSpec news summary (tree construction: one forward gives the
+// logits of every depth, keep the top-W per depth, score branches by the
+// cumulative draft log-probability and fill greedily up to the budget B,
+// depth at most N) and "加速AI思考…推测解码新方法" section 五 (best-first
+// expansion with a priority queue: pop the best node, give it up to W
+// children, push them, stop at B nodes).
+//
+// Kernels
+//   topw_partial_kernel  one CTA per (row, 4096-entry chunk): vectorised
+//                        coalesced loads, per-thread top-W in registers,
+//                        warp-shuffle merge; chunk max and the chunk's
+//                        sum of exp(z - max) from the table-driven fp32 exp
+//                        with float-float accumulation (fp64 per CTA).
+//   topw_merge_kernel    one warp per row: merges the chunk partials into
+//                        top-W ids, log-probs and lse (fp64).
+//   expand_kernel        one CTA per sequence: merges its N rows, then one
+//                        warp runs the best-first expansion with a lazy
+//                        frontier (only a popped node's best child and a
+//                        popped child's next sibling are pushed, which pops
+//                        the same sequence as pushing all W children), then
+//                        all threads derive the 256-bit ancestor sets.
+#include <float.h>
+
+#include "ffexp.cuh"
+#include "jt_common.cuh"
+#include "jt_internal.h"
+
+namespace jt {
+
+constexpr int kTopwThreads = 256;
+constexpr int kTopwPerThread = 16;
+constexpr int kExpandThreads = 256;
+constexpr unsigned kFull = 0xFFFFFFFFu;
+
+struct ExpTable {
+    float hi[64];
+    float lo[64];
+};
+
+// (value desc, id asc); id -1 marks an empty entry and loses every tie.
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && static_cast<unsigned>(ia) < static_cast<unsigned>(ib));
+}
+
+template <int W>
+struct TopList {
+    float v[W];
+    int id[W];
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            v[k] = -INFINITY;
+            id[k] = -1;
+        }
+    }
+    __device__ __forceinline__ void push(float x, int i) {
+        if (!better(x, i, v[W - 1], id[W - 1])) return;
+        bool placed = false;
+#pragma unroll
+        for (int k = W - 1; k >= 1; --k) {
+            if (!placed) {
+                if (better(x, i, v[k - 1], id[k - 1])) {
+                    v[k] = v[k - 1];
+                    id[k] = id[k - 1];
+                } else {
+                    v[k] = x;
+                    id[k] = i;
+                    placed = true;
+                }
+            }
+        }
+        if (!placed) {
+            v[0] = x;
+            id[0] = i;
+        }
+    }
+    __device__ __forceinline__ void pop_front() {
+#pragma unroll
+        for (int k = 0; k < W - 1; ++k) {
+            v[k] = v[k + 1];
+            id[k] = id[k + 1];
+        }
+        v[W - 1] = -INFINITY;
+        id[W - 1] = -1;
+    }
+};
+
+// Merge the 32 lanes' sorted lists into the warp's top-W (result in every
+// lane): W rounds of a shuffle arg-max over the lanes' heads.
+template <int W>
+__device__ __forceinline__ void warp_merge(TopList<W>& L, float (&rv)[W], int (&rid)[W]) {
+#pragma unroll
+    for (int r = 0; r < W; ++r) {
+        float bv = L.v[0];
+        int bi = L.id[0];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(kFull, bv, off);
+            const int oi = __shfl_xor_sync(kFull, bi, off);
+            if (better(ov, oi, bv, bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        rv[r] = bv;
+        rid[r] = bi;
+        if (bi != -1 && L.id[0] == bi) L.pop_front();
+    }
+}
+
+__device__ __forceinline__ double warp_sum_d(double x) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
+    return x;
+}
+__device__ __forceinline__ float warp_max_f(float x) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
+    return x;
+}
+
+// ---------------------------------------------------------------------------
+// Step 1a: per-chunk top-W, max and sum of exp(z - max).
+// grid = (splits, rows); chunk = kTopwThreads*kTopwPerThread entries.
+// ---------------------------------------------------------------------------
+template <int W, bool VEC>
+__global__ void __launch_bounds__(kTopwThreads)
+    topw_partial_kernel(const float* __restrict__ z, long long V, int splits, ExpTable tab,
+                        float* __restrict__ part_v, int* __restrict__ part_id,
+                        float* __restrict__ part_m, double* __restrict__ part_s) {
+    constexpr int CH = kTopwThreads * kTopwPerThread;
+    __shared__ float s_thi[64], s_tlo[64];
+    __shared__ float s_wv[kTopwThreads / 32][W];
+    __shared__ int s_wi[kTopwThreads / 32][W];
+    __shared__ float s_wmax[kTopwThreads / 32];
+    __shared__ double s_wsum[kTopwThreads / 32];
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long row = blockIdx.y;
+    const int sp = blockIdx.x;
+    if (tid < 64) {
+        s_thi[tid] = tab.hi[tid];
+        s_tlo[tid] = tab.lo[tid];
+    }
+    const float* zr = z + row * V;
+    const long long begin = static_cast<long long>(sp) * CH;
+    const long long end = min(V, begin + CH);
+
+    float x[kTopwPerThread];
+    TopList<W> L;
+    L.init();
+    if (VEC) {
+#pragma unroll
+        for (int i = 0; i < kTopwPerThread / 4; ++i) {
+            const long long e = begin + 4ll * (tid + kTopwThreads * i);
+            float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (e < end) f = __ldg(reinterpret_cast<const float4*>(zr + e));
+            x[4 * i + 0] = f.x;
+            x[4 * i + 1] = f.y;
+            x[4 * i + 2] = f.z;
+            x[4 * i + 3] = f.w;
+            if (e < end) {
+                L.push(f.x, static_cast<int>(e));
+                L.push(f.y, static_cast<int>(e + 1));
+                L.push(f.z, static_cast<int>(e + 2));
+                L.push(f.w, static_cast<int>(e + 3));
+            }
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < kTopwPerThread; ++i) {
+            const long long e = begin + tid + static_cast<long long>(kTopwThreads) * i;
+            x[i] = -INFINITY;
+            if (e < end) {
+                x[i] = __ldg(zr + e);
+                L.push(x[i], static_cast<int>(e));
+            }
+        }
+    }
+
+    // chunk maximum
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kTopwPerThread; ++i) m = fmaxf(m, x[i]);
+    m = warp_max_f(m);
+    if (lane == 0) s_wmax[warp] = m;
+    __syncthreads();
+    m = (lane < kTopwThreads / 32) ? s_wmax[lane] : -INFINITY;
+    m = warp_max_f(m);
+
+    // sum of exp(z - m): exact difference as a float pair, table-driven exp,
+    // float-float accumulation, fp64 across threads
+    float acc_hi = 0.0f, acc_lo = 0.0f;
+    if (m != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < kTopwPerThread; ++i) {
+            float dh, dl;
+            two_sum(x[i], -m, dh, dl);
+            const ffloat y = ffexp(dh, dl, s_thi, s_tlo);
+            float s, e;
+            two_sum(acc_hi, y.hi, s, e);
+            acc_hi = s;
+            acc_lo = jt_add(acc_lo, jt_add(e, y.lo));
+        }
+    }
+    double S = warp_sum_d(static_cast<double>(acc_hi) + static_cast<double>(acc_lo));
+    if (lane == 0) s_wsum[warp] = S;
+
+    // top-W across the CTA
+    float rv[W];
+    int rid[W];
+    warp_merge<W>(L, rv, rid);
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            s_wv[warp][k] = rv[k];
+            s_wi[warp][k] = rid[k];
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        TopList<W> M;
+        M.init();
+        if (lane < kTopwThreads / 32) {
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                M.v[k] = s_wv[lane][k];
+                M.id[k] = s_wi[lane][k];
+            }
+        }
+        warp_merge<W>(M, rv, rid);
+        S = (lane < kTopwThreads / 32) ? s_wsum[lane] : 0.0;
+        S = warp_sum_d(S);
+        const long long p = row * splits + sp;
+        if (lane == 0) {
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                part_v[p * W + k] = rv[k];
+                part_id[p * W + k] = rid[k];
+            }
+            part_m[p] = m;
+            part_s[p] = S;
+        }
+    }
+}
+
+// Merge the partials of one row (whole warp): top-W ids/values and lse.
+template <int W>
+__device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
+                                          const int* __restrict__ part_id,
+                                          const float* __restrict__ part_m,
+                                          const double* __restrict__ part_s, int splits,
+                                          long long row, int lane, int (&tok)[W],
+                                          double (&lp)[W], double& lse) {
+    const long long base = row * splits;
+    float M = -INFINITY;
+    for (int s = lane; s < splits; s += 32) M = fmaxf(M, part_m[base + s]);
+    M = warp_max_f(M);
+    double S = 0.0;
+    if (M != -INFINITY)
+        for (int s = lane; s < splits; s += 32) {
+            const float ms = part_m[base + s];
+            if (ms != -INFINITY) S += part_s[base + s] * exp(static_cast<double>(ms) - M);
+        }
+    S = warp_sum_d(S);
+    lse = (M == -INFINITY) ? -INFINITY : static_cast<double>(M) + log(S);
+
+    TopList<W> L;
+    L.init();
+    for (int s = lane; s < splits; s += 32)
+#pragma unroll
+        for (int k = 0; k < W; ++k) L.push(part_v[(base + s) * W + k], part_id[(base + s) * W + k]);
+    float rv[W];
+    int rid[W];
+    warp_merge<W>(L, rv, rid);
+#pragma unroll
+    for (int k = 0; k < W; ++k) {
+        tok[k] = rid[k];
+        lp[k] = static_cast<double>(rv[k]) - lse;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Step 1b (jt_tree_topw only): one warp per row.
+// ---------------------------------------------------------------------------
+template <int W>
+__global__ void __launch_bounds__(256)
+    topw_merge_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id,
+                      const float* __restrict__ part_m, const double* __restrict__ part_s,
+                      int splits, long long rows, int32_t* __restrict__ tok_out,
+                      double* __restrict__ lp_out, double* __restrict__ lse_out) {
+    const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    int tok[W];
+    double lp[W], lse;
+    merge_row<W>(part_v, part_id, part_m, part_s, splits, row, lane, tok, lp, lse);
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            tok_out[row * W + k] = tok[k];
+            lp_out[row * W + k] = lp[k];
+        }
+        lse_out[row] = lse;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Step 2: best-first expansion, one CTA per sequence.
+// ---------------------------------------------------------------------------
+// Secondary key: larger = earlier.  depth asc, token asc, parent asc.
+__device__ __forceinline__ unsigned long long make_k2(int depth, int token, int parent) {
+    return (static_cast<unsigned long long>(255 - depth) << 56) |
+           (static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(token)) << 24) |
+           static_cast<unsigned long long>(0xFFFFFFu - static_cast<uint32_t>(parent));
+}
+
+__device__ __forceinline__ double double_from_order_key(unsigned long long k) {
+    const unsigned long long u = (k & 0x8000000000000000ull) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
+    return __longlong_as_double(static_cast<long long>(u));
+}
+
+__device__ __forceinline__ bool key_better(unsigned long long a1, unsigned long long a2,
+                                           unsigned long long b1, unsigned long long b2) {
+    return a1 > b1 || (a1 == b1 && a2 > b2);
+}
+
+__host__ __device__ inline int full_tree_nodes(int N, int W, int cap) {
+    long long total = 1, level = 1;
+    for (int d = 1; d <= N; ++d) {
+        level *= W;
+        total += level;
+        if (total >= cap || level >= cap) return cap;
+    }
+    return static_cast<int>(total);
+}
+
+template <int W>
+__global__ void __launch_bounds__(kExpandThreads)
+    expand_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id,
+                  const float* __restrict__ part_m, const double* __restrict__ part_s,
+                  int splits, const int32_t* __restrict__ tok_in, const double* __restrict__ lp_in,
+                  const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
+                  int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
+                  int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
+    __shared__ int s_tok[JT_MAX_N * W];
+    __shared__ double s_lp[JT_MAX_N * W];
+    __shared__ int s_par[JT_MAX_TREE];
+    __shared__ int s_tokn[JT_MAX_TREE];
+    __shared__ int s_dep[JT_MAX_TREE];
+    __shared__ double s_score[JT_MAX_TREE];
+    __shared__ int s_count;
+
+    const int b = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int off = tree_off[b];
+    const int B = tree_off[b + 1] - off;
+    if (B < 1 || B > JT_MAX_TREE || B > full_tree_nodes(N, W, JT_MAX_TREE + 1)) {
+        if (tid == 0) raise_error(err, DEVERR_INVALID);
+        return;
+    }
+
+    // per-depth tables for this sequence
+    if (tok_in) {
+        for (int i = tid; i < N * W; i += kExpandThreads) {
+            s_tok[i] = tok_in[static_cast<long long>(b) * N * W + i];
+            s_lp[i] = lp_in[static_cast<long long>(b) * N * W + i];
+        }
+    } else {
+        for (int d = warp; d < N; d += kExpandThreads / 32) {
+            int tk[W];
+            double lq[W], lse;
+            merge_row<W>(part_v, part_id, part_m, part_s, splits, static_cast<long long>(b) * N + d,
+                         lane, tk, lq, lse);
+            if (lane == 0)
+#pragma unroll
+                for (int k = 0; k < W; ++k) {
+                    s_tok[d * W + k] = tk[k];
+                    s_lp[d * W + k] = lq[k];
+                }
+        }
+    }
+    if (tid == 0) {
+        s_par[0] = -1;
+        s_tokn[0] = root_token[b];
+        s_dep[0] = 0;
+        s_score[0] = 0.0;
+        s_count = 1;
+    }
+    __syncthreads();
+
+    if (warp == 0 && B > 1) {
+        // frontier: slot s lives in lane s&31, register position s>>5
+        unsigned long long k1[8], k2[8];
+        int kr[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            k1[i] = 0ull;
+            k2[i] = 0ull;
+            kr[i] = 0;
+        }
+        int nslots = 1;
+        if (lane == 0) {  // first child of the root
+            k1[0] = double_order_key(__dadd_rn(0.0, s_lp[0]));
+            k2[0] = make_k2(1, s_tok[0], 0);
+            kr[0] = 0;
+        }
+        int lb = (lane == 0) ? 0 : -1;  // lane-local best slot
+        unsigned long long b1 = (lane == 0) ? k1[0] : 0ull, b2 = (lane == 0) ? k2[0] : 0ull;
+
+        for (int count = 1; count < B; ++count) {
+            // warp arg-max of (b1, b2) with REDUX on 32-bit pieces
+            const bool valid = lb >= 0;
+            uint32_t piece = valid ? static_cast<uint32_t>(b1 >> 32) : 0u;
+            uint32_t mx = __reduce_max_sync(kFull, piece);
+            unsigned cand = __ballot_sync(kFull, valid && piece == mx);
+            if (__popc(cand) > 1) {
+                piece = ((cand >> lane) & 1u) ? static_cast<uint32_t>(b1) : 0u;
+                mx = __reduce_max_sync(kFull, piece);
+                cand &= __ballot_sync(kFull, piece == mx);
+            }
+            if (__popc(cand) > 1) {
+                piece = ((cand >> lane) & 1u) ? static_cast<uint32_t>(b2 >> 32) : 0u;
+                mx = __reduce_max_sync(kFull, piece);
+                cand &= __ballot_sync(kFull, piece == mx);
+            }
+            if (__popc(cand) > 1) {
+                piece = ((cand >> lane) & 1u) ? static_cast<uint32_t>(b2) : 0u;
+                mx = __reduce_max_sync(kFull, piece);
+                cand &= __ballot_sync(kFull, piece == mx);
+            }
+            if (cand == 0u) break;  // frontier empty: cannot happen for B <= full tree
+            const int wl = __ffs(cand) - 1;
+            int wkr = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i == lb) wkr = kr[i];
+            const unsigned long long w1 = __shfl_sync(kFull, b1, wl);
+            const unsigned long long w2 = __shfl_sync(kFull, b2, wl);
+            wkr = __shfl_sync(kFull, wkr, wl);
+            const double wscore = double_from_order_key(w1);
+            const int wdepth = 255 - static_cast<int>(w2 >> 56);
+            const int wtoken = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>((w2 >> 24) & 0xFFFFFFFFull));
+            const int wpar = static_cast<int>(0xFFFFFFu - static_cast<uint32_t>(w2 & 0xFFFFFFull));
+            const int n = count;
+            if (lane == 0) {
+                s_par[n] = wpar;
+                s_tokn[n] = wtoken;
+                s_dep[n] = wdepth;
+                s_score[n] = wscore;
+                s_count = n + 1;
+            }
+            __syncwarp();
+            // popped slot -> next sibling (rank wkr+1) or empty
+            if (lane == wl) {
+                unsigned long long n1 = 0ull, n2 = 0ull;
+                if (wkr + 1 < W) {
+                    const int r = (wdepth - 1) * W + wkr + 1;
+                    n1 = double_order_key(__dadd_rn(s_score[wpar], s_lp[r]));
+                    n2 = make_k2(wdepth, s_tok[r], wpar);
+                }
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (i == lb) {
+                        k1[i] = n1;
+                        k2[i] = n2;
+                        kr[i] = wkr + 1;
+                    }
+            }
+            // best child of the new node -> new slot
+            if (wdepth < N) {
+                const int s = nslots++;
+                if (lane == (s & 31)) {
+                    const int pos = s >> 5;
+                    const unsigned long long n1 = double_order_key(__dadd_rn(wscore, s_lp[wdepth * W]));
+                    const unsigned long long n2 = make_k2(wdepth + 1, s_tok[wdepth * W], n);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (i == pos) {
+                            k1[i] = n1;
+                            k2[i] = n2;
+                            kr[i] = 0;
+                        }
+                }
+            }
+            // lanes whose slots changed rescan their best
+            if (lane == wl || (wdepth < N && lane == ((nslots - 1) & 31))) {
+                lb = -1;
+                b1 = 0ull;
+                b2 = 0ull;
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (k1[i] != 0ull && (lb < 0 || key_better(k1[i], k2[i], b1, b2))) {
+                        lb = i;
+                        b1 = k1[i];
+                        b2 = k2[i];
+                    }
+            }
+        }
+    }
+    __syncthreads();
+
+    // outputs and ancestor-or-self sets
+    if (s_count != B) {  // the expansion stopped early: report, write nothing
+        if (tid == 0) raise_error(err, DEVERR_INVALID);
+        return;
+    }
+    for (int n = tid; n < B; n += kExpandThreads) {
+        uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        for (int u = n; u >= 0; u = s_par[u]) {
+#pragma unroll
+            for (int w = 0; w < 8; ++w)
+                if (w == (u >> 5)) a[w] |= 1u << (u & 31);
+        }
+        const long long g = off + n;
+        parent[g] = s_par[n];
+        token[g] = s_tokn[n];
+        depth[g] = s_dep[n];
+        uint4* ap = reinterpret_cast<uint4*>(anc + g * 8);
+        ap[0] = make_uint4(a[0], a[1], a[2], a[3]);
+        ap[1] = make_uint4(a[4], a[5], a[6], a[7]);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host launchers
+// ---------------------------------------------------------------------------
+static ExpTable make_exp_table() {
+    ExpTable t;
+    ffexp_table(t.hi, t.lo);
+    return t;
+}
+
+static int topw_splits(long long V) {
+    const long long CH = kTopwThreads * kTopwPerThread;
+    return static_cast<int>((V + CH - 1) / CH);
+}
+
+size_t topw_workspace_bytes(long long rows, long long V, int W) {
+    const long long p = rows * topw_splits(V);
+    size_t bytes = 0;
+    bytes += align_up(p * W * sizeof(float));
+    bytes += align_up(p * W * sizeof(int));
+    bytes += align_up(p * sizeof(float));
+    bytes += align_up(p * sizeof(double));
+    return bytes;
+}
+
+struct TopwParts {
+    float* v;
+    int* id;
+    float* m;
+    double* s;
+    int splits;
+};
+
+static TopwParts carve_topw(char* base, long long rows, long long V, int W) {
+    TopwParts t;
+    t.splits = topw_splits(V);
+    const long long p = rows * t.splits;
+    t.v = reinterpret_cast<float*>(base);
+    base += align_up(p * W * sizeof(float));
+    t.id = reinterpret_cast<int*>(base);
+    base += align_up(p * W * sizeof(int));
+    t.m = reinterpret_cast<float*>(base);
+    base += align_up(p * sizeof(float));
+    t.s = reinterpret_cast<double*>(base);
+    return t;
+}
+
+template <int W>
+static cudaError_t launch_topw_partial(const float* z, long long rows, long long V, TopwParts& t,
+                                       cudaStream_t st) {
+    static const ExpTable tab = make_exp_table();
+    const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
+    dim3 grid(t.splits, static_cast<unsigned>(rows));
+    if (vec)
+        topw_partial_kernel<W, true><<<grid, kTopwThreads, 0, st>>>(z, V, t.splits, tab, t.v, t.id,
+                                                                     t.m, t.s);
+    else
+        topw_partial_kernel<W, false><<<grid, kTopwThreads, 0, st>>>(z, V, t.splits, tab, t.v, t.id,
+                                                                      t.m, t.s);
+    return cudaGetLastError();
+}
+
+template <int W>
+static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t* tok, double* lp,
+                            double* lse, char* ws_parts, cudaStream_t st) {
+    TopwParts t = carve_topw(ws_parts, rows, V, W);
+    cudaError_t e = launch_topw_partial<W>(z, rows, V, t, st);
+    if (e != cudaSuccess) return e;
+    const long long warps_per_block = 8;
+    const unsigned blocks = static_cast<unsigned>((rows + warps_per_block - 1) / warps_per_block);
+    topw_merge_kernel<W><<<blocks, 256, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, rows, tok, lp, lse);
+    return cudaGetLastError();
+}
+
+template <int W>
+static cudaError_t run_build(const float* z, const int32_t* root_token, const int32_t* tree_off,
+                             int nseq, int N, long long V, int32_t* parent, int32_t* token,
+                             int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
+                             cudaStream_t st) {
+    const long long rows = static_cast<long long>(nseq) * N;
+    TopwParts t = carve_topw(ws_parts, rows, V, W);
+    if (rows > 0) {
+        cudaError_t e = launch_topw_partial<W>(z, rows, V, t, st);
+        if (e != cudaSuccess) return e;
+    }
+    expand_kernel<W><<<nseq, kExpandThreads, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, nullptr,
+                                                       nullptr, root_token, tree_off, N, parent,
+                                                       token, depth, anc, err);
+    return cudaGetLastError();
+}
+
+template <int W>
+static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
+                              const int32_t* tree_off, int nseq, int N, int32_t* parent,
+                              int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
+                              cudaStream_t st) {
+    expand_kernel<W><<<nseq, kExpandThreads, 0, st>>>(nullptr, nullptr, nullptr, nullptr, 0, tok, lp,
+                                                       root_token, tree_off, N, parent, token,
+                                                       depth, anc, err);
+    return cudaGetLastError();
+}
+
+#define JT_DISPATCH_W(W, CALL)           \
+    switch (W) {                          \
+        case 1: { constexpr int kW = 1; return CALL; } \
+        case 2: { constexpr int kW = 2; return CALL; } \
+        case 3: { constexpr int kW = 3; return CALL; } \
+        case 4: { constexpr int kW = 4; return CALL; } \
+        case 5: { constexpr int kW = 5; return CALL; } \
+        case 6: { constexpr int kW = 6; return CALL; } \
+        case 7: { constexpr int kW = 7; return CALL; } \
+        case 8: { constexpr int kW = 8; return CALL; } \
+        default: return cudaErrorInvalidValue; \
+    }
+
+cudaError_t tree_topw_launch(const float* z, long long rows, long long V, int W, int32_t* tok,
+                             double* lp, double* lse, char* ws_parts, cudaStream_t st) {
+    JT_DISPATCH_W(W, run_topw<kW>(z, rows, V, tok, lp, lse, ws_parts, st));
+}
+
+cudaError_t tree_build_launch(const float* z, const int32_t* root_token, const int32_t* tree_off,
+                              int nseq, int N, int W, long long V, int32_t* parent, int32_t* token,
+                              int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
+                              cudaStream_t st) {
+    JT_DISPATCH_W(W, run_build<kW>(z, root_token, tree_off, nseq, N, V, parent, token, depth, anc,
+                                   ws_parts, err, st));
+}
+
+cudaError_t tree_expand_launch(const int32_t* tok, const double* lp, const int32_t* root_token,
+                               const int32_t* tree_off, int nseq, int N, int W, int32_t* parent,
+                               int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
+                               cudaStream_t st) {
+    JT_DISPATCH_W(W, run_expand<kW>(tok, lp, root_token, tree_off, nseq, N, parent, token, depth,
+                                    anc, err, st));
+}
+
+}  // namespace jt
