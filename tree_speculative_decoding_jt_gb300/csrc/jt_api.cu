@@ -115,7 +115,7 @@ jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
     char* base = static_cast<char*>(ws);
     cudaError_t e = cudaMemsetAsync(base, 0, sizeof(WsHeader), stream);
     if (e == cudaSuccess)
-        e = tree_build_launch(draft_logits, root_token, tree_off, nseq, N, W, V, parent, token,
+        e = tree_build_launch(draft_logits, root_token, tree_off, nseq, total_nodes, N, W, V, parent, token,
                               depth, anc, base + kWsHeader, reinterpret_cast<uint32_t*>(base),
                               stream);
     return from_cuda(e);
@@ -134,7 +134,7 @@ jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* ro
     char* base = static_cast<char*>(ws);
     cudaError_t e = cudaMemsetAsync(base, 0, sizeof(WsHeader), stream);
     if (e == cudaSuccess)
-        e = tree_expand_launch(tok, lp, root_token, tree_off, nseq, N, W, parent, token, depth, anc,
+        e = tree_expand_launch(tok, lp, root_token, tree_off, nseq, total_nodes, N, W, parent, token, depth, anc,
                                reinterpret_cast<uint32_t*>(base), stream);
     return from_cuda(e);
 }
@@ -175,7 +175,7 @@ jt_status jt_tree_attn_paged(const void* q, const void* k_cache, const void* v_c
     else
         e = tree_attn_f32_launch(static_cast<const float*>(q), static_cast<const float*>(k_cache),
                                  static_cast<const float*>(v_cache), block_table, max_pages,
-                                 prefix_len, tree_off, anc, nseq, total_nodes, Hq, Hkv, D, scale,
+                                 num_pages, prefix_len, tree_off, anc, nseq, total_nodes, Hq, Hkv, D, scale,
                                  static_cast<float*>(out), lse, err, stream);
     return from_cuda(e);
 }

@@ -26,11 +26,11 @@ size_t topw_workspace_bytes(long long rows, long long V, int W);
 cudaError_t tree_topw_launch(const float* z, long long rows, long long V, int W, int32_t* tok,
                              double* lp, double* lse, char* ws_parts, cudaStream_t st);
 cudaError_t tree_build_launch(const float* z, const int32_t* root_token, const int32_t* tree_off,
-                              int nseq, int N, int W, long long V, int32_t* parent, int32_t* token,
+                              int nseq, int total_nodes, int N, int W, long long V, int32_t* parent, int32_t* token,
                               int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
                               cudaStream_t st);
 cudaError_t tree_expand_launch(const int32_t* tok, const double* lp, const int32_t* root_token,
-                               const int32_t* tree_off, int nseq, int N, int W, int32_t* parent,
+                               const int32_t* tree_off, int nseq, int total_nodes, int N, int W, int32_t* parent,
                                int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
                                cudaStream_t st);
 
@@ -56,7 +56,7 @@ cudaError_t tree_attn_bf16_launch(const void* q, const void* k_cache, const void
                                   int D, float scale, void* out, float* lse, const AttnPlan& plan,
                                   char* ws_parts, uint32_t* err, cudaStream_t st);
 cudaError_t tree_attn_f32_launch(const float* q, const float* k_cache, const float* v_cache,
-                                 const int32_t* block_table, int max_pages,
+                                 const int32_t* block_table, int max_pages, int num_pages,
                                  const int32_t* prefix_len, const int32_t* tree_off,
                                  const uint32_t* anc, int nseq, int total_nodes, int Hq, int Hkv,
                                  int D, float scale, float* out, float* lse, uint32_t* err,

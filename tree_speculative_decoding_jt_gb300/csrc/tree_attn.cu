@@ -54,7 +54,7 @@ struct AttnParams {
     float* part_o;   // [total*Hq*splits, D] when splits > 1
     float2* part_ml; // [total*Hq*splits]: running max (log2 units), sum
     uint32_t* err;
-    int max_pages, nseq, Hq, G, npt, splits;
+    int max_pages, nseq, total_nodes, Hq, G, npt, splits;
     float scale_log2;
 };
 
@@ -119,8 +119,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const int B = p.tree_off[b + 1] - off;
     const int L = p.prefix_len[b];
     if (m * p.npt >= B) return;  // row tile past this sequence's tree
-    if (B > JT_MAX_TREE || L < 0 || static_cast<long long>(L) + B >
-                                        static_cast<long long>(p.max_pages) * JT_PAGE_SIZE) {
+    if (B > JT_MAX_TREE || L < 0 || off < 0 || off + B > p.total_nodes ||
+        static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE) {
         if (tid == 0) raise_error(p.err, DEVERR_INVALID);
         return;
     }
@@ -437,7 +437,7 @@ __global__ void __launch_bounds__(128)
     const int b = lo, off = p.tree_off[b];
     const int B = p.tree_off[b + 1] - off;
     const int L = p.prefix_len[b];
-    if (B > JT_MAX_TREE || L < 0 ||
+    if (B < 1 || B > JT_MAX_TREE || L < 0 || off < 0 || off + B > p.total_nodes ||
         static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE)
         return;  // reported by the main kernel
     const int node = n - off;
@@ -578,6 +578,7 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
     prm.err = err;
     prm.max_pages = max_pages;
     prm.nseq = nseq;
+    prm.total_nodes = total_nodes;
     prm.Hq = Hq;
     prm.G = G;
     prm.npt = plan.rows_per_tile_nodes;

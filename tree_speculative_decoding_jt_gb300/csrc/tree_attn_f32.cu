@@ -17,7 +17,7 @@ template <int DPL>  // elements per lane = D / 32
 __global__ void __launch_bounds__(128)
     tree_attn_f32_kernel(const float* __restrict__ q, const float* __restrict__ kc,
                          const float* __restrict__ vc, const int32_t* __restrict__ block_table,
-                         int max_pages, const int32_t* __restrict__ prefix_len,
+                         int max_pages, int num_pages, const int32_t* __restrict__ prefix_len,
                          const int32_t* __restrict__ tree_off, const uint32_t* __restrict__ anc,
                          int nseq, int total_nodes, int Hq, int Hkv, float scale,
                          float* __restrict__ out, float* __restrict__ lse, uint32_t* err) {
@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(128)
     const int b = lo, off = tree_off[b];
     const int B = tree_off[b + 1] - off;
     const int L = prefix_len[b];
-    if (B > JT_MAX_TREE || L < 0 ||
+    if (B < 1 || B > JT_MAX_TREE || L < 0 || off < 0 || off + B > total_nodes ||
         static_cast<long long>(L) + B > static_cast<long long>(max_pages) * JT_PAGE_SIZE) {
         if (lane == 0) raise_error(err, DEVERR_INVALID);
         return;
@@ -48,8 +48,13 @@ __global__ void __launch_bounds__(128)
         acc[k] = 0.0f;
     }
     float mrun = -INFINITY, lrun = 0.0f;
+    bool bad_page = false;
     auto visit = [&](int slot) {
         const long long page = block_table[static_cast<long long>(b) * max_pages + slot / JT_PAGE_SIZE];
+        if (page < 0 || page >= num_pages) {  // warp-uniform: every lane reads the same entry
+            bad_page = true;
+            return;
+        }
         const long long base = ((page * JT_PAGE_SIZE + slot % JT_PAGE_SIZE) * Hkv + kvh) * D;
         float d = 0.0f;
 #pragma unroll
@@ -75,6 +80,7 @@ __global__ void __launch_bounds__(128)
             if (j < B) visit(L + j);
         }
     }
+    if (bad_page && lane == 0) raise_error(err, DEVERR_INVALID);
     const float inv = 1.0f / lrun;
 #pragma unroll
     for (int k = 0; k < DPL; ++k) out[rowid * D + lane + 32 * k] = acc[k] * inv;
@@ -82,14 +88,14 @@ __global__ void __launch_bounds__(128)
 }
 
 cudaError_t tree_attn_f32_launch(const float* q, const float* k_cache, const float* v_cache,
-                                 const int32_t* block_table, int max_pages,
+                                 const int32_t* block_table, int max_pages, int num_pages,
                                  const int32_t* prefix_len, const int32_t* tree_off,
                                  const uint32_t* anc, int nseq, int total_nodes, int Hq, int Hkv,
                                  int D, float scale, float* out, float* lse, uint32_t* err,
                                  cudaStream_t st) {
     dim3 grid(total_nodes, (Hq + 3) / 4);
 #define JT_F32_CASE(DPL_)                                                                      \
-    tree_attn_f32_kernel<DPL_><<<grid, 128, 0, st>>>(q, k_cache, v_cache, block_table, max_pages, \
+    tree_attn_f32_kernel<DPL_><<<grid, 128, 0, st>>>(q, k_cache, v_cache, block_table, max_pages, num_pages, \
                                                      prefix_len, tree_off, anc, nseq, total_nodes, \
                                                      Hq, Hkv, scale, out, lse, err);              \
     return cudaGetLastError();

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(kExpandThreads)
                   const float* __restrict__ part_m, const double* __restrict__ part_s,
                   int splits, const int32_t* __restrict__ tok_in, const double* __restrict__ lp_in,
                   const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
-                  int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
+                  int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
     __shared__ int s_tok[JT_MAX_N * W];
     __shared__ double s_lp[JT_MAX_N * W];
@@ -357,7 +357,8 @@ __global__ void __launch_bounds__(kExpandThreads)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int off = tree_off[b];
     const int B = tree_off[b + 1] - off;
-    if (B < 1 || B > JT_MAX_TREE || B > full_tree_nodes(N, W, JT_MAX_TREE + 1)) {
+    if (B < 1 || B > JT_MAX_TREE || B > full_tree_nodes(N, W, JT_MAX_TREE + 1) || off < 0 ||
+        off + B > total_nodes) {
         if (tid == 0) raise_error(err, DEVERR_INVALID);
         return;
     }
@@ -599,7 +600,7 @@ static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t
 
 template <int W>
 static cudaError_t run_build(const float* z, const int32_t* root_token, const int32_t* tree_off,
-                             int nseq, int N, long long V, int32_t* parent, int32_t* token,
+                             int nseq, int total_nodes, int N, long long V, int32_t* parent, int32_t* token,
                              int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
                              cudaStream_t st) {
     const long long rows = static_cast<long long>(nseq) * N;
@@ -609,18 +610,18 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
         if (e != cudaSuccess) return e;
     }
     expand_kernel<W><<<nseq, kExpandThreads, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, nullptr,
-                                                       nullptr, root_token, tree_off, N, parent,
+                                                       nullptr, root_token, tree_off, total_nodes, N, parent,
                                                        token, depth, anc, err);
     return cudaGetLastError();
 }
 
 template <int W>
 static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
-                              const int32_t* tree_off, int nseq, int N, int32_t* parent,
+                              const int32_t* tree_off, int nseq, int total_nodes, int N, int32_t* parent,
                               int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
                               cudaStream_t st) {
     expand_kernel<W><<<nseq, kExpandThreads, 0, st>>>(nullptr, nullptr, nullptr, nullptr, 0, tok, lp,
-                                                       root_token, tree_off, N, parent, token,
+                                                       root_token, tree_off, total_nodes, N, parent, token,
                                                        depth, anc, err);
     return cudaGetLastError();
 }
@@ -644,18 +645,18 @@ cudaError_t tree_topw_launch(const float* z, long long rows, long long V, int W,
 }
 
 cudaError_t tree_build_launch(const float* z, const int32_t* root_token, const int32_t* tree_off,
-                              int nseq, int N, int W, long long V, int32_t* parent, int32_t* token,
+                              int nseq, int total_nodes, int N, int W, long long V, int32_t* parent, int32_t* token,
                               int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
                               cudaStream_t st) {
-    JT_DISPATCH_W(W, run_build<kW>(z, root_token, tree_off, nseq, N, V, parent, token, depth, anc,
+    JT_DISPATCH_W(W, run_build<kW>(z, root_token, tree_off, nseq, total_nodes, N, V, parent, token, depth, anc,
                                    ws_parts, err, st));
 }
 
 cudaError_t tree_expand_launch(const int32_t* tok, const double* lp, const int32_t* root_token,
-                               const int32_t* tree_off, int nseq, int N, int W, int32_t* parent,
+                               const int32_t* tree_off, int nseq, int total_nodes, int N, int W, int32_t* parent,
                                int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
                                cudaStream_t st) {
-    JT_DISPATCH_W(W, run_expand<kW>(tok, lp, root_token, tree_off, nseq, N, parent, token, depth,
+    JT_DISPATCH_W(W, run_expand<kW>(tok, lp, root_token, tree_off, nseq, total_nodes, N, parent, token, depth,
                                     anc, err, st));
 }
 

@@ -101,7 +101,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kAccThreads)
     accept_kernel(const float* __restrict__ z, const int32_t* __restrict__ parent,
                   const int32_t* __restrict__ token, const int32_t* __restrict__ tree_off,
-                  int nseq, int N, long long V, int rule, double log_t,
+                  int nseq, int total_nodes, int N, long long V, int rule, double log_t,
                   int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
                   int32_t* __restrict__ bonus, AcceptWs w) {
     extern __shared__ int s_prefix[];  // [nseq + 1]
@@ -116,11 +116,13 @@ __global__ void __launch_bounds__(kAccThreads)
     // prologue: root of every sequence is the level-0 frontier
     for (int b = blockIdx.x * kAccThreads + tid; b < nseq; b += gridDim.x * kAccThreads) {
         const int B = tree_off[b + 1] - tree_off[b];
-        const bool ok = (B >= 1 && B <= JT_MAX_TREE);
+        const bool ok = (B >= 1 && B <= JT_MAX_TREE && tree_off[b] >= 0 &&
+                         tree_off[b + 1] <= total_nodes);
         if (!ok) raise_error(&w.hdr->err, DEVERR_INVALID);
         w.state[b] = ok ? 0 : 2;
         w.frontier[(b * 2 + 0) * JT_MAX_TREE] = 0;
         w.fcount[b * 2 + 0] = ok ? 1 : 0;
+        w.fcount[b * 2 + 1] = 0;
         w.final_node[b] = 0;
         if (ok) w.keys[tree_off[b]] = 0ull;
     }
@@ -128,15 +130,16 @@ __global__ void __launch_bounds__(kAccThreads)
 
     for (int lvl = 0; lvl <= N; ++lvl) {
         const int cur = lvl & 1, nxt = cur ^ 1;
-        if (blockIdx.x == 0 && tid == 0) w.hdr->active[nxt] = 0u;
 
         // ---- phase 1: packed max/argmax keys of the frontier rows
         if (warp == 0) {
-            // exclusive prefix of frontier sizes over sequences
+            // exclusive prefix of frontier sizes over the sequences still
+            // walking (finished or invalid ones contribute nothing)
             const int per = (nseq + 31) / 32;
             const int lo = lane * per, hi = min(nseq, lo + per);
             int sum = 0;
-            for (int b = lo; b < hi; ++b) sum += w.fcount[b * 2 + cur];
+            for (int b = lo; b < hi; ++b)
+                sum += (w.state[b] == 0) ? min(w.fcount[b * 2 + cur], JT_MAX_TREE) : 0;
             int incl = sum;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -146,7 +149,7 @@ __global__ void __launch_bounds__(kAccThreads)
             int run = incl - sum;
             for (int b = lo; b < hi; ++b) {
                 s_prefix[b] = run;
-                run += w.fcount[b * 2 + cur];
+                run += (w.state[b] == 0) ? min(w.fcount[b * 2 + cur], JT_MAX_TREE) : 0;
             }
             if (lane == 31) s_prefix[nseq] = incl;
         }
@@ -193,6 +196,9 @@ __global__ void __launch_bounds__(kAccThreads)
             __syncthreads();
         }
         if (!grid_barrier(w.hdr, nblocks)) return;
+        // The counter of the next level was last read before the barrier
+        // just passed and is next incremented after the following one.
+        if (blockIdx.x == 0 && tid == 0) w.hdr->active[nxt] = 0u;
 
         // ---- phase 2: one warp per sequence tests the frontier's children
         for (int b = gwarp; b < nseq; b += nwarps) {
@@ -246,6 +252,7 @@ __global__ void __launch_bounds__(kAccThreads)
                 if (cnt == 0) {
                     w.final_node[b] = fmin;
                     w.state[b] = 1;
+                    w.fcount[b * 2 + nxt] = 0;
                 } else {
                     w.fcount[b * 2 + nxt] = cnt;
                     atomicAdd(&w.hdr->active[cur], 1u);
@@ -304,7 +311,7 @@ cudaError_t verify_accept_launch(const float* z, const int32_t* parent, const in
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int grid = device_sm_count() * (occ < 2 ? occ : 2);
     void* args[] = {(void*)&z,      (void*)&parent, (void*)&token, (void*)&tree_off,
-                    (void*)&nseq,   (void*)&N,      (void*)&V,     (void*)&rule,
+                    (void*)&nseq,   (void*)&total_nodes, (void*)&N, (void*)&V, (void*)&rule,
                     (void*)&log_t,  (void*)&accept_len, (void*)&path, (void*)&bonus,
                     (void*)&w};
     return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kAccThreads), args, smem, st);
