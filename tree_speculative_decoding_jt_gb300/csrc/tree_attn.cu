@@ -91,6 +91,25 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// Visibility of 32 consecutive keys starting at tree-relative position rel0
+// (bit c <-> rel0 + c): negative positions are prefix slots (visible),
+// positions in [0, 256) read the ancestor-or-self set a[], the rest are not
+// visible.
+__device__ __forceinline__ uint32_t visible_bits(const uint32_t (&a)[8], int rel0) {
+    if (rel0 >= JT_MAX_TREE) return 0u;
+    if (rel0 + 32 <= 0) return 0xFFFFFFFFu;
+    const int w0 = rel0 >> 5;  // floor division
+    const int sh = rel0 & 31;
+    uint32_t lo = 0u, hi = 0u;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        if (w == w0) lo = a[w];
+        if (w == w0 + 1) hi = a[w];
+    }
+    if (w0 < 0) lo = 0xFFFFFFFFu;
+    return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
+}
+
 // Tile range [t0, t1) of split sp for a unit whose needed keys end at
 // valid_end; returns the count.
 __device__ __forceinline__ int split_range(int valid_end, int splits, int sp, int& t0) {
@@ -288,13 +307,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!mbar_wait_warp(&bars->s_full[sb], (j >> 1) & 1, p.err, abort)) { ok = false; break; }
             tc_fence_after();
             float s[kTileN];
+            {
+                uint32_t v[kTileN / 32][32];
 #pragma unroll
-            for (int q = 0; q < kTileN / 32; ++q) {
-                uint32_t v[32];
-                tmem_ld32(tS0 + sb * 128 + lane_off + q * 32, v);
+                for (int q = 0; q < kTileN / 32; ++q) tmem_ld32(tS0 + sb * 128 + lane_off + q * 32, v[q]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int c = 0; c < 32; ++c) s[q * 32 + c] = __uint_as_float(v[c]);
+                for (int q = 0; q < kTileN / 32; ++q)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) s[q * 32 + c] = __uint_as_float(v[q][c]);
             }
             tc_fence_before();
             mbar_arrive(&bars->s_free[sb]);
@@ -302,22 +323,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int slot0 = (t0 + j) * kTileN;
             if (slot0 + kTileN > L) {  // tile reaches the tree tail: ancestor mask
 #pragma unroll
-                for (int c = 0; c < kTileN; ++c) {
-                    const int rel = slot0 + c - L;
-                    bool vis = rel < 0;
-                    if (rel >= 0 && rel < JT_MAX_TREE) {
-                        uint32_t word = 0;
+                for (int q = 0; q < kTileN / 32; ++q) {
+                    const uint32_t vis = visible_bits(a, slot0 + q * 32 - L);
 #pragma unroll
-                        for (int w = 0; w < 8; ++w)
-                            if (w == (rel >> 5)) word = a[w];
-                        vis = (word >> (rel & 31)) & 1u;
-                    }
-                    if (!vis) s[c] = -INFINITY;
+                    for (int c = 0; c < 32; ++c)
+                        if (!((vis >> c) & 1u)) s[q * 32 + c] = -INFINITY;
                 }
             }
-            float mx = -INFINITY;
+            float mx;
+            {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int c = 0; c < kTileN; ++c) mx = fmaxf(mx, s[c]);
+                for (int c = 0; c < kTileN; c += 4) {
+                    m4[0] = fmaxf(m4[0], s[c]);
+                    m4[1] = fmaxf(m4[1], s[c + 1]);
+                    m4[2] = fmaxf(m4[2], s[c + 2]);
+                    m4[3] = fmaxf(m4[3], s[c + 3]);
+                }
+                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            }
             const float mx_s = mx * sl2;
             bool resc = false;
             float factor = 1.0f;
@@ -357,6 +381,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 break;
             }
             const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+            float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 uint32_t pr[32];
@@ -364,11 +389,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int c2 = 0; c2 < 32; ++c2) {
                     const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * c2], sl2, -m_use));
                     const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * c2 + 1], sl2, -m_use));
-                    l_run += p0 + p1;
+                    l4[c2 & 3] += p0 + p1;
                     pr[c2] = pack_bf16x2(p0, p1);
                 }
                 tmem_st32(tP0 + sb * 64 + lane_off + h * 32, pr);
             }
+            l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars->p_full[sb]);

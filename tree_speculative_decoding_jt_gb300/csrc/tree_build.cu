@@ -309,13 +309,37 @@ __global__ void __launch_bounds__(256)
 
 // ---------------------------------------------------------------------------
 // Step 2: best-first expansion, one CTA per sequence.
+//
+// The nodes best-first pops, in pop order, are exactly the B-1 best non-root
+// nodes of the full depth-N tree under the queue key, in key order: a child
+// never beats its parent (log-probs are <= 0, and depth breaks exact ties in
+// the parent's favour) and a later sibling never beats an earlier one.  So
+// instead of B-1 dependent pops the CTA builds that set level by level:
+// S holds the best candidates seen so far, sorted by key and cut to B-1; at
+// level d the children (depth d+1) of S's depth-d nodes are generated, a
+// child that is not better than S's current (B-1)-th entry is dropped (it
+// has B-1 better nodes, and so has every descendant), and S is re-sorted
+// (block bitonic sort) and cut again.  After the last level S is the pop
+// sequence.  Scores are the same fp64 root-to-node sums as the reference
+// definition, so the integer outputs are identical.
 // ---------------------------------------------------------------------------
-// Secondary key: larger = earlier.  depth asc, token asc, parent asc.
-__device__ __forceinline__ unsigned long long make_k2(int depth, int token, int parent) {
+constexpr int kExpCap = 2048;  // candidates held at once (set + new children)
+
+// Tie key (larger = earlier): depth asc, token asc, parent position asc;
+// bits 0..11 carry the candidate's own slot and never decide an order
+// (no two candidates agree on all the bits above them).
+__device__ __forceinline__ unsigned long long make_k2(int depth, int token, int parent_pos,
+                                                      int slot) {
     return (static_cast<unsigned long long>(255 - depth) << 56) |
            (static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(token)) << 24) |
-           static_cast<unsigned long long>(0xFFFFFFu - static_cast<uint32_t>(parent));
+           (static_cast<unsigned long long>(0xFFF - (parent_pos + 1)) << 12) |
+           static_cast<unsigned long long>(slot);
 }
+__device__ __forceinline__ int k2_depth(unsigned long long k2) { return 255 - static_cast<int>(k2 >> 56); }
+__device__ __forceinline__ int k2_token(unsigned long long k2) {
+    return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>((k2 >> 24) & 0xFFFFFFFFull));
+}
+__device__ __forceinline__ int k2_slot(unsigned long long k2) { return static_cast<int>(k2 & 0xFFF); }
 
 __device__ __forceinline__ double double_from_order_key(unsigned long long k) {
     const unsigned long long u = (k & 0x8000000000000000ull) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
@@ -337,6 +361,59 @@ __host__ __device__ inline int full_tree_nodes(int N, int W, int cap) {
     return static_cast<int>(total);
 }
 
+// Inclusive prefix sum over the CTA (kExpandThreads threads).
+__device__ __forceinline__ int block_incl_scan(int v, int* s_warp) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, v, o);
+        if (lane >= o) v += t;
+    }
+    if (lane == 31) s_warp[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < kExpandThreads / 32) ? s_warp[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += t;
+        }
+        if (lane < kExpandThreads / 32) s_warp[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) v += s_warp[warp - 1];
+    __syncthreads();
+    return v;
+}
+
+// Sort k1/k2[0, n) descending by (k1, k2); entries [n, P) are padding.
+__device__ void block_bitonic_desc(unsigned long long* k1, unsigned long long* k2, int n) {
+    int P = 1;
+    while (P < n) P <<= 1;
+    for (int i = n + threadIdx.x; i < P; i += kExpandThreads) {
+        k1[i] = 0ull;
+        k2[i] = 0ull;
+    }
+    __syncthreads();
+    for (int size = 2; size <= P; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            for (int q = threadIdx.x; q < (P >> 1); q += kExpandThreads) {
+                const int i = 2 * stride * (q / stride) + (q % stride);
+                const int j = i + stride;
+                const bool desc = (i & size) == 0;
+                const unsigned long long a1 = k1[i], a2 = k2[i], b1 = k1[j], b2 = k2[j];
+                if (key_better(a1, a2, b1, b2) != desc) {
+                    k1[i] = b1;
+                    k2[i] = b2;
+                    k1[j] = a1;
+                    k2[j] = a2;
+                }
+            }
+            __syncthreads();
+        }
+    }
+}
+
 template <int W>
 __global__ void __launch_bounds__(kExpandThreads)
     expand_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id,
@@ -345,13 +422,16 @@ __global__ void __launch_bounds__(kExpandThreads)
                   const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
                   int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
+    extern __shared__ __align__(16) unsigned char dsm[];
+    unsigned long long* k1 = reinterpret_cast<unsigned long long*>(dsm);  // [kExpCap]
+    unsigned long long* k2 = k1 + kExpCap;                                // [kExpCap]
+    short* par = reinterpret_cast<short*>(k2 + kExpCap);                  // [2][kExpCap]
+    short* inv = par + 2 * kExpCap;                                       // [kExpCap]
+    short* front = inv + kExpCap;                                         // [kExpCap]
     __shared__ int s_tok[JT_MAX_N * W];
     __shared__ double s_lp[JT_MAX_N * W];
-    __shared__ int s_par[JT_MAX_TREE];
-    __shared__ int s_tokn[JT_MAX_TREE];
-    __shared__ int s_dep[JT_MAX_TREE];
-    __shared__ double s_score[JT_MAX_TREE];
-    __shared__ int s_count;
+    __shared__ int s_warp[kExpandThreads / 32];
+    __shared__ int s_nf, s_total, s_take;
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -383,147 +463,133 @@ __global__ void __launch_bounds__(kExpandThreads)
                 }
         }
     }
-    if (tid == 0) {
-        s_par[0] = -1;
-        s_tokn[0] = root_token[b];
-        s_dep[0] = 0;
-        s_score[0] = 0.0;
-        s_count = 1;
-    }
     __syncthreads();
 
-    if (warp == 0 && B > 1) {
-        // frontier: slot s lives in lane s&31, register position s>>5
-        unsigned long long k1[8], k2[8];
-        int kr[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            k1[i] = 0ull;
-            k2[i] = 0ull;
-            kr[i] = 0;
+    const int K = B - 1;  // non-root nodes
+    int m = 0;            // size of the sorted set S
+    int cb = 0;           // current parent buffer
+    for (int d = 0; d < N && K > 0; ++d) {
+        // frontier: the root at d == 0, else S's depth-d entries (positions)
+        if (d == 0) {
+            if (tid == 0) {
+                front[0] = -1;
+                s_nf = 1;
+            }
+        } else {
+            int nf = 0;
+            for (int p0 = 0; p0 < m; p0 += kExpandThreads) {
+                const int p = p0 + tid;
+                const int is_f = (p < m && k2_depth(k2[p]) == d) ? 1 : 0;
+                const int incl = block_incl_scan(is_f, s_warp);
+                if (is_f) front[nf + incl - 1] = static_cast<short>(p);
+                nf += s_warp[kExpandThreads / 32 - 1];
+                __syncthreads();
+            }
+            if (tid == 0) s_nf = nf;
         }
-        int nslots = 1;
-        if (lane == 0) {  // first child of the root
-            k1[0] = double_order_key(__dadd_rn(0.0, s_lp[0]));
-            k2[0] = make_k2(1, s_tok[0], 0);
-            kr[0] = 0;
-        }
-        int lb = (lane == 0) ? 0 : -1;  // lane-local best slot
-        unsigned long long b1 = (lane == 0) ? k1[0] : 0ull, b2 = (lane == 0) ? k2[0] : 0ull;
-
-        for (int count = 1; count < B; ++count) {
-            // warp arg-max of (b1, b2) with REDUX on 32-bit pieces
-            const bool valid = lb >= 0;
-            uint32_t piece = valid ? static_cast<uint32_t>(b1 >> 32) : 0u;
-            uint32_t mx = __reduce_max_sync(kFull, piece);
-            unsigned cand = __ballot_sync(kFull, valid && piece == mx);
-            if (__popc(cand) > 1) {
-                piece = ((cand >> lane) & 1u) ? static_cast<uint32_t>(b1) : 0u;
-                mx = __reduce_max_sync(kFull, piece);
-                cand &= __ballot_sync(kFull, piece == mx);
-            }
-            if (__popc(cand) > 1) {
-                piece = ((cand >> lane) & 1u) ? static_cast<uint32_t>(b2 >> 32) : 0u;
-                mx = __reduce_max_sync(kFull, piece);
-                cand &= __ballot_sync(kFull, piece == mx);
-            }
-            if (__popc(cand) > 1) {
-                piece = ((cand >> lane) & 1u) ? static_cast<uint32_t>(b2) : 0u;
-                mx = __reduce_max_sync(kFull, piece);
-                cand &= __ballot_sync(kFull, piece == mx);
-            }
-            if (cand == 0u) break;  // frontier empty: cannot happen for B <= full tree
-            const int wl = __ffs(cand) - 1;
-            int wkr = 0;
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i == lb) wkr = kr[i];
-            const unsigned long long w1 = __shfl_sync(kFull, b1, wl);
-            const unsigned long long w2 = __shfl_sync(kFull, b2, wl);
-            wkr = __shfl_sync(kFull, wkr, wl);
-            const double wscore = double_from_order_key(w1);
-            const int wdepth = 255 - static_cast<int>(w2 >> 56);
-            const int wtoken = static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>((w2 >> 24) & 0xFFFFFFFFull));
-            const int wpar = static_cast<int>(0xFFFFFFu - static_cast<uint32_t>(w2 & 0xFFFFFFull));
-            const int n = count;
-            if (lane == 0) {
-                s_par[n] = wpar;
-                s_tokn[n] = wtoken;
-                s_dep[n] = wdepth;
-                s_score[n] = wscore;
-                s_count = n + 1;
-            }
-            __syncwarp();
-            // popped slot -> next sibling (rank wkr+1) or empty
-            if (lane == wl) {
-                unsigned long long n1 = 0ull, n2 = 0ull;
-                if (wkr + 1 < W) {
-                    const int r = (wdepth - 1) * W + wkr + 1;
-                    n1 = double_order_key(__dadd_rn(s_score[wpar], s_lp[r]));
-                    n2 = make_k2(wdepth, s_tok[r], wpar);
-                }
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (i == lb) {
-                        k1[i] = n1;
-                        k2[i] = n2;
-                        kr[i] = wkr + 1;
+        __syncthreads();
+        const int nf = s_nf;
+        if (nf == 0) break;
+        for (int fi = 0; fi < nf;) {
+            // threshold: S's (B-1)-th entry once S is full; accept all before
+            const bool full = (m >= K);
+            const unsigned long long t1 = full ? k1[K - 1] : 0ull, t2 = full ? k2[K - 1] : 0ull;
+            const int e = fi + tid;
+            int pos = -2, c = 0;
+            double su = 0.0;
+            if (e < nf) {
+                pos = front[e];
+                if (pos >= -1) {
+                    su = (pos < 0) ? 0.0 : double_from_order_key(k1[pos]);
+                    for (int k = 0; k < W; ++k) {
+                        const unsigned long long c1 = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
+                        const unsigned long long c2 = make_k2(d + 1, s_tok[d * W + k], pos, 0);
+                        if (full && !key_better(c1, c2, t1, t2)) break;
+                        ++c;
                     }
-            }
-            // best child of the new node -> new slot
-            if (wdepth < N) {
-                const int s = nslots++;
-                if (lane == (s & 31)) {
-                    const int pos = s >> 5;
-                    const unsigned long long n1 = double_order_key(__dadd_rn(wscore, s_lp[wdepth * W]));
-                    const unsigned long long n2 = make_k2(wdepth + 1, s_tok[wdepth * W], n);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        if (i == pos) {
-                            k1[i] = n1;
-                            k2[i] = n2;
-                            kr[i] = 0;
-                        }
                 }
             }
-            // lanes whose slots changed rescan their best
-            if (lane == wl || (wdepth < N && lane == ((nslots - 1) & 31))) {
-                lb = -1;
-                b1 = 0ull;
-                b2 = 0ull;
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    if (k1[i] != 0ull && (lb < 0 || key_better(k1[i], k2[i], b1, b2))) {
-                        lb = i;
-                        b1 = k1[i];
-                        b2 = k2[i];
-                    }
+            const int room = kExpCap - m;
+            const int incl = block_incl_scan(c, s_warp);
+            const int take = __syncthreads_count(e < nf && incl <= room);
+            if (tid == take - 1) s_total = incl;
+            if (tid == 0) s_take = take;
+            __syncthreads();
+            const int ntake = s_take, total = s_total;
+            if (tid < ntake) {  // write the children of the accepted entries
+                const int o0 = m + incl - c;
+                for (int k = 0; k < c; ++k) {
+                    const int slot = o0 + k;
+                    k1[slot] = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
+                    k2[slot] = make_k2(d + 1, s_tok[d * W + k], pos, slot);
+                    par[cb * kExpCap + slot] = static_cast<short>(pos);
+                }
+            }
+            __syncthreads();
+            fi += ntake;
+            const int mall = m + total;
+            if (total > 0) {
+                block_bitonic_desc(k1, k2, mall);
+                const int mnew = min(K, mall);
+                for (int p = tid; p < mall; p += kExpandThreads) inv[p] = -2;
+                __syncthreads();
+                for (int p = tid; p < mnew; p += kExpandThreads) inv[k2_slot(k2[p])] = static_cast<short>(p);
+                __syncthreads();
+                for (int p = tid; p < mnew; p += kExpandThreads) {
+                    const int old = k2_slot(k2[p]);
+                    const int pp = par[cb * kExpCap + old];
+                    const int np = (pp < 0) ? pp : inv[pp];
+                    par[(cb ^ 1) * kExpCap + p] = static_cast<short>(np);
+                    k2[p] = (k2[p] & ~0xFFFFFFull) |
+                            (static_cast<unsigned long long>(0xFFF - (np + 1)) << 12) |
+                            static_cast<unsigned long long>(p);
+                }
+                for (int q = fi + tid; q < nf; q += kExpandThreads) {
+                    const int f = front[q];
+                    front[q] = static_cast<short>((f >= 0) ? inv[f] : f);
+                }
+                __syncthreads();
+                cb ^= 1;
+                m = mnew;
             }
         }
     }
-    __syncthreads();
-
-    // outputs and ancestor-or-self sets
-    if (s_count != B) {  // the expansion stopped early: report, write nothing
+    if (m != K) {  // cannot happen when B fits the full tree
         if (tid == 0) raise_error(err, DEVERR_INVALID);
         return;
     }
+
+    // outputs: node 0 = root, node p+1 = S[p]; ancestor-or-self sets
     for (int n = tid; n < B; n += kExpandThreads) {
+        int pn, tn, dn;
+        if (n == 0) {
+            pn = -1;
+            tn = root_token[b];
+            dn = 0;
+        } else {
+            pn = par[cb * kExpCap + n - 1] + 1;
+            tn = k2_token(k2[n - 1]);
+            dn = k2_depth(k2[n - 1]);
+        }
         uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        for (int u = n; u >= 0; u = s_par[u]) {
+        int u = n;
+        for (int steps = 0; u >= 0 && steps <= JT_MAX_N; ++steps) {
 #pragma unroll
             for (int w = 0; w < 8; ++w)
                 if (w == (u >> 5)) a[w] |= 1u << (u & 31);
+            u = (u == 0) ? -1 : par[cb * kExpCap + u - 1] + 1;
         }
         const long long g = off + n;
-        parent[g] = s_par[n];
-        token[g] = s_tokn[n];
-        depth[g] = s_dep[n];
+        parent[g] = pn;
+        token[g] = tn;
+        depth[g] = dn;
         uint4* ap = reinterpret_cast<uint4*>(anc + g * 8);
         ap[0] = make_uint4(a[0], a[1], a[2], a[3]);
         ap[1] = make_uint4(a[4], a[5], a[6], a[7]);
     }
 }
+
+constexpr size_t kExpandSmem = sizeof(unsigned long long) * 2 * kExpCap + sizeof(short) * 5 * kExpCap;
 
 // ---------------------------------------------------------------------------
 // Host launchers
@@ -532,6 +598,12 @@ static ExpTable make_exp_table() {
     ExpTable t;
     ffexp_table(t.hi, t.lo);
     return t;
+}
+
+template <int W>
+static cudaError_t set_expand_smem() {
+    return cudaFuncSetAttribute(expand_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kExpandSmem));
 }
 
 static int topw_splits(long long V) {
@@ -609,7 +681,9 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
         cudaError_t e = launch_topw_partial<W>(z, rows, V, t, st);
         if (e != cudaSuccess) return e;
     }
-    expand_kernel<W><<<nseq, kExpandThreads, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, nullptr,
+    cudaError_t ea = set_expand_smem<W>();
+    if (ea != cudaSuccess) return ea;
+    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(t.v, t.id, t.m, t.s, t.splits, nullptr,
                                                        nullptr, root_token, tree_off, total_nodes, N, parent,
                                                        token, depth, anc, err);
     return cudaGetLastError();
@@ -620,7 +694,9 @@ static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_
                               const int32_t* tree_off, int nseq, int total_nodes, int N, int32_t* parent,
                               int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
                               cudaStream_t st) {
-    expand_kernel<W><<<nseq, kExpandThreads, 0, st>>>(nullptr, nullptr, nullptr, nullptr, 0, tok, lp,
+    cudaError_t ea = set_expand_smem<W>();
+    if (ea != cudaSuccess) return ea;
+    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(nullptr, nullptr, nullptr, nullptr, 0, tok, lp,
                                                        root_token, tree_off, total_nodes, N, parent, token,
                                                        depth, anc, err);
     return cudaGetLastError();

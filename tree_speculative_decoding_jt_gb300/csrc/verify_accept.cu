@@ -309,7 +309,12 @@ cudaError_t verify_accept_launch(const float* z, const int32_t* parent, const in
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kAccThreads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
-    const int grid = device_sm_count() * (occ < 2 ? occ : 2);
+    // one CTA per 4096-entry chunk of one row per sequence (the greedy
+    // frontier), at least 16, at most what is co-resident: fewer CTAs make
+    // the grid barriers cheaper
+    const long long chunks = static_cast<long long>(nseq) * ((V + kAccChunk - 1) / kAccChunk);
+    const long long cap = static_cast<long long>(device_sm_count()) * (occ < 2 ? occ : 2);
+    const int grid = static_cast<int>(chunks < 16 ? (cap < 16 ? cap : 16) : (chunks < cap ? chunks : cap));
     void* args[] = {(void*)&z,      (void*)&parent, (void*)&token, (void*)&tree_off,
                     (void*)&nseq,   (void*)&total_nodes, (void*)&N, (void*)&V, (void*)&rule,
                     (void*)&log_t,  (void*)&accept_len, (void*)&path, (void*)&bonus,
