@@ -38,7 +38,8 @@
 namespace jt {
 
 constexpr int kAttnThreads = 192;
-constexpr int kStages = 2;
+constexpr int kStages = 3;   // K ring and V ring depth
+constexpr int kPrefetch = 4; // tiles ahead whose pages are prefetched into L2
 constexpr int kTileN = 128;  // keys per KV tile
 constexpr int kTileM = 128;  // query rows per tile
 constexpr float kRescaleLog2 = 8.0f;
@@ -74,7 +75,8 @@ struct Bars {
     uint64_t q_full;
     uint64_t k_full[kStages];
     uint64_t v_full[kStages];
-    uint64_t kv_empty[kStages];
+    uint64_t k_empty[kStages];
+    uint64_t v_empty[kStages];
     uint64_t s_full[2];
     uint64_t s_free[2];
     uint64_t p_full[2];
@@ -154,7 +156,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->v_full[s], 1);
-            mbar_init(&bars->kv_empty[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->s_full[s], 1);
@@ -194,9 +197,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         int issued = 0;
         for (int j = 0; j < nt; ++j) {
             const int st = j % kStages;
-            if (j >= kStages &&
-                !mbar_wait_warp(&bars->kv_empty[st], ((j / kStages) & 1) ^ 1, p.err, abort))
-                break;
+            const uint32_t empty_parity = ((j / kStages) & 1) ^ 1;
             const int slot0 = (t0 + j) * kTileN;
             const int nvalid = min(kTileN, valid_end - slot0);
             const int npg = (nvalid + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
@@ -204,20 +205,37 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                 ? p.block_table[static_cast<long long>(b) * p.max_pages +
                                                 slot0 / JT_PAGE_SIZE + lane]
                                 : 0;
-            if (lane == 0) {
-                const uint32_t bytes = npg * SL::kChunks * (JT_PAGE_SIZE * 128);
-                mbar_arrive_expect_tx(&bars->k_full[st], bytes);
-                mbar_arrive_expect_tx(&bars->v_full[st], bytes);
-            }
+            const uint32_t bytes = npg * SL::kChunks * (JT_PAGE_SIZE * 128);
+            // K of tile j: its slot is free once QK^T of tile j-kStages is done
+            if (j >= kStages && !mbar_wait_warp(&bars->k_empty[st], empty_parity, p.err, abort)) break;
+            if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], bytes);
             __syncwarp();
-            if (lane < npg) {
-                for (int c = 0; c < SL::kChunks; ++c) {
-                    const int dst = st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128);
-                    tma_load_4d(sK + dst, &tm_k, &bars->k_full[st], c * 64, g, 0, pid);
-                    tma_load_4d(sV + dst, &tm_v, &bars->v_full[st], c * 64, g, 0, pid);
+            if (lane < npg)
+                for (int c = 0; c < SL::kChunks; ++c)
+                    tma_load_4d(sK + st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128),
+                                &tm_k, &bars->k_full[st], c * 64, g, 0, pid);
+            // V of tile j: free once PV of tile j-kStages is done
+            if (j >= kStages && !mbar_wait_warp(&bars->v_empty[st], empty_parity, p.err, abort)) break;
+            if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+            __syncwarp();
+            if (lane < npg)
+                for (int c = 0; c < SL::kChunks; ++c)
+                    tma_load_4d(sV + st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128),
+                                &tm_v, &bars->v_full[st], c * 64, g, 0, pid);
+            issued = j + 1;
+            // pull the pages of a tile further ahead from HBM into L2
+            if (j + kPrefetch < nt) {
+                const int ps0 = (t0 + j + kPrefetch) * kTileN;
+                const int pn = (min(kTileN, valid_end - ps0) + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
+                if (lane < pn) {
+                    const int ppid = p.block_table[static_cast<long long>(b) * p.max_pages +
+                                                   ps0 / JT_PAGE_SIZE + lane];
+                    for (int c = 0; c < SL::kChunks; ++c) {
+                        tma_prefetch_l2_4d(&tm_k, c * 64, g, 0, ppid);
+                        tma_prefetch_l2_4d(&tm_v, c * 64, g, 0, ppid);
+                    }
                 }
             }
-            issued = j + 1;
             if (j == nt - 1) {
                 // final tile: once its V has landed, zero rows past the last
                 // needed slot (stale or foreign data; P is 0 there but
@@ -262,7 +280,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                            SL::kChunkBytes, 1024);
                     mma_ts(tO, tP0 + pb * 64 + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(&bars->kv_empty[st]);
+                mma_commit(&bars->v_empty[st]);
                 mma_commit(&bars->pv_done[pb]);
                 return true;
             };
@@ -281,6 +299,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     mma_ss(tS0 + sb * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
                 }
                 mma_commit(&bars->s_full[sb]);
+                mma_commit(&bars->k_empty[st]);
                 if (j >= 1) ok = issue_pv(j - 1);
             }
             if (ok) issue_pv(nt - 1);
