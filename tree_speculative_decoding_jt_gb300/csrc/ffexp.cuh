@@ -137,4 +137,27 @@ JT_HD void two_sum(float a, float b, float& s, float& e) {
     e = jt_add(jt_add(a, -jt_add(s, -bb)), jt_add(b, -bb));
 }
 
+// Float-float (unevaluated sum hi + lo) arithmetic from error-free
+// transforms (Dekker / Knuth): |lo| <= ulp(hi)/2 after normalisation.
+JT_HD ffloat ff_norm(float a, float b) {  // requires |a| >= |b| or a == 0
+    ffloat r;
+    r.hi = jt_add(a, b);
+    r.lo = jt_add(b, -jt_add(r.hi, -a));
+    return r;
+}
+
+JT_HD ffloat ff_add(ffloat a, ffloat b) {
+    float s, e;
+    two_sum(a.hi, b.hi, s, e);
+    e = jt_add(e, jt_add(a.lo, b.lo));
+    return ff_norm(s, e);
+}
+
+JT_HD ffloat ff_mul(ffloat a, ffloat b) {
+    const float p = jt_mul(a.hi, b.hi);
+    float e = jt_fmaf(a.hi, b.hi, -p);
+    e = jt_fmaf(a.hi, b.lo, jt_fmaf(a.lo, b.hi, e));
+    return ff_norm(p, e);
+}
+
 }  // namespace jt

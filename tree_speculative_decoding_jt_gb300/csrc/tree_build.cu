@@ -115,6 +115,16 @@ __device__ __forceinline__ double warp_sum_d(double x) {
     for (int off = 16; off >= 1; off >>= 1) x += __shfl_xor_sync(kFull, x, off);
     return x;
 }
+__device__ __forceinline__ ffloat warp_sum_ff(ffloat x) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        ffloat o;
+        o.hi = __shfl_xor_sync(kFull, x.hi, off);
+        o.lo = __shfl_xor_sync(kFull, x.lo, off);
+        x = ff_add(x, o);
+    }
+    return x;
+}
 __device__ __forceinline__ float warp_max_f(float x) {
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) x = fmaxf(x, __shfl_xor_sync(kFull, x, off));
@@ -129,13 +139,13 @@ template <int W, bool VEC>
 __global__ void __launch_bounds__(kTopwThreads)
     topw_partial_kernel(const float* __restrict__ z, long long V, int splits, ExpTable tab,
                         float* __restrict__ part_v, int* __restrict__ part_id,
-                        float* __restrict__ part_m, double* __restrict__ part_s) {
+                        float* __restrict__ part_m, float2* __restrict__ part_s) {
     constexpr int CH = kTopwThreads * kTopwPerThread;
     __shared__ float s_thi[64], s_tlo[64];
     __shared__ float s_wv[kTopwThreads / 32][W];
     __shared__ int s_wi[kTopwThreads / 32][W];
     __shared__ float s_wmax[kTopwThreads / 32];
-    __shared__ double s_wsum[kTopwThreads / 32];
+    __shared__ float2 s_wsum[kTopwThreads / 32];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long row = blockIdx.y;
@@ -191,7 +201,7 @@ __global__ void __launch_bounds__(kTopwThreads)
     m = warp_max_f(m);
 
     // sum of exp(z - m): exact difference as a float pair, table-driven exp,
-    // float-float accumulation, fp64 across threads
+    // float-float accumulation within and across threads
     float acc_hi = 0.0f, acc_lo = 0.0f;
     if (m != -INFINITY) {
 #pragma unroll
@@ -205,8 +215,8 @@ __global__ void __launch_bounds__(kTopwThreads)
             acc_lo = jt_add(acc_lo, jt_add(e, y.lo));
         }
     }
-    double S = warp_sum_d(static_cast<double>(acc_hi) + static_cast<double>(acc_lo));
-    if (lane == 0) s_wsum[warp] = S;
+    ffloat S = warp_sum_ff(ff_norm(acc_hi, acc_lo));
+    if (lane == 0) s_wsum[warp] = make_float2(S.hi, S.lo);
 
     // top-W across the CTA
     float rv[W];
@@ -231,8 +241,12 @@ __global__ void __launch_bounds__(kTopwThreads)
             }
         }
         warp_merge<W>(M, rv, rid);
-        S = (lane < kTopwThreads / 32) ? s_wsum[lane] : 0.0;
-        S = warp_sum_d(S);
+        S.hi = S.lo = 0.0f;
+        if (lane < kTopwThreads / 32) {
+            S.hi = s_wsum[lane].x;
+            S.lo = s_wsum[lane].y;
+        }
+        S = warp_sum_ff(S);
         const long long p = row * splits + sp;
         if (lane == 0) {
 #pragma unroll
@@ -241,31 +255,53 @@ __global__ void __launch_bounds__(kTopwThreads)
                 part_id[p * W + k] = rid[k];
             }
             part_m[p] = m;
-            part_s[p] = S;
+            part_s[p] = make_float2(S.hi, S.lo);
         }
     }
 }
 
 // Merge the partials of one row (whole warp): top-W ids/values and lse.
+// lse = M + log(sum_j S_j exp(m_j - M)) in float-float: the chunk sums are
+// rescaled with the table-driven exp, and log is one fp32 logf refined by a
+// Newton step (y = y0 + e - e^2/2 with 1 + e = S exp(-y0)), accurate to
+// ~1e-11; only the final assembly and lp = z - lse are fp64.
 template <int W>
 __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
                                           const int* __restrict__ part_id,
                                           const float* __restrict__ part_m,
-                                          const double* __restrict__ part_s, int splits,
-                                          long long row, int lane, int (&tok)[W],
-                                          double (&lp)[W], double& lse) {
+                                          const float2* __restrict__ part_s, int splits,
+                                          long long row, int lane, const float* tab_hi,
+                                          const float* tab_lo, int (&tok)[W], double (&lp)[W],
+                                          double& lse) {
     const long long base = row * splits;
     float M = -INFINITY;
     for (int s = lane; s < splits; s += 32) M = fmaxf(M, part_m[base + s]);
     M = warp_max_f(M);
-    double S = 0.0;
+    ffloat S;
+    S.hi = S.lo = 0.0f;
     if (M != -INFINITY)
         for (int s = lane; s < splits; s += 32) {
             const float ms = part_m[base + s];
-            if (ms != -INFINITY) S += part_s[base + s] * exp(static_cast<double>(ms) - M);
+            if (ms != -INFINITY) {
+                float dh, dl;
+                two_sum(ms, -M, dh, dl);
+                const float2 ps = part_s[base + s];
+                ffloat Sj;
+                Sj.hi = ps.x;
+                Sj.lo = ps.y;
+                S = ff_add(S, ff_mul(Sj, ffexp(dh, dl, tab_hi, tab_lo)));
+            }
         }
-    S = warp_sum_d(S);
-    lse = (M == -INFINITY) ? -INFINITY : static_cast<double>(M) + log(S);
+    S = warp_sum_ff(S);
+    if (M == -INFINITY) {
+        lse = -INFINITY;
+    } else {
+        const float y0 = logf(S.hi);
+        const ffloat t = ff_mul(S, ffexp(-y0, 0.0f, tab_hi, tab_lo));
+        float e = jt_add(jt_add(t.hi, -1.0f), t.lo);
+        e = jt_add(e, -0.5f * e * e);
+        lse = static_cast<double>(M) + (static_cast<double>(y0) + static_cast<double>(e));
+    }
 
     TopList<W> L;
     L.init();
@@ -288,15 +324,21 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
 template <int W>
 __global__ void __launch_bounds__(256)
     topw_merge_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id,
-                      const float* __restrict__ part_m, const double* __restrict__ part_s,
-                      int splits, long long rows, int32_t* __restrict__ tok_out,
+                      const float* __restrict__ part_m, const float2* __restrict__ part_s,
+                      int splits, long long rows, ExpTable tab, int32_t* __restrict__ tok_out,
                       double* __restrict__ lp_out, double* __restrict__ lse_out) {
+    __shared__ float s_thi[64], s_tlo[64];
+    if (threadIdx.x < 64) {
+        s_thi[threadIdx.x] = tab.hi[threadIdx.x];
+        s_tlo[threadIdx.x] = tab.lo[threadIdx.x];
+    }
+    __syncthreads();
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     int tok[W];
     double lp[W], lse;
-    merge_row<W>(part_v, part_id, part_m, part_s, splits, row, lane, tok, lp, lse);
+    merge_row<W>(part_v, part_id, part_m, part_s, splits, row, lane, s_thi, s_tlo, tok, lp, lse);
     if (lane == 0) {
 #pragma unroll
         for (int k = 0; k < W; ++k) {
@@ -417,8 +459,9 @@ __device__ void block_bitonic_desc(unsigned long long* k1, unsigned long long* k
 template <int W>
 __global__ void __launch_bounds__(kExpandThreads)
     expand_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id,
-                  const float* __restrict__ part_m, const double* __restrict__ part_s,
-                  int splits, const int32_t* __restrict__ tok_in, const double* __restrict__ lp_in,
+                  const float* __restrict__ part_m, const float2* __restrict__ part_s,
+                  int splits, ExpTable tab, const int32_t* __restrict__ tok_in,
+                  const double* __restrict__ lp_in,
                   const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
                   int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
@@ -443,6 +486,12 @@ __global__ void __launch_bounds__(kExpandThreads)
         return;
     }
 
+    __shared__ float s_thi[64], s_tlo[64];
+    if (tid < 64) {
+        s_thi[tid] = tab.hi[tid];
+        s_tlo[tid] = tab.lo[tid];
+    }
+    __syncthreads();
     // per-depth tables for this sequence
     if (tok_in) {
         for (int i = tid; i < N * W; i += kExpandThreads) {
@@ -454,7 +503,7 @@ __global__ void __launch_bounds__(kExpandThreads)
             int tk[W];
             double lq[W], lse;
             merge_row<W>(part_v, part_id, part_m, part_s, splits, static_cast<long long>(b) * N + d,
-                         lane, tk, lq, lse);
+                         lane, s_thi, s_tlo, tk, lq, lse);
             if (lane == 0)
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
@@ -496,16 +545,17 @@ __global__ void __launch_bounds__(kExpandThreads)
             const unsigned long long t1 = full ? k1[K - 1] : 0ull, t2 = full ? k2[K - 1] : 0ull;
             const int e = fi + tid;
             int pos = -2, c = 0;
-            double su = 0.0;
+            unsigned long long ck[W];  // children's score keys, computed once
             if (e < nf) {
                 pos = front[e];
                 if (pos >= -1) {
-                    su = (pos < 0) ? 0.0 : double_from_order_key(k1[pos]);
+                    const double su = (pos < 0) ? 0.0 : double_from_order_key(k1[pos]);
+#pragma unroll
+                    for (int k = 0; k < W; ++k) ck[k] = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
+#pragma unroll
                     for (int k = 0; k < W; ++k) {
-                        const unsigned long long c1 = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
-                        const unsigned long long c2 = make_k2(d + 1, s_tok[d * W + k], pos, 0);
-                        if (full && !key_better(c1, c2, t1, t2)) break;
-                        ++c;
+                        if (c == k && (!full || key_better(ck[k], make_k2(d + 1, s_tok[d * W + k], pos, 0), t1, t2)))
+                            ++c;
                     }
                 }
             }
@@ -518,11 +568,14 @@ __global__ void __launch_bounds__(kExpandThreads)
             const int ntake = s_take, total = s_total;
             if (tid < ntake) {  // write the children of the accepted entries
                 const int o0 = m + incl - c;
-                for (int k = 0; k < c; ++k) {
-                    const int slot = o0 + k;
-                    k1[slot] = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
-                    k2[slot] = make_k2(d + 1, s_tok[d * W + k], pos, slot);
-                    par[cb * kExpCap + slot] = static_cast<short>(pos);
+#pragma unroll
+                for (int k = 0; k < W; ++k) {
+                    if (k < c) {
+                        const int slot = o0 + k;
+                        k1[slot] = ck[k];
+                        k2[slot] = make_k2(d + 1, s_tok[d * W + k], pos, slot);
+                        par[cb * kExpCap + slot] = static_cast<short>(pos);
+                    }
                 }
             }
             __syncthreads();
@@ -594,10 +647,13 @@ constexpr size_t kExpandSmem = sizeof(unsigned long long) * 2 * kExpCap + sizeof
 // ---------------------------------------------------------------------------
 // Host launchers
 // ---------------------------------------------------------------------------
-static ExpTable make_exp_table() {
-    ExpTable t;
-    ffexp_table(t.hi, t.lo);
-    return t;
+static const ExpTable& exp_table() {
+    static const ExpTable tab = [] {
+        ExpTable t;
+        ffexp_table(t.hi, t.lo);
+        return t;
+    }();
+    return tab;
 }
 
 template <int W>
@@ -617,7 +673,7 @@ size_t topw_workspace_bytes(long long rows, long long V, int W) {
     bytes += align_up(p * W * sizeof(float));
     bytes += align_up(p * W * sizeof(int));
     bytes += align_up(p * sizeof(float));
-    bytes += align_up(p * sizeof(double));
+    bytes += align_up(p * sizeof(float2));
     return bytes;
 }
 
@@ -625,7 +681,7 @@ struct TopwParts {
     float* v;
     int* id;
     float* m;
-    double* s;
+    float2* s;
     int splits;
 };
 
@@ -639,14 +695,14 @@ static TopwParts carve_topw(char* base, long long rows, long long V, int W) {
     base += align_up(p * W * sizeof(int));
     t.m = reinterpret_cast<float*>(base);
     base += align_up(p * sizeof(float));
-    t.s = reinterpret_cast<double*>(base);
+    t.s = reinterpret_cast<float2*>(base);
     return t;
 }
 
 template <int W>
 static cudaError_t launch_topw_partial(const float* z, long long rows, long long V, TopwParts& t,
                                        cudaStream_t st) {
-    static const ExpTable tab = make_exp_table();
+    const ExpTable& tab = exp_table();
     const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
     dim3 grid(t.splits, static_cast<unsigned>(rows));
     if (vec)
@@ -666,7 +722,8 @@ static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t
     if (e != cudaSuccess) return e;
     const long long warps_per_block = 8;
     const unsigned blocks = static_cast<unsigned>((rows + warps_per_block - 1) / warps_per_block);
-    topw_merge_kernel<W><<<blocks, 256, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, rows, tok, lp, lse);
+    topw_merge_kernel<W><<<blocks, 256, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, rows, exp_table(),
+                                                  tok, lp, lse);
     return cudaGetLastError();
 }
 
@@ -683,7 +740,7 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
     }
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(t.v, t.id, t.m, t.s, t.splits, nullptr,
+    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(t.v, t.id, t.m, t.s, t.splits, exp_table(), nullptr,
                                                        nullptr, root_token, tree_off, total_nodes, N, parent,
                                                        token, depth, anc, err);
     return cudaGetLastError();
@@ -696,7 +753,7 @@ static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_
                               cudaStream_t st) {
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(nullptr, nullptr, nullptr, nullptr, 0, tok, lp,
+    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(nullptr, nullptr, nullptr, nullptr, 0, exp_table(), tok, lp,
                                                        root_token, tree_off, total_nodes, N, parent, token,
                                                        depth, anc, err);
     return cudaGetLastError();

@@ -5,92 +5,30 @@
 // prefix the target agrees with, along the best path) and AdaptiveSpec's
 // "逐步Margin规则" (accept a drafted token when p(draft)/p(top1) >= t).
 //
-// One cooperative kernel walks all sequences level by level.  At level d
-// the frontier of a sequence is the set of reached nodes of depth d (one
-// node under the greedy rule).  Phase 1: every CTA streams 4096-entry chunks
-// of the frontier rows (vectorised coalesced loads) and folds a packed
-// (order-preserving value, inverted id) 64-bit key into the row's slot with
-// atomicMax, which yields max and lowest-id argmax in one word.  Phase 2:
-// one warp per sequence tests the frontier's children against those keys and
-// forms the next frontier.  Only rows of reached nodes are read, so a step
-// costs (accepted length + 1) rows under the greedy rule instead of B rows.
-// Grid-wide barriers are bounded in time (error flag, then exit).
+// One thread-block cluster per sequence walks its tree level by level.  At
+// level d the frontier is the set of reached nodes of depth d (one node under
+// the greedy rule).  Phase 1: every warp of the cluster streams 1024-entry
+// chunks of the frontier rows (coalesced 16-byte loads) and folds a packed
+// 64-bit key (order-preserving value, inverted id) into the row's slot in
+// rank 0's shared memory with a distributed-shared-memory atomicMax; the
+// word holds the row maximum and its lowest-id argmax.  Phase 2: one warp of
+// rank 0 tests the frontier's children against those keys and forms the next
+// frontier.  Hardware cluster barriers separate the phases.  Only rows of
+// reached nodes are read: (accepted length + 1) rows per sequence under the
+// greedy rule.
+#include <cooperative_groups.h>
+
 #include "jt_common.cuh"
 #include "jt_internal.h"
+
+namespace cg = cooperative_groups;
 
 namespace jt {
 
 constexpr int kAccThreads = 256;
-constexpr int kAccChunk = 4096;
-constexpr int kAccMaxSeq = 8192;
+constexpr int kAccChunk = 1024;  // entries per warp work item
 
-struct AcceptWs {
-    WsHeader* hdr;
-    unsigned long long* keys;  // [total_nodes]
-    int* frontier;             // [nseq][2][JT_MAX_TREE]
-    int* fcount;               // [nseq][2]
-    int* final_node;           // [nseq]
-    int* state;                // [nseq]: 0 walking, 1 done, 2 invalid
-};
-
-size_t accept_workspace_bytes(int nseq, int total_nodes) {
-    size_t b = kWsHeader;
-    b += align_up(sizeof(unsigned long long) * static_cast<size_t>(total_nodes));
-    b += align_up(sizeof(int) * static_cast<size_t>(nseq) * 2 * JT_MAX_TREE);
-    b += align_up(sizeof(int) * static_cast<size_t>(nseq) * 2);
-    b += align_up(sizeof(int) * static_cast<size_t>(nseq));
-    b += align_up(sizeof(int) * static_cast<size_t>(nseq));
-    return b;
-}
-
-static AcceptWs carve_accept(char* ws, int nseq, int total_nodes) {
-    AcceptWs w;
-    w.hdr = reinterpret_cast<WsHeader*>(ws);
-    char* p = ws + kWsHeader;
-    w.keys = reinterpret_cast<unsigned long long*>(p);
-    p += align_up(sizeof(unsigned long long) * static_cast<size_t>(total_nodes));
-    w.frontier = reinterpret_cast<int*>(p);
-    p += align_up(sizeof(int) * static_cast<size_t>(nseq) * 2 * JT_MAX_TREE);
-    w.fcount = reinterpret_cast<int*>(p);
-    p += align_up(sizeof(int) * static_cast<size_t>(nseq) * 2);
-    w.final_node = reinterpret_cast<int*>(p);
-    p += align_up(sizeof(int) * static_cast<size_t>(nseq));
-    w.state = reinterpret_cast<int*>(p);
-    return w;
-}
-
-// Grid-wide barrier over co-resident CTAs (cooperative launch).  Returns
-// false, with DEVERR_TIMEOUT raised, if the others do not arrive in time.
-__device__ __forceinline__ bool grid_barrier(WsHeader* hdr, unsigned nblocks) {
-    __shared__ int s_ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        int ok = 1;
-        volatile unsigned* gen = &hdr->bar_gen;
-        const unsigned g = *gen;
-        __threadfence();
-        const unsigned arrived = atomicAdd(&hdr->bar_count, 1u);
-        if (arrived == nblocks - 1) {
-            atomicExch(&hdr->bar_count, 0u);
-            __threadfence();
-            atomicAdd(&hdr->bar_gen, 1u);
-        } else {
-            const unsigned long long t0 = globaltimer_ns();
-            while (*gen == g) {
-                __nanosleep(64);
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    raise_error(&hdr->err, DEVERR_TIMEOUT);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        __threadfence();
-        s_ok = ok;
-    }
-    __syncthreads();
-    return s_ok != 0;
-}
+size_t accept_workspace_bytes(int /*nseq*/, int /*total_nodes*/) { return kWsHeader; }
 
 __device__ __forceinline__ unsigned long long pack_argmax_key(float v, long long id) {
     return (static_cast<unsigned long long>(float_order_key(v)) << 32) |
@@ -99,80 +37,59 @@ __device__ __forceinline__ unsigned long long pack_argmax_key(float v, long long
 
 template <bool VEC>
 __global__ void __launch_bounds__(kAccThreads)
-    accept_kernel(const float* __restrict__ z, const int32_t* __restrict__ parent,
-                  const int32_t* __restrict__ token, const int32_t* __restrict__ tree_off,
-                  int nseq, int total_nodes, int N, long long V, int rule, double log_t,
-                  int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
-                  int32_t* __restrict__ bonus, AcceptWs w) {
-    extern __shared__ int s_prefix[];  // [nseq + 1]
-    __shared__ unsigned long long s_red[kAccThreads / 32];
-    __shared__ uint32_t s_mask[kAccThreads / 32][8];
+    accept_cluster_kernel(const float* __restrict__ z, const int32_t* __restrict__ parent,
+                          const int32_t* __restrict__ token, const int32_t* __restrict__ tree_off,
+                          int total_nodes, int N, long long V, int rule, double log_t,
+                          int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
+                          int32_t* __restrict__ bonus, uint32_t* err) {
+    __shared__ unsigned long long s_rowkey[JT_MAX_TREE];  // rank 0: key per frontier slot
+    __shared__ int s_front[2][JT_MAX_TREE];               // frontier lists (node ids)
+    __shared__ int s_slot[JT_MAX_TREE];                   // rank 0: node -> frontier slot
+    __shared__ int s_n[2];
+    __shared__ int s_done, s_final;
+    __shared__ unsigned long long s_finalkey;
+
+    cg::cluster_group cl = cg::this_cluster();
+    const unsigned rank = cl.block_rank(), csize = cl.num_blocks();
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const unsigned nblocks = gridDim.x;
-    const int gwarp = blockIdx.x * (kAccThreads / 32) + warp;
-    const int nwarps = gridDim.x * (kAccThreads / 32);
-    const long long C = (V + kAccChunk - 1) / kAccChunk;
-
-    // prologue: root of every sequence is the level-0 frontier
-    for (int b = blockIdx.x * kAccThreads + tid; b < nseq; b += gridDim.x * kAccThreads) {
-        const int B = tree_off[b + 1] - tree_off[b];
-        const bool ok = (B >= 1 && B <= JT_MAX_TREE && tree_off[b] >= 0 &&
-                         tree_off[b + 1] <= total_nodes);
-        if (!ok) raise_error(&w.hdr->err, DEVERR_INVALID);
-        w.state[b] = ok ? 0 : 2;
-        w.frontier[(b * 2 + 0) * JT_MAX_TREE] = 0;
-        w.fcount[b * 2 + 0] = ok ? 1 : 0;
-        w.fcount[b * 2 + 1] = 0;
-        w.final_node[b] = 0;
-        if (ok) w.keys[tree_off[b]] = 0ull;
+    const int b = blockIdx.x / csize;
+    const int off = tree_off[b];
+    const int B = tree_off[b + 1] - off;
+    if (B < 1 || B > JT_MAX_TREE || off < 0 || off + B > total_nodes) {
+        if (rank == 0 && tid == 0) raise_error(err, DEVERR_INVALID);
+        return;  // the whole cluster leaves before any cluster barrier
     }
-    if (!grid_barrier(w.hdr, nblocks)) return;
+    if (tid == 0) {
+        s_front[0][0] = 0;
+        s_n[0] = 1;
+        s_done = 0;
+        s_final = 0;
+    }
+    for (int i = tid; i < JT_MAX_TREE; i += kAccThreads) s_rowkey[i] = 0ull;
+    cl.sync();
+    unsigned long long* rk0 = cl.map_shared_rank(s_rowkey, 0);
+    int* fr0 = cl.map_shared_rank(&s_front[0][0], 0);
+    int* n0 = cl.map_shared_rank(s_n, 0);
+    int* done0 = cl.map_shared_rank(&s_done, 0);
 
+    const long long C = (V + kAccChunk - 1) / kAccChunk;
+    const int gw = static_cast<int>(rank) * (kAccThreads / 32) + warp;
+    const int nw = static_cast<int>(csize) * (kAccThreads / 32);
+    bool finished = false;
     for (int lvl = 0; lvl <= N; ++lvl) {
         const int cur = lvl & 1, nxt = cur ^ 1;
-
-        // ---- phase 1: packed max/argmax keys of the frontier rows
-        if (warp == 0) {
-            // exclusive prefix of frontier sizes over the sequences still
-            // walking (finished or invalid ones contribute nothing)
-            const int per = (nseq + 31) / 32;
-            const int lo = lane * per, hi = min(nseq, lo + per);
-            int sum = 0;
-            for (int b = lo; b < hi; ++b)
-                sum += (w.state[b] == 0) ? min(w.fcount[b * 2 + cur], JT_MAX_TREE) : 0;
-            int incl = sum;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const int t = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-                if (lane >= off) incl += t;
-            }
-            int run = incl - sum;
-            for (int b = lo; b < hi; ++b) {
-                s_prefix[b] = run;
-                run += (w.state[b] == 0) ? min(w.fcount[b * 2 + cur], JT_MAX_TREE) : 0;
-            }
-            if (lane == 31) s_prefix[nseq] = incl;
-        }
-        __syncthreads();
-        const long long total_rows = s_prefix[nseq];
-        for (long long it = blockIdx.x; it < total_rows * C; it += gridDim.x) {
-            const long long r = it / C;
-            const long long c = it - r * C;
-            int lo = 0, hi = nseq;  // last b with s_prefix[b] <= r
-            while (hi - lo > 1) {
-                const int mid = (lo + hi) >> 1;
-                if (s_prefix[mid] <= r) lo = mid; else hi = mid;
-            }
-            const int b = lo;
-            const int u = w.frontier[(b * 2 + cur) * JT_MAX_TREE + (r - s_prefix[b])];
-            const long long grow = tree_off[b] + u;
-            const float* zr = z + grow * V;
+        const int n = s_n[cur];
+        // ---- phase 1: row keys of the frontier
+        for (long long it = gw; it < n * C; it += nw) {
+            const int i = static_cast<int>(it / C);
+            const long long c = it - static_cast<long long>(i) * C;
+            const float* zr = z + static_cast<long long>(off + s_front[cur][i]) * V;
             const long long begin = c * kAccChunk, end = min(V, begin + kAccChunk);
             unsigned long long best = 0ull;
             if (VEC) {
 #pragma unroll
-                for (int i = 0; i < kAccChunk / (4 * kAccThreads); ++i) {
-                    const long long e = begin + 4ll * (tid + kAccThreads * i);
+                for (int q = 0; q < kAccChunk / 128; ++q) {
+                    const long long e = begin + 4ll * (lane + 32 * q);
                     if (e < end) {
                         const float4 f = __ldg(reinterpret_cast<const float4*>(zr + e));
                         best = max(best, pack_argmax_key(f.x, e));
@@ -182,43 +99,26 @@ __global__ void __launch_bounds__(kAccThreads)
                     }
                 }
             } else {
-                for (long long e = begin + tid; e < end; e += kAccThreads)
+                for (long long e = begin + lane; e < end; e += 32)
                     best = max(best, pack_argmax_key(__ldg(zr + e), e));
             }
 #pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, off));
-            if (lane == 0) s_red[warp] = best;
-            __syncthreads();
-            if (tid == 0) {
-                for (int i = 1; i < kAccThreads / 32; ++i) best = max(best, s_red[i]);
-                atomicMax(&w.keys[grow], best);
-            }
-            __syncthreads();
+            for (int o = 16; o >= 1; o >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
+            if (lane == 0) atomicMax(&rk0[i], best);
         }
-        if (!grid_barrier(w.hdr, nblocks)) return;
-        // The counter of the next level was last read before the barrier
-        // just passed and is next incremented after the following one.
-        if (blockIdx.x == 0 && tid == 0) w.hdr->active[nxt] = 0u;
-
-        // ---- phase 2: one warp per sequence tests the frontier's children
-        for (int b = gwarp; b < nseq; b += nwarps) {
-            if (w.state[b] != 0) continue;
-            const int off = tree_off[b];
-            const int B = tree_off[b + 1] - off;
-            const int ncur = w.fcount[b * 2 + cur];
-            const int* fl = w.frontier + (b * 2 + cur) * JT_MAX_TREE;
-            if (lane < 8) s_mask[warp][lane] = 0u;
+        cl.sync();
+        // ---- phase 2: rank 0 tests the frontier's children
+        if (rank == 0 && warp == 0) {
+            for (int i = lane; i < JT_MAX_TREE; i += 32) s_slot[i] = -1;
             __syncwarp();
             int fmin = JT_MAX_TREE;
-            for (int i = lane; i < ncur; i += 32) {
-                const int u = fl[i];
-                atomicOr(&s_mask[warp][u >> 5], 1u << (u & 31));
-                fmin = min(fmin, u);
+            for (int i = lane; i < n; i += 32) {
+                s_slot[s_front[cur][i]] = i;
+                fmin = min(fmin, s_front[cur][i]);
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) fmin = min(fmin, __shfl_xor_sync(0xFFFFFFFFu, fmin, o));
             __syncwarp();
-            int* nl = w.frontier + (b * 2 + nxt) * JT_MAX_TREE;
             int cnt = 0;
             for (int c0 = 1; c0 < B; c0 += 32) {
                 const int c = c0 + lane;
@@ -227,9 +127,9 @@ __global__ void __launch_bounds__(kAccThreads)
                     const int p = parent[off + c];
                     const int tk = token[off + c];
                     if (p < 0 || p >= c || tk < 0 || tk >= V) {
-                        raise_error(&w.hdr->err, DEVERR_INVALID);
-                    } else if ((s_mask[warp][p >> 5] >> (p & 31)) & 1u) {
-                        const unsigned long long key = w.keys[off + p];
+                        raise_error(err, DEVERR_INVALID);
+                    } else if (s_slot[p] >= 0) {
+                        const unsigned long long key = s_rowkey[s_slot[p]];
                         if (rule == JT_RULE_GREEDY) {
                             acc = static_cast<uint32_t>(tk) == 0xFFFFFFFFu - static_cast<uint32_t>(key);
                         } else {
@@ -240,86 +140,121 @@ __global__ void __launch_bounds__(kAccThreads)
                     }
                 }
                 const unsigned bal = __ballot_sync(0xFFFFFFFFu, acc);
-                if (acc) {
-                    const int pos = cnt + __popc(bal & ((1u << lane) - 1u));
-                    nl[pos] = c;
-                    w.keys[off + c] = 0ull;
-                }
+                if (acc) s_front[nxt][cnt + __popc(bal & ((1u << lane) - 1u))] = c;
                 cnt += __popc(bal);
             }
             if (rule == JT_RULE_GREEDY && cnt > 1) cnt = 1;  // first accepted child in node order
             if (lane == 0) {
                 if (cnt == 0) {
-                    w.final_node[b] = fmin;
-                    w.state[b] = 1;
-                    w.fcount[b * 2 + nxt] = 0;
-                } else {
-                    w.fcount[b * 2 + nxt] = cnt;
-                    atomicAdd(&w.hdr->active[cur], 1u);
+                    s_final = fmin;
+                    s_finalkey = s_rowkey[s_slot[fmin]];
+                    s_done = 1;
                 }
+                s_n[nxt] = cnt;
             }
+            __syncwarp();
+            for (int i = lane; i < JT_MAX_TREE; i += 32) s_rowkey[i] = 0ull;  // next level's slots
         }
-        if (!grid_barrier(w.hdr, nblocks)) return;
-        if (*reinterpret_cast<volatile unsigned*>(&w.hdr->active[cur]) == 0u) break;
+        cl.sync();
+        if (*done0) {
+            finished = true;
+            break;
+        }
+        const int nn = n0[nxt];
+        if (rank != 0)
+            for (int i = tid; i < nn; i += kAccThreads) s_front[nxt][i] = fr0[nxt * JT_MAX_TREE + i];
+        if (tid == 0) s_n[nxt] = nn;
+        __syncthreads();
     }
 
     // epilogue: path, accepted length, bonus token
-    for (int b = gwarp; b < nseq; b += nwarps) {
-        const int st = w.state[b];
-        if (st == 2) continue;
-        if (st != 1) {  // deeper than N
-            if (lane == 0) raise_error(&w.hdr->err, DEVERR_INVALID);
-            continue;
-        }
-        const int off = tree_off[b];
-        const int f = w.final_node[b];
-        int d = 0;  // the chain root..f was validated edge by edge when it was accepted
-        for (int u = f; d <= N && parent[off + u] >= 0; u = parent[off + u]) ++d;
-        if (d > N) {
-            if (lane == 0) raise_error(&w.hdr->err, DEVERR_INVALID);
-            continue;
-        }
-        int32_t* pb = path + static_cast<long long>(b) * (N + 1);
-        for (int k = lane; k <= N; k += 32) pb[k] = -1;
-        __syncwarp();
-        if (lane == 0) {
-            int k = d;
-            for (int u = f; u >= 0 && k >= 0; u = parent[off + u]) pb[k--] = u;
-            accept_len[b] = d;
-            bonus[b] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(w.keys[off + f]));
+    if (rank == 0 && warp == 0) {
+        if (!finished) {  // tree deeper than N
+            if (lane == 0) raise_error(err, DEVERR_INVALID);
+        } else {
+            const int f = s_final;
+            int d = 0;  // the chain root..f was validated edge by edge when it was accepted
+            for (int u = f; d <= N && parent[off + u] >= 0; u = parent[off + u]) ++d;
+            int32_t* pb = path + static_cast<long long>(b) * (N + 1);
+            for (int k = lane; k <= N; k += 32) pb[k] = -1;
+            __syncwarp();
+            if (lane == 0 && d <= N) {
+                int k = d;
+                for (int u = f; u >= 0 && k >= 0; u = parent[off + u]) pb[k--] = u;
+                accept_len[b] = d;
+                bonus[b] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(s_finalkey));
+            } else if (lane == 0) {
+                raise_error(err, DEVERR_INVALID);
+            }
         }
     }
+    cl.sync();  // rank 0's shared memory stays alive until every rank is done with it
+}
+
+// Largest cluster size (16, 8, 4, 2, 1) the device can schedule for this kernel.
+template <bool VEC>
+static int accept_cluster_size() {
+    static int cached = 0;
+    if (cached) return cached;
+    cudaFuncSetAttribute(accept_cluster_kernel<VEC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    for (int cs = 16; cs >= 1; cs >>= 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(cs);
+        cfg.blockDim = dim3(kAccThreads);
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = cs;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int nclusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&nclusters, accept_cluster_kernel<VEC>, &cfg) == cudaSuccess &&
+            nclusters > 0) {
+            cached = cs;
+            return cs;
+        }
+        cudaGetLastError();
+    }
+    cached = 1;
+    return 1;
+}
+
+template <bool VEC>
+static cudaError_t launch_accept(const float* z, const int32_t* parent, const int32_t* token,
+                                 const int32_t* tree_off, int nseq, int N, long long V,
+                                 int total_nodes, int rule, double log_t, int32_t* accept_len,
+                                 int32_t* path, int32_t* bonus, uint32_t* err, cudaStream_t st) {
+    const int cs = accept_cluster_size<VEC>();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(nseq) * cs);
+    cfg.blockDim = dim3(kAccThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = cs;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_cluster_kernel<VEC>, z, parent, token, tree_off,
+                              total_nodes, N, V, rule, log_t, accept_len, path, bonus, err);
 }
 
 cudaError_t verify_accept_launch(const float* z, const int32_t* parent, const int32_t* token,
                                  const int32_t* tree_off, int nseq, int N, long long V,
                                  int total_nodes, int rule, double log_t, int32_t* accept_len,
                                  int32_t* path, int32_t* bonus, char* ws, cudaStream_t st) {
-    if (nseq > kAccMaxSeq) return cudaErrorInvalidValue;
-    AcceptWs w = carve_accept(ws, nseq, total_nodes);
+    uint32_t* err = reinterpret_cast<uint32_t*>(ws);
     cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), st);
     if (e != cudaSuccess) return e;
     const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
-    const void* fn = vec ? reinterpret_cast<const void*>(&accept_kernel<true>)
-                         : reinterpret_cast<const void*>(&accept_kernel<false>);
-    const size_t smem = sizeof(int) * static_cast<size_t>(nseq + 1);
-    int dev = 0, occ = 0;
-    e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, kAccThreads, smem);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    // one CTA per 4096-entry chunk of one row per sequence (the greedy
-    // frontier), at least 16, at most what is co-resident: fewer CTAs make
-    // the grid barriers cheaper
-    const long long chunks = static_cast<long long>(nseq) * ((V + kAccChunk - 1) / kAccChunk);
-    const long long cap = static_cast<long long>(device_sm_count()) * (occ < 2 ? occ : 2);
-    const int grid = static_cast<int>(chunks < 16 ? (cap < 16 ? cap : 16) : (chunks < cap ? chunks : cap));
-    void* args[] = {(void*)&z,      (void*)&parent, (void*)&token, (void*)&tree_off,
-                    (void*)&nseq,   (void*)&total_nodes, (void*)&N, (void*)&V, (void*)&rule,
-                    (void*)&log_t,  (void*)&accept_len, (void*)&path, (void*)&bonus,
-                    (void*)&w};
-    return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kAccThreads), args, smem, st);
+    if (vec)
+        return launch_accept<true>(z, parent, token, tree_off, nseq, N, V, total_nodes, rule, log_t,
+                                   accept_len, path, bonus, err, st);
+    return launch_accept<false>(z, parent, token, tree_off, nseq, N, V, total_nodes, rule, log_t,
+                                accept_len, path, bonus, err, st);
 }
 
 }  // namespace jt
