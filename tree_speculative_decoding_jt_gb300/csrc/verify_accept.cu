@@ -9,13 +9,13 @@
 // level d the frontier is the set of reached nodes of depth d (one node under
 // the greedy rule).  Phase 1: every warp of the cluster streams 1024-entry
 // chunks of the frontier rows (coalesced 16-byte loads) and folds a packed
-// 64-bit key (order-preserving value, inverted id) into the row's slot in
-// rank 0's shared memory with a distributed-shared-memory atomicMax; the
-// word holds the row maximum and its lowest-id argmax.  Phase 2: one warp of
-// rank 0 tests the frontier's children against those keys and forms the next
-// frontier.  Hardware cluster barriers separate the phases.  Only rows of
-// reached nodes are read: (accepted length + 1) rows per sequence under the
-// greedy rule.
+// 64-bit key (order-preserving value, inverted id) into its CTA's slot for
+// the row with a shared-memory atomicMax; the word holds the row maximum and
+// its lowest-id argmax.  Phase 2: one warp of rank 0 combines the ranks'
+// words through distributed shared memory, tests the frontier's children
+// against the row keys and forms the next frontier.  Hardware cluster
+// barriers separate the phases.  Only rows of reached nodes are read:
+// (accepted length + 1) rows per sequence under the greedy rule.
 #include <cooperative_groups.h>
 
 #include "jt_common.cuh"
@@ -42,7 +42,8 @@ __global__ void __launch_bounds__(kAccThreads)
                           int total_nodes, int N, long long V, int rule, double log_t,
                           int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
                           int32_t* __restrict__ bonus, uint32_t* err) {
-    __shared__ unsigned long long s_rowkey[JT_MAX_TREE];  // rank 0: key per frontier slot
+    __shared__ unsigned long long s_part[JT_MAX_TREE];    // this CTA's key per frontier slot
+    __shared__ unsigned long long s_rowkey[JT_MAX_TREE];  // rank 0: combined key per slot
     __shared__ int s_front[2][JT_MAX_TREE];               // frontier lists (node ids)
     __shared__ int s_slot[JT_MAX_TREE];                   // rank 0: node -> frontier slot
     __shared__ int s_n[2];
@@ -65,9 +66,8 @@ __global__ void __launch_bounds__(kAccThreads)
         s_done = 0;
         s_final = 0;
     }
-    for (int i = tid; i < JT_MAX_TREE; i += kAccThreads) s_rowkey[i] = 0ull;
+    for (int i = tid; i < JT_MAX_TREE; i += kAccThreads) s_part[i] = 0ull;
     cl.sync();
-    unsigned long long* rk0 = cl.map_shared_rank(s_rowkey, 0);
     int* fr0 = cl.map_shared_rank(&s_front[0][0], 0);
     int* n0 = cl.map_shared_rank(s_n, 0);
     int* done0 = cl.map_shared_rank(&s_done, 0);
@@ -104,11 +104,16 @@ __global__ void __launch_bounds__(kAccThreads)
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-            if (lane == 0) atomicMax(&rk0[i], best);
+            if (lane == 0) atomicMax(&s_part[i], best);
         }
         cl.sync();
-        // ---- phase 2: rank 0 tests the frontier's children
+        // ---- phase 2: rank 0 combines the ranks' keys and tests the children
         if (rank == 0 && warp == 0) {
+            for (int i = lane; i < n; i += 32) {
+                unsigned long long k = 0ull;
+                for (unsigned r = 0; r < csize; ++r) k = max(k, cl.map_shared_rank(s_part, r)[i]);
+                s_rowkey[i] = k;
+            }
             for (int i = lane; i < JT_MAX_TREE; i += 32) s_slot[i] = -1;
             __syncwarp();
             int fmin = JT_MAX_TREE;
@@ -152,10 +157,9 @@ __global__ void __launch_bounds__(kAccThreads)
                 }
                 s_n[nxt] = cnt;
             }
-            __syncwarp();
-            for (int i = lane; i < JT_MAX_TREE; i += 32) s_rowkey[i] = 0ull;  // next level's slots
         }
         cl.sync();
+        for (int i = tid; i < JT_MAX_TREE; i += kAccThreads) s_part[i] = 0ull;  // next level's slots
         if (*done0) {
             finished = true;
             break;
