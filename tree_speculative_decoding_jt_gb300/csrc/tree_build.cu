@@ -171,7 +171,10 @@ __global__ void __launch_bounds__(kTopwThreads)
             x[4 * i + 1] = f.y;
             x[4 * i + 2] = f.z;
             x[4 * i + 3] = f.w;
-            if (e < end) {
+            // cheap filter first (entries reach the list rarely): only a
+            // value >= the current W-th best can enter it
+            const float t = L.v[W - 1];
+            if (e < end && (f.x >= t || f.y >= t || f.z >= t || f.w >= t)) {
                 L.push(f.x, static_cast<int>(e));
                 L.push(f.y, static_cast<int>(e + 1));
                 L.push(f.z, static_cast<int>(e + 2));
@@ -185,7 +188,7 @@ __global__ void __launch_bounds__(kTopwThreads)
             x[i] = -INFINITY;
             if (e < end) {
                 x[i] = __ldg(zr + e);
-                L.push(x[i], static_cast<int>(e));
+                if (x[i] >= L.v[W - 1]) L.push(x[i], static_cast<int>(e));
             }
         }
     }
@@ -274,24 +277,57 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
                                           const float* tab_lo, int (&tok)[W], double (&lp)[W],
                                           double& lse) {
     const long long base = row * splits;
+    // every load of the row is issued up front (one memory round trip):
+    // lane handles chunks s = lane + 32 r, r < kMergeR
+    constexpr int kMergeR = 4;  // covers 128 chunks = 512k vocabulary entries
+    float pm[kMergeR];
+    float2 ps[kMergeR];
+    float pv[kMergeR][W];
+    int pi[kMergeR][W];
+#pragma unroll
+    for (int r = 0; r < kMergeR; ++r) {
+        const int s = lane + 32 * r;
+        const bool in = s < splits;
+        pm[r] = in ? part_m[base + s] : -INFINITY;
+        ps[r] = in ? part_s[base + s] : make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            pv[r][k] = in ? part_v[(base + s) * W + k] : -INFINITY;
+            pi[r][k] = in ? part_id[(base + s) * W + k] : -1;
+        }
+    }
     float M = -INFINITY;
-    for (int s = lane; s < splits; s += 32) M = fmaxf(M, part_m[base + s]);
+#pragma unroll
+    for (int r = 0; r < kMergeR; ++r) M = fmaxf(M, pm[r]);
+    for (int s = lane + 32 * kMergeR; s < splits; s += 32) M = fmaxf(M, part_m[base + s]);
     M = warp_max_f(M);
     ffloat S;
     S.hi = S.lo = 0.0f;
-    if (M != -INFINITY)
-        for (int s = lane; s < splits; s += 32) {
+    if (M != -INFINITY) {
+#pragma unroll
+        for (int r = 0; r < kMergeR; ++r) {
+            if (pm[r] != -INFINITY) {
+                float dh, dl;
+                two_sum(pm[r], -M, dh, dl);
+                ffloat Sj;
+                Sj.hi = ps[r].x;
+                Sj.lo = ps[r].y;
+                S = ff_add(S, ff_mul(Sj, ffexp(dh, dl, tab_hi, tab_lo)));
+            }
+        }
+        for (int s = lane + 32 * kMergeR; s < splits; s += 32) {
             const float ms = part_m[base + s];
             if (ms != -INFINITY) {
                 float dh, dl;
                 two_sum(ms, -M, dh, dl);
-                const float2 ps = part_s[base + s];
+                const float2 q = part_s[base + s];
                 ffloat Sj;
-                Sj.hi = ps.x;
-                Sj.lo = ps.y;
+                Sj.hi = q.x;
+                Sj.lo = q.y;
                 S = ff_add(S, ff_mul(Sj, ffexp(dh, dl, tab_hi, tab_lo)));
             }
         }
+    }
     S = warp_sum_ff(S);
     if (M == -INFINITY) {
         lse = -INFINITY;
@@ -305,7 +341,11 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
 
     TopList<W> L;
     L.init();
-    for (int s = lane; s < splits; s += 32)
+#pragma unroll
+    for (int r = 0; r < kMergeR; ++r)
+#pragma unroll
+        for (int k = 0; k < W; ++k) L.push(pv[r][k], pi[r][k]);
+    for (int s = lane + 32 * kMergeR; s < splits; s += 32)
 #pragma unroll
         for (int k = 0; k < W; ++k) L.push(part_v[(base + s) * W + k], part_id[(base + s) * W + k]);
     float rv[W];
@@ -428,8 +468,85 @@ __device__ __forceinline__ int block_incl_scan(int v, int* s_warp) {
     return v;
 }
 
+// Bitonic sort of 32*E (k1, k2) pairs held in one warp's registers
+// (element i = lane + 32*e), descending.  Strides below 32 exchange through
+// shuffles, larger strides swap registers; no block barriers.
+template <int E>
+__device__ __forceinline__ void warp_bitonic_desc(unsigned long long (&a1)[E],
+                                                  unsigned long long (&a2)[E], int lane) {
+    constexpr int P = 32 * E;
+#pragma unroll
+    for (int size = 2; size <= P; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride >= 32) {
+                const int es = stride >> 5;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int f = e ^ es;
+                    if (f > e) {
+                        const bool desc = ((lane + 32 * e) & size) == 0;
+                        if (key_better(a1[e], a2[e], a1[f], a2[f]) != desc) {
+                            const unsigned long long t1 = a1[e], t2 = a2[e];
+                            a1[e] = a1[f];
+                            a2[e] = a2[f];
+                            a1[f] = t1;
+                            a2[f] = t2;
+                        }
+                    }
+                }
+            } else {
+                const bool lower = (lane & stride) == 0;
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const unsigned long long o1 = __shfl_xor_sync(kFull, a1[e], stride);
+                    const unsigned long long o2 = __shfl_xor_sync(kFull, a2[e], stride);
+                    const bool desc = ((lane + 32 * e) & size) == 0;
+                    const bool mine_better = key_better(a1[e], a2[e], o1, o2);
+                    if (mine_better != (lower == desc)) {
+                        a1[e] = o1;
+                        a2[e] = o2;
+                    }
+                }
+            }
+        }
+    }
+}
+
+template <int E>
+__device__ __forceinline__ void warp_sort_smem(unsigned long long* k1, unsigned long long* k2, int n,
+                                               int lane) {
+    unsigned long long a1[E], a2[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int i = lane + 32 * e;
+        a1[e] = (i < n) ? k1[i] : 0ull;
+        a2[e] = (i < n) ? k2[i] : 0ull;
+    }
+    warp_bitonic_desc<E>(a1, a2, lane);
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const int i = lane + 32 * e;
+        k1[i] = a1[e];
+        k2[i] = a2[e];
+    }
+}
+
 // Sort k1/k2[0, n) descending by (k1, k2); entries [n, P) are padding.
+// Up to 512 entries one warp sorts in registers; beyond, the whole block.
 __device__ void block_bitonic_desc(unsigned long long* k1, unsigned long long* k2, int n) {
+    if (n <= 512) {
+        if (threadIdx.x < 32) {
+            const int lane = threadIdx.x;
+            if (n <= 32) warp_sort_smem<1>(k1, k2, n, lane);
+            else if (n <= 64) warp_sort_smem<2>(k1, k2, n, lane);
+            else if (n <= 128) warp_sort_smem<4>(k1, k2, n, lane);
+            else if (n <= 256) warp_sort_smem<8>(k1, k2, n, lane);
+            else warp_sort_smem<16>(k1, k2, n, lane);
+        }
+        __syncthreads();
+        return;
+    }
     int P = 1;
     while (P < n) P <<= 1;
     for (int i = n + threadIdx.x; i < P; i += kExpandThreads) {
@@ -438,9 +555,9 @@ __device__ void block_bitonic_desc(unsigned long long* k1, unsigned long long* k
     }
     __syncthreads();
     for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+        for (int stride = size >> 1, ls = __ffs(size) - 2; stride > 0; stride >>= 1, --ls) {
             for (int q = threadIdx.x; q < (P >> 1); q += kExpandThreads) {
-                const int i = 2 * stride * (q / stride) + (q % stride);
+                const int i = ((q >> ls) << (ls + 1)) | (q & (stride - 1));  // 2*stride*(q/stride) + q%stride
                 const int j = i + stride;
                 const bool desc = (i & size) == 0;
                 const unsigned long long a1 = k1[i], a2 = k2[i], b1 = k1[j], b2 = k2[j];
@@ -457,7 +574,7 @@ __device__ void block_bitonic_desc(unsigned long long* k1, unsigned long long* k
 }
 
 template <int W>
-__global__ void __launch_bounds__(kExpandThreads)
+__global__ void __launch_bounds__(kExpandThreads, 1)
     expand_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id,
                   const float* __restrict__ part_m, const float2* __restrict__ part_s,
                   int splits, ExpTable tab, const int32_t* __restrict__ tok_in,

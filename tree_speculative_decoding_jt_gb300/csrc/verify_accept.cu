@@ -7,13 +7,14 @@
 //
 // One thread-block cluster per sequence walks its tree level by level.  At
 // level d the frontier is the set of reached nodes of depth d (one node under
-// the greedy rule).  Phase 1: every warp of the cluster streams 1024-entry
+// the greedy rule).  Phase 1: every warp of the cluster streams 2048-entry
 // chunks of the frontier rows (coalesced 16-byte loads) and folds a packed
 // 64-bit key (order-preserving value, inverted id) into its CTA's slot for
 // the row with a shared-memory atomicMax; the word holds the row maximum and
-// its lowest-id argmax.  Phase 2: one warp of rank 0 combines the ranks'
-// words through distributed shared memory, tests the frontier's children
-// against the row keys and forms the next frontier.  Hardware cluster
+// its lowest-id argmax.  Phase 2: rank 0 combines the ranks' words through
+// distributed shared memory, tests every child of the frontier against the
+// row keys (one thread per child) and compacts the accepted ones, in node
+// order, into the next frontier.  Hardware cluster
 // barriers separate the phases.  Only rows of reached nodes are read:
 // (accepted length + 1) rows per sequence under the greedy rule.
 #include <cooperative_groups.h>
@@ -26,7 +27,7 @@ namespace cg = cooperative_groups;
 namespace jt {
 
 constexpr int kAccThreads = 256;
-constexpr int kAccChunk = 1024;  // entries per warp work item
+constexpr int kAccChunk = 2048;  // entries per warp work item (one load round per level)
 
 size_t accept_workspace_bytes(int /*nseq*/, int /*total_nodes*/) { return kWsHeader; }
 
@@ -44,8 +45,10 @@ __global__ void __launch_bounds__(kAccThreads)
                           int32_t* __restrict__ bonus, uint32_t* err) {
     __shared__ unsigned long long s_part[JT_MAX_TREE];    // this CTA's key per frontier slot
     __shared__ unsigned long long s_rowkey[JT_MAX_TREE];  // rank 0: combined key per slot
-    __shared__ int s_front[2][JT_MAX_TREE];               // frontier lists (node ids)
+    __shared__ int s_front[2][JT_MAX_TREE];               // frontier lists (node ids, ascending)
     __shared__ int s_slot[JT_MAX_TREE];                   // rank 0: node -> frontier slot
+    __shared__ int s_par[JT_MAX_TREE], s_tok[JT_MAX_TREE];
+    __shared__ int s_wcnt[kAccThreads / 32];
     __shared__ int s_n[2];
     __shared__ int s_done, s_final;
     __shared__ unsigned long long s_finalkey;
@@ -60,13 +63,22 @@ __global__ void __launch_bounds__(kAccThreads)
         if (rank == 0 && tid == 0) raise_error(err, DEVERR_INVALID);
         return;  // the whole cluster leaves before any cluster barrier
     }
+    // rank 0 fetches the tree now; the loads land while phase 1 streams rows
+    int my_par = -1, my_tok = 0;
+    if (rank == 0 && tid < B) {
+        my_par = parent[off + tid];
+        my_tok = token[off + tid];
+    }
     if (tid == 0) {
         s_front[0][0] = 0;
         s_n[0] = 1;
         s_done = 0;
         s_final = 0;
     }
-    for (int i = tid; i < JT_MAX_TREE; i += kAccThreads) s_part[i] = 0ull;
+    for (int i = tid; i < JT_MAX_TREE; i += kAccThreads) {
+        s_part[i] = 0ull;
+        s_rowkey[i] = 0ull;
+    }
     cl.sync();
     int* fr0 = cl.map_shared_rank(&s_front[0][0], 0);
     int* n0 = cl.map_shared_rank(s_n, 0);
@@ -87,15 +99,21 @@ __global__ void __launch_bounds__(kAccThreads)
             const long long begin = c * kAccChunk, end = min(V, begin + kAccChunk);
             unsigned long long best = 0ull;
             if (VEC) {
+                float4 f[kAccChunk / 128];
+#pragma unroll
+                for (int q = 0; q < kAccChunk / 128; ++q) {
+                    const long long e = begin + 4ll * (lane + 32 * q);
+                    f[q] = (e < end) ? __ldg(reinterpret_cast<const float4*>(zr + e))
+                                     : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                }
 #pragma unroll
                 for (int q = 0; q < kAccChunk / 128; ++q) {
                     const long long e = begin + 4ll * (lane + 32 * q);
                     if (e < end) {
-                        const float4 f = __ldg(reinterpret_cast<const float4*>(zr + e));
-                        best = max(best, pack_argmax_key(f.x, e));
-                        best = max(best, pack_argmax_key(f.y, e + 1));
-                        best = max(best, pack_argmax_key(f.z, e + 2));
-                        best = max(best, pack_argmax_key(f.w, e + 3));
+                        best = max(best, pack_argmax_key(f[q].x, e));
+                        best = max(best, pack_argmax_key(f[q].y, e + 1));
+                        best = max(best, pack_argmax_key(f[q].z, e + 2));
+                        best = max(best, pack_argmax_key(f[q].w, e + 3));
                     }
                 }
             } else {
@@ -106,57 +124,61 @@ __global__ void __launch_bounds__(kAccThreads)
             for (int o = 16; o >= 1; o >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
             if (lane == 0) atomicMax(&s_part[i], best);
         }
+        if (lvl == 0 && rank == 0) {
+            s_par[tid] = my_par;
+            s_tok[tid] = my_tok;
+        }
         cl.sync();
-        // ---- phase 2: rank 0 combines the ranks' keys and tests the children
-        if (rank == 0 && warp == 0) {
-            for (int i = lane; i < n; i += 32) {
-                unsigned long long k = 0ull;
-                for (unsigned r = 0; r < csize; ++r) k = max(k, cl.map_shared_rank(s_part, r)[i]);
-                s_rowkey[i] = k;
+        // ---- phase 2 (rank 0): combine the ranks' keys, test the children
+        if (rank == 0) {
+            for (int q = tid; q < n * static_cast<int>(csize); q += kAccThreads) {
+                const int i = q / static_cast<int>(csize);
+                const unsigned r = static_cast<unsigned>(q) % csize;
+                atomicMax(&s_rowkey[i], cl.map_shared_rank(s_part, r)[i]);
             }
-            for (int i = lane; i < JT_MAX_TREE; i += 32) s_slot[i] = -1;
-            __syncwarp();
-            int fmin = JT_MAX_TREE;
-            for (int i = lane; i < n; i += 32) {
-                s_slot[s_front[cur][i]] = i;
-                fmin = min(fmin, s_front[cur][i]);
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) fmin = min(fmin, __shfl_xor_sync(0xFFFFFFFFu, fmin, o));
-            __syncwarp();
-            int cnt = 0;
-            for (int c0 = 1; c0 < B; c0 += 32) {
-                const int c = c0 + lane;
-                bool acc = false;
-                if (c < B) {
-                    const int p = parent[off + c];
-                    const int tk = token[off + c];
-                    if (p < 0 || p >= c || tk < 0 || tk >= V) {
-                        raise_error(err, DEVERR_INVALID);
-                    } else if (s_slot[p] >= 0) {
-                        const unsigned long long key = s_rowkey[s_slot[p]];
-                        if (rule == JT_RULE_GREEDY) {
-                            acc = static_cast<uint32_t>(tk) == 0xFFFFFFFFu - static_cast<uint32_t>(key);
-                        } else {
-                            const float zmax = float_from_order_key(static_cast<uint32_t>(key >> 32));
-                            const float zt = z[static_cast<long long>(off + p) * V + tk];
-                            acc = (static_cast<double>(zt) - static_cast<double>(zmax)) >= log_t;
-                        }
+            s_slot[tid] = -1;
+            __syncthreads();
+            if (tid < n) s_slot[s_front[cur][tid]] = tid;
+            __syncthreads();
+            const int c = tid;  // one thread per child
+            bool acc = false;
+            if (c >= 1 && c < B) {
+                const int p = s_par[c];
+                const int tk = s_tok[c];
+                if (p < 0 || p >= c || tk < 0 || tk >= V) {
+                    raise_error(err, DEVERR_INVALID);
+                } else if (s_slot[p] >= 0) {
+                    const unsigned long long key = s_rowkey[s_slot[p]];
+                    if (rule == JT_RULE_GREEDY) {
+                        acc = static_cast<uint32_t>(tk) == 0xFFFFFFFFu - static_cast<uint32_t>(key);
+                    } else {
+                        const float zmax = float_from_order_key(static_cast<uint32_t>(key >> 32));
+                        const float zt = z[static_cast<long long>(off + p) * V + tk];
+                        acc = (static_cast<double>(zt) - static_cast<double>(zmax)) >= log_t;
                     }
                 }
-                const unsigned bal = __ballot_sync(0xFFFFFFFFu, acc);
-                if (acc) s_front[nxt][cnt + __popc(bal & ((1u << lane) - 1u))] = c;
-                cnt += __popc(bal);
             }
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, acc);
+            if (lane == 0) s_wcnt[warp] = __popc(bal);
+            __syncthreads();
+            int wbase = 0, cnt = 0;
+#pragma unroll
+            for (int w = 0; w < kAccThreads / 32; ++w) {
+                wbase += (w < warp) ? s_wcnt[w] : 0;
+                cnt += s_wcnt[w];
+            }
+            if (acc) s_front[nxt][wbase + __popc(bal & ((1u << lane) - 1u))] = c;
             if (rule == JT_RULE_GREEDY && cnt > 1) cnt = 1;  // first accepted child in node order
-            if (lane == 0) {
-                if (cnt == 0) {
-                    s_final = fmin;
-                    s_finalkey = s_rowkey[s_slot[fmin]];
+            if (tid == 0) {
+                if (cnt == 0) {  // frontier lists are ascending: slot 0 is the lowest node
+                    s_final = s_front[cur][0];
+                    s_finalkey = s_rowkey[0];
                     s_done = 1;
                 }
                 s_n[nxt] = cnt;
             }
+            __syncthreads();
+            for (int i = tid; i < n; i += kAccThreads) s_rowkey[i] = 0ull;  // next level's slots
         }
         cl.sync();
         for (int i = tid; i < JT_MAX_TREE; i += kAccThreads) s_part[i] = 0ull;  // next level's slots
@@ -178,13 +200,13 @@ __global__ void __launch_bounds__(kAccThreads)
         } else {
             const int f = s_final;
             int d = 0;  // the chain root..f was validated edge by edge when it was accepted
-            for (int u = f; d <= N && parent[off + u] >= 0; u = parent[off + u]) ++d;
+            for (int u = f; d <= N && s_par[u] >= 0; u = s_par[u]) ++d;
             int32_t* pb = path + static_cast<long long>(b) * (N + 1);
             for (int k = lane; k <= N; k += 32) pb[k] = -1;
             __syncwarp();
             if (lane == 0 && d <= N) {
                 int k = d;
-                for (int u = f; u >= 0 && k >= 0; u = parent[off + u]) pb[k--] = u;
+                for (int u = f; u >= 0 && k >= 0; u = s_par[u]) pb[k--] = u;
                 accept_len[b] = d;
                 bonus[b] = static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(s_finalkey));
             } else if (lane == 0) {
