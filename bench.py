@@ -173,31 +173,51 @@ def attn_sample_nodes(wl, k):
 
 
 def run_reference(args, rank):
+    """The oracle, as it stands, on the host cores.  One reference step is
+    the attention of one tree node (rotating over the batch) plus a 1/B
+    share of the full tree build and of both acceptance rules, which are
+    timed once over the whole batch; so a run of K steps costs about K
+    single-node attentions and stays within minutes."""
     if rank != 0:
         return
-    wl = wk.make(args.config)
     import oracle
-    tr = oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"])
+
+    wl = wk.make(args.config)
+    c = wl.cfg
+    t0 = time.perf_counter()
+    tr = oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, c["W"])
+    t_build = time.perf_counter() - t0
     target = wk.target_logits(wl, tr["parent"], tr["token"])
-    nodes = attn_sample_nodes(wl, args.cpu_attn_nodes)
-    vals = []
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        cpu_oracle_sample(wl, tr["parent"], tr["token"], target, nodes[:2])
+    t0 = time.perf_counter()
+    oracle.verify_accept(target, tr["parent"], tr["token"], wl.tree_off, c["N"], 0)
+    oracle.verify_accept(target, tr["parent"], tr["token"], wl.tree_off, c["N"], 1, math.log(c["t"]))
+    t_accept = time.perf_counter() - t0
+
+    def attn_one(n):
+        oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len, wl.tree_off,
+                         tr["parent"], wl.scale, rows=np.array([n], np.int32))
+
+    for i in range(min(args.warmup, 3)):
+        attn_one(i % wl.total)
+    times = []
     t_start = time.perf_counter()
-    for _ in range(args.steps):
-        v, _ = cpu_oracle_sample(wl, tr["parent"], tr["token"], target, nodes)
-        vals.append(v)
+    for i in range(args.steps):
+        t0 = time.perf_counter()
+        attn_one((i * 37) % wl.total)
+        times.append(time.perf_counter() - t0)
     wall = time.perf_counter() - t_start
-    value = statistics.mean(vals)
+    per_node = t_build / wl.total + t_accept / wl.total + statistics.mean(times)
+    value = 1.0 / per_node
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * wl.total / value,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_node,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": wl.cfg["name"], "sample": "see cpu_baseline"},
+        "data": "synthetic", "config": {"workload": c["name"], "nseq": wl.nseq, "tree_nodes": wl.total},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"full tree build and both acceptance rules over all {wl.total} "
-                                   f"nodes, attention for {len(nodes)} of {wl.total} nodes; "
-                                   f"single-threaded C, fp64; {wall:.1f} s for {args.steps} steps"},
+                         "sample": f"tree build ({t_build:.2f} s) and both acceptance rules "
+                                   f"({t_accept:.2f} s) over all {wl.total} nodes once, attention "
+                                   f"of one node per step for {args.steps} steps ({wall:.1f} s); "
+                                   f"single-threaded C, fp64"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -217,6 +237,7 @@ def main():
     ap.add_argument("--cpu-attn-nodes", type=int, default=48)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush-mb", type=int, default=512)
+    ap.add_argument("--no-graph", action="store_true", help="launch every call eagerly")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -296,18 +317,11 @@ def main():
     stream = torch.cuda.current_stream()
     attn_ev = []
 
-    def step(inp, record_attn=False):
+    def step(inp):
         jt.jt_tree_build(inp["draft"], inp["root"], inp["off"], W, total_nodes=total,
                          out=(parent, token, depth, anc), ws=ws_b)
-        if record_attn:
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
         jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], inp["off"], anc,
                               scale=wl.scale, max_tree=max_tree, out=out, lse=lse, ws=ws_a)
-        if record_attn:
-            e1.record(stream)
-            attn_ev.append((e0, e1))
         for i, rule in enumerate((jt.JT_RULE_GREEDY, jt.JT_RULE_MARGIN)):
             jt.jt_verify_accept(inp["target"], parent, token, inp["off"], N, rule=rule, log_t=log_t,
                                 out=(acc[i], path[i], bonus[i]), ws=ws_v[i])
@@ -320,6 +334,26 @@ def main():
     for ws in (ws_b, ws_a, *ws_v):
         jt.jt_check(ws)
 
+    def attn_only(inp):
+        jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], inp["off"], anc,
+                              scale=wl.scale, max_tree=max_tree, out=out, lse=lse, ws=ws_a)
+
+    # The step's kernels are replayed from a CUDA graph (as a serving engine
+    # would), so host launch overhead stays out of the device timeline.
+    g_step, g_attn = None, None
+    if not args.no_graph:
+        g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step):
+            step(d)
+        with torch.cuda.graph(g_attn):
+            attn_only(d)
+        for _ in range(args.warmup):
+            flush.zero_()
+            g_step.replay()
+        torch.cuda.synchronize()
+        for ws in (ws_b, ws_a, *ws_v):
+            jt.jt_check(ws)
+
     # ---- timed region (inputs resident in HBM; L2 flushed before each step)
     evs = []
     with ClockSampler(local_rank) as clocks:
@@ -331,12 +365,28 @@ def main():
             e0 = torch.cuda.Event(enable_timing=True)
             e1 = torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            step(d, record_attn=True)
+            if g_step is not None:
+                g_step.replay()
+            else:
+                step(d)
             e1.record(stream)
             evs.append((e0, e1))
         torch.cuda.synchronize()
         barrier()
         wall = time.perf_counter() - t_wall0
+    # the dominant kernel alone, same inputs, same L2 flush, for the roofline
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if g_attn is not None:
+            g_attn.replay()
+        else:
+            attn_only(d)
+        e1.record(stream)
+        attn_ev.append((e0, e1))
+    torch.cuda.synchronize()
     step_ms = [a.elapsed_time(b) for a, b in evs]
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
     ms = statistics.mean(step_ms)
@@ -417,6 +467,7 @@ def main():
                        "Hq": Hq, "Hkv": Hkv, "head_dim": D, "N": N, "W": W, "V": c["V"],
                        "step": "tree_build + tree_attn_paged + verify_accept(greedy) + verify_accept(margin t=0.8)",
                        "l2": f"flushed before every step ({args.flush_mb} MiB write)",
+                       "launch": "eager" if args.no_graph else "cuda_graph replay of the step",
                        "parallelism": f"replicas x{world}"},
             "roofline": roof,
             "cpu_baseline": cpu,

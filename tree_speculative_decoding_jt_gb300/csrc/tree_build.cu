@@ -396,32 +396,33 @@ __global__ void __launch_bounds__(256)
 // nodes of the full depth-N tree under the queue key, in key order: a child
 // never beats its parent (log-probs are <= 0, and depth breaks exact ties in
 // the parent's favour) and a later sibling never beats an earlier one.  So
-// instead of B-1 dependent pops the CTA builds that set level by level:
-// S holds the best candidates seen so far, sorted by key and cut to B-1; at
-// level d the children (depth d+1) of S's depth-d nodes are generated, a
-// child that is not better than S's current (B-1)-th entry is dropped (it
-// has B-1 better nodes, and so has every descendant), and S is re-sorted
-// (block bitonic sort) and cut again.  After the last level S is the pop
-// sequence.  Scores are the same fp64 root-to-node sums as the reference
-// definition, so the integer outputs are identical.
+// instead of B-1 dependent pops the CTA builds that set level by level.  S
+// holds the best candidates seen so far, sorted by key and cut to B-1.  At
+// level d every depth-d entry of S generates its children (depth d+1) that
+// beat S's current (B-1)-th entry (any other child has B-1 better nodes, and
+// so has every descendant).  Those children form W runs, one per child rank
+// k, each already sorted (the parents are sorted and the k-th log-prob is
+// shared).  Every candidate's new position is its index in its own sorted
+// run plus, per other run, a binary search for the number of better entries;
+// no sort is needed.  After the last level S is the pop sequence.  Scores are
+// the same fp64 root-to-node sums as the reference definition, so the integer
+// outputs are identical.
 // ---------------------------------------------------------------------------
-constexpr int kExpCap = 2048;  // candidates held at once (set + new children)
+constexpr int kExpCap = JT_MAX_TREE + JT_MAX_TREE * JT_MAX_W;  // set + all new children
 
-// Tie key (larger = earlier): depth asc, token asc, parent position asc;
-// bits 0..11 carry the candidate's own slot and never decide an order
-// (no two candidates agree on all the bits above them).
-__device__ __forceinline__ unsigned long long make_k2(int depth, int token, int parent_pos,
-                                                      int slot) {
+// Tie key (larger = earlier): depth asc, token asc, parent position asc.
+// The parent field only ever decides between children of the same depth
+// created at the same level, whose parent positions refer to the same
+// (sorted) set.
+__device__ __forceinline__ unsigned long long make_k2(int depth, int token, int parent_pos) {
     return (static_cast<unsigned long long>(255 - depth) << 56) |
            (static_cast<unsigned long long>(0xFFFFFFFFu - static_cast<uint32_t>(token)) << 24) |
-           (static_cast<unsigned long long>(0xFFF - (parent_pos + 1)) << 12) |
-           static_cast<unsigned long long>(slot);
+           static_cast<unsigned long long>(0xFFFFFF - (parent_pos + 1));
 }
 __device__ __forceinline__ int k2_depth(unsigned long long k2) { return 255 - static_cast<int>(k2 >> 56); }
 __device__ __forceinline__ int k2_token(unsigned long long k2) {
     return static_cast<int>(0xFFFFFFFFu - static_cast<uint32_t>((k2 >> 24) & 0xFFFFFFFFull));
 }
-__device__ __forceinline__ int k2_slot(unsigned long long k2) { return static_cast<int>(k2 & 0xFFF); }
 
 __device__ __forceinline__ double double_from_order_key(unsigned long long k) {
     const unsigned long long u = (k & 0x8000000000000000ull) ? (k & 0x7FFFFFFFFFFFFFFFull) : ~k;
@@ -431,6 +432,18 @@ __device__ __forceinline__ double double_from_order_key(unsigned long long k) {
 __device__ __forceinline__ bool key_better(unsigned long long a1, unsigned long long a2,
                                            unsigned long long b1, unsigned long long b2) {
     return a1 > b1 || (a1 == b1 && a2 > b2);
+}
+
+// Number of entries of a[0, len) (sorted best first) better than (x1, x2).
+__device__ __forceinline__ int count_better(const unsigned long long* a1, const unsigned long long* a2,
+                                            int len, unsigned long long x1, unsigned long long x2) {
+    int lo = 0, hi = len;
+    while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (key_better(a1[mid], a2[mid], x1, x2)) lo = mid + 1;
+        else hi = mid;
+    }
+    return lo;
 }
 
 __host__ __device__ inline int full_tree_nodes(int N, int W, int cap) {
@@ -468,133 +481,31 @@ __device__ __forceinline__ int block_incl_scan(int v, int* s_warp) {
     return v;
 }
 
-// Bitonic sort of 32*E (k1, k2) pairs held in one warp's registers
-// (element i = lane + 32*e), descending.  Strides below 32 exchange through
-// shuffles, larger strides swap registers; no block barriers.
-template <int E>
-__device__ __forceinline__ void warp_bitonic_desc(unsigned long long (&a1)[E],
-                                                  unsigned long long (&a2)[E], int lane) {
-    constexpr int P = 32 * E;
-#pragma unroll
-    for (int size = 2; size <= P; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride >= 32) {
-                const int es = stride >> 5;
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const int f = e ^ es;
-                    if (f > e) {
-                        const bool desc = ((lane + 32 * e) & size) == 0;
-                        if (key_better(a1[e], a2[e], a1[f], a2[f]) != desc) {
-                            const unsigned long long t1 = a1[e], t2 = a2[e];
-                            a1[e] = a1[f];
-                            a2[e] = a2[f];
-                            a1[f] = t1;
-                            a2[f] = t2;
-                        }
-                    }
-                }
-            } else {
-                const bool lower = (lane & stride) == 0;
-#pragma unroll
-                for (int e = 0; e < E; ++e) {
-                    const unsigned long long o1 = __shfl_xor_sync(kFull, a1[e], stride);
-                    const unsigned long long o2 = __shfl_xor_sync(kFull, a2[e], stride);
-                    const bool desc = ((lane + 32 * e) & size) == 0;
-                    const bool mine_better = key_better(a1[e], a2[e], o1, o2);
-                    if (mine_better != (lower == desc)) {
-                        a1[e] = o1;
-                        a2[e] = o2;
-                    }
-                }
-            }
-        }
-    }
-}
-
-template <int E>
-__device__ __forceinline__ void warp_sort_smem(unsigned long long* k1, unsigned long long* k2, int n,
-                                               int lane) {
-    unsigned long long a1[E], a2[E];
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const int i = lane + 32 * e;
-        a1[e] = (i < n) ? k1[i] : 0ull;
-        a2[e] = (i < n) ? k2[i] : 0ull;
-    }
-    warp_bitonic_desc<E>(a1, a2, lane);
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-        const int i = lane + 32 * e;
-        k1[i] = a1[e];
-        k2[i] = a2[e];
-    }
-}
-
-// Sort k1/k2[0, n) descending by (k1, k2); entries [n, P) are padding.
-// Up to 512 entries one warp sorts in registers; beyond, the whole block.
-__device__ void block_bitonic_desc(unsigned long long* k1, unsigned long long* k2, int n) {
-    if (n <= 512) {
-        if (threadIdx.x < 32) {
-            const int lane = threadIdx.x;
-            if (n <= 32) warp_sort_smem<1>(k1, k2, n, lane);
-            else if (n <= 64) warp_sort_smem<2>(k1, k2, n, lane);
-            else if (n <= 128) warp_sort_smem<4>(k1, k2, n, lane);
-            else if (n <= 256) warp_sort_smem<8>(k1, k2, n, lane);
-            else warp_sort_smem<16>(k1, k2, n, lane);
-        }
-        __syncthreads();
-        return;
-    }
-    int P = 1;
-    while (P < n) P <<= 1;
-    for (int i = n + threadIdx.x; i < P; i += kExpandThreads) {
-        k1[i] = 0ull;
-        k2[i] = 0ull;
-    }
-    __syncthreads();
-    for (int size = 2; size <= P; size <<= 1) {
-        for (int stride = size >> 1, ls = __ffs(size) - 2; stride > 0; stride >>= 1, --ls) {
-            for (int q = threadIdx.x; q < (P >> 1); q += kExpandThreads) {
-                const int i = ((q >> ls) << (ls + 1)) | (q & (stride - 1));  // 2*stride*(q/stride) + q%stride
-                const int j = i + stride;
-                const bool desc = (i & size) == 0;
-                const unsigned long long a1 = k1[i], a2 = k2[i], b1 = k1[j], b2 = k2[j];
-                if (key_better(a1, a2, b1, b2) != desc) {
-                    k1[i] = b1;
-                    k2[i] = b2;
-                    k1[j] = a1;
-                    k2[j] = a2;
-                }
-            }
-            __syncthreads();
-        }
-    }
-}
-
 template <int W>
 __global__ void __launch_bounds__(kExpandThreads, 1)
-    expand_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id,
-                  const float* __restrict__ part_m, const float2* __restrict__ part_s,
-                  int splits, ExpTable tab, const int32_t* __restrict__ tok_in,
-                  const double* __restrict__ lp_in,
+    expand_kernel(const int32_t* __restrict__ tok_in, const double* __restrict__ lp_in,
                   const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
                   int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
     extern __shared__ __align__(16) unsigned char dsm[];
-    unsigned long long* k1 = reinterpret_cast<unsigned long long*>(dsm);  // [kExpCap]
-    unsigned long long* k2 = k1 + kExpCap;                                // [kExpCap]
-    short* par = reinterpret_cast<short*>(k2 + kExpCap);                  // [2][kExpCap]
-    short* inv = par + 2 * kExpCap;                                       // [kExpCap]
-    short* front = inv + kExpCap;                                         // [kExpCap]
+    unsigned long long* kb1[2];
+    unsigned long long* kb2[2];
+    kb1[0] = reinterpret_cast<unsigned long long*>(dsm);  // [kExpCap] x 4
+    kb2[0] = kb1[0] + kExpCap;
+    kb1[1] = kb2[0] + kExpCap;
+    kb2[1] = kb1[1] + kExpCap;
+    short* pb[2];
+    pb[0] = reinterpret_cast<short*>(kb2[1] + kExpCap);  // [kExpCap] x 2
+    pb[1] = pb[0] + kExpCap;
+    short* rank_of = pb[1] + kExpCap;                      // [kExpCap]
     __shared__ int s_tok[JT_MAX_N * W];
     __shared__ double s_lp[JT_MAX_N * W];
+    __shared__ short s_front[JT_MAX_TREE];
     __shared__ int s_warp[kExpandThreads / 32];
-    __shared__ int s_nf, s_total, s_take;
+    __shared__ int s_nf;
 
     const int b = blockIdx.x;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
     const int off = tree_off[b];
     const int B = tree_off[b + 1] - off;
     if (B < 1 || B > JT_MAX_TREE || B > full_tree_nodes(N, W, JT_MAX_TREE + 1) || off < 0 ||
@@ -602,127 +513,103 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
         if (tid == 0) raise_error(err, DEVERR_INVALID);
         return;
     }
-
-    __shared__ float s_thi[64], s_tlo[64];
-    if (tid < 64) {
-        s_thi[tid] = tab.hi[tid];
-        s_tlo[tid] = tab.lo[tid];
-    }
-    __syncthreads();
-    // per-depth tables for this sequence
-    if (tok_in) {
-        for (int i = tid; i < N * W; i += kExpandThreads) {
-            s_tok[i] = tok_in[static_cast<long long>(b) * N * W + i];
-            s_lp[i] = lp_in[static_cast<long long>(b) * N * W + i];
-        }
-    } else {
-        for (int d = warp; d < N; d += kExpandThreads / 32) {
-            int tk[W];
-            double lq[W], lse;
-            merge_row<W>(part_v, part_id, part_m, part_s, splits, static_cast<long long>(b) * N + d,
-                         lane, s_thi, s_tlo, tk, lq, lse);
-            if (lane == 0)
-#pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    s_tok[d * W + k] = tk[k];
-                    s_lp[d * W + k] = lq[k];
-                }
-        }
+    for (int i = tid; i < N * W; i += kExpandThreads) {
+        s_tok[i] = tok_in[static_cast<long long>(b) * N * W + i];
+        s_lp[i] = lp_in[static_cast<long long>(b) * N * W + i];
     }
     __syncthreads();
 
     const int K = B - 1;  // non-root nodes
-    int m = 0;            // size of the sorted set S
-    int cb = 0;           // current parent buffer
+    int m = 0;            // size of the sorted set S (buffer cb)
+    int cb = 0;
     for (int d = 0; d < N && K > 0; ++d) {
-        // frontier: the root at d == 0, else S's depth-d entries (positions)
+        unsigned long long* k1 = kb1[cb];
+        unsigned long long* k2 = kb2[cb];
+        short* par = pb[cb];
+        // frontier: the root at d == 0, else S's depth-d entries (ascending positions)
+        int nf;
         if (d == 0) {
-            if (tid == 0) {
-                front[0] = -1;
-                s_nf = 1;
-            }
+            if (tid == 0) s_front[0] = -1;
+            nf = 1;
         } else {
-            int nf = 0;
-            for (int p0 = 0; p0 < m; p0 += kExpandThreads) {
-                const int p = p0 + tid;
-                const int is_f = (p < m && k2_depth(k2[p]) == d) ? 1 : 0;
-                const int incl = block_incl_scan(is_f, s_warp);
-                if (is_f) front[nf + incl - 1] = static_cast<short>(p);
-                nf += s_warp[kExpandThreads / 32 - 1];
-                __syncthreads();
-            }
-            if (tid == 0) s_nf = nf;
+            const int is_f = (tid < m && k2_depth(k2[tid]) == d) ? 1 : 0;  // m <= 255 < threads
+            const int incl = block_incl_scan(is_f, s_warp);
+            if (is_f) s_front[incl - 1] = static_cast<short>(tid);
+            nf = s_warp[kExpandThreads / 32 - 1];
         }
         __syncthreads();
-        const int nf = s_nf;
         if (nf == 0) break;
-        for (int fi = 0; fi < nf;) {
-            // threshold: S's (B-1)-th entry once S is full; accept all before
-            const bool full = (m >= K);
-            const unsigned long long t1 = full ? k1[K - 1] : 0ull, t2 = full ? k2[K - 1] : 0ull;
-            const int e = fi + tid;
-            int pos = -2, c = 0;
-            unsigned long long ck[W];  // children's score keys, computed once
-            if (e < nf) {
-                pos = front[e];
-                if (pos >= -1) {
-                    const double su = (pos < 0) ? 0.0 : double_from_order_key(k1[pos]);
+        // children of frontier entry e better than S's (B-1)-th entry
+        const bool full = (m >= K);
+        const unsigned long long t1 = full ? k1[K - 1] : 0ull, t2 = full ? k2[K - 1] : 0ull;
+        const int e = tid;
+        int pos = -2, c = 0;
+        unsigned long long ck[W];
+        if (e < nf) {
+            pos = s_front[e];
+            const double su = (pos < 0) ? 0.0 : double_from_order_key(k1[pos]);
 #pragma unroll
-                    for (int k = 0; k < W; ++k) ck[k] = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
-#pragma unroll
-                    for (int k = 0; k < W; ++k) {
-                        if (c == k && (!full || key_better(ck[k], make_k2(d + 1, s_tok[d * W + k], pos, 0), t1, t2)))
-                            ++c;
-                    }
-                }
-            }
-            const int room = kExpCap - m;
-            const int incl = block_incl_scan(c, s_warp);
-            const int take = __syncthreads_count(e < nf && incl <= room);
-            if (tid == take - 1) s_total = incl;
-            if (tid == 0) s_take = take;
-            __syncthreads();
-            const int ntake = s_take, total = s_total;
-            if (tid < ntake) {  // write the children of the accepted entries
-                const int o0 = m + incl - c;
-#pragma unroll
-                for (int k = 0; k < W; ++k) {
-                    if (k < c) {
-                        const int slot = o0 + k;
-                        k1[slot] = ck[k];
-                        k2[slot] = make_k2(d + 1, s_tok[d * W + k], pos, slot);
-                        par[cb * kExpCap + slot] = static_cast<short>(pos);
-                    }
-                }
-            }
-            __syncthreads();
-            fi += ntake;
-            const int mall = m + total;
-            if (total > 0) {
-                block_bitonic_desc(k1, k2, mall);
-                const int mnew = min(K, mall);
-                for (int p = tid; p < mall; p += kExpandThreads) inv[p] = -2;
-                __syncthreads();
-                for (int p = tid; p < mnew; p += kExpandThreads) inv[k2_slot(k2[p])] = static_cast<short>(p);
-                __syncthreads();
-                for (int p = tid; p < mnew; p += kExpandThreads) {
-                    const int old = k2_slot(k2[p]);
-                    const int pp = par[cb * kExpCap + old];
-                    const int np = (pp < 0) ? pp : inv[pp];
-                    par[(cb ^ 1) * kExpCap + p] = static_cast<short>(np);
-                    k2[p] = (k2[p] & ~0xFFFFFFull) |
-                            (static_cast<unsigned long long>(0xFFF - (np + 1)) << 12) |
-                            static_cast<unsigned long long>(p);
-                }
-                for (int q = fi + tid; q < nf; q += kExpandThreads) {
-                    const int f = front[q];
-                    front[q] = static_cast<short>((f >= 0) ? inv[f] : f);
-                }
-                __syncthreads();
-                cb ^= 1;
-                m = mnew;
+            for (int k = 0; k < W; ++k) {
+                ck[k] = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
+                if (c == k && (!full || key_better(ck[k], make_k2(d + 1, s_tok[d * W + k], pos), t1, t2)))
+                    ++c;
             }
         }
+        // run k = children of rank k of entries 0..L_k-1 (L_k non-increasing in k)
+        int L[W], R[W];
+        int total = 0;
+#pragma unroll
+        for (int k = 0; k < W; ++k) {
+            L[k] = __syncthreads_count(e < nf && c > k);
+            R[k] = total;
+            total += L[k];
+        }
+        if (total == 0) break;
+#pragma unroll
+        for (int k = 0; k < W; ++k)
+            if (k < c) {
+                const int x = m + R[k] + e;
+                k1[x] = ck[k];
+                k2[x] = make_k2(d + 1, s_tok[d * W + k], pos);
+                par[x] = static_cast<short>(pos);
+            }
+        __syncthreads();
+        // rank of every candidate in S + runs
+        const int M = m + total;
+        for (int x = tid; x < M; x += kExpandThreads) {
+            const unsigned long long x1 = k1[x], x2 = k2[x];
+            int rank, own = -1;
+            if (x < m) {
+                rank = x;
+            } else {
+                const int y = x - m;
+#pragma unroll
+                for (int k = 0; k < W; ++k)
+                    if (y >= R[k] && y < R[k] + L[k]) own = k;
+                rank = (y - R[own]) + count_better(k1, k2, m, x1, x2);
+            }
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+                if (k != own && L[k] > 0)
+                    rank += count_better(k1 + m + R[k], k2 + m + R[k], L[k], x1, x2);
+            rank_of[x] = static_cast<short>(rank < K ? rank : -2);
+        }
+        __syncthreads();
+        unsigned long long* n1 = kb1[cb ^ 1];
+        unsigned long long* n2 = kb2[cb ^ 1];
+        short* npar = pb[cb ^ 1];
+        for (int x = tid; x < M; x += kExpandThreads) {
+            const int r = rank_of[x];
+            if (r >= 0) {
+                const int pp = par[x];
+                n1[r] = k1[x];
+                n2[r] = k2[x];
+                npar[r] = static_cast<short>(pp < 0 ? pp : rank_of[pp]);
+            }
+        }
+        __syncthreads();
+        cb ^= 1;
+        m = min(K, M);
     }
     if (m != K) {  // cannot happen when B fits the full tree
         if (tid == 0) raise_error(err, DEVERR_INVALID);
@@ -730,6 +617,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     }
 
     // outputs: node 0 = root, node p+1 = S[p]; ancestor-or-self sets
+    const unsigned long long* k2f = kb2[cb];
+    const short* parf = pb[cb];
     for (int n = tid; n < B; n += kExpandThreads) {
         int pn, tn, dn;
         if (n == 0) {
@@ -737,9 +626,9 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             tn = root_token[b];
             dn = 0;
         } else {
-            pn = par[cb * kExpCap + n - 1] + 1;
-            tn = k2_token(k2[n - 1]);
-            dn = k2_depth(k2[n - 1]);
+            pn = parf[n - 1] + 1;
+            tn = k2_token(k2f[n - 1]);
+            dn = k2_depth(k2f[n - 1]);
         }
         uint32_t a[8] = {0, 0, 0, 0, 0, 0, 0, 0};
         int u = n;
@@ -747,7 +636,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 #pragma unroll
             for (int w = 0; w < 8; ++w)
                 if (w == (u >> 5)) a[w] |= 1u << (u & 31);
-            u = (u == 0) ? -1 : par[cb * kExpCap + u - 1] + 1;
+            u = (u == 0) ? -1 : parf[u - 1] + 1;
         }
         const long long g = off + n;
         parent[g] = pn;
@@ -759,7 +648,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     }
 }
 
-constexpr size_t kExpandSmem = sizeof(unsigned long long) * 2 * kExpCap + sizeof(short) * 5 * kExpCap;
+constexpr size_t kExpandSmem = sizeof(unsigned long long) * 4 * kExpCap + sizeof(short) * 3 * kExpCap;
 
 // ---------------------------------------------------------------------------
 // Host launchers
@@ -773,10 +662,13 @@ static const ExpTable& exp_table() {
     return tab;
 }
 
+// One-time (per process) attribute set-up; the first call should come before
+// any stream capture.
 template <int W>
 static cudaError_t set_expand_smem() {
-    return cudaFuncSetAttribute(expand_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kExpandSmem));
+    static cudaError_t done = cudaFuncSetAttribute(
+        expand_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kExpandSmem));
+    return done;
 }
 
 static int topw_splits(long long V) {
@@ -787,6 +679,9 @@ static int topw_splits(long long V) {
 size_t topw_workspace_bytes(long long rows, long long V, int W) {
     const long long p = rows * topw_splits(V);
     size_t bytes = 0;
+    bytes += align_up(rows * W * sizeof(int32_t));  // merged tables (tree build)
+    bytes += align_up(rows * W * sizeof(double));
+    bytes += align_up(rows * sizeof(double));
     bytes += align_up(p * W * sizeof(float));
     bytes += align_up(p * W * sizeof(int));
     bytes += align_up(p * sizeof(float));
@@ -795,6 +690,9 @@ size_t topw_workspace_bytes(long long rows, long long V, int W) {
 }
 
 struct TopwParts {
+    int32_t* tok;
+    double* lp;
+    double* lse;
     float* v;
     int* id;
     float* m;
@@ -806,6 +704,12 @@ static TopwParts carve_topw(char* base, long long rows, long long V, int W) {
     TopwParts t;
     t.splits = topw_splits(V);
     const long long p = rows * t.splits;
+    t.tok = reinterpret_cast<int32_t*>(base);
+    base += align_up(rows * W * sizeof(int32_t));
+    t.lp = reinterpret_cast<double*>(base);
+    base += align_up(rows * W * sizeof(double));
+    t.lse = reinterpret_cast<double*>(base);
+    base += align_up(rows * sizeof(double));
     t.v = reinterpret_cast<float*>(base);
     base += align_up(p * W * sizeof(float));
     t.id = reinterpret_cast<int*>(base);
@@ -846,20 +750,25 @@ static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t
 
 template <int W>
 static cudaError_t run_build(const float* z, const int32_t* root_token, const int32_t* tree_off,
-                             int nseq, int total_nodes, int N, long long V, int32_t* parent, int32_t* token,
-                             int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
-                             cudaStream_t st) {
+                             int nseq, int total_nodes, int N, long long V, int32_t* parent,
+                             int32_t* token, int32_t* depth, uint32_t* anc, char* ws_parts,
+                             uint32_t* err, cudaStream_t st) {
     const long long rows = static_cast<long long>(nseq) * N;
     TopwParts t = carve_topw(ws_parts, rows, V, W);
     if (rows > 0) {
         cudaError_t e = launch_topw_partial<W>(z, rows, V, t, st);
         if (e != cudaSuccess) return e;
+        const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+        topw_merge_kernel<W><<<blocks, 256, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, rows,
+                                                      exp_table(), t.tok, t.lp, t.lse);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
     }
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(t.v, t.id, t.m, t.s, t.splits, exp_table(), nullptr,
-                                                       nullptr, root_token, tree_off, total_nodes, N, parent,
-                                                       token, depth, anc, err);
+    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(t.tok, t.lp, root_token, tree_off,
+                                                                  total_nodes, N, parent, token,
+                                                                  depth, anc, err);
     return cudaGetLastError();
 }
 
@@ -870,7 +779,7 @@ static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_
                               cudaStream_t st) {
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(nullptr, nullptr, nullptr, nullptr, 0, exp_table(), tok, lp,
+    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(tok, lp,
                                                        root_token, tree_off, total_nodes, N, parent, token,
                                                        depth, anc, err);
     return cudaGetLastError();
