@@ -9,39 +9,45 @@
 // pages' own kernel (SM90, CuTe DSL, shared-memory mask staging) is prior
 // art; this is a Blackwell design.
 //
-// Work unit (one CTA): sequence b, KV head g, a 128-row tile of query rows
-// = 128/G tree nodes x G query heads of that KV head (GQA heads share the
-// K/V tile because they are stacked in the M dimension), and a contiguous
-// range of 128-key tiles of the logical key sequence (prefix + tree tail).
-// Keys past the last node of the row tile are never loaded (ancestors have
-// smaller indices).  Several ranges of one row tile (KV split) are merged by
-// tree_attn_combine_kernel.
+// Work unit (one CTA): sequence b, KV head g, two 128-row query tiles A and
+// B (each = 128/G tree nodes x the G query heads of that KV head: GQA heads
+// share K/V because they are stacked in the MMA's M dimension), and a
+// contiguous range of 128-key tiles of the logical key sequence (prefix +
+// tree tail).  Both query tiles consume every K/V tile, halving the paged TMA
+// traffic per FLOP.  Keys past the last node of tile B are never loaded
+// (ancestors have smaller indices).  Several key ranges of one unit (KV
+// split) are merged by tree_attn_combine_kernel.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax + epilogue, one query row per thread (TMEM lane);
-//   warp 4     TMA producer: Q tile once, then per KV tile one 16-row box
-//              per 16-token page for K and for V (128-byte swizzle), page ids
-//              from the block table; zero-fills V rows past the last needed
-//              slot of the final tile;
-//   warp 5     TMEM allocator and single-thread MMA issuer.
-// TMEM (512 columns): S[2] (128 fp32 cols each), O (D fp32 cols),
-// P[2] (64 cols each: 128 bf16 probabilities packed in pairs).
-// Per KV tile j: S[j%2] = Q K^T (SS MMA, K-major operands, M=128, N=128,
-// K=D), softmax reads S, writes P in TMEM, O += P V (TS MMA: A = P from
-// TMEM, B = V MN-major, N=D).  QK^T of tile j+1 is issued before PV of tile
-// j so the tensor core overlaps the softmax.  Online softmax in the log2
-// domain with lazy rescaling of O (only when the running max grows by more
-// than 2^8).  All waits are bounded in time.
+// Warp roles (320 threads):
+//   warps 0-3 / 4-7  softmax + epilogue of query tile A / B, one query row
+//                    per thread (TMEM lane);
+//   warp 8           TMA producer: both Q tiles once, then per KV tile one
+//                    16-row box per 16-token page for K and for V (128-byte
+//                    swizzle); page ids are held in registers, loaded two
+//                    groups of four tiles ahead; zero-fills V rows past the
+//                    last needed slot of the final tile;
+//   warp 9           TMEM allocator and single-thread MMA issuer.
+// TMEM (512 columns): per query tile X, S_X (128 fp32 columns) and O_X (D
+// fp32 columns).  Per KV tile j: S_X = Q_X K^T (SS MMA, K-major operands,
+// M=128, N=128, K=D); softmax X reads S_X and writes P_X (bf16, packed in
+// pairs) over the first 64 columns of S_X; O_X += P_X V (TS MMA: A = P_X
+// from TMEM, B = V MN-major, N=D).  Issue order per KV tile: PV_A(j),
+// QK_A(j+1), PV_B(j), QK_B(j+1): the tensor core runs tile A's MMAs while
+// softmax B works and the other way round.  MMAs from one thread execute in
+// issue order, so QK_X(j+1) overwrites S_X only after PV_X(j) has read P_X,
+// and the completion of QK_X(j+1) tells softmax X that O_X holds PV_X(j).
+// Online softmax in the log2 domain, two passes over S in TMEM (row max,
+// then exp and P), lazy rescaling of O (only when the running max grows by
+// more than 2^8).  All waits are bounded in time.
 #include "jt_common.cuh"
 #include "jt_internal.h"
 
 namespace jt {
 
-constexpr int kAttnThreads = 192;
-constexpr int kStages = 3;   // K ring and V ring depth
-constexpr int kPrefetch = 4; // tiles ahead whose pages are prefetched into L2
+constexpr int kAttnThreads = 320;
+constexpr int kStages = 2;   // K ring and V ring depth
 constexpr int kTileN = 128;  // keys per KV tile
-constexpr int kTileM = 128;  // query rows per tile
+constexpr int kTileM = 128;  // query rows per query tile
 constexpr float kRescaleLog2 = 8.0f;
 constexpr int kMaxSplits = 32;
 
@@ -63,10 +69,11 @@ template <int D>
 struct SmemLayout {
     static constexpr int kChunks = D / 64;            // 64-element (128-byte) column blocks
     static constexpr int kChunkBytes = kTileM * 128;  // 128 rows x 128 bytes
-    static constexpr int kQ = 0;
-    static constexpr int kK = kQ + kChunks * kChunkBytes;
-    static constexpr int kV = kK + kStages * kChunks * kChunkBytes;
-    static constexpr int kBar = kV + kStages * kChunks * kChunkBytes;
+    static constexpr int kTileBytes = kChunks * kChunkBytes;
+    static constexpr int kQ = 0;                      // Q_A, Q_B
+    static constexpr int kK = kQ + 2 * kTileBytes;
+    static constexpr int kV = kK + kStages * kTileBytes;
+    static constexpr int kBar = kV + kStages * kTileBytes;
     static constexpr int kBytes = kBar + 256;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
@@ -78,9 +85,8 @@ struct Bars {
     uint64_t k_empty[kStages];
     uint64_t v_empty[kStages];
     uint64_t s_full[2];
-    uint64_t s_free[2];
     uint64_t p_full[2];
-    uint64_t pv_done[2];
+    uint64_t o_final[2];
     uint64_t v_last;
     uint64_t mma_final;
     uint32_t tmem_base;
@@ -112,8 +118,8 @@ __device__ __forceinline__ uint32_t visible_bits(const uint32_t (&a)[8], int rel
     return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
 }
 
-// Tile range [t0, t1) of split sp for a unit whose needed keys end at
-// valid_end; returns the count.
+// Tile range [t0, t0 + count) of split sp for a unit whose needed keys end
+// at valid_end; returns the count.
 __device__ __forceinline__ int split_range(int valid_end, int splits, int sp, int& t0) {
     const int T = (valid_end + kTileN - 1) / kTileN;
     const int tps = (T + splits - 1) / splits;
@@ -122,12 +128,57 @@ __device__ __forceinline__ int split_range(int valid_end, int splits, int sp, in
     return max(0, t1 - t0);
 }
 
+// Keys needed by the unit of query-tile pair mp: through the last node of
+// its second tile.
+__device__ __forceinline__ int unit_valid_end(int L, int B, int mp, int npt) {
+    return L + min(B, (2 * mp + 2) * npt);
+}
+
+// S_x = Q_x K^T for the K tile in stage st (8 or 4 MMAs of K=16).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t aQ, uint32_t aK, int x, int st) {
+    using SL = SmemLayout<D>;
+    constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, false);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t koff = (kk >> 2) * SL::kChunkBytes + (kk & 3) * 32;
+        const uint64_t adesc = smem_desc_sw128(aQ + x * SL::kTileBytes + koff, 16, 1024);
+        const uint64_t bdesc = smem_desc_sw128(aK + st * SL::kTileBytes + koff, 16, 1024);
+        mma_ss(tmem + 256 * x, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+    }
+}
+
+// O_x (+)= P_x V for the V tile in stage st (P_x from TMEM, 8 MMAs of K=16).
+template <int D>
+__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t aV, int x, int st, bool accumulate) {
+    using SL = SmemLayout<D>;
+    constexpr uint32_t idesc = idesc_bf16_f32(kTileM, D, true);
+#pragma unroll
+    for (int kk = 0; kk < kTileN / 16; ++kk) {
+        const uint64_t bdesc = smem_desc_sw128(aV + st * SL::kTileBytes + kk * 16 * 128, SL::kChunkBytes, 1024);
+        mma_ts(tmem + 256 * x + 128, tmem + 256 * x + kk * 8, bdesc, idesc,
+               (accumulate || kk > 0) ? 1u : 0u);
+    }
+}
+
+// Page ids of 4 consecutive tiles (group g4): lane l holds page l%8 of tile
+// 4*g4 + l/8 of the unit.
+__device__ __forceinline__ int bt_group(const AttnParams& p, int b, int t0, int nt, int valid_end,
+                                        int g4, int lane) {
+    const int tile = 4 * g4 + (lane >> 3);
+    const int slot = (t0 + tile) * kTileN + (lane & 7) * JT_PAGE_SIZE;
+    return (tile < nt && slot < valid_end)
+               ? p.block_table[static_cast<long long>(b) * p.max_pages + slot / JT_PAGE_SIZE]
+               : 0;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
     using SL = SmemLayout<D>;
+    constexpr int kTileBytes = SL::kTileBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -135,17 +186,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, g = blockIdx.y;
-    const int m = blockIdx.x / p.splits, sp = blockIdx.x % p.splits;
+    const int mp = blockIdx.x / p.splits, sp = blockIdx.x % p.splits;
     const int off = p.tree_off[b];
     const int B = p.tree_off[b + 1] - off;
     const int L = p.prefix_len[b];
-    if (m * p.npt >= B) return;  // row tile past this sequence's tree
+    const int m0 = 2 * mp;                    // query tile A; tile B = m0 + 1
+    if (m0 * p.npt >= B) return;              // pair past this sequence's tree
     if (B > JT_MAX_TREE || L < 0 || off < 0 || off + B > p.total_nodes ||
         static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE) {
         if (tid == 0) raise_error(p.err, DEVERR_INVALID);
         return;
     }
-    const int n_end = min(B, (m + 1) * p.npt);
+    const bool hasB = (m0 + 1) * p.npt < B;
+    const int n_end = min(B, (m0 + 2) * p.npt);
     const int valid_end = L + n_end;
     int t0;
     const int nt = split_range(valid_end, p.splits, sp, t0);
@@ -159,52 +212,56 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(&bars->k_empty[s], 1);
             mbar_init(&bars->v_empty[s], 1);
         }
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(&bars->s_full[s], 1);
-            mbar_init(&bars->s_free[s], 128);
-            mbar_init(&bars->p_full[s], 128);
-            mbar_init(&bars->pv_done[s], 1);
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(&bars->s_full[x], 1);
+            mbar_init(&bars->p_full[x], 128);
+            mbar_init(&bars->o_final[x], 1);
         }
         mbar_init(&bars->v_last, 1);
         mbar_init(&bars->mma_final, 1);
         bars->abort = 0;
         fence_mbar_init();
     }
-    if (warp == 5) tmem_alloc(&bars->tmem_base, 512);
+    if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    const uint32_t tS0 = tmem, tO = tmem + 256, tP0 = tmem + 384;
     volatile int* abort = &bars->abort;
 
     uint8_t* sQ = smem + SL::kQ;
     uint8_t* sK = smem + SL::kK;
     uint8_t* sV = smem + SL::kV;
-    constexpr int kTileBytes = SL::kChunks * SL::kChunkBytes;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
-            mbar_arrive_expect_tx(&bars->q_full, kTileBytes);
-            for (int c = 0; c < SL::kChunks; ++c)
-                tma_load_3d(sQ + c * SL::kChunkBytes, &tm_q, &bars->q_full, c * 64, g * p.G,
-                            off + m * p.npt);
+            mbar_arrive_expect_tx(&bars->q_full, (hasB ? 2 : 1) * kTileBytes);
+            for (int x = 0; x < (hasB ? 2 : 1); ++x)
+                for (int c = 0; c < SL::kChunks; ++c)
+                    tma_load_3d(sQ + x * kTileBytes + c * SL::kChunkBytes, &tm_q, &bars->q_full,
+                                c * 64, g * p.G, off + (m0 + x) * p.npt);
         }
+        // page ids held in registers, loaded two groups of four tiles ahead
+        int bt_cur = bt_group(p, b, t0, nt, valid_end, 0, lane);
+        int bt_nxt = bt_group(p, b, t0, nt, valid_end, 1, lane);
+        int bt_nn = bt_group(p, b, t0, nt, valid_end, 2, lane);
         int issued = 0;
         for (int j = 0; j < nt; ++j) {
             const int st = j % kStages;
             const uint32_t empty_parity = ((j / kStages) & 1) ^ 1;
+            if (j > 0 && (j & 3) == 0) {
+                bt_cur = bt_nxt;
+                bt_nxt = bt_nn;
+                bt_nn = bt_group(p, b, t0, nt, valid_end, (j >> 2) + 2, lane);
+            }
             const int slot0 = (t0 + j) * kTileN;
             const int nvalid = min(kTileN, valid_end - slot0);
             const int npg = (nvalid + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
-            const int pid = (lane < npg)
-                                ? p.block_table[static_cast<long long>(b) * p.max_pages +
-                                                slot0 / JT_PAGE_SIZE + lane]
-                                : 0;
+            const int pid = __shfl_sync(0xFFFFFFFFu, bt_cur, ((j & 3) << 3) + (lane & 7));
             const uint32_t bytes = npg * SL::kChunks * (JT_PAGE_SIZE * 128);
             // K of tile j: its slot is free once QK^T of tile j-kStages is done
             if (j >= kStages && !mbar_wait_warp(&bars->k_empty[st], empty_parity, p.err, abort)) break;
@@ -223,19 +280,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tma_load_4d(sV + st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128),
                                 &tm_v, &bars->v_full[st], c * 64, g, 0, pid);
             issued = j + 1;
-            // pull the pages of a tile further ahead from HBM into L2
-            if (j + kPrefetch < nt) {
-                const int ps0 = (t0 + j + kPrefetch) * kTileN;
-                const int pn = (min(kTileN, valid_end - ps0) + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
-                if (lane < pn) {
-                    const int ppid = p.block_table[static_cast<long long>(b) * p.max_pages +
-                                                   ps0 / JT_PAGE_SIZE + lane];
-                    for (int c = 0; c < SL::kChunks; ++c) {
-                        tma_prefetch_l2_4d(&tm_k, c * 64, g, 0, ppid);
-                        tma_prefetch_l2_4d(&tm_v, c * 64, g, 0, ppid);
-                    }
-                }
-            }
             if (j == nt - 1) {
                 // final tile: once its V has landed, zero rows past the last
                 // needed slot (stale or foreign data; P is 0 there but
@@ -259,108 +303,87 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, p.err, nullptr);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kTileM, kTileN, false);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kTileM, D, true);
             const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-            auto issue_pv = [&](int i) -> bool {
-                const int st = i % kStages, pb = i & 1;
-                if (!mbar_wait(&bars->p_full[pb], (i >> 1) & 1, p.err, abort)) return false;
-                if (i == nt - 1) {
-                    if (!mbar_wait(&bars->v_last, 0, p.err, abort)) return false;
-                } else if (!mbar_wait(&bars->v_full[st], (i / kStages) & 1, p.err, abort)) {
-                    return false;
-                }
+            const int nx = hasB ? 2 : 1;
+            bool ok = mbar_wait(&bars->q_full, 0, p.err, abort) &&
+                      mbar_wait(&bars->k_full[0], 0, p.err, abort);
+            if (ok) {
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kTileN / 16; ++kk) {
-                    const uint64_t bdesc = smem_desc_sw128(aV + st * kTileBytes + kk * 16 * 128,
-                                                           SL::kChunkBytes, 1024);
-                    mma_ts(tO, tP0 + pb * 64 + kk * 8, bdesc, idesc_pv, (i > 0 || kk > 0) ? 1u : 0u);
+                for (int x = 0; x < nx; ++x) {
+                    issue_qk<D>(tmem, aQ, aK, x, 0);
+                    mma_commit(&bars->s_full[x]);
                 }
-                mma_commit(&bars->v_empty[st]);
-                mma_commit(&bars->pv_done[pb]);
-                return true;
-            };
-            bool ok = mbar_wait(&bars->q_full, 0, p.err, abort);
-            for (int j = 0; ok && j < nt; ++j) {
-                const int st = j % kStages, sb = j & 1;
-                ok = mbar_wait(&bars->k_full[st], (j / kStages) & 1, p.err, abort);
-                if (ok && j >= 2) ok = mbar_wait(&bars->s_free[sb], ((j >> 1) - 1) & 1, p.err, abort);
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t koff = (kk >> 2) * SL::kChunkBytes + (kk & 3) * 32;
-                    const uint64_t adesc = smem_desc_sw128(aQ + koff, 16, 1024);
-                    const uint64_t bdesc = smem_desc_sw128(aK + st * kTileBytes + koff, 16, 1024);
-                    mma_ss(tS0 + sb * 128, adesc, bdesc, idesc_qk, kk > 0 ? 1u : 0u);
-                }
-                mma_commit(&bars->s_full[sb]);
-                mma_commit(&bars->k_empty[st]);
-                if (j >= 1) ok = issue_pv(j - 1);
+                mma_commit(&bars->k_empty[0]);
             }
-            if (ok) issue_pv(nt - 1);
+            for (int j = 0; ok && j < nt; ++j) {
+                const int st = j % kStages;
+                const bool more = j + 1 < nt;
+                for (int x = 0; ok && x < nx; ++x) {
+                    ok = mbar_wait(&bars->p_full[x], j & 1, p.err, abort);
+                    if (ok && x == 0)
+                        ok = (j == nt - 1) ? mbar_wait(&bars->v_last, 0, p.err, abort)
+                                           : mbar_wait(&bars->v_full[st], (j / kStages) & 1, p.err, abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv<D>(tmem, aV, x, st, j > 0);
+                    if (x == nx - 1) mma_commit(&bars->v_empty[st]);
+                    if (!more) {
+                        mma_commit(&bars->o_final[x]);
+                    } else {
+                        if (x == 0) ok = mbar_wait(&bars->k_full[(j + 1) % kStages],
+                                                   ((j + 1) / kStages) & 1, p.err, abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_qk<D>(tmem, aQ, aK, x, (j + 1) % kStages);
+                        mma_commit(&bars->s_full[x]);
+                        if (x == nx - 1) mma_commit(&bars->k_empty[(j + 1) % kStages]);
+                    }
+                }
+            }
             // every MMA issued above completes before TMEM is released
             mma_commit(&bars->mma_final);
             mbar_wait(&bars->mma_final, 0, p.err, nullptr);
         }
-    } else {
-        // ------------------------------------------------------- softmax
-        const int r = tid;  // query row = TMEM lane
-        const int node = m * p.npt + r / p.G;
+    } else if (warp < 4 || hasB) {
+        // ---------------------------------------------- softmax of tile X
+        const int x = warp >> 2;
+        const int r = tid & 127;  // query row = TMEM lane
+        const int node = (m0 + x) * p.npt + r / p.G;
         const int head = g * p.G + r % p.G;
         const bool valid_row = node < n_end;
         uint32_t a[8];
 #pragma unroll
         for (int w = 0; w < 8; ++w)
             a[w] = valid_row ? p.anc[static_cast<long long>(off + node) * 8 + w] : 0u;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t tS = tmem + 256 * x + lane_off, tO = tS + 128;
         const float sl2 = p.scale_log2;
         float m_run = -INFINITY, l_run = 0.0f;
         bool ok = true;
         for (int j = 0; j < nt && ok; ++j) {
-            const int sb = j & 1;
-            if (!mbar_wait_warp(&bars->s_full[sb], (j >> 1) & 1, p.err, abort)) { ok = false; break; }
+            if (!mbar_wait_warp(&bars->s_full[x], j & 1, p.err, abort)) { ok = false; break; }
             tc_fence_after();
-            float s[kTileN];
-            {
-                uint32_t v[kTileN / 32][32];
-#pragma unroll
-                for (int q = 0; q < kTileN / 32; ++q) tmem_ld32(tS0 + sb * 128 + lane_off + q * 32, v[q]);
+            const int slot0 = (t0 + j) * kTileN;
+            const bool tail = slot0 + kTileN > L;
+            // pass 1: row maximum (one 32-column chunk at a time keeps the
+            // register count low enough for 10 warps)
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+            for (int q = 0; q < kTileN / 32; ++q) {
+                const uint32_t vis = tail ? visible_bits(a, slot0 + q * 32 - L) : 0xFFFFFFFFu;
+                uint32_t v[32];
+                tmem_ld32(tS + q * 32, v);
                 tmem_wait_ld();
 #pragma unroll
-                for (int q = 0; q < kTileN / 32; ++q)
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) s[q * 32 + c] = __uint_as_float(v[q][c]);
-            }
-            tc_fence_before();
-            mbar_arrive(&bars->s_free[sb]);
-
-            const int slot0 = (t0 + j) * kTileN;
-            if (slot0 + kTileN > L) {  // tile reaches the tree tail: ancestor mask
-#pragma unroll
-                for (int q = 0; q < kTileN / 32; ++q) {
-                    const uint32_t vis = visible_bits(a, slot0 + q * 32 - L);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        if (!((vis >> c) & 1u)) s[q * 32 + c] = -INFINITY;
+                for (int c = 0; c < 32; ++c) {
+                    const float sv = ((vis >> c) & 1u) ? __uint_as_float(v[c]) : -INFINITY;
+                    m4[c & 3] = fmaxf(m4[c & 3], sv);
                 }
             }
-            float mx;
-            {
-                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-                for (int c = 0; c < kTileN; c += 4) {
-                    m4[0] = fmaxf(m4[0], s[c]);
-                    m4[1] = fmaxf(m4[1], s[c + 1]);
-                    m4[2] = fmaxf(m4[2], s[c + 2]);
-                    m4[3] = fmaxf(m4[3], s[c + 3]);
-                }
-                mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-            }
+            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
             const float mx_s = mx * sl2;
             bool resc = false;
             float factor = 1.0f;
@@ -376,57 +399,56 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 m_run = m_new;
             }
             if (__any_sync(0xFFFFFFFFu, resc)) {
-                // O must hold PV(j-1) before it is rescaled
-                if (!mbar_wait_warp(&bars->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, p.err, abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll
+                // S_X(j) done implies PV_X(j-1) done: O_X is current
+#pragma unroll 1
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t v[32];
-                    tmem_ld32(tO + lane_off + q * 32, v);
+                    tmem_ld32(tO + q * 32, v);
                     tmem_wait_ld();
 #pragma unroll
                     for (int c = 0; c < 32; ++c)
                         v[c] = __float_as_uint(__uint_as_float(v[c]) * (resc ? factor : 1.0f));
-                    tmem_st32(tO + lane_off + q * 32, v);
+                    tmem_st32(tO + q * 32, v);
                 }
                 tmem_wait_st();
             }
-            // P buffer sb is free once PV(j-2) has completed
-            if (j >= 2 && !mbar_wait_warp(&bars->pv_done[sb], ((j - 2) >> 1) & 1, p.err, abort)) {
-                ok = false;
-                break;
-            }
+            // pass 2: P = exp2(s*scale*log2e - m), written over S (bf16 pairs);
+            // quarter q writes P columns [16q, 16q+16), already read
             const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
             float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+            for (int q = 0; q < kTileN / 32; ++q) {
+                const uint32_t vis = tail ? visible_bits(a, slot0 + q * 32 - L) : 0xFFFFFFFFu;
+                uint32_t v[32];
+                tmem_ld32(tS + q * 32, v);
+                tmem_wait_ld();
+                uint32_t pr[16];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t pr[32];
-#pragma unroll
-                for (int c2 = 0; c2 < 32; ++c2) {
-                    const float p0 = ex2_approx(fmaf(s[h * 64 + 2 * c2], sl2, -m_use));
-                    const float p1 = ex2_approx(fmaf(s[h * 64 + 2 * c2 + 1], sl2, -m_use));
+                for (int c2 = 0; c2 < 16; ++c2) {
+                    const int c = 2 * c2;
+                    const float s0 = ((vis >> c) & 1u) ? __uint_as_float(v[c]) : -INFINITY;
+                    const float s1 = ((vis >> (c + 1)) & 1u) ? __uint_as_float(v[c + 1]) : -INFINITY;
+                    const float p0 = ex2_approx(fmaf(s0, sl2, -m_use));
+                    const float p1 = ex2_approx(fmaf(s1, sl2, -m_use));
                     l4[c2 & 3] += p0 + p1;
                     pr[c2] = pack_bf16x2(p0, p1);
                 }
-                tmem_st32(tP0 + sb * 64 + lane_off + h * 32, pr);
+                tmem_st16(tS + q * 16, pr);
             }
             l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(&bars->p_full[sb]);
+            mbar_arrive(&bars->p_full[x]);
         }
         // epilogue
-        if (ok && mbar_wait_warp(&bars->pv_done[(nt - 1) & 1], ((nt - 1) >> 1) & 1, p.err, abort)) {
+        if (ok && mbar_wait_warp(&bars->o_final[x], 0, p.err, abort)) {
             tc_fence_after();
             const long long rowid = static_cast<long long>(off + node) * p.Hq + head;
             const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-#pragma unroll
+#pragma unroll 1
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t v[32];
-                tmem_ld32(tO + lane_off + q * 32, v);
+                tmem_ld32(tO + q * 32, v);
                 tmem_wait_ld();
                 if (valid_row) {
                     if (p.splits == 1) {
@@ -460,7 +482,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -486,8 +508,7 @@ __global__ void __launch_bounds__(128)
         static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE)
         return;  // reported by the main kernel
     const int node = n - off;
-    const int m = node / p.npt;
-    const int valid_end = L + min(B, (m + 1) * p.npt);
+    const int valid_end = unit_valid_end(L, B, (node / p.npt) >> 1, p.npt);
     const long long rowid = static_cast<long long>(n) * p.Hq + h;
     float M = -INFINITY;
     int ns = 0;
@@ -543,7 +564,7 @@ AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int d
     pl.mtiles = (max_tree + pl.rows_per_tile_nodes - 1) / pl.rows_per_tile_nodes;
     pl.splits = 1;
     if (dtype == JT_DTYPE_BF16) {
-        const long long units = static_cast<long long>(nseq) * Hkv * pl.mtiles;
+        const long long units = static_cast<long long>(nseq) * Hkv * ((pl.mtiles + 1) / 2);
         const int sms = device_sm_count();
         const int tmax = (max_pages * JT_PAGE_SIZE + kTileN - 1) / kTileN;
         if (units > 0 && units < sms) {
@@ -638,7 +659,7 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    dim3 grid(plan.mtiles * plan.splits, Hkv, nseq);
+    dim3 grid(((plan.mtiles + 1) / 2) * plan.splits, Hkv, nseq);
     tree_attn_tc_kernel<D><<<grid, kAttnThreads, SL::kAlloc, st>>>(tq, tk, tv, prm);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess || plan.splits == 1) return e;
