@@ -118,6 +118,76 @@ __device__ __forceinline__ uint32_t visible_bits(const uint32_t (&a)[8], int rel
     return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
 }
 
+// Row maximum of a 128-column S tile (raw scores), two 64-column halves, one
+// TMEM round trip each.  MASKED applies the visibility of tree-relative key
+// positions rel0 + c.
+template <bool MASKED>
+__device__ __forceinline__ float row_max_tile(uint32_t tS, const uint32_t (&a)[8], int rel0) {
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tS + h * 64, v0);
+        tmem_ld32(tS + h * 64 + 32, v1);
+        tmem_wait_ld();
+        uint32_t vis0 = 0xFFFFFFFFu, vis1 = 0xFFFFFFFFu;
+        if (MASKED) {
+            vis0 = visible_bits(a, rel0 + h * 64);
+            vis1 = visible_bits(a, rel0 + h * 64 + 32);
+        }
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            float s0 = __uint_as_float(v0[c]), s1 = __uint_as_float(v1[c]);
+            if (MASKED) {
+                if (!((vis0 >> c) & 1u)) s0 = -INFINITY;
+                if (!((vis1 >> c) & 1u)) s1 = -INFINITY;
+            }
+            m4[c & 3] = fmaxf(m4[c & 3], fmaxf(s0, s1));
+        }
+    }
+    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+}
+
+// P = exp2(s * sl2 - m) for the 128 columns of S, packed to bf16 pairs and
+// written over the first 64 columns of S (half h writes P columns
+// [32h, 32h+32), which this thread has already read); row sums into l4.
+template <bool MASKED>
+__device__ __forceinline__ void exp_tile(uint32_t tS, const uint32_t (&a)[8], int rel0, float sl2,
+                                         float m, float (&l4)[4]) {
+#pragma unroll 1
+    for (int h = 0; h < 2; ++h) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tS + h * 64, v0);
+        tmem_ld32(tS + h * 64 + 32, v1);
+        tmem_wait_ld();
+        uint32_t vis0 = 0xFFFFFFFFu, vis1 = 0xFFFFFFFFu;
+        if (MASKED) {
+            vis0 = visible_bits(a, rel0 + h * 64);
+            vis1 = visible_bits(a, rel0 + h * 64 + 32);
+        }
+        uint32_t p0[16], p1[16];
+#pragma unroll
+        for (int c2 = 0; c2 < 16; ++c2) {
+            const int c = 2 * c2;
+            float a0 = __uint_as_float(v0[c]), a1 = __uint_as_float(v0[c + 1]);
+            float b0 = __uint_as_float(v1[c]), b1 = __uint_as_float(v1[c + 1]);
+            if (MASKED) {
+                if (!((vis0 >> c) & 1u)) a0 = -INFINITY;
+                if (!((vis0 >> (c + 1)) & 1u)) a1 = -INFINITY;
+                if (!((vis1 >> c) & 1u)) b0 = -INFINITY;
+                if (!((vis1 >> (c + 1)) & 1u)) b1 = -INFINITY;
+            }
+            const float ea0 = ex2_approx(fmaf(a0, sl2, -m)), ea1 = ex2_approx(fmaf(a1, sl2, -m));
+            const float eb0 = ex2_approx(fmaf(b0, sl2, -m)), eb1 = ex2_approx(fmaf(b1, sl2, -m));
+            l4[c2 & 3] += (ea0 + ea1) + (eb0 + eb1);
+            p0[c2] = pack_bf16x2(ea0, ea1);
+            p1[c2] = pack_bf16x2(eb0, eb1);
+        }
+        tmem_st16(tS + h * 32, p0);
+        tmem_st16(tS + h * 32 + 16, p1);
+    }
+}
+
 // Tile range [t0, t0 + count) of split sp for a unit whose needed keys end
 // at valid_end; returns the count.
 __device__ __forceinline__ int split_range(int valid_end, int splits, int sp, int& t0) {
@@ -368,22 +438,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             const int slot0 = (t0 + j) * kTileN;
             const bool tail = slot0 + kTileN > L;
-            // pass 1: row maximum (one 32-column chunk at a time keeps the
-            // register count low enough for 10 warps)
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-            for (int q = 0; q < kTileN / 32; ++q) {
-                const uint32_t vis = tail ? visible_bits(a, slot0 + q * 32 - L) : 0xFFFFFFFFu;
-                uint32_t v[32];
-                tmem_ld32(tS + q * 32, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const float sv = ((vis >> c) & 1u) ? __uint_as_float(v[c]) : -INFINITY;
-                    m4[c & 3] = fmaxf(m4[c & 3], sv);
-                }
-            }
-            const float mx = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+            // pass 1: row maximum; tiles inside the prefix need no mask
+            const float mx = tail ? row_max_tile<true>(tS, a, slot0 - L) : row_max_tile<false>(tS, a, 0);
             const float mx_s = mx * sl2;
             bool resc = false;
             float factor = 1.0f;
@@ -412,29 +468,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 tmem_wait_st();
             }
-            // pass 2: P = exp2(s*scale*log2e - m), written over S (bf16 pairs);
-            // quarter q writes P columns [16q, 16q+16), already read
+            // pass 2: P = exp2(s*scale*log2e - m), written over S (bf16 pairs)
             const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
             float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
-            for (int q = 0; q < kTileN / 32; ++q) {
-                const uint32_t vis = tail ? visible_bits(a, slot0 + q * 32 - L) : 0xFFFFFFFFu;
-                uint32_t v[32];
-                tmem_ld32(tS + q * 32, v);
-                tmem_wait_ld();
-                uint32_t pr[16];
-#pragma unroll
-                for (int c2 = 0; c2 < 16; ++c2) {
-                    const int c = 2 * c2;
-                    const float s0 = ((vis >> c) & 1u) ? __uint_as_float(v[c]) : -INFINITY;
-                    const float s1 = ((vis >> (c + 1)) & 1u) ? __uint_as_float(v[c + 1]) : -INFINITY;
-                    const float p0 = ex2_approx(fmaf(s0, sl2, -m_use));
-                    const float p1 = ex2_approx(fmaf(s1, sl2, -m_use));
-                    l4[c2 & 3] += p0 + p1;
-                    pr[c2] = pack_bf16x2(p0, p1);
-                }
-                tmem_st16(tS + q * 16, pr);
-            }
+            if (tail) exp_tile<true>(tS, a, slot0 - L, sl2, m_use, l4);
+            else exp_tile<false>(tS, a, 0, sl2, m_use, l4);
             l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             tmem_wait_st();
             tc_fence_before();
