@@ -117,6 +117,33 @@ jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
                         uint32_t* anc, void* ws, size_t ws_bytes, jt_stream_t stream);
 
 /*
+ * jt_tree_build_noalloc -- jt_tree_build with no caller workspace and no
+ * allocation.  The pages have no counterpart: this entry point exists for
+ * host integrations that cannot give the library device memory (memory owned
+ * by another allocator, or a decode loop that must not call cudaMalloc, which
+ * synchronises the device).
+ *   Arguments, outputs and results are those of jt_tree_build; the scratch
+ *   is a fixed device array of JT_NOALLOC_SCRATCH_BYTES inside the library.
+ *   It must hold 256 bytes of header plus the build's tables, i.e.
+ *   jt_workspace_size(JT_OP_TREE_BUILD, nseq, N, W, V) bytes; a larger need
+ *   (about nseq*N > 2400 rows at V = 151936, W = 4) returns
+ *   JT_ERR_WORKSPACE before anything is enqueued.
+ *   sync_check: 0 = asynchronous, like jt_tree_build (device-side errors are
+ *   then not reported); nonzero = synchronise `stream` after the launch and
+ *   return the device-side status (JT_ERR_INVALID / JT_ERR_TIMEOUT).
+ *   The first call on a device looks up the array's address
+ *   (cudaGetSymbolAddress); make it before any stream capture.
+ *   There is ONE scratch array per device: calls whose executions overlap on
+ *   the device (different streams, or different host threads without
+ *   ordering) race on it and give wrong trees.  Serialise them.
+ */
+#define JT_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+jt_status jt_tree_build_noalloc(const float* draft_logits, const int32_t* root_token,
+                                const int32_t* tree_off, int nseq, int N, int W, int64_t V,
+                                int total_nodes, int32_t* parent, int32_t* token, int32_t* depth,
+                                uint32_t* anc, int sync_check, jt_stream_t stream);
+
+/*
  * jt_tree_topw -- step 1 of jt_tree_build alone, on `rows` rows of V fp32
  * logits: tok int32 [rows, W], lp fp64 [rows, W] (= z[tok] - lse), lse fp64
  * [rows].  Same kernels as jt_tree_build.

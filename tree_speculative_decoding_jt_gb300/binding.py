@@ -26,7 +26,8 @@ JT_MAX_TREE, JT_MAX_W, JT_MAX_N, JT_PAGE_SIZE = 256, 8, 64, 16
 
 # every symbol include/jt.h declares
 EXPORTS = ("jt_workspace_size", "jt_tree_build", "jt_tree_topw", "jt_tree_expand",
-           "jt_tree_attn_paged", "jt_verify_accept", "jt_check", "jt_status_str", "jt_version")
+           "jt_tree_attn_paged", "jt_verify_accept", "jt_check", "jt_status_str", "jt_version",
+           "jt_tree_build_noalloc")
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +59,7 @@ def load(build_if_missing: bool = True):
         lib.jt_workspace_size.restype = sz
         lib.jt_tree_build.argtypes = [P, P, P, i32, i32, i32, i64, i32, P, P, P, P, P, sz, P]
         lib.jt_tree_topw.argtypes = [P, i64, i64, i32, P, P, P, P, sz, P]
+        lib.jt_tree_build_noalloc.argtypes = [P, P, P, i32, i32, i32, i64, i32, P, P, P, P, i32, P]
         lib.jt_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz, P]
         lib.jt_tree_attn_paged.argtypes = [P, P, P, i32, P, i32, i32, P, P, P, i32, i32, i32, i32,
                                            i32, i32, i32, f32, P, P, P, sz, P]
@@ -67,7 +69,7 @@ def load(build_if_missing: bool = True):
         lib.jt_status_str.restype = ctypes.c_char_p
         lib.jt_version.argtypes = []
         for name in ("jt_tree_build", "jt_tree_topw", "jt_tree_expand", "jt_tree_attn_paged",
-                     "jt_verify_accept", "jt_check", "jt_version"):
+                     "jt_verify_accept", "jt_check", "jt_version", "jt_tree_build_noalloc"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -149,6 +151,33 @@ def jt_tree_build(draft_logits, root_token, tree_off, W, total_nodes=None, out=N
                            total_nodes, _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc),
                            _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "jt_tree_build")
+    return parent, token, depth, anc
+
+
+def jt_tree_build_noalloc(draft_logits, root_token, tree_off, W, total_nodes=None, out=None,
+                          sync_check=True, stream=None):
+    """jt_tree_build with the library's fixed device scratch instead of a
+    workspace (no allocation inside the library; the output tensors are the
+    caller's).  Calls whose executions overlap on one device race on that
+    scratch.  Returns (parent, token, depth, anc) on the device."""
+    lib = load()
+    _need(draft_logits, "draft_logits", torch.float32)
+    _need(root_token, "root_token", torch.int32)
+    _need(tree_off, "tree_off", torch.int32)
+    nseq, N, V = draft_logits.shape
+    if total_nodes is None:
+        total_nodes = int(tree_off[-1].item())
+    dev = draft_logits.device
+    if out is None:
+        out = (torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty((total_nodes, 8), dtype=torch.int32, device=dev))
+    parent, token, depth, anc = out
+    rc = lib.jt_tree_build_noalloc(_ptr(draft_logits), _ptr(root_token), _ptr(tree_off), nseq, N, W,
+                                   V, total_nodes, _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc),
+                                   1 if sync_check else 0, _stream(stream))
+    _check(rc, "jt_tree_build_noalloc")
     return parent, token, depth, anc
 
 
