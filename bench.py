@@ -455,8 +455,11 @@ def main():
                          f"attention for {len(nodes)} of {total} nodes ({secs:.1f} s, "
                          f"single-threaded C, fp64)"}
 
-    launches_per_step = 2 + (2 if jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq,
-                                                       Hkv, D, max_pages, max_tree) > 256 else 1) + 2
+    # tree build: top-W partials, row merge, expansion; attention: main
+    # kernel (+ split combine when the plan splits the keys); two acceptances
+    attn_split = jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq, Hkv, D,
+                                      max_pages, max_tree) > 256
+    launches_per_step = 3 + (2 if attn_split else 1) + 2
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -155,8 +155,7 @@ jt_status jt_tree_topw(const float* logits, int64_t rows, int64_t V, int W, int3
  * jt_tree_expand -- step 2 of jt_tree_build alone, from given per-depth
  * tables tok int32 [nseq, N, W] and lp fp64 [nseq, N, W] (row d = candidates
  * of depth d+1, best first).  Same outputs as jt_tree_build.  Needs a
- * workspace of jt_workspace_size(JT_OP_VERIFY_ACCEPT, nseq, ...) or more
- * (only its error word is used).
+ * workspace of at least 256 bytes (only its error word is used).
  */
 jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
                          const int32_t* tree_off, int nseq, int N, int W, int total_nodes,
