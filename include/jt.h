@@ -6,7 +6,8 @@
  * Conventions shared by every entry point
  *  - Array arguments are DEVICE pointers owned by the caller, unless a
  *    comment says "host".  The library allocates no memory and keeps no
- *    state besides a per-device cache of device properties.
+ *    state besides a per-device cache of device properties (and the fixed
+ *    scratch array behind jt_tree_build_noalloc).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Outputs are valid once the stream reaches the call.
  *  - Arguments checkable on the host (null pointers, sizes, limits, the
@@ -20,8 +21,16 @@
  *    that flag into a status.  Device-side waits are bounded in time; a wait
  *    that runs out raises JT_ERR_TIMEOUT the same way.
  *  - Every call needs a caller-allocated device workspace of at least
- *    jt_workspace_size(...) bytes, 256-byte aligned.  Calls that share one
- *    workspace must not overlap on the device.
+ *    jt_workspace_size(...) bytes, 256-byte aligned, whose first 256 bytes
+ *    (the header holding the error word) are ZERO before its first use
+ *    (e.g. one cudaMemset after allocating it).  Calls never clear the
+ *    header themselves: a raised flag stays set until jt_check() reads and
+ *    clears it.  Calls that share one workspace must not overlap on the
+ *    device.
+ *  - Kernels are launched with programmatic stream serialisation: a kernel
+ *    of the library may become resident while the previous kernel of the
+ *    stream drains, and waits for that kernel's completion before it reads
+ *    or writes global memory.
  *
  * Tree layout shared by the three steps
  *  - nseq sequences; sequence b owns global node indices

@@ -116,9 +116,10 @@ def jt_workspace_size(op, nseq=0, N=0, W=0, V=0, total_nodes=0, Hq=0, Hkv=0, D=0
 
 
 def workspace(nbytes: int, device=None) -> torch.Tensor:
-    """A device buffer usable as a libjt workspace (torch allocations are
-    256-byte aligned)."""
-    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+    """A zeroed device buffer usable as a libjt workspace (torch allocations
+    are 256-byte aligned; the library needs the header zero before first
+    use)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
 
 
 def jt_check(ws: torch.Tensor, stream=None) -> None:

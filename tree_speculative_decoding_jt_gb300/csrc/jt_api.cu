@@ -94,9 +94,7 @@ jt_status jt_tree_topw(const float* logits, int64_t rows, int64_t V, int W, int3
     if (s != JT_OK) return s;
     if (rows == 0) return JT_OK;
     char* base = static_cast<char*>(ws);
-    cudaError_t e = cudaMemsetAsync(base, 0, sizeof(WsHeader), stream);
-    if (e == cudaSuccess)
-        e = tree_topw_launch(logits, rows, V, W, tok, lp, lse, base + kWsHeader, stream);
+    cudaError_t e = tree_topw_launch(logits, rows, V, W, tok, lp, lse, base + kWsHeader, stream);
     return from_cuda(e);
 }
 
@@ -113,9 +111,7 @@ jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
     jt_status s = check_ws(ws, ws_bytes, build_ws(nseq, N, W, V));
     if (s != JT_OK) return s;
     char* base = static_cast<char*>(ws);
-    cudaError_t e = cudaMemsetAsync(base, 0, sizeof(WsHeader), stream);
-    if (e == cudaSuccess)
-        e = tree_build_launch(draft_logits, root_token, tree_off, nseq, total_nodes, N, W, V, parent, token,
+    cudaError_t e = tree_build_launch(draft_logits, root_token, tree_off, nseq, total_nodes, N, W, V, parent, token,
                               depth, anc, base + kWsHeader, reinterpret_cast<uint32_t*>(base),
                               stream);
     return from_cuda(e);
@@ -132,9 +128,7 @@ jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* ro
     jt_status s = check_ws(ws, ws_bytes, kWsHeader);
     if (s != JT_OK) return s;
     char* base = static_cast<char*>(ws);
-    cudaError_t e = cudaMemsetAsync(base, 0, sizeof(WsHeader), stream);
-    if (e == cudaSuccess)
-        e = tree_expand_launch(tok, lp, root_token, tree_off, nseq, total_nodes, N, W, parent, token, depth, anc,
+    cudaError_t e = tree_expand_launch(tok, lp, root_token, tree_off, nseq, total_nodes, N, W, parent, token, depth, anc,
                                reinterpret_cast<uint32_t*>(base), stream);
     return from_cuda(e);
 }
@@ -166,8 +160,7 @@ jt_status jt_tree_attn_paged(const void* q, const void* k_cache, const void* v_c
     if (s != JT_OK) return s;
     char* base = static_cast<char*>(ws);
     uint32_t* err = reinterpret_cast<uint32_t*>(base);
-    cudaError_t e = cudaMemsetAsync(base, 0, sizeof(WsHeader), stream);
-    if (e != cudaSuccess) return from_cuda(e);
+    cudaError_t e;
     if (dtype == JT_DTYPE_BF16)
         e = tree_attn_bf16_launch(q, k_cache, v_cache, block_table, max_pages, num_pages,
                                   prefix_len, tree_off, anc, nseq, total_nodes, Hq, Hkv, D, scale,

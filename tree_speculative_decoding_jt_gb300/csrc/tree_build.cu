@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(kTopwThreads)
     topw_partial_kernel(const float* __restrict__ z, long long V, int splits, ExpTable tab,
                         float* __restrict__ part_v, int* __restrict__ part_id,
                         float* __restrict__ part_m, float2* __restrict__ part_s) {
+    pdl_wait();     // inputs may come from the previous kernel of the stream
+    pdl_trigger();
     constexpr int CH = kTopwThreads * kTopwPerThread;
     __shared__ float s_thi[64], s_tlo[64];
     __shared__ float s_wv[kTopwThreads / 32][W];
@@ -367,6 +369,8 @@ __global__ void __launch_bounds__(256)
                       const float* __restrict__ part_m, const float2* __restrict__ part_s,
                       int splits, long long rows, ExpTable tab, int32_t* __restrict__ tok_out,
                       double* __restrict__ lp_out, double* __restrict__ lse_out) {
+    pdl_wait();     // inputs may come from the previous kernel of the stream
+    pdl_trigger();
     __shared__ float s_thi[64], s_tlo[64];
     if (threadIdx.x < 64) {
         s_thi[threadIdx.x] = tab.hi[threadIdx.x];
@@ -487,6 +491,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                   const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
                   int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
+    pdl_wait();     // inputs may come from the previous kernel of the stream
+    pdl_trigger();
     extern __shared__ __align__(16) unsigned char dsm[];
     unsigned long long* kb1[2];
     unsigned long long* kb2[2];
@@ -502,7 +508,6 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     __shared__ double s_lp[JT_MAX_N * W];
     __shared__ short s_front[JT_MAX_TREE];
     __shared__ int s_warp[kExpandThreads / 32];
-    __shared__ int s_nf;
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
@@ -727,12 +732,10 @@ static cudaError_t launch_topw_partial(const float* z, long long rows, long long
     const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
     dim3 grid(t.splits, static_cast<unsigned>(rows));
     if (vec)
-        topw_partial_kernel<W, true><<<grid, kTopwThreads, 0, st>>>(z, V, t.splits, tab, t.v, t.id,
-                                                                     t.m, t.s);
-    else
-        topw_partial_kernel<W, false><<<grid, kTopwThreads, 0, st>>>(z, V, t.splits, tab, t.v, t.id,
-                                                                      t.m, t.s);
-    return cudaGetLastError();
+        return launch_pdl(topw_partial_kernel<W, true>, grid, dim3(kTopwThreads), 0, st, 0, z, V,
+                          t.splits, tab, t.v, t.id, t.m, t.s);
+    return launch_pdl(topw_partial_kernel<W, false>, grid, dim3(kTopwThreads), 0, st, 0, z, V, t.splits,
+                      tab, t.v, t.id, t.m, t.s);
 }
 
 template <int W>
@@ -743,9 +746,8 @@ static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t
     if (e != cudaSuccess) return e;
     const long long warps_per_block = 8;
     const unsigned blocks = static_cast<unsigned>((rows + warps_per_block - 1) / warps_per_block);
-    topw_merge_kernel<W><<<blocks, 256, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, rows, exp_table(),
-                                                  tok, lp, lse);
-    return cudaGetLastError();
+    return launch_pdl(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
+                      t.splits, rows, exp_table(), tok, lp, lse);
 }
 
 template <int W>
@@ -759,17 +761,14 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
         cudaError_t e = launch_topw_partial<W>(z, rows, V, t, st);
         if (e != cudaSuccess) return e;
         const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-        topw_merge_kernel<W><<<blocks, 256, 0, st>>>(t.v, t.id, t.m, t.s, t.splits, rows,
-                                                      exp_table(), t.tok, t.lp, t.lse);
-        e = cudaGetLastError();
+        e = launch_pdl(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
+                       t.splits, rows, exp_table(), t.tok, t.lp, t.lse);
         if (e != cudaSuccess) return e;
     }
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(t.tok, t.lp, root_token, tree_off,
-                                                                  total_nodes, N, parent, token,
-                                                                  depth, anc, err);
-    return cudaGetLastError();
+    return launch_pdl(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, t.tok, t.lp,
+                      root_token, tree_off, total_nodes, N, parent, token, depth, anc, err);
 }
 
 template <int W>
@@ -779,10 +778,8 @@ static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_
                               cudaStream_t st) {
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    expand_kernel<W><<<nseq, kExpandThreads, kExpandSmem, st>>>(tok, lp,
-                                                       root_token, tree_off, total_nodes, N, parent, token,
-                                                       depth, anc, err);
-    return cudaGetLastError();
+    return launch_pdl(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, tok, lp,
+                      root_token, tree_off, total_nodes, N, parent, token, depth, anc, err);
 }
 
 #define JT_DISPATCH_W(W, CALL)           \

@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(kAccThreads)
                           int total_nodes, int N, long long V, int rule, double log_t,
                           int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
                           int32_t* __restrict__ bonus, uint32_t* err) {
+    pdl_wait();     // inputs may come from the previous kernel of the stream
+    pdl_trigger();
     __shared__ unsigned long long s_part[JT_MAX_TREE];    // this CTA's key per frontier slot
     __shared__ unsigned long long s_rowkey[JT_MAX_TREE];  // rank 0: combined key per slot
     __shared__ int s_front[2][JT_MAX_TREE];               // frontier lists (node ids, ascending)
@@ -252,20 +254,9 @@ static cudaError_t launch_accept(const float* z, const int32_t* parent, const in
                                  int total_nodes, int rule, double log_t, int32_t* accept_len,
                                  int32_t* path, int32_t* bonus, uint32_t* err, cudaStream_t st) {
     const int cs = accept_cluster_size<VEC>();
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(nseq) * cs);
-    cfg.blockDim = dim3(kAccThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = st;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = cs;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, accept_cluster_kernel<VEC>, z, parent, token, tree_off,
-                              total_nodes, N, V, rule, log_t, accept_len, path, bonus, err);
+    return launch_pdl(accept_cluster_kernel<VEC>, dim3(static_cast<unsigned>(nseq) * cs), dim3(kAccThreads),
+                      0, st, static_cast<unsigned>(cs), z, parent, token, tree_off, total_nodes, N, V, rule,
+                      log_t, accept_len, path, bonus, err);
 }
 
 cudaError_t verify_accept_launch(const float* z, const int32_t* parent, const int32_t* token,
@@ -273,8 +264,6 @@ cudaError_t verify_accept_launch(const float* z, const int32_t* parent, const in
                                  int total_nodes, int rule, double log_t, int32_t* accept_len,
                                  int32_t* path, int32_t* bonus, char* ws, cudaStream_t st) {
     uint32_t* err = reinterpret_cast<uint32_t*>(ws);
-    cudaError_t e = cudaMemsetAsync(ws, 0, sizeof(WsHeader), st);
-    if (e != cudaSuccess) return e;
     const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
     if (vec)
         return launch_accept<true>(z, parent, token, tree_off, nseq, N, V, total_nodes, rule, log_t,
