@@ -118,73 +118,55 @@ __device__ __forceinline__ uint32_t visible_bits(const uint32_t (&a)[8], int rel
     return sh ? ((lo >> sh) | (hi << (32 - sh))) : lo;
 }
 
-// Row maximum of a 128-column S tile (raw scores), two 64-column halves, one
-// TMEM round trip each.  MASKED applies the visibility of tree-relative key
-// positions rel0 + c.
-template <bool MASKED>
-__device__ __forceinline__ float row_max_tile(uint32_t tS, const uint32_t (&a)[8], int rel0) {
-    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tS + h * 64, v0);
-        tmem_ld32(tS + h * 64 + 32, v1);
-        tmem_wait_ld();
-        uint32_t vis0 = 0xFFFFFFFFu, vis1 = 0xFFFFFFFFu;
-        if (MASKED) {
-            vis0 = visible_bits(a, rel0 + h * 64);
-            vis1 = visible_bits(a, rel0 + h * 64 + 32);
-        }
+// The 128 fp32 scores of this thread's S row, held in registers as four
+// 32-column chunks (one TMEM round trip per tile).
+struct SRow {
+    uint32_t c[4][32];
+};
+
+__device__ __forceinline__ void load_srow(uint32_t tS, SRow& s) {
+    tmem_ld32(tS, s.c[0]);
+    tmem_ld32(tS + 32, s.c[1]);
+    tmem_ld32(tS + 64, s.c[2]);
+    tmem_ld32(tS + 96, s.c[3]);
+    tmem_wait_ld();
+}
+
+// Columns whose key (tree-relative position rel0 + c) is not visible -> -inf.
+__device__ __forceinline__ void mask_srow(SRow& s, const uint32_t (&a)[8], int rel0) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            float s0 = __uint_as_float(v0[c]), s1 = __uint_as_float(v1[c]);
-            if (MASKED) {
-                if (!((vis0 >> c) & 1u)) s0 = -INFINITY;
-                if (!((vis1 >> c) & 1u)) s1 = -INFINITY;
-            }
-            m4[c & 3] = fmaxf(m4[c & 3], fmaxf(s0, s1));
-        }
+    for (int q = 0; q < 4; ++q) {
+        const uint32_t vis = visible_bits(a, rel0 + 32 * q);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            if (!((vis >> c) & 1u)) s.c[q][c] = __float_as_uint(-INFINITY);
     }
+}
+
+__device__ __forceinline__ float max_srow(const SRow& s) {
+    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+#pragma unroll
+        for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(s.c[q][c]));
     return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
 }
 
-// P = exp2(s * sl2 - m) for the 128 columns of S, packed to bf16 pairs and
-// written over the first 64 columns of S (half h writes P columns
-// [32h, 32h+32), which this thread has already read); row sums into l4.
-template <bool MASKED>
-__device__ __forceinline__ void exp_tile(uint32_t tS, const uint32_t (&a)[8], int rel0, float sl2,
-                                         float m, float (&l4)[4]) {
-#pragma unroll 1
-    for (int h = 0; h < 2; ++h) {
-        uint32_t v0[32], v1[32];
-        tmem_ld32(tS + h * 64, v0);
-        tmem_ld32(tS + h * 64 + 32, v1);
-        tmem_wait_ld();
-        uint32_t vis0 = 0xFFFFFFFFu, vis1 = 0xFFFFFFFFu;
-        if (MASKED) {
-            vis0 = visible_bits(a, rel0 + h * 64);
-            vis1 = visible_bits(a, rel0 + h * 64 + 32);
-        }
-        uint32_t p0[16], p1[16];
+// P = exp2(s * sl2 - m), packed to bf16 pairs into the first 64 columns of
+// the S region (the scores are already in registers); row sums into l4.
+__device__ __forceinline__ void exp_store_srow(const SRow& s, uint32_t tS, float sl2, float m,
+                                               float (&l4)[4]) {
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t pk[16];
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
-            const int c = 2 * c2;
-            float a0 = __uint_as_float(v0[c]), a1 = __uint_as_float(v0[c + 1]);
-            float b0 = __uint_as_float(v1[c]), b1 = __uint_as_float(v1[c + 1]);
-            if (MASKED) {
-                if (!((vis0 >> c) & 1u)) a0 = -INFINITY;
-                if (!((vis0 >> (c + 1)) & 1u)) a1 = -INFINITY;
-                if (!((vis1 >> c) & 1u)) b0 = -INFINITY;
-                if (!((vis1 >> (c + 1)) & 1u)) b1 = -INFINITY;
-            }
-            const float ea0 = ex2_approx(fmaf(a0, sl2, -m)), ea1 = ex2_approx(fmaf(a1, sl2, -m));
-            const float eb0 = ex2_approx(fmaf(b0, sl2, -m)), eb1 = ex2_approx(fmaf(b1, sl2, -m));
-            l4[c2 & 3] += (ea0 + ea1) + (eb0 + eb1);
-            p0[c2] = pack_bf16x2(ea0, ea1);
-            p1[c2] = pack_bf16x2(eb0, eb1);
+            const float e0 = ex2_approx(fmaf(__uint_as_float(s.c[q][2 * c2]), sl2, -m));
+            const float e1 = ex2_approx(fmaf(__uint_as_float(s.c[q][2 * c2 + 1]), sl2, -m));
+            l4[c2 & 3] += e0 + e1;
+            pk[c2] = pack_bf16x2(e0, e1);
         }
-        tmem_st16(tS + h * 32, p0);
-        tmem_st16(tS + h * 32 + 16, p1);
+        tmem_st16(tS + 16 * q, pk);
     }
 }
 
@@ -204,7 +186,8 @@ __device__ __forceinline__ int unit_valid_end(int L, int B, int mp, int npt) {
     return L + min(B, (2 * mp + 2) * npt);
 }
 
-// S_x = Q_x K^T for the K tile in stage st (8 or 4 MMAs of K=16).
+// S_x = Q_x K^T for the K tile in stage st (8 or 4 MMAs of K=16).  Called by
+// the whole MMA warp; one elected lane issues.
 template <int D>
 __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t aQ, uint32_t aK, int x, int st) {
     using SL = SmemLayout<D>;
@@ -214,11 +197,13 @@ __device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t aQ, uint32_t aK
         const uint32_t koff = (kk >> 2) * SL::kChunkBytes + (kk & 3) * 32;
         const uint64_t adesc = smem_desc_sw128(aQ + x * SL::kTileBytes + koff, 16, 1024);
         const uint64_t bdesc = smem_desc_sw128(aK + st * SL::kTileBytes + koff, 16, 1024);
-        mma_ss(tmem + 256 * x, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+        if (elect_one()) mma_ss(tmem + 256 * x, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
+        __syncwarp();
     }
 }
 
 // O_x (+)= P_x V for the V tile in stage st (P_x from TMEM, 8 MMAs of K=16).
+// Called by the whole MMA warp; one elected lane issues.
 template <int D>
 __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t aV, int x, int st, bool accumulate) {
     using SL = SmemLayout<D>;
@@ -226,9 +211,16 @@ __device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t aV, int x, int 
 #pragma unroll
     for (int kk = 0; kk < kTileN / 16; ++kk) {
         const uint64_t bdesc = smem_desc_sw128(aV + st * SL::kTileBytes + kk * 16 * 128, SL::kChunkBytes, 1024);
-        mma_ts(tmem + 256 * x + 128, tmem + 256 * x + kk * 8, bdesc, idesc,
-               (accumulate || kk > 0) ? 1u : 0u);
+        if (elect_one())
+            mma_ts(tmem + 256 * x + 128, tmem + 256 * x + kk * 8, bdesc, idesc, (accumulate || kk > 0) ? 1u : 0u);
+        __syncwarp();
     }
+}
+
+// tcgen05.commit from the elected lane (the lane that issued the MMAs).
+__device__ __forceinline__ void commit_warp(uint64_t* bar) {
+    if (elect_one()) mma_commit(bar);
+    __syncwarp();
 }
 
 // Page ids of 4 consecutive tiles (group g4): lane l holds page l%8 of tile
@@ -377,48 +369,48 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0) {
-            const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
-            const int nx = hasB ? 2 : 1;
-            bool ok = mbar_wait(&bars->q_full, 0, p.err, abort) &&
-                      mbar_wait(&bars->k_full[0], 0, p.err, abort);
-            if (ok) {
-                tc_fence_after();
-                for (int x = 0; x < nx; ++x) {
-                    issue_qk<D>(tmem, aQ, aK, x, 0);
-                    mma_commit(&bars->s_full[x]);
-                }
-                mma_commit(&bars->k_empty[0]);
+        // the whole warp runs this loop (uniform control flow, operands in
+        // uniform registers); one elected lane issues every tcgen05 op
+        const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+        const int nx = hasB ? 2 : 1;
+        bool ok = mbar_wait_warp(&bars->q_full, 0, p.err, abort) &&
+                  mbar_wait_warp(&bars->k_full[0], 0, p.err, abort);
+        if (ok) {
+            tc_fence_after();
+            for (int x = 0; x < nx; ++x) {
+                issue_qk<D>(tmem, aQ, aK, x, 0);
+                commit_warp(&bars->s_full[x]);
             }
-            for (int j = 0; ok && j < nt; ++j) {
-                const int st = j % kStages;
-                const bool more = j + 1 < nt;
-                for (int x = 0; ok && x < nx; ++x) {
-                    ok = mbar_wait(&bars->p_full[x], j & 1, p.err, abort);
-                    if (ok && x == 0)
-                        ok = (j == nt - 1) ? mbar_wait(&bars->v_last, 0, p.err, abort)
-                                           : mbar_wait(&bars->v_full[st], (j / kStages) & 1, p.err, abort);
+            commit_warp(&bars->k_empty[0]);
+        }
+        for (int j = 0; ok && j < nt; ++j) {
+            const int st = j % kStages;
+            const bool more = j + 1 < nt;
+            for (int x = 0; ok && x < nx; ++x) {
+                ok = mbar_wait_warp(&bars->p_full[x], j & 1, p.err, abort);
+                if (ok && x == 0)
+                    ok = (j == nt - 1) ? mbar_wait_warp(&bars->v_last, 0, p.err, abort)
+                                       : mbar_wait_warp(&bars->v_full[st], (j / kStages) & 1, p.err, abort);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv<D>(tmem, aV, x, st, j > 0);
+                if (x == nx - 1) commit_warp(&bars->v_empty[st]);
+                if (!more) {
+                    commit_warp(&bars->o_final[x]);
+                } else {
+                    if (x == 0) ok = mbar_wait_warp(&bars->k_full[(j + 1) % kStages],
+                                                    ((j + 1) / kStages) & 1, p.err, abort);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv<D>(tmem, aV, x, st, j > 0);
-                    if (x == nx - 1) mma_commit(&bars->v_empty[st]);
-                    if (!more) {
-                        mma_commit(&bars->o_final[x]);
-                    } else {
-                        if (x == 0) ok = mbar_wait(&bars->k_full[(j + 1) % kStages],
-                                                   ((j + 1) / kStages) & 1, p.err, abort);
-                        if (!ok) break;
-                        tc_fence_after();
-                        issue_qk<D>(tmem, aQ, aK, x, (j + 1) % kStages);
-                        mma_commit(&bars->s_full[x]);
-                        if (x == nx - 1) mma_commit(&bars->k_empty[(j + 1) % kStages]);
-                    }
+                    issue_qk<D>(tmem, aQ, aK, x, (j + 1) % kStages);
+                    commit_warp(&bars->s_full[x]);
+                    if (x == nx - 1) commit_warp(&bars->k_empty[(j + 1) % kStages]);
                 }
             }
-            // every MMA issued above completes before TMEM is released
-            mma_commit(&bars->mma_final);
-            mbar_wait(&bars->mma_final, 0, p.err, nullptr);
         }
+        // every MMA issued above completes before TMEM is released
+        commit_warp(&bars->mma_final);
+        mbar_wait_warp(&bars->mma_final, 0, p.err, nullptr);
     } else if (warp < 4 || hasB) {
         // ---------------------------------------------- softmax of tile X
         const int x = warp >> 2;
@@ -440,8 +432,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             const int slot0 = (t0 + j) * kTileN;
             const bool tail = slot0 + kTileN > L;
-            // pass 1: row maximum; tiles inside the prefix need no mask
-            const float mx = tail ? row_max_tile<true>(tS, a, slot0 - L) : row_max_tile<false>(tS, a, 0);
+            SRow sr;
+            load_srow(tS, sr);
+            if (tail) mask_srow(sr, a, slot0 - L);  // tiles inside the prefix need no mask
+            const float mx = max_srow(sr);
             const float mx_s = mx * sl2;
             bool resc = false;
             float factor = 1.0f;
@@ -456,8 +450,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 l_run *= factor;
                 m_run = m_new;
             }
+            // P = exp2(s*scale*log2e - m), written over S (bf16 pairs)
+            const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+            float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            exp_store_srow(sr, tS, sl2, m_use, l4);
+            l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             if (__any_sync(0xFFFFFFFFu, resc)) {
-                // S_X(j) done implies PV_X(j-1) done: O_X is current
+                // O_X from the earlier tiles, rescaled before PV_X(j) adds to it
+                // (S_X(j) done implies PV_X(j-1) done: O_X is current)
 #pragma unroll 1
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t v[32];
@@ -468,14 +468,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         v[c] = __float_as_uint(__uint_as_float(v[c]) * (resc ? factor : 1.0f));
                     tmem_st32(tO + q * 32, v);
                 }
-                tmem_wait_st();
             }
-            // pass 2: P = exp2(s*scale*log2e - m), written over S (bf16 pairs)
-            const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-            float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (tail) exp_tile<true>(tS, a, slot0 - L, sl2, m_use, l4);
-            else exp_tile<false>(tS, a, 0, sl2, m_use, l4);
-            l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(&bars->p_full[x]);
