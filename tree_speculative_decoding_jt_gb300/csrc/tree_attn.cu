@@ -186,35 +186,37 @@ __device__ __forceinline__ int unit_valid_end(int L, int B, int mp, int npt) {
     return L + min(B, (2 * mp + 2) * npt);
 }
 
-// S_x = Q_x K^T for the K tile in stage st (8 or 4 MMAs of K=16).  Called by
-// the whole MMA warp; one elected lane issues.
+// Operand descriptors are built once (dq: Q tile, dk / dv: K / V stage) and
+// stepped by adding the byte offset / 16 to the start-address field (the
+// field cannot carry: shared memory addresses stay below 256 KB).  The whole
+// MMA warp calls these; one elected lane issues, with as few instructions per
+// MMA as possible because the softmax warps compete for the same issue slots.
+
+// S (+)= Q K^T: 8 (D = 128) or 4 (D = 64) MMAs of K = 16.
 template <int D>
-__device__ __forceinline__ void issue_qk(uint32_t tmem, uint32_t aQ, uint32_t aK, int x, int st) {
+__device__ __forceinline__ void issue_qk(uint32_t tS, uint64_t dq, uint64_t dk) {
     using SL = SmemLayout<D>;
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kTileN, false);
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = (kk >> 2) * SL::kChunkBytes + (kk & 3) * 32;
-        const uint64_t adesc = smem_desc_sw128(aQ + x * SL::kTileBytes + koff, 16, 1024);
-        const uint64_t bdesc = smem_desc_sw128(aK + st * SL::kTileBytes + koff, 16, 1024);
-        if (elect_one()) mma_ss(tmem + 256 * x, adesc, bdesc, idesc, kk > 0 ? 1u : 0u);
-        __syncwarp();
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t ko = ((kk >> 2) * SL::kChunkBytes + (kk & 3) * 32) >> 4;
+            mma_ss(tS, dq + ko, dk + ko, idesc, kk > 0 ? 1u : 0u);
+        }
     }
+    __syncwarp();
 }
 
-// O_x (+)= P_x V for the V tile in stage st (P_x from TMEM, 8 MMAs of K=16).
-// Called by the whole MMA warp; one elected lane issues.
+// O (+)= P V with P (bf16 pairs) in the first 64 columns of S: 8 MMAs of K = 16.
 template <int D>
-__device__ __forceinline__ void issue_pv(uint32_t tmem, uint32_t aV, int x, int st, bool accumulate) {
-    using SL = SmemLayout<D>;
+__device__ __forceinline__ void issue_pv(uint32_t tS, uint64_t dv, bool accumulate) {
     constexpr uint32_t idesc = idesc_bf16_f32(kTileM, D, true);
+    if (elect_one()) {
 #pragma unroll
-    for (int kk = 0; kk < kTileN / 16; ++kk) {
-        const uint64_t bdesc = smem_desc_sw128(aV + st * SL::kTileBytes + kk * 16 * 128, SL::kChunkBytes, 1024);
-        if (elect_one())
-            mma_ts(tmem + 256 * x + 128, tmem + 256 * x + kk * 8, bdesc, idesc, (accumulate || kk > 0) ? 1u : 0u);
-        __syncwarp();
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ts(tS + 128, tS + kk * 8, dv + kk * ((16 * 128) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
     }
+    __syncwarp();
 }
 
 // tcgen05.commit from the elected lane (the lane that issued the MMAs).
@@ -371,14 +373,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // ------------------------------------------------------------ MMA
         // the whole warp runs this loop (uniform control flow, operands in
         // uniform registers); one elected lane issues every tcgen05 op
-        const uint32_t aQ = smem_u32(sQ), aK = smem_u32(sK), aV = smem_u32(sV);
+        using SLm = SmemLayout<D>;
+        const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+        const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+        const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), SLm::kChunkBytes, 1024);
+        constexpr uint32_t kTileStep = SLm::kTileBytes >> 4;  // one tile / stage in 16-byte units
         const int nx = hasB ? 2 : 1;
         bool ok = mbar_wait_warp(&bars->q_full, 0, p.err, abort) &&
                   mbar_wait_warp(&bars->k_full[0], 0, p.err, abort);
         if (ok) {
             tc_fence_after();
             for (int x = 0; x < nx; ++x) {
-                issue_qk<D>(tmem, aQ, aK, x, 0);
+                issue_qk<D>(tmem + 256 * x, dq0 + x * kTileStep, dk0);
                 commit_warp(&bars->s_full[x]);
             }
             commit_warp(&bars->k_empty[0]);
@@ -393,7 +399,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                        : mbar_wait_warp(&bars->v_full[st], (j / kStages) & 1, p.err, abort);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv<D>(tmem, aV, x, st, j > 0);
+                issue_pv<D>(tmem + 256 * x, dv0 + st * kTileStep, j > 0);
                 if (x == nx - 1) commit_warp(&bars->v_empty[st]);
                 if (!more) {
                     commit_warp(&bars->o_final[x]);
@@ -402,7 +408,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                     ((j + 1) / kStages) & 1, p.err, abort);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk<D>(tmem, aQ, aK, x, (j + 1) % kStages);
+                    issue_qk<D>(tmem + 256 * x, dq0 + x * kTileStep, dk0 + ((j + 1) % kStages) * kTileStep);
                     commit_warp(&bars->s_full[x]);
                     if (x == nx - 1) commit_warp(&bars->k_empty[(j + 1) % kStages]);
                 }
