@@ -27,10 +27,6 @@
  *    header themselves: a raised flag stays set until jt_check() reads and
  *    clears it.  Calls that share one workspace must not overlap on the
  *    device.
- *  - Kernels are launched with programmatic stream serialisation: a kernel
- *    of the library may become resident while the previous kernel of the
- *    stream drains, and waits for that kernel's completion before it reads
- *    or writes global memory.
  *
  * Tree layout shared by the three steps
  *  - nseq sequences; sequence b owns global node indices
@@ -134,8 +130,8 @@ jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
  *   Arguments, outputs and results are those of jt_tree_build; the scratch
  *   is a fixed device array of JT_NOALLOC_SCRATCH_BYTES inside the library.
  *   It must hold 256 bytes of header plus the build's tables, i.e.
- *   jt_workspace_size(JT_OP_TREE_BUILD, nseq, N, W, V) bytes; a larger need
- *   (about nseq*N > 2400 rows at V = 151936, W = 4) returns
+ *   jt_workspace_size(JT_OP_TREE_BUILD, nseq, N, W, V) bytes (about 4096
+ *   draft rows nseq*N at V = 151936, W = 4); a larger need returns
  *   JT_ERR_WORKSPACE before anything is enqueued.
  *   sync_check: 0 = asynchronous, like jt_tree_build (device-side errors are
  *   then not reported); nonzero = synchronise `stream` after the launch and

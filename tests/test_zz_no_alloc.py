@@ -20,15 +20,15 @@ SCRATCH_BYTES = 4 * 1024 * 1024
 
 def test_oversized_build_is_refused_on_the_host():
     lib = jt.load()
-    nseq, N, W, V = 256, 16, 4, 151936          # 4096 rows: well past 4 MiB of tables
+    nseq, N, W, V = 1024, 16, 4, 151936         # 16384 rows: well past 4 MiB of tables
     need = jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, nseq, N, W, V)
     assert need > SCRATCH_BYTES
     fake = ctypes.c_void_p(4096)                  # never dereferenced: refused before any CUDA call
     rc = lib.jt_tree_build_noalloc(fake, fake, fake, nseq, N, W, V, nseq * 16, fake, fake, fake,
                                    fake, 1, None)
     assert rc == JT_ERR_WORKSPACE
-    # the largest case the scratch is documented to hold still passes the size check
-    assert jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, 150, 16, 4, 151936) <= SCRATCH_BYTES
+    # the case size the scratch is documented to hold still passes the size check
+    assert jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, 256, 16, 4, 151936) <= SCRATCH_BYTES
 
 
 @pytest.mark.gpu

@@ -65,14 +65,6 @@ JT_HD float jt_add(float a, float b) {
 #endif
 }
 
-JT_HD float jt_rintf(float a) {
-#ifdef __CUDA_ARCH__
-    return rintf(a);
-#else
-    return std::nearbyintf(a);
-#endif
-}
-
 JT_HD float jt_pow2i(int n) {  // 2^n for -126 <= n <= 127
     uint32_t u = static_cast<uint32_t>(n + 127) << 23;
 #ifdef __CUDA_ARCH__
@@ -84,17 +76,28 @@ JT_HD float jt_pow2i(int n) {  // 2^n for -126 <= n <= 127
 #endif
 }
 
-// exp(xh + xl) with xl a small correction (|xl| <= ulp(xh)).  tab_hi/tab_lo:
-// 2^(j/64), j = 0..63, as float pairs.
-JT_HD ffloat ffexp(float xh, float xl, const float* tab_hi, const float* tab_lo) {
+JT_HD uint32_t jt_float_bits(float f) {
+#ifdef __CUDA_ARCH__
+    return __float_as_uint(f);
+#else
+    uint32_t u;
+    std::memcpy(&u, &f, sizeof u);
+    return u;
+#endif
+}
+
+// 1.5 * 2^23: adding it to |v| < 2^22 leaves round-to-nearest(v) in the low
+// mantissa bits, so the reduction needs no float-to-int conversion.
+constexpr float kRoundMagic = 12582912.0f;
+
+// exp(xh + xl) for finite xh >= -87, with xl a small correction
+// (|xl| <= ulp(xh)).  tab_hi/tab_lo: 2^(j/64), j = 0..63, as float pairs.
+JT_HD ffloat ffexp_in_range(float xh, float xl, const float* tab_hi, const float* tab_lo) {
     ffloat res;
-    if (!(xh >= -87.0f)) {  // also catches NaN and -inf
-        res.hi = 0.0f;
-        res.lo = 0.0f;
-        return res;
-    }
-    const float kf = jt_rintf(xh * kExpInvL);
-    const int k = static_cast<int>(kf);
+    // k = nearest integer to xh * 64/ln2 (|k| < 2^13)
+    const float tk = jt_fmaf(xh, kExpInvL, kRoundMagic);
+    const float kf = jt_add(tk, -kRoundMagic);
+    const int k = static_cast<int>(jt_float_bits(tk)) - 0x4B400000;
     const float r1 = jt_fmaf(-kf, kExpC1, xh);   // exact
     const float rh = jt_fmaf(-kf, kExpC2, r1);   // exact
     const float rl = jt_fmaf(-kf, kExpC3, xl);   // |rl| < 4e-7
@@ -118,6 +121,17 @@ JT_HD ffloat ffexp(float xh, float xl, const float* tab_hi, const float* tab_lo)
     res.hi = jt_mul(s, sc);
     res.lo = jt_mul(jt_add(e, small), sc);
     return res;
+}
+
+// exp(xh + xl) for any xh <= 0: 0 below -87 and for -inf or NaN.
+JT_HD ffloat ffexp(float xh, float xl, const float* tab_hi, const float* tab_lo) {
+    if (!(xh >= -87.0f)) {  // also catches NaN and -inf
+        ffloat res;
+        res.hi = 0.0f;
+        res.lo = 0.0f;
+        return res;
+    }
+    return ffexp_in_range(xh, xl, tab_hi, tab_lo);
 }
 
 // Fill the 64-entry table 2^(j/64) = hi + lo (host side).

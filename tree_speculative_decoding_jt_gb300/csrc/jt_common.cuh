@@ -33,39 +33,24 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t code) {
     if (err) atomicOr(err, code);
 }
 
-// ---------------------------------------------------------------------------
-// Programmatic dependent launch.  Every kernel of the library is launched with
-// programmatic stream serialisation (launch_pdl), so its CTAs may become
-// resident while the previous kernel of the stream drains.  pdl_wait() blocks
-// until that kernel has completed and its writes are visible; each kernel
-// calls it before its first global memory access.  pdl_trigger() lets the
-// next kernel of the stream start launching (it still waits for this one).
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-__device__ __forceinline__ void pdl_trigger() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// cudaLaunchKernelEx with programmatic stream serialisation and, when
-// cluster_x > 0, a (cluster_x, 1, 1) thread-block cluster.
+// cudaLaunchKernelEx with, when cluster_x > 0, a (cluster_x, 1, 1)
+// thread-block cluster.
 template <typename... KArgs, typename... Args>
-inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                              cudaStream_t st, unsigned cluster_x, Args... args) {
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t st, unsigned cluster_x, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    unsigned n = 1;
+    cudaLaunchAttribute attr[1];
+    unsigned n = 0;
     if (cluster_x > 0) {
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = cluster_x;
-        attr[1].val.clusterDim.y = 1;
-        attr[1].val.clusterDim.z = 1;
-        n = 2;
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cluster_x;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        n = 1;
     }
     cfg.attrs = attr;
     cfg.numAttrs = n;

@@ -241,8 +241,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
-    pdl_wait();     // inputs may come from the previous kernel of the stream
-    pdl_trigger();
     using SL = SmemLayout<D>;
     constexpr int kTileBytes = SL::kTileBytes;
     extern __shared__ uint8_t smem_raw[];
@@ -531,8 +529,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(128)
     tree_attn_combine_kernel(const AttnParams p, int total_nodes) {
-    pdl_wait();     // inputs may come from the previous kernel of the stream
-    pdl_trigger();
     const int lane = threadIdx.x & 31;
     const int n = blockIdx.x;
     const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
@@ -701,11 +697,11 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
         attr_done = true;
     }
     dim3 grid(((plan.mtiles + 1) / 2) * plan.splits, Hkv, nseq);
-    cudaError_t e = launch_pdl(tree_attn_tc_kernel<D>, grid, dim3(kAttnThreads), SL::kAlloc, st, 0, tq,
+    cudaError_t e = launch_kernel(tree_attn_tc_kernel<D>, grid, dim3(kAttnThreads), SL::kAlloc, st, 0, tq,
                                tk, tv, prm);
     if (e != cudaSuccess || plan.splits == 1) return e;
     dim3 cgrid(total_nodes, (Hq + 3) / 4);
-    return launch_pdl(tree_attn_combine_kernel<D>, cgrid, dim3(128), 0, st, 0, prm, total_nodes);
+    return launch_kernel(tree_attn_combine_kernel<D>, cgrid, dim3(128), 0, st, 0, prm, total_nodes);
 }
 
 cudaError_t tree_attn_bf16_launch(const void* q, const void* k_cache, const void* v_cache,

@@ -30,7 +30,7 @@
 namespace jt {
 
 constexpr int kTopwThreads = 256;
-constexpr int kTopwPerThread = 16;
+constexpr int kTopwPerThread = 32;
 constexpr int kExpandThreads = 256;
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -133,21 +133,73 @@ __device__ __forceinline__ float warp_max_f(float x) {
 
 // ---------------------------------------------------------------------------
 // Step 1a: per-chunk top-W, max and sum of exp(z - max).
-// grid = (splits, rows); chunk = kTopwThreads*kTopwPerThread entries.
+// grid = (splits, rows); chunk = kTopwThreads*kTopwPerThread entries; every
+// thread holds kTopwPerThread entries in registers (ids increase with the
+// slot index, out-of-range slots form a suffix).
+//   top-W: each lane tracks the arg-max of its own entries (strict '>' over
+//   ascending slots keeps the lowest id among equal values); W warp rounds
+//   take the best lane head (value desc, id asc) and let the winning lane
+//   rescan its remaining entries; warp 0 then merges the warps' lists the
+//   same way.  Exact under ties, and the per-entry cost is a few compares.
+//   sum: per warp, exp(z - warp max) summed in float-float from the
+//   table-driven exp; warp 0 rescales the warp sums to the chunk maximum.
 // ---------------------------------------------------------------------------
+template <bool VEC>
+__device__ __forceinline__ long long topw_slot_id(long long begin, int tid, int s) {
+    return VEC ? begin + 4ll * (tid + kTopwThreads * (s >> 2)) + (s & 3)
+               : begin + tid + static_cast<long long>(kTopwThreads) * s;
+}
+
+// Best two remaining in-range slots of this lane (value desc, slot asc);
+// `avail` has a bit per slot still eligible (in range and not taken).  The
+// eligible slots are scanned once; a lane only rescans after both of its
+// heads were taken (rare: two of the warp's top-W in one lane).
+__device__ __forceinline__ void lane_best2(const float (&x)[kTopwPerThread], uint32_t avail, float& v1,
+                                           int& s1, float& v2, int& s2) {
+    v1 = v2 = -INFINITY;
+    s1 = s2 = -1;
+#pragma unroll
+    for (int s = 0; s < kTopwPerThread; ++s) {
+        if ((avail >> s) & 1u) {
+            const float xs = x[s];
+            if (s1 < 0 || xs > v1) {
+                v2 = v1;
+                s2 = s1;
+                v1 = xs;
+                s1 = s;
+            } else if (s2 < 0 || xs > v2) {
+                v2 = xs;
+                s2 = s;
+            }
+        }
+    }
+}
+
+// One round of the warp arg-max over (value, id) heads (id -1 = empty).
+__device__ __forceinline__ void warp_best(float& v, int& id) {
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(kFull, v, off);
+        const int oi = __shfl_xor_sync(kFull, id, off);
+        if (better(ov, oi, v, id)) {
+            v = ov;
+            id = oi;
+        }
+    }
+}
+
 template <int W, bool VEC>
 __global__ void __launch_bounds__(kTopwThreads)
     topw_partial_kernel(const float* __restrict__ z, long long V, int splits, ExpTable tab,
                         float* __restrict__ part_v, int* __restrict__ part_id,
                         float* __restrict__ part_m, float2* __restrict__ part_s) {
-    pdl_wait();     // inputs may come from the previous kernel of the stream
-    pdl_trigger();
     constexpr int CH = kTopwThreads * kTopwPerThread;
+    constexpr int NW = kTopwThreads / 32;
     __shared__ float s_thi[64], s_tlo[64];
-    __shared__ float s_wv[kTopwThreads / 32][W];
-    __shared__ int s_wi[kTopwThreads / 32][W];
-    __shared__ float s_wmax[kTopwThreads / 32];
-    __shared__ float2 s_wsum[kTopwThreads / 32];
+    __shared__ float s_wv[NW][W];
+    __shared__ int s_wi[NW][W];
+    __shared__ float s_wmax[NW];
+    __shared__ float2 s_wsum[NW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long row = blockIdx.y;
@@ -161,8 +213,6 @@ __global__ void __launch_bounds__(kTopwThreads)
     const long long end = min(V, begin + CH);
 
     float x[kTopwPerThread];
-    TopList<W> L;
-    L.init();
     if (VEC) {
 #pragma unroll
         for (int i = 0; i < kTopwPerThread / 4; ++i) {
@@ -173,92 +223,140 @@ __global__ void __launch_bounds__(kTopwThreads)
             x[4 * i + 1] = f.y;
             x[4 * i + 2] = f.z;
             x[4 * i + 3] = f.w;
-            // cheap filter first (entries reach the list rarely): only a
-            // value >= the current W-th best can enter it
-            const float t = L.v[W - 1];
-            if (e < end && (f.x >= t || f.y >= t || f.z >= t || f.w >= t)) {
-                L.push(f.x, static_cast<int>(e));
-                L.push(f.y, static_cast<int>(e + 1));
-                L.push(f.z, static_cast<int>(e + 2));
-                L.push(f.w, static_cast<int>(e + 3));
-            }
         }
     } else {
 #pragma unroll
         for (int i = 0; i < kTopwPerThread; ++i) {
             const long long e = begin + tid + static_cast<long long>(kTopwThreads) * i;
-            x[i] = -INFINITY;
-            if (e < end) {
-                x[i] = __ldg(zr + e);
-                if (x[i] >= L.v[W - 1]) L.push(x[i], static_cast<int>(e));
-            }
+            x[i] = (e < end) ? __ldg(zr + e) : -INFINITY;
         }
     }
+    // in-range slots form a prefix of the lane's slots
+    int nvalid = 0;
+    if (VEC) {
+        const long long g = (end - begin - 4ll * tid + 4ll * kTopwThreads - 1) / (4ll * kTopwThreads);
+        nvalid = 4 * static_cast<int>(max(0ll, min(static_cast<long long>(kTopwPerThread / 4), g)));
+    } else {
+        const long long g = (end - begin - tid + kTopwThreads - 1) / kTopwThreads;
+        nvalid = static_cast<int>(max(0ll, min(static_cast<long long>(kTopwPerThread), g)));
+    }
+    uint32_t avail = (nvalid >= 32) ? 0xFFFFFFFFu : ((1u << nvalid) - 1u);
+    float bv, bv2;
+    int bs, bs2;
+    lane_best2(x, avail, bv, bs, bv2, bs2);
 
-    // chunk maximum
-    float m = -INFINITY;
-#pragma unroll
-    for (int i = 0; i < kTopwPerThread; ++i) m = fmaxf(m, x[i]);
-    m = warp_max_f(m);
-    if (lane == 0) s_wmax[warp] = m;
-    __syncthreads();
-    m = (lane < kTopwThreads / 32) ? s_wmax[lane] : -INFINITY;
-    m = warp_max_f(m);
-
-    // sum of exp(z - m): exact difference as a float pair, table-driven exp,
-    // float-float accumulation within and across threads
+    // warp maximum, then this lane's share of sum exp(z - max) (float-float)
+    const float mw = warp_max_f(bv);
+    __syncthreads();  // exp table ready
     float acc_hi = 0.0f, acc_lo = 0.0f;
-    if (m != -INFINITY) {
+    if (mw != -INFINITY) {
+        // entries more than 87 below the maximum (and -inf padding) are
+        // lifted to max - 87 (~87 after rounding): they then add ~1e-38 each
+        // instead of 0, far below the sum's rounding (the sum is >= 1)
+        const float floor_v = mw - 87.0f;
 #pragma unroll
         for (int i = 0; i < kTopwPerThread; ++i) {
             float dh, dl;
-            two_sum(x[i], -m, dh, dl);
-            const ffloat y = ffexp(dh, dl, s_thi, s_tlo);
-            float s, e;
-            two_sum(acc_hi, y.hi, s, e);
-            acc_hi = s;
-            acc_lo = jt_add(acc_lo, jt_add(e, y.lo));
+            two_sum(fmaxf(x[i], floor_v), -mw, dh, dl);
+            const ffloat y = ffexp_in_range(fmaxf(dh, -87.0f), dl, s_thi, s_tlo);
+            float sum, err;
+            two_sum(acc_hi, y.hi, sum, err);
+            acc_hi = sum;
+            acc_lo = jt_add(acc_lo, jt_add(err, y.lo));
         }
     }
-    ffloat S = warp_sum_ff(ff_norm(acc_hi, acc_lo));
-    if (lane == 0) s_wsum[warp] = make_float2(S.hi, S.lo);
+    const ffloat Sw = warp_sum_ff(ff_norm(acc_hi, acc_lo));
 
-    // top-W across the CTA
-    float rv[W];
-    int rid[W];
-    warp_merge<W>(L, rv, rid);
-    if (lane == 0) {
+    // warp top-W: W extraction rounds over the lanes' heads
 #pragma unroll
-        for (int k = 0; k < W; ++k) {
-            s_wv[warp][k] = rv[k];
-            s_wi[warp][k] = rid[k];
+    for (int r = 0; r < W; ++r) {
+        float v = bv;
+        int id = (bs >= 0) ? static_cast<int>(topw_slot_id<VEC>(begin, tid, bs)) : -1;
+        const int mine = id;
+        warp_best(v, id);
+        if (lane == 0) {
+            s_wv[warp][r] = v;
+            s_wi[warp][r] = id;
         }
+        if (id != -1 && id == mine) {  // this lane's head was taken
+            avail &= ~(1u << bs);
+            if (bs2 >= 0) {
+                bv = bv2;
+                bs = bs2;
+                bs2 = -1;  // the next head after this one needs a rescan
+            } else {
+                float v3;
+                int s3;
+                lane_best2(x, avail, bv, bs, v3, s3);
+                bv2 = v3;
+                bs2 = s3;
+            }
+        }
+    }
+    if (lane == 0) {
+        s_wmax[warp] = mw;
+        s_wsum[warp] = make_float2(Sw.hi, Sw.lo);
     }
     __syncthreads();
     if (warp == 0) {
-        TopList<W> M;
-        M.init();
-        if (lane < kTopwThreads / 32) {
-#pragma unroll
-            for (int k = 0; k < W; ++k) {
-                M.v[k] = s_wv[lane][k];
-                M.id[k] = s_wi[lane][k];
-            }
-        }
-        warp_merge<W>(M, rv, rid);
+        // chunk max and sum: rescale each warp's sum to the chunk maximum
+        float m = (lane < NW) ? s_wmax[lane] : -INFINITY;
+        m = warp_max_f(m);
+        ffloat S;
         S.hi = S.lo = 0.0f;
-        if (lane < kTopwThreads / 32) {
-            S.hi = s_wsum[lane].x;
-            S.lo = s_wsum[lane].y;
+        if (lane < NW && m != -INFINITY) {
+            const float mj = s_wmax[lane];
+            if (mj != -INFINITY) {
+                float dh, dl;
+                two_sum(mj, -m, dh, dl);
+                ffloat Sj;
+                Sj.hi = s_wsum[lane].x;
+                Sj.lo = s_wsum[lane].y;
+                S = ff_mul(Sj, ffexp(dh, dl, s_thi, s_tlo));
+            }
         }
         S = warp_sum_ff(S);
-        const long long p = row * splits + sp;
-        if (lane == 0) {
+        // chunk top-W from the warps' sorted lists (NW*W <= 64 entries; each
+        // lane holds up to two, best first)
+        constexpr int PER = (NW * W + 31) / 32;
+        float hv[PER];
+        int hi[PER];
 #pragma unroll
-            for (int k = 0; k < W; ++k) {
-                part_v[p * W + k] = rv[k];
-                part_id[p * W + k] = rid[k];
+        for (int q = 0; q < PER; ++q) {
+            const int c = lane + 32 * q;
+            hv[q] = (c < NW * W) ? s_wv[c / W][c % W] : -INFINITY;
+            hi[q] = (c < NW * W) ? s_wi[c / W][c % W] : -1;
+        }
+        if (PER == 2 && better(hv[PER - 1], hi[PER - 1], hv[0], hi[0])) {
+            const float tv = hv[0];
+            const int ti = hi[0];
+            hv[0] = hv[PER - 1];
+            hi[0] = hi[PER - 1];
+            hv[PER - 1] = tv;
+            hi[PER - 1] = ti;
+        }
+        const long long p = row * splits + sp;
+#pragma unroll
+        for (int r = 0; r < W; ++r) {
+            float v = hv[0];
+            int id = hi[0];
+            const int mine = id;
+            warp_best(v, id);
+            if (lane == 0) {
+                part_v[p * W + r] = v;
+                part_id[p * W + r] = id;
             }
+            if (id != -1 && id == mine) {  // pop this lane's head
+#pragma unroll
+                for (int q = 0; q + 1 < PER; ++q) {
+                    hv[q] = hv[q + 1];
+                    hi[q] = hi[q + 1];
+                }
+                hv[PER - 1] = -INFINITY;
+                hi[PER - 1] = -1;
+            }
+        }
+        if (lane == 0) {
             part_m[p] = m;
             part_s[p] = make_float2(S.hi, S.lo);
         }
@@ -369,8 +467,6 @@ __global__ void __launch_bounds__(256)
                       const float* __restrict__ part_m, const float2* __restrict__ part_s,
                       int splits, long long rows, ExpTable tab, int32_t* __restrict__ tok_out,
                       double* __restrict__ lp_out, double* __restrict__ lse_out) {
-    pdl_wait();     // inputs may come from the previous kernel of the stream
-    pdl_trigger();
     __shared__ float s_thi[64], s_tlo[64];
     if (threadIdx.x < 64) {
         s_thi[threadIdx.x] = tab.hi[threadIdx.x];
@@ -491,8 +587,6 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                   const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
                   int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
-    pdl_wait();     // inputs may come from the previous kernel of the stream
-    pdl_trigger();
     extern __shared__ __align__(16) unsigned char dsm[];
     unsigned long long* kb1[2];
     unsigned long long* kb2[2];
@@ -732,9 +826,9 @@ static cudaError_t launch_topw_partial(const float* z, long long rows, long long
     const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
     dim3 grid(t.splits, static_cast<unsigned>(rows));
     if (vec)
-        return launch_pdl(topw_partial_kernel<W, true>, grid, dim3(kTopwThreads), 0, st, 0, z, V,
+        return launch_kernel(topw_partial_kernel<W, true>, grid, dim3(kTopwThreads), 0, st, 0, z, V,
                           t.splits, tab, t.v, t.id, t.m, t.s);
-    return launch_pdl(topw_partial_kernel<W, false>, grid, dim3(kTopwThreads), 0, st, 0, z, V, t.splits,
+    return launch_kernel(topw_partial_kernel<W, false>, grid, dim3(kTopwThreads), 0, st, 0, z, V, t.splits,
                       tab, t.v, t.id, t.m, t.s);
 }
 
@@ -746,7 +840,7 @@ static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t
     if (e != cudaSuccess) return e;
     const long long warps_per_block = 8;
     const unsigned blocks = static_cast<unsigned>((rows + warps_per_block - 1) / warps_per_block);
-    return launch_pdl(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
+    return launch_kernel(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
                       t.splits, rows, exp_table(), tok, lp, lse);
 }
 
@@ -761,13 +855,13 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
         cudaError_t e = launch_topw_partial<W>(z, rows, V, t, st);
         if (e != cudaSuccess) return e;
         const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-        e = launch_pdl(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
+        e = launch_kernel(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
                        t.splits, rows, exp_table(), t.tok, t.lp, t.lse);
         if (e != cudaSuccess) return e;
     }
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    return launch_pdl(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, t.tok, t.lp,
+    return launch_kernel(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, t.tok, t.lp,
                       root_token, tree_off, total_nodes, N, parent, token, depth, anc, err);
 }
 
@@ -778,7 +872,7 @@ static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_
                               cudaStream_t st) {
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    return launch_pdl(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, tok, lp,
+    return launch_kernel(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, tok, lp,
                       root_token, tree_off, total_nodes, N, parent, token, depth, anc, err);
 }
 

@@ -43,8 +43,6 @@ __global__ void __launch_bounds__(kAccThreads)
                           int total_nodes, int N, long long V, int rule, double log_t,
                           int32_t* __restrict__ accept_len, int32_t* __restrict__ path,
                           int32_t* __restrict__ bonus, uint32_t* err) {
-    pdl_wait();     // inputs may come from the previous kernel of the stream
-    pdl_trigger();
     __shared__ unsigned long long s_part[JT_MAX_TREE];    // this CTA's key per frontier slot
     __shared__ unsigned long long s_rowkey[JT_MAX_TREE];  // rank 0: combined key per slot
     __shared__ int s_front[2][JT_MAX_TREE];               // frontier lists (node ids, ascending)
@@ -254,7 +252,7 @@ static cudaError_t launch_accept(const float* z, const int32_t* parent, const in
                                  int total_nodes, int rule, double log_t, int32_t* accept_len,
                                  int32_t* path, int32_t* bonus, uint32_t* err, cudaStream_t st) {
     const int cs = accept_cluster_size<VEC>();
-    return launch_pdl(accept_cluster_kernel<VEC>, dim3(static_cast<unsigned>(nseq) * cs), dim3(kAccThreads),
+    return launch_kernel(accept_cluster_kernel<VEC>, dim3(static_cast<unsigned>(nseq) * cs), dim3(kAccThreads),
                       0, st, static_cast<unsigned>(cs), z, parent, token, tree_off, total_nodes, N, V, rule,
                       log_t, accept_len, path, bonus, err);
 }
