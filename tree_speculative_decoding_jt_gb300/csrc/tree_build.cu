@@ -31,7 +31,7 @@ namespace jt {
 
 constexpr int kTopwThreads = 256;
 constexpr int kTopwPerThread = 32;
-constexpr int kExpandThreads = 256;
+constexpr int kExpandThreads = 1024;  // ranking uses all; set-sized steps use the first 256
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
 struct ExpTable {
@@ -534,14 +534,24 @@ __device__ __forceinline__ bool key_better(unsigned long long a1, unsigned long 
     return a1 > b1 || (a1 == b1 && a2 > b2);
 }
 
-// Number of entries of a[0, len) (sorted best first) better than (x1, x2).
+// Number of entries of a[0, len) (sorted best first) better than (x1, x2):
+// a binary search on the score key alone, then, only when the score is tied,
+// one on the tie key inside the equal-score range.
 __device__ __forceinline__ int count_better(const unsigned long long* a1, const unsigned long long* a2,
                                             int len, unsigned long long x1, unsigned long long x2) {
     int lo = 0, hi = len;
     while (lo < hi) {
         const int mid = (lo + hi) >> 1;
-        if (key_better(a1[mid], a2[mid], x1, x2)) lo = mid + 1;
+        if (a1[mid] > x1) lo = mid + 1;
         else hi = mid;
+    }
+    if (lo < len && a1[lo] == x1) {
+        hi = len;
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (a1[mid] == x1 && a2[mid] > x2) lo = mid + 1;
+            else hi = mid;
+        }
     }
     return lo;
 }
@@ -556,8 +566,17 @@ __host__ __device__ inline int full_tree_nodes(int N, int W, int cap) {
     return static_cast<int>(total);
 }
 
-// Inclusive prefix sum over the CTA (kExpandThreads threads).
-__device__ __forceinline__ int block_incl_scan(int v, int* s_warp) {
+// Barrier among the first kSetWarps warps only (named barrier 1): the
+// set-sized steps run on them while the other warps wait at the next full
+// barrier without spending issue slots.
+constexpr int kSetWarps = JT_MAX_TREE / 32;
+__device__ __forceinline__ void set_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kSetWarps * 32) : "memory");
+}
+
+// Inclusive prefix sum of v over threads 0..255; called by warps 0..7 only.
+// s_warp[kSetWarps - 1] ends as the total.
+__device__ __forceinline__ int set_incl_scan(int v, int* s_warp) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -565,19 +584,18 @@ __device__ __forceinline__ int block_incl_scan(int v, int* s_warp) {
         if (lane >= o) v += t;
     }
     if (lane == 31) s_warp[warp] = v;
-    __syncthreads();
+    set_sync();
     if (warp == 0) {
-        int w = (lane < kExpandThreads / 32) ? s_warp[lane] : 0;
+        int w = (lane < kSetWarps) ? s_warp[lane] : 0;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
+        for (int o = 1; o < kSetWarps; o <<= 1) {
             const int t = __shfl_up_sync(kFull, w, o);
             if (lane >= o) w += t;
         }
-        if (lane < kExpandThreads / 32) s_warp[lane] = w;
+        if (lane < kSetWarps) s_warp[lane] = w;
     }
-    __syncthreads();
+    set_sync();
     if (warp > 0) v += s_warp[warp - 1];
-    __syncthreads();
     return v;
 }
 
@@ -588,20 +606,20 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                   int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
     extern __shared__ __align__(16) unsigned char dsm[];
-    unsigned long long* kb1[2];
-    unsigned long long* kb2[2];
-    kb1[0] = reinterpret_cast<unsigned long long*>(dsm);  // [kExpCap] x 4
-    kb2[0] = kb1[0] + kExpCap;
-    kb1[1] = kb2[0] + kExpCap;
-    kb2[1] = kb1[1] + kExpCap;
-    short* pb[2];
-    pb[0] = reinterpret_cast<short*>(kb2[1] + kExpCap);  // [kExpCap] x 2
-    pb[1] = pb[0] + kExpCap;
-    short* rank_of = pb[1] + kExpCap;                      // [kExpCap]
+    // two buffers c = 0, 1 of (score key, tie key, parent position), each
+    // kExpCap entries: score keys at kb + 2c*kExpCap, tie keys right after
+    unsigned long long* const kb = reinterpret_cast<unsigned long long*>(dsm);  // [kExpCap] x 4
+    short* const pb = reinterpret_cast<short*>(kb + 4 * kExpCap);               // [kExpCap] x 2
+    short* const rank_of = pb + 2 * kExpCap;                                   // [kExpCap]
+    auto kb1 = [&](int c) { return kb + 2 * c * kExpCap; };
+    auto kb2 = [&](int c) { return kb + (2 * c + 1) * kExpCap; };
+    auto pbuf = [&](int c) { return pb + c * kExpCap; };
     __shared__ int s_tok[JT_MAX_N * W];
     __shared__ double s_lp[JT_MAX_N * W];
     __shared__ short s_front[JT_MAX_TREE];
     __shared__ int s_warp[kExpandThreads / 32];
+    __shared__ int s_cnt[kSetWarps][W];
+    __shared__ int s_L[W];
 
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
@@ -619,61 +637,82 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     __syncthreads();
 
     const int K = B - 1;  // non-root nodes
+    const int lane = tid & 31, warp = tid >> 5;
     int m = 0;            // size of the sorted set S (buffer cb)
     int cb = 0;
     for (int d = 0; d < N && K > 0; ++d) {
-        unsigned long long* k1 = kb1[cb];
-        unsigned long long* k2 = kb2[cb];
-        short* par = pb[cb];
-        // frontier: the root at d == 0, else S's depth-d entries (ascending positions)
-        int nf;
-        if (d == 0) {
-            if (tid == 0) s_front[0] = -1;
-            nf = 1;
-        } else {
-            const int is_f = (tid < m && k2_depth(k2[tid]) == d) ? 1 : 0;  // m <= 255 < threads
-            const int incl = block_incl_scan(is_f, s_warp);
-            if (is_f) s_front[incl - 1] = static_cast<short>(tid);
-            nf = s_warp[kExpandThreads / 32 - 1];
-        }
-        __syncthreads();
-        if (nf == 0) break;
-        // children of frontier entry e better than S's (B-1)-th entry
-        const bool full = (m >= K);
-        const unsigned long long t1 = full ? k1[K - 1] : 0ull, t2 = full ? k2[K - 1] : 0ull;
-        const int e = tid;
-        int pos = -2, c = 0;
-        unsigned long long ck[W];
-        if (e < nf) {
-            pos = s_front[e];
-            const double su = (pos < 0) ? 0.0 : double_from_order_key(k1[pos]);
+        unsigned long long* k1 = kb1(cb);
+        unsigned long long* k2 = kb2(cb);
+        short* par = pbuf(cb);
+        if (warp < kSetWarps) {
+            // frontier: the root at d == 0, else S's depth-d entries (ascending positions)
+            int nf;
+            if (d == 0) {
+                if (tid == 0) s_front[0] = -1;
+                nf = 1;
+            } else {
+                const int is_f = (tid < m && k2_depth(k2[tid]) == d) ? 1 : 0;  // m <= 255
+                const int incl = set_incl_scan(is_f, s_warp);
+                if (is_f) s_front[incl - 1] = static_cast<short>(tid);
+                nf = s_warp[kSetWarps - 1];
+            }
+            set_sync();
+            // children of frontier entry e better than S's (B-1)-th entry
+            const bool full = (m >= K);
+            const unsigned long long t1 = full ? k1[K - 1] : 0ull, t2 = full ? k2[K - 1] : 0ull;
+            const int e = tid;
+            int pos = -2, c = 0;
+            unsigned long long ck[W];
+            if (e < nf) {
+                pos = s_front[e];
+                const double su = (pos < 0) ? 0.0 : double_from_order_key(k1[pos]);
+#pragma unroll
+                for (int k = 0; k < W; ++k) {
+                    ck[k] = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
+                    if (c == k &&
+                        (!full || key_better(ck[k], make_k2(d + 1, s_tok[d * W + k], pos), t1, t2)))
+                        ++c;
+                }
+            }
+            // run k = children of rank k of entries 0..L_k-1 (L_k
+            // non-increasing in k), counted with per-warp ballots
 #pragma unroll
             for (int k = 0; k < W; ++k) {
-                ck[k] = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
-                if (c == k && (!full || key_better(ck[k], make_k2(d + 1, s_tok[d * W + k], pos), t1, t2)))
-                    ++c;
+                const unsigned bal = __ballot_sync(kFull, e < nf && c > k);
+                if (lane == 0) s_cnt[warp][k] = __popc(bal);
+            }
+            set_sync();
+            if (warp == 0 && lane < W) {
+                int l = 0;
+#pragma unroll
+                for (int w = 0; w < kSetWarps; ++w) l += s_cnt[w][lane];
+                s_L[lane] = l;
+            }
+            set_sync();
+            int Rk = 0;  // start of run k
+#pragma unroll
+            for (int k = 0; k < W; ++k) {
+                if (k < c) {
+                    const int x = m + Rk + e;
+                    k1[x] = ck[k];
+                    k2[x] = make_k2(d + 1, s_tok[d * W + k], pos);
+                    par[x] = static_cast<short>(pos);
+                }
+                Rk += s_L[k];
             }
         }
-        // run k = children of rank k of entries 0..L_k-1 (L_k non-increasing in k)
+        __syncthreads();
         int L[W], R[W];
         int total = 0;
 #pragma unroll
         for (int k = 0; k < W; ++k) {
-            L[k] = __syncthreads_count(e < nf && c > k);
+            L[k] = s_L[k];
             R[k] = total;
             total += L[k];
         }
         if (total == 0) break;
-#pragma unroll
-        for (int k = 0; k < W; ++k)
-            if (k < c) {
-                const int x = m + R[k] + e;
-                k1[x] = ck[k];
-                k2[x] = make_k2(d + 1, s_tok[d * W + k], pos);
-                par[x] = static_cast<short>(pos);
-            }
-        __syncthreads();
-        // rank of every candidate in S + runs
+        // rank of every candidate in S + runs; a candidate stops searching as
+        // soon as its partial rank reaches B-1 (it is dropped)
         const int M = m + total;
         for (int x = tid; x < M; x += kExpandThreads) {
             const unsigned long long x1 = k1[x], x2 = k2[x];
@@ -682,21 +721,26 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
                 rank = x;
             } else {
                 const int y = x - m;
+                int rbase = 0;
 #pragma unroll
                 for (int k = 0; k < W; ++k)
-                    if (y >= R[k] && y < R[k] + L[k]) own = k;
-                rank = (y - R[own]) + count_better(k1, k2, m, x1, x2);
+                    if (y >= R[k] && y < R[k] + L[k]) {
+                        own = k;
+                        rbase = R[k];
+                    }
+                rank = y - rbase;
+                if (rank < K) rank += count_better(k1, k2, m, x1, x2);
             }
 #pragma unroll
             for (int k = 0; k < W; ++k)
-                if (k != own && L[k] > 0)
+                if (rank < K && k != own && L[k] > 0)
                     rank += count_better(k1 + m + R[k], k2 + m + R[k], L[k], x1, x2);
             rank_of[x] = static_cast<short>(rank < K ? rank : -2);
         }
         __syncthreads();
-        unsigned long long* n1 = kb1[cb ^ 1];
-        unsigned long long* n2 = kb2[cb ^ 1];
-        short* npar = pb[cb ^ 1];
+        unsigned long long* n1 = kb1(cb ^ 1);
+        unsigned long long* n2 = kb2(cb ^ 1);
+        short* npar = pbuf(cb ^ 1);
         for (int x = tid; x < M; x += kExpandThreads) {
             const int r = rank_of[x];
             if (r >= 0) {
@@ -716,8 +760,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     }
 
     // outputs: node 0 = root, node p+1 = S[p]; ancestor-or-self sets
-    const unsigned long long* k2f = kb2[cb];
-    const short* parf = pb[cb];
+    const unsigned long long* k2f = kb2(cb);
+    const short* parf = pbuf(cb);
     for (int n = tid; n < B; n += kExpandThreads) {
         int pn, tn, dn;
         if (n == 0) {
