@@ -40,6 +40,34 @@ UNIT = "tree-node tokens/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+# --------------------------------------------------------------------------
+# Multi-rank host logic (N > 1): every rank runs an independent replica on
+# its own GPU and its own seeded batch; the job's time is the slowest rank's.
+# --------------------------------------------------------------------------
+def replica_seed(config: int, rank: int) -> int:
+    """Seed of rank `rank`'s batch: the workload's default seed for rank 0,
+    distinct seeds for the other replicas."""
+    return 1000 + config + 7919 * rank
+
+
+def max_over_ranks(values, device, world):
+    """Element-wise maximum of a list of floats over all ranks (identity at
+    world == 1)."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def whole_job_rate(units_per_rank: int, seconds: float, world: int) -> float:
+    """Units all ranks processed per second of the slowest rank's time."""
+    return world * units_per_rank / seconds
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -263,7 +291,7 @@ def main():
             dist.barrier()
 
     cfg = args.config
-    wl = wk.make(cfg)
+    wl = wk.make(cfg, seed=replica_seed(cfg, rank))
     c = wl.cfg
     dev = torch.device("cuda", local_rank)
 
@@ -391,11 +419,8 @@ def main():
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
     ms = statistics.mean(step_ms)
     attn_mean = statistics.mean(attn_ms)
-    if world > 1:
-        t = torch.tensor([ms, attn_mean], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, attn_mean = float(t[0]), float(t[1])
-    value = world * total / (ms * 1e-3)
+    ms, attn_mean = max_over_ranks([ms, attn_mean], dev, world)
+    value = whole_job_rate(total, ms * 1e-3, world)
 
     # ---- end to end: pinned host inputs -> C-ABI calls -> host results
     e2e = None
@@ -418,11 +443,8 @@ def main():
                 dst.copy_(src, non_blocking=True)
             torch.cuda.synchronize()
         e2e_s = (time.perf_counter() - t0) / args.e2e_steps
-        if world > 1:
-            t = torch.tensor([e2e_s], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_s = float(t[0])
-        e2e = {"value": world * total / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+        e2e_s = max_over_ranks([e2e_s], dev, world)[0]
+        e2e = {"value": whole_job_rate(total, e2e_s, world), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
 
     # ---- roofline of the dominant kernel (the attention call)
