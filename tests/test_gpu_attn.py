@@ -60,10 +60,10 @@ def _small(seed, nseq, Hq, Hkv, D, prefix, budgets, N=6, W=3, dtype="bf16", q_mu
     (6, 2, 16, 8, 128, [64, 257], (48, 90)),       # G = 2
     (7, 2, 64, 8, 128, [100, 50], (20, 40)),       # G = 8
     (8, 2, 32, 8, 64, [500, 33], (77, 12)),        # D = 64
-    (9, 1, 32, 2, 128, [2000], (256,)),            # few KV heads: 9 KV splits, merged by the combine kernel
-    (10, 1, 32, 8, 128, [1500], (100,)),           # 6 splits in a cluster, the last one empty
-    (11, 1, 32, 8, 64, [900], (37,)),              # 4 splits in a cluster, D = 64
-    (12, 1, 32, 8, 128, [700], (20,)),             # 3 splits (uneven row shares), one query tile
+    (9, 1, 32, 2, 128, [2000], (256,)),            # few KV heads: 9 KV splits
+    (10, 1, 32, 8, 128, [1500], (100,)),           # 6 KV splits, the last one empty
+    (11, 1, 32, 8, 64, [900], (37,)),              # 4 KV splits, D = 64
+    (12, 1, 32, 8, 128, [700], (20,)),             # 3 KV splits, one query tile
 ])
 def test_bf16_matches_oracle_all_nodes(case):
     seed, nseq, Hq, Hkv, D, prefix, budgets = case
