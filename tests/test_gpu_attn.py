@@ -125,6 +125,14 @@ def _sample_rows(wl, k_per_seq=3):
     return np.array(rows, np.int32)
 
 
+def test_bf16_drafter_tree_only_all_nodes():
+    """The drafter-shaped workload: every node attends to its ancestors
+    only (no prefix); all 16 x 256 nodes and 32 heads against the oracle."""
+    wl = wk.make(6)
+    tree = oracle_tree(wl)
+    _check_bf16(*_run(wl, tree))
+
+
 @pytest.mark.parametrize("cfg", [2, 3, 5])
 def test_bf16_full_configs_sampled(cfg):
     wl = wk.make(cfg)

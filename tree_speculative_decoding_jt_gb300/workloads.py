@@ -5,7 +5,7 @@ method's arithmetic (no top-W, no softmax, no acceptance).  Both the CUDA path
 (tests, bench) and the CPU oracle are fed from here, so the two sides always
 see identical inputs.
 
-The five workloads mirror the shapes of the pages' setting (a Qwen3-8B-shaped
+The workloads mirror the shapes of the pages' setting (a Qwen3-8B-shaped
 attention layer: 32 query heads, 8 KV heads, head dim 128, bf16, vocab
 151936, paged KV with 16-token pages) with values drawn from fixed
 distributions.  No model weights or benchmark data are involved.
@@ -36,6 +36,11 @@ CONFIGS = {
             boost=4.0, boost_frac=0.8, t=0.8),
     5: dict(name="verify-step-b8-L2k-16k-B256", dtype="bf16", nseq=8, Hq=32, Hkv=8, D=128,
             prefix=("uniform", 2048, 16384), budgets=(256,), N=16, W=4, V=151936,
+            qkv_std=0.5, boost=4.0, boost_frac=0.8, t=0.8),
+    # the drafter's own tree forward: a draft head with the target layer's
+    # attention shape attends among the tree nodes only (no prefix slots)
+    6: dict(name="drafter-tree-b16-L0-B256", dtype="bf16", nseq=16, Hq=32, Hkv=8, D=128,
+            prefix=("fixed", 0), budgets=(256,), N=16, W=4, V=151936,
             qkv_std=0.5, boost=4.0, boost_frac=0.8, t=0.8),
 }
 
