@@ -10,11 +10,12 @@
  *
  * Sources (the method is described in prose only; no code is printed there):
  *  [JS-news]  JetSpec news summary, mlqm.cn/news/158889, paragraph on
- *             building the candidate tree ("构造候选树时 ... 贪心扩展直到预算填满")
- *             and on the tree-causal attention mask ("树形因果注意力掩码").
+ *             building the candidate tree (top W per depth, greedy fill
+ *             to the budget) and on the tree-causal attention mask.
  *  [JS-art]   "加速AI思考：UC San Diego等机构研究出让大模型“一心多用”的推测解码新方法",
  *             section 三 (tree-causal mask, parallel verification) and
- *             section 五 (树的建造: priority queue, cumulative log-prob, W, B).
+ *             section 五 (tree construction: priority queue, cumulative
+ *             log-prob, W, B).
  *  [AS]       "AdaptiveSpec：免训练推测解码方案提速56%的技术解析",
  *             section "逐步Margin规则" (accept if p(draft)/p(top1) >= t,
  *             worked example 0.30/0.35 ~ 0.86 >= 0.8).
