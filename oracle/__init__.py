@@ -48,8 +48,10 @@ def _load():
             lib.jto_tree_attn.argtypes = [P, P, P, i32, P, i32, P, P, P, i32, i32, i32, i32, i32,
                                           dbl, P, i64, P, P]
             lib.jto_verify_accept.argtypes = [P, P, P, P, i32, i32, i64, i32, dbl, P, P, P]
+            lib.jto_verify_accept_stochastic.argtypes = [P, P, P, P, P, i32, i32, i64, P, P, P, P,
+                                                         P, P]
             for f in (lib.jto_topw_lse, lib.jto_tree_expand, lib.jto_tree_build,
-                      lib.jto_tree_attn, lib.jto_verify_accept):
+                      lib.jto_tree_attn, lib.jto_verify_accept, lib.jto_verify_accept_stochastic):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -176,3 +178,24 @@ def verify_accept(target_logits, parent, token, tree_off, N, rule, log_t=0.0):
                                      V, rule, float(log_t), _ptr(acc), _ptr(path), _ptr(bonus)),
            "verify_accept")
     return acc, path, bonus
+
+def verify_accept_stochastic(target_logits, draft_logits, parent, token, tree_off, N, u_accept,
+                             u_bonus):
+    """Temperature-1 speculative-sampling acceptance over the tree with the
+    caller's uniforms.  Returns (accept_len, path, bonus, min_margin)."""
+    z = _c(target_logits, np.float32)
+    V = z.shape[-1]
+    dz = _c(draft_logits, np.float32) if draft_logits is not None else None
+    parent, token, tree_off = (_c(a, np.int32) for a in (parent, token, tree_off))
+    ua, ub = _c(u_accept, np.float64), _c(u_bonus, np.float64)
+    nseq = len(tree_off) - 1
+    acc = np.empty(nseq, np.int32)
+    path = np.empty((nseq, N + 1), np.int32)
+    bonus = np.empty(nseq, np.int32)
+    margin = np.empty(nseq, np.float64)
+    _check(_load().jto_verify_accept_stochastic(_ptr(z), _ptr(dz) if dz is not None else None,
+                                                _ptr(parent), _ptr(token), _ptr(tree_off), nseq, N,
+                                                V, _ptr(ua), _ptr(ub), _ptr(acc), _ptr(path),
+                                                _ptr(bonus), _ptr(margin)),
+           "verify_accept_stochastic")
+    return acc, path, bonus, margin

@@ -455,3 +455,141 @@ int jto_verify_accept(const float* target_logits, const int32_t* parent, const i
     }
     return JTO_OK;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Stochastic (temperature 1) tree acceptance.                               */
+/* [SD-overview] chooseai.io/news/6515, section "推测解码是什么：草稿模型先猜，  */
+/* 目标模型验收", and [AS] section "严格的token匹配验证机制": a drafted token x is   */
+/* accepted with probability min(1, p(x)/q(x)), p the target and q the draft */
+/* distribution; after a rejection the next token is drawn from             */
+/* norm(max(0, p - q)).                                                      */
+/* Tree reading (the pages describe one chain): at the current node u the   */
+/* children are tried in node order against a running residual r (r = p_u  */
+/* at first); child c with token t is accepted when u_accept[c] <            */
+/* min(1, r(t)/q(t)); after a rejection r <- norm(max(0, r - q)).  An        */
+/* accepted child becomes the current node.  When every child is rejected,  */
+/* or u has none, the bonus token is drawn from r by inverse CDF with        */
+/* u_bonus[u]: the smallest x with r(0) + ... + r(x) > u_bonus[u] * sum(r).  */
+/* p_u = softmax(target row u), q = softmax(draft row of the children's     */
+/* depth), both at temperature 1.                                            */
+/* ------------------------------------------------------------------------ */
+
+/* softmax of a float row in fp64 (max-subtracted) */
+static void softmax_row(const float* z, int64_t V, double* p)
+{
+    double m = -INFINITY;
+    for (int64_t i = 0; i < V; ++i)
+        if ((double)z[i] > m) m = (double)z[i];
+    double s = 0.0;
+    for (int64_t i = 0; i < V; ++i) {
+        p[i] = exp((double)z[i] - m);
+        s += p[i];
+    }
+    for (int64_t i = 0; i < V; ++i) p[i] /= s;
+}
+
+/*
+ * draft_logits: [nseq, N, V] fp32 (row d = draft distribution of depth d+1).
+ * u_accept, u_bonus: [total] uniforms in [0, 1) (u_accept of a root and
+ * u_bonus of a node the walk never stops at are unused).
+ * Outputs as jto_verify_accept; min_margin[b] (may be NULL) = the smallest
+ * distance, over every decision taken for sequence b, between the uniform
+ * and the threshold it was compared with (acceptance: |u - min(1, ratio)|;
+ * sampling: the distance of u*sum(r) to the nearest edge of the chosen bin,
+ * divided by sum(r)).
+ */
+int jto_verify_accept_stochastic(const float* target_logits, const float* draft_logits,
+                                 const int32_t* parent, const int32_t* token,
+                                 const int32_t* tree_off, int nseq, int N, int64_t V,
+                                 const double* u_accept, const double* u_bonus,
+                                 int32_t* accept_len, int32_t* path, int32_t* bonus,
+                                 double* min_margin)
+{
+    if (!target_logits || (!draft_logits && N > 0) || !parent || !token || !tree_off ||
+        !u_accept || !u_bonus || !accept_len || !path || !bonus || nseq < 0 || N < 0 || V < 1)
+        return JTO_ERR_INVALID;
+    double* r = (double*)malloc(sizeof(double) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)V);
+    if (!r || !q) {
+        free(r);
+        free(q);
+        return JTO_ERR_INVALID;
+    }
+    int status = JTO_OK;
+    for (int b = 0; b < nseq && status == JTO_OK; ++b) {
+        const int off = tree_off[b];
+        const int B = tree_off[b + 1] - off;
+        if (B < 1 || B > JTO_MAX_TREE || parent[off] != -1) { status = JTO_ERR_INVALID; break; }
+        for (int n = 1; n < B; ++n)
+            if (parent[off + n] < 0 || parent[off + n] >= n || token[off + n] < 0 ||
+                token[off + n] >= V)
+                status = JTO_ERR_INVALID;
+        if (status != JTO_OK) break;
+        double margin = INFINITY;
+        int u = 0, d = 0;
+        int32_t* pb = path + (int64_t)b * (N + 1);
+        for (int k = 0; k <= N; ++k) pb[k] = -1;
+        pb[0] = 0;
+        for (;;) {
+            softmax_row(target_logits + (int64_t)(off + u) * V, V, r);
+            int next = -1;
+            if (d < N) {
+                int have_child = 0;
+                for (int c = u + 1; c < B; ++c)
+                    if (parent[off + c] == u) { have_child = 1; break; }
+                if (have_child)
+                    softmax_row(draft_logits + ((int64_t)b * N + d) * V, V, q);
+                for (int c = u + 1; c < B && next < 0; ++c) {
+                    if (parent[off + c] != u) continue;
+                    const int t = token[off + c];
+                    const double ratio = (q[t] > 0.0) ? r[t] / q[t] : INFINITY;
+                    const double a = ratio < 1.0 ? ratio : 1.0;
+                    const double ua = u_accept[off + c];
+                    if (fabs(ua - a) < margin) margin = fabs(ua - a);
+                    if (ua < a) {
+                        next = c;
+                    } else {
+                        double z = 0.0;
+                        for (int64_t x = 0; x < V; ++x) {
+                            r[x] = r[x] - q[x] > 0.0 ? r[x] - q[x] : 0.0;
+                            z += r[x];
+                        }
+                        for (int64_t x = 0; x < V; ++x) r[x] /= z;
+                    }
+                }
+            }
+            if (next < 0) break;
+            u = next;
+            ++d;
+            pb[d] = u;
+        }
+        /* bonus: inverse CDF of r with u_bonus[u] */
+        double total = 0.0;
+        for (int64_t x = 0; x < V; ++x) total += r[x];
+        const double target = u_bonus[off + u] * total;
+        double cum = 0.0;
+        int64_t pick = -1;
+        for (int64_t x = 0; x < V; ++x) {
+            if (r[x] <= 0.0) continue;
+            const double lo = cum;
+            cum += r[x];
+            if (cum > target) {
+                const double m2 = (target - lo) < (cum - target) ? (target - lo) : (cum - target);
+                if (m2 / total < margin) margin = m2 / total;
+                pick = x;
+                break;
+            }
+        }
+        if (pick < 0) { /* rounding left target at the very top: the last bin */
+            for (int64_t x = V - 1; x >= 0; --x)
+                if (r[x] > 0.0) { pick = x; break; }
+            margin = 0.0;
+        }
+        accept_len[b] = d;
+        bonus[b] = (int32_t)pick;
+        if (min_margin) min_margin[b] = margin;
+    }
+    free(r);
+    free(q);
+    return status;
+}
