@@ -50,6 +50,8 @@
  *      without a dense mask).
  *  [AS] "AdaptiveSpec：免训练推测解码方案提速56%的技术解析", section
  *      "逐步Margin规则": accept when p(draft)/p(top1) >= t.
+ *  [SD] speculative-decoding overview, chooseai.io/news/6515, section
+ *      "推测解码是什么：草稿模型先猜，目标模型验收" (rejection-sampling acceptance).
  */
 #ifndef JT_H
 #define JT_H
@@ -223,6 +225,39 @@ jt_status jt_verify_accept(const float* target_logits, const int32_t* parent,
                            int64_t V, int total_nodes, int rule, double log_t,
                            int32_t* accept_len, int32_t* path, int32_t* bonus, void* ws,
                            size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_verify_accept_stochastic -- temperature-1 tree acceptance by rejection
+ * sampling ([SD] acceptance paragraph; [AS] section "严格的token匹配验证机制":
+ * accept a drafted token x with probability min(1, p(x)/q(x)); after a
+ * rejection draw from norm(max(0, p - q))).
+ *   target_logits: fp32 [total_nodes, V]; row u is the target after node u.
+ *   draft_logits:  fp32 [nseq, N, V]; row (b, d) is the draft distribution
+ *                  of depth d+1 (the rows the tree was built from).
+ *   u_accept, u_bonus: fp64 [total_nodes], the caller's uniforms in [0, 1):
+ *                  u_accept[c] decides the test of node c, u_bonus[u] the
+ *                  bonus draw when the walk stops at node u.
+ * From the root: the current node's children are tried in node order
+ * against a running residual r (first r = p = softmax of the node's target
+ * row; q = softmax of the draft row of the children's depth, both at
+ * temperature 1): child c with token t is accepted when
+ * u_accept[c] < min(1, r(t)/q(t)); after a rejection r <- norm(max(0, r - q)).
+ * An accepted child becomes the current node.  When no child is accepted
+ * (or there is none) the bonus is the smallest token x with
+ * r(0) + ... + r(x) > u_bonus[u] * sum(r).  Outputs as jt_verify_accept.
+ * Softmax and sums are fp32: a decision whose uniform lies within ~1e-5 of
+ * its threshold can differ from an fp64 evaluation.
+ * V <= JT_STOCHASTIC_MAX_V (the vocabulary is held in shared memory across
+ * one thread-block cluster per sequence), else JT_ERR_UNSUPPORTED.
+ * Workspace: jt_workspace_size(JT_OP_VERIFY_ACCEPT, nseq, ...).
+ */
+#define JT_STOCHASTIC_MAX_V 409600
+jt_status jt_verify_accept_stochastic(const float* target_logits, const float* draft_logits,
+                                      const int32_t* parent, const int32_t* token,
+                                      const int32_t* tree_off, int nseq, int N, int64_t V,
+                                      int total_nodes, const double* u_accept, const double* u_bonus,
+                                      int32_t* accept_len, int32_t* path, int32_t* bonus, void* ws,
+                                      size_t ws_bytes, jt_stream_t stream);
 
 /*
  * jt_check -- synchronise `stream`, read the device-side error flag of a

@@ -49,7 +49,7 @@ def _load():
                                           dbl, P, i64, P, P]
             lib.jto_verify_accept.argtypes = [P, P, P, P, i32, i32, i64, i32, dbl, P, P, P]
             lib.jto_verify_accept_stochastic.argtypes = [P, P, P, P, P, i32, i32, i64, P, P, P, P,
-                                                         P, P]
+                                                         P, P, P, P]
             for f in (lib.jto_topw_lse, lib.jto_tree_expand, lib.jto_tree_build,
                       lib.jto_tree_attn, lib.jto_verify_accept, lib.jto_verify_accept_stochastic):
                 f.restype = ctypes.c_int
@@ -180,9 +180,11 @@ def verify_accept(target_logits, parent, token, tree_off, N, rule, log_t=0.0):
     return acc, path, bonus
 
 def verify_accept_stochastic(target_logits, draft_logits, parent, token, tree_off, N, u_accept,
-                             u_bonus):
+                             u_bonus, with_residual=False):
     """Temperature-1 speculative-sampling acceptance over the tree with the
-    caller's uniforms.  Returns (accept_len, path, bonus, min_margin)."""
+    caller's uniforms.  Returns (accept_len, path, bonus, min_margin), and
+    with with_residual=True also (final_r [nseq, V], final_u [nseq]): the
+    normalised residual each bonus was drawn from and the draw's uniform."""
     z = _c(target_logits, np.float32)
     V = z.shape[-1]
     dz = _c(draft_logits, np.float32) if draft_logits is not None else None
@@ -193,9 +195,13 @@ def verify_accept_stochastic(target_logits, draft_logits, parent, token, tree_of
     path = np.empty((nseq, N + 1), np.int32)
     bonus = np.empty(nseq, np.int32)
     margin = np.empty(nseq, np.float64)
+    fr = np.empty((nseq, V), np.float64) if with_residual else None
+    fu = np.empty(nseq, np.float64) if with_residual else None
     _check(_load().jto_verify_accept_stochastic(_ptr(z), _ptr(dz) if dz is not None else None,
                                                 _ptr(parent), _ptr(token), _ptr(tree_off), nseq, N,
                                                 V, _ptr(ua), _ptr(ub), _ptr(acc), _ptr(path),
-                                                _ptr(bonus), _ptr(margin)),
+                                                _ptr(bonus), _ptr(margin), _ptr(fr), _ptr(fu)),
            "verify_accept_stochastic")
+    if with_residual:
+        return acc, path, bonus, margin, fr, fu
     return acc, path, bonus, margin

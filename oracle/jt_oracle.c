@@ -492,18 +492,19 @@ static void softmax_row(const float* z, int64_t V, double* p)
  * draft_logits: [nseq, N, V] fp32 (row d = draft distribution of depth d+1).
  * u_accept, u_bonus: [total] uniforms in [0, 1) (u_accept of a root and
  * u_bonus of a node the walk never stops at are unused).
- * Outputs as jto_verify_accept; min_margin[b] (may be NULL) = the smallest
- * distance, over every decision taken for sequence b, between the uniform
- * and the threshold it was compared with (acceptance: |u - min(1, ratio)|;
- * sampling: the distance of u*sum(r) to the nearest edge of the chosen bin,
- * divided by sum(r)).
+ * Outputs as jto_verify_accept.  Optional outputs (NULL to skip), so that a
+ * caller can tell rounding-sensitive cases apart: min_margin[b] = the
+ * smallest |u_accept - min(1, ratio)| over the acceptance tests taken for
+ * sequence b (infinity when there were none); final_r[b*V + x] = the
+ * normalised residual the bonus was drawn from; final_u[b] = the uniform of
+ * that draw.
  */
 int jto_verify_accept_stochastic(const float* target_logits, const float* draft_logits,
                                  const int32_t* parent, const int32_t* token,
                                  const int32_t* tree_off, int nseq, int N, int64_t V,
                                  const double* u_accept, const double* u_bonus,
                                  int32_t* accept_len, int32_t* path, int32_t* bonus,
-                                 double* min_margin)
+                                 double* min_margin, double* final_r, double* final_u)
 {
     if (!target_logits || (!draft_logits && N > 0) || !parent || !token || !tree_off ||
         !u_accept || !u_bonus || !accept_len || !path || !bonus || nseq < 0 || N < 0 || V < 1)
@@ -571,11 +572,8 @@ int jto_verify_accept_stochastic(const float* target_logits, const float* draft_
         int64_t pick = -1;
         for (int64_t x = 0; x < V; ++x) {
             if (r[x] <= 0.0) continue;
-            const double lo = cum;
             cum += r[x];
             if (cum > target) {
-                const double m2 = (target - lo) < (cum - target) ? (target - lo) : (cum - target);
-                if (m2 / total < margin) margin = m2 / total;
                 pick = x;
                 break;
             }
@@ -583,11 +581,13 @@ int jto_verify_accept_stochastic(const float* target_logits, const float* draft_
         if (pick < 0) { /* rounding left target at the very top: the last bin */
             for (int64_t x = V - 1; x >= 0; --x)
                 if (r[x] > 0.0) { pick = x; break; }
-            margin = 0.0;
         }
         accept_len[b] = d;
         bonus[b] = (int32_t)pick;
         if (min_margin) min_margin[b] = margin;
+        if (final_r)
+            for (int64_t x = 0; x < V; ++x) final_r[(int64_t)b * V + x] = r[x] / total;
+        if (final_u) final_u[b] = u_bonus[off + u];
     }
     free(r);
     free(q);

@@ -91,7 +91,12 @@ def test_hand_worked_residual():
             np.array([0.0, 0.5]), np.array([ub, 0.0]))
         assert acc[0] == 0 and path[0, 0] == 0 and path[0, 1] == -1
         assert bonus[0] == want
-        assert margin[0] == pytest.approx(min(abs(ub - 0.6), ub if ub < 0.6 else 1 - ub), abs=1e-6)
+        assert margin[0] == pytest.approx(0.5)   # |u_accept - min(1, ratio ~ 1e-87)|
+    _, _, _, _, fr, fu = oracle.verify_accept_stochastic(
+        target, q, np.array([-1, 0]), np.array([0, 2]), np.array([0, 2]), 1,
+        np.array([0.0, 0.5]), np.array([0.3, 0.0]), with_residual=True)
+    np.testing.assert_allclose(fr[0], [0.6, 0.4, 0.0], atol=1e-7)
+    assert fu[0] == 0.3
 
 
 def test_draft_equal_to_target_always_accepts_and_leaf_samples_its_row():

@@ -27,7 +27,7 @@ JT_MAX_TREE, JT_MAX_W, JT_MAX_N, JT_PAGE_SIZE = 256, 8, 64, 16
 # every symbol include/jt.h declares
 EXPORTS = ("jt_workspace_size", "jt_tree_build", "jt_tree_topw", "jt_tree_expand",
            "jt_tree_attn_paged", "jt_verify_accept", "jt_check", "jt_status_str", "jt_version",
-           "jt_tree_build_noalloc")
+           "jt_tree_build_noalloc", "jt_verify_accept_stochastic")
 
 _lock = threading.Lock()
 _lib = None
@@ -64,12 +64,15 @@ def load(build_if_missing: bool = True):
         lib.jt_tree_attn_paged.argtypes = [P, P, P, i32, P, i32, i32, P, P, P, i32, i32, i32, i32,
                                            i32, i32, i32, f32, P, P, P, sz, P]
         lib.jt_verify_accept.argtypes = [P, P, P, P, i32, i32, i64, i32, i32, f64, P, P, P, P, sz, P]
+        lib.jt_verify_accept_stochastic.argtypes = [P, P, P, P, P, i32, i32, i64, i32, P, P, P, P, P,
+                                                    P, sz, P]
         lib.jt_check.argtypes = [P, P]
         lib.jt_status_str.argtypes = [i32]
         lib.jt_status_str.restype = ctypes.c_char_p
         lib.jt_version.argtypes = []
         for name in ("jt_tree_build", "jt_tree_topw", "jt_tree_expand", "jt_tree_attn_paged",
-                     "jt_verify_accept", "jt_check", "jt_version", "jt_tree_build_noalloc"):
+                     "jt_verify_accept", "jt_check", "jt_version", "jt_tree_build_noalloc",
+                     "jt_verify_accept_stochastic"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -120,6 +123,35 @@ def workspace(nbytes: int, device=None) -> torch.Tensor:
     are 256-byte aligned; the library needs the header zero before first
     use)."""
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def jt_verify_accept_stochastic(target_logits, draft_logits, parent, token, tree_off, N, u_accept,
+                                u_bonus, out=None, ws=None, stream=None):
+    """Temperature-1 tree acceptance by rejection sampling with the caller's
+    uniforms (fp64 [total_nodes] each).  Returns (accept_len, path, bonus)."""
+    lib = load()
+    _need(target_logits, "target_logits", torch.float32)
+    _need(draft_logits, "draft_logits", torch.float32)
+    for t, n in ((parent, "parent"), (token, "token"), (tree_off, "tree_off")):
+        _need(t, n, torch.int32)
+    _need(u_accept, "u_accept", torch.float64)
+    _need(u_bonus, "u_bonus", torch.float64)
+    total, V = target_logits.shape
+    nseq = tree_off.numel() - 1
+    dev = target_logits.device
+    if out is None:
+        out = (torch.empty(nseq, dtype=torch.int32, device=dev),
+               torch.empty((nseq, N + 1), dtype=torch.int32, device=dev),
+               torch.empty(nseq, dtype=torch.int32, device=dev))
+    acc, path, bonus = out
+    if ws is None:
+        ws = workspace(jt_workspace_size(JT_OP_VERIFY_ACCEPT, nseq, 0, 0, 0, total), dev)
+    rc = lib.jt_verify_accept_stochastic(_ptr(target_logits), _ptr(draft_logits), _ptr(parent), _ptr(token),
+                                         _ptr(tree_off), nseq, N, V, total, _ptr(u_accept), _ptr(u_bonus),
+                                         _ptr(acc), _ptr(path), _ptr(bonus), _ptr(ws), ws.numel(),
+                                         _stream(stream))
+    _check(rc, "jt_verify_accept_stochastic")
+    return acc, path, bonus
 
 
 def jt_check(ws: torch.Tensor, stream=None) -> None:

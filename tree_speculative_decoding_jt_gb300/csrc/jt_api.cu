@@ -190,6 +190,24 @@ jt_status jt_verify_accept(const float* target_logits, const int32_t* parent,
                                           static_cast<char*>(ws), stream));
 }
 
+jt_status jt_verify_accept_stochastic(const float* target_logits, const float* draft_logits,
+                                      const int32_t* parent, const int32_t* token,
+                                      const int32_t* tree_off, int nseq, int N, int64_t V,
+                                      int total_nodes, const double* u_accept, const double* u_bonus,
+                                      int32_t* accept_len, int32_t* path, int32_t* bonus, void* ws,
+                                      size_t ws_bytes, jt_stream_t stream) {
+    if (!target_logits || (!draft_logits && N > 0) || !parent || !token || !tree_off || !u_accept ||
+        !u_bonus || !accept_len || !path || !bonus || nseq < 1 || nseq > 8192 || N < 0 ||
+        N > JT_MAX_TREE || V < 1 || V > 0x7FFFFFFFll || total_nodes < nseq)
+        return JT_ERR_INVALID;
+    if (V > JT_STOCHASTIC_MAX_V) return JT_ERR_UNSUPPORTED;
+    jt_status s = check_ws(ws, ws_bytes, accept_workspace_bytes(nseq, total_nodes));
+    if (s != JT_OK) return s;
+    return from_cuda(verify_stochastic_launch(target_logits, draft_logits, parent, token, tree_off, nseq, N, V,
+                                              total_nodes, u_accept, u_bonus, accept_len, path, bonus,
+                                              static_cast<char*>(ws), stream));
+}
+
 jt_status jt_check(void* ws, jt_stream_t stream) {
     if (!ws) return JT_ERR_WORKSPACE;
     cudaError_t e = cudaStreamSynchronize(stream);

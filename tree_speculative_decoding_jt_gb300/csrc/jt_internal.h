@@ -41,6 +41,13 @@ cudaError_t verify_accept_launch(const float* z, const int32_t* parent, const in
                                  int total_nodes, int rule, double log_t, int32_t* accept_len,
                                  int32_t* path, int32_t* bonus, char* ws, cudaStream_t st);
 
+// verify_stochastic.cu
+cudaError_t verify_stochastic_launch(const float* z, const float* zd, const int32_t* parent,
+                                     const int32_t* token, const int32_t* tree_off, int nseq, int N,
+                                     long long V, int total_nodes, const double* u_accept,
+                                     const double* u_bonus, int32_t* accept_len, int32_t* path,
+                                     int32_t* bonus, char* ws, cudaStream_t st);
+
 // tree_attn.cu / tree_attn_f32.cu
 struct AttnPlan {
     int splits;      // KV splits per (sequence, kv head, row tile)
