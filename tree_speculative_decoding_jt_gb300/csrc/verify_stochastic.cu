@@ -35,51 +35,55 @@ constexpr int kStThreads = 256;
 constexpr int kStWarps = kStThreads / 32;
 
 struct StSlot {   // one exchange: per-CTA values read by every CTA
-    float m_p, s_p, m_q, s_q;  // online (max, sum exp) of the target / draft chunk
+    float m_p, s_p, m_q, s_q;  // max and sum of exp(x - max) of the target / draft chunk
     float rsum;                // sum of the current residual over the chunk
 };
 
 struct StShared {
     StSlot slot[2];            // double-buffered by exchange parity
-    float red_m[kStWarps], red_s[kStWarps], red_m2[kStWarps], red_s2[kStWarps];
+    float red_m[kStWarps], red_s[kStWarps], red_m2[kStWarps], red_s2[kStWarps];  // block reductions
     float scan[kStThreads];
     int par[JT_MAX_TREE], tok[JT_MAX_TREE];
 };
 
-__device__ __forceinline__ void online_merge(float& m, float& s, float m2, float s2) {
-    if (m2 == -INFINITY) return;
-    if (m == -INFINITY) {
-        m = m2;
-        s = s2;
-        return;
-    }
-    const float mm = fmaxf(m, m2);
-    s = s * __expf(m - mm) + s2 * __expf(m2 - mm);
-    m = mm;
-}
-
-// (max, sum exp(x - max)) over the block; result valid in every thread.
-__device__ __forceinline__ void block_online(float& m, float& s, float& m2, float& s2, StShared& sh) {
+// Block-wide max of two values; results valid in every thread.
+__device__ __forceinline__ void block_max2(float& a, float& b, StShared& sh) {
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) {
-        online_merge(m, s, __shfl_xor_sync(0xFFFFFFFFu, m, o), __shfl_xor_sync(0xFFFFFFFFu, s, o));
-        online_merge(m2, s2, __shfl_xor_sync(0xFFFFFFFFu, m2, o), __shfl_xor_sync(0xFFFFFFFFu, s2, o));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+        b = fmaxf(b, __shfl_xor_sync(0xFFFFFFFFu, b, o));
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) {
-        sh.red_m[warp] = m;
-        sh.red_s[warp] = s;
-        sh.red_m2[warp] = m2;
-        sh.red_s2[warp] = s2;
+        sh.red_m[warp] = a;
+        sh.red_m2[warp] = b;
     }
     __syncthreads();
-    m = -INFINITY;
-    s = 0.0f;
-    m2 = -INFINITY;
-    s2 = 0.0f;
+    a = b = -INFINITY;
     for (int w = 0; w < kStWarps; ++w) {
-        online_merge(m, s, sh.red_m[w], sh.red_s[w]);
-        online_merge(m2, s2, sh.red_m2[w], sh.red_s2[w]);
+        a = fmaxf(a, sh.red_m[w]);
+        b = fmaxf(b, sh.red_m2[w]);
+    }
+    __syncthreads();
+}
+
+// Block-wide sum of two values (fixed order); results valid in every thread.
+__device__ __forceinline__ void block_sum2(float& a, float& b, StShared& sh) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        a += __shfl_xor_sync(0xFFFFFFFFu, a, o);
+        b += __shfl_xor_sync(0xFFFFFFFFu, b, o);
+    }
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    if (lane == 0) {
+        sh.red_s[warp] = a;
+        sh.red_s2[warp] = b;
+    }
+    __syncthreads();
+    a = b = 0.0f;
+    for (int w = 0; w < kStWarps; ++w) {
+        a += sh.red_s[w];
+        b += sh.red_s2[w];
     }
     __syncthreads();
 }
@@ -104,8 +108,8 @@ __global__ void __launch_bounds__(kStThreads)
                              const double* __restrict__ u_bonus, int32_t* __restrict__ accept_len,
                              int32_t* __restrict__ path, int32_t* __restrict__ bonus, uint32_t* err) {
     extern __shared__ __align__(16) unsigned char st_dyn[];
-    float* r = reinterpret_cast<float*>(st_dyn);  // [chunk] residual (unnormalised, scale 1/Z)
-    float* q = r + chunk;                         // [chunk] draft distribution
+    float* r = reinterpret_cast<float*>(st_dyn);  // [chunk] residual, r / Z is the distribution
+    float* q = r + chunk;                         // [chunk] exp(draft - max), q / Sq is the distribution
     __shared__ StShared sh;
 
     cg::cluster_group cl = cg::this_cluster();
@@ -143,38 +147,56 @@ __global__ void __launch_bounds__(kStThreads)
                     break;
                 }
         const bool has_children = first_child >= 0;
-        // ---- target row of u and draft row of depth d: chunk values and (max, sum)
+        // ---- target row of u and draft row of depth d: max pass, then one
+        // exp per entry; r holds exp(z - max) (r / Z is p), q holds
+        // exp(zd - max) (q / Sq is the draft distribution)
         const float* zr = z + static_cast<long long>(off + u) * V + x0;
         const float* dr = zd + (static_cast<long long>(b) * N + d) * V + x0;
-        float mp = -INFINITY, sp = 0.0f, mq = -INFINITY, sq = 0.0f;
+        float mp = -INFINITY, mq = -INFINITY;
         for (int i = tid; i < n_loc; i += kStThreads) {
             const float zv = zr[i];
             r[i] = zv;
-            online_merge(mp, sp, zv, 1.0f);
+            mp = fmaxf(mp, zv);
             if (has_children) {
                 const float dv = dr[i];
                 q[i] = dv;
-                online_merge(mq, sq, dv, 1.0f);
+                mq = fmaxf(mq, dv);
             }
         }
-        block_online(mp, sp, mq, sq, sh);
-        if (tid == 0) sh.slot[ex].m_p = mp, sh.slot[ex].s_p = sp, sh.slot[ex].m_q = mq, sh.slot[ex].s_q = sq;
+        block_max2(mp, mq, sh);
+        if (tid == 0) sh.slot[ex].m_p = mp, sh.slot[ex].m_q = mq;
         cl.sync();
-        float Mp = -INFINITY, Sp = 0.0f, Mq = -INFINITY, Sq = 0.0f;
-        for (unsigned k = 0; k < cs; ++k) {  // same order on every CTA
-            const StSlot o = cl.map_shared_rank(&sh.slot[ex], k)[0];
-            online_merge(Mp, Sp, o.m_p, o.s_p);
-            online_merge(Mq, Sq, o.m_q, o.s_q);
+        float Mp = -INFINITY, Mq = -INFINITY;
+        for (unsigned k = 0; k < cs; ++k) {
+            const StSlot* o = cl.map_shared_rank(&sh.slot[ex], k);
+            Mp = fmaxf(Mp, o->m_p);
+            Mq = fmaxf(Mq, o->m_q);
         }
         ex ^= 1;
-        const float inv_p = 1.0f / Sp, inv_q = has_children ? 1.0f / Sq : 0.0f;
+        float sp = 0.0f, sq = 0.0f;
         for (int i = tid; i < n_loc; i += kStThreads) {
-            r[i] = __expf(r[i] - Mp) * inv_p;
-            if (has_children) q[i] = __expf(q[i] - Mq) * inv_q;
+            const float e = __expf(r[i] - Mp);
+            r[i] = e;
+            sp += e;
+            if (has_children) {
+                const float eq = __expf(q[i] - Mq);
+                q[i] = eq;
+                sq += eq;
+            }
         }
+        block_sum2(sp, sq, sh);
+        if (tid == 0) sh.slot[ex].s_p = sp, sh.slot[ex].s_q = sq;
         cl.sync();  // r and q of every chunk are final for the tests below
+        float Sp = 0.0f, Sq = 0.0f;
+        for (unsigned k = 0; k < cs; ++k) {  // same order on every CTA
+            const StSlot* o = cl.map_shared_rank(&sh.slot[ex], k);
+            Sp += o->s_p;
+            Sq += o->s_q;
+        }
+        ex ^= 1;
+        const float inv_q = has_children ? 1.0f / Sq : 0.0f;
         // ---- children in node order
-        float Z = 1.0f;  // r / Z is the current residual distribution
+        float Z = Sp;  // r / Z is the current residual distribution
         int next = -1;
         for (int c = first_child; has_children && c < B && next < 0; ++c) {
             if (sh.par[c] != u) continue;
@@ -182,7 +204,7 @@ __global__ void __launch_bounds__(kStThreads)
             const unsigned owner = static_cast<unsigned>(t / chunk);
             const int lt = t - static_cast<int>(owner) * chunk;
             const float rt = cl.map_shared_rank(r, owner)[lt] / Z;
-            const float qt = cl.map_shared_rank(q, owner)[lt];
+            const float qt = cl.map_shared_rank(q, owner)[lt] * inv_q;
             const float ratio = (qt > 0.0f) ? rt / qt : INFINITY;
             const double a = ratio < 1.0f ? static_cast<double>(ratio) : 1.0;
             if (u_accept[off + c] < a) {
@@ -194,7 +216,7 @@ __global__ void __launch_bounds__(kStThreads)
             const float invZ = 1.0f / Z;
             float ls = 0.0f;
             for (int i = tid; i < n_loc; i += kStThreads) {
-                const float v = fmaxf(r[i] * invZ - q[i], 0.0f);
+                const float v = fmaxf(r[i] * invZ - q[i] * inv_q, 0.0f);
                 r[i] = v;
                 ls += v;
             }
