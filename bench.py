@@ -266,6 +266,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush-mb", type=int, default=512)
     ap.add_argument("--no-graph", action="store_true", help="launch every call eagerly")
+    ap.add_argument("--stochastic", action="store_true",
+                    help="add the temperature-1 acceptance (jt_verify_accept_stochastic) to the step")
     args = ap.parse_args()
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -324,14 +326,14 @@ def main():
     anc = torch.empty((total, 8), dtype=torch.int32, device=dev)
     out = torch.empty_like(d["q"])
     lse = torch.empty((total, Hq), dtype=torch.float32, device=dev)
-    acc = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(2)]
-    path = [torch.empty((nseq, N + 1), dtype=torch.int32, device=dev) for _ in range(2)]
-    bonus = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(2)]
+    acc = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(3)]
+    path = [torch.empty((nseq, N + 1), dtype=torch.int32, device=dev) for _ in range(3)]
+    bonus = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(3)]
     ws_b = jt.workspace(jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, nseq, N, W, c["V"]), dev)
     ws_a = jt.workspace(jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq, Hkv, D,
                                              max_pages, max_tree), dev)
     ws_v = [jt.workspace(jt.jt_workspace_size(jt.JT_OP_VERIFY_ACCEPT, nseq, 0, 0, 0, total), dev)
-            for _ in range(2)]
+            for _ in range(3)]
 
     # target logits need the drafted tokens: build the tree once, then draw
     jt.jt_tree_build(d["draft"], d["root"], d["off"], W, total_nodes=total,
@@ -341,6 +343,10 @@ def main():
     target_np = wk.target_logits(wl, par_h, tok_h)
     h["target"] = torch.from_numpy(target_np)
     d["target"] = h["target"].to(dev)
+    if args.stochastic:  # seeded uniforms of the temperature-1 acceptance, one pair per node
+        _u = np.random.default_rng(replica_seed(cfg, rank) + 1).random((2, total))
+        h["u_acc"], h["u_bon"] = torch.from_numpy(_u[0].copy()), torch.from_numpy(_u[1].copy())
+        d["u_acc"], d["u_bon"] = h["u_acc"].to(dev), h["u_bon"].to(dev)
 
     stream = torch.cuda.current_stream()
     attn_ev = []
@@ -353,6 +359,10 @@ def main():
         for i, rule in enumerate((jt.JT_RULE_GREEDY, jt.JT_RULE_MARGIN)):
             jt.jt_verify_accept(inp["target"], parent, token, inp["off"], N, rule=rule, log_t=log_t,
                                 out=(acc[i], path[i], bonus[i]), ws=ws_v[i])
+        if args.stochastic:
+            jt.jt_verify_accept_stochastic(inp["target"], inp["draft"], parent, token, inp["off"], N,
+                                           inp["u_acc"], inp["u_bon"], out=(acc[2], path[2], bonus[2]),
+                                           ws=ws_v[2])
 
     flush = torch.empty(args.flush_mb * (1 << 20), dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -426,8 +436,10 @@ def main():
     e2e = None
     if args.e2e_steps > 0:
         hp = {k: v.pin_memory() for k, v in h.items()}
-        res_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in
-                 (parent, token, out, acc[0], path[0], bonus[0], acc[1], path[1], bonus[1])]
+        results = [parent, token, out, acc[0], path[0], bonus[0], acc[1], path[1], bonus[1]]
+        if args.stochastic:
+            results += [acc[2], path[2], bonus[2]]
+        res_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
         h2d = sum(v.numel() * v.element_size() for v in hp.values())
         d2h = sum(v.numel() * v.element_size() for v in res_h)
         dd = {k: torch.empty_like(v) for k, v in d.items()}
@@ -438,8 +450,7 @@ def main():
             for k in hp:
                 dd[k].copy_(hp[k], non_blocking=True)
             step(dd)
-            for dst, src in zip(res_h, (parent, token, out, acc[0], path[0], bonus[0], acc[1],
-                                        path[1], bonus[1])):
+            for dst, src in zip(res_h, results):
                 dst.copy_(src, non_blocking=True)
             torch.cuda.synchronize()
         e2e_s = (time.perf_counter() - t0) / args.e2e_steps
@@ -481,7 +492,7 @@ def main():
     # kernel (+ split combine when the plan splits the keys); two acceptances
     attn_split = jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq, Hkv, D,
                                       max_pages, max_tree) > 256
-    launches_per_step = 3 + (2 if attn_split else 1) + 2
+    launches_per_step = 3 + (2 if attn_split else 1) + 2 + (1 if args.stochastic else 0)
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -490,7 +501,8 @@ def main():
             "config": {"workload": c["name"], "nseq": nseq, "tree_nodes": total,
                        "prefix_len": [int(x) for x in wl.prefix_len[:4]] + (["..."] if nseq > 4 else []),
                        "Hq": Hq, "Hkv": Hkv, "head_dim": D, "N": N, "W": W, "V": c["V"],
-                       "step": "tree_build + tree_attn_paged + verify_accept(greedy) + verify_accept(margin t=0.8)",
+                       "step": "tree_build + tree_attn_paged + verify_accept(greedy) + verify_accept(margin t=0.8)"
+                               + (" + verify_accept_stochastic(T=1)" if args.stochastic else ""),
                        "l2": f"flushed before every step ({args.flush_mb} MiB write)",
                        "launch": "eager" if args.no_graph else "cuda_graph replay of the step",
                        "parallelism": f"replicas x{world}"},
