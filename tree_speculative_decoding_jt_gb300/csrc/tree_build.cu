@@ -30,7 +30,8 @@
 namespace jt {
 
 constexpr int kTopwThreads = 256;
-constexpr int kTopwPerThread = 32;
+constexpr int kTopwPerThread = 32;     // entries per thread with many rows
+constexpr int kTopwPerThreadMin = 16;  // with few rows: more, shorter CTAs
 constexpr int kExpandThreads = 1024;  // ranking uses all; set-sized steps use the first 256
 constexpr unsigned kFull = 0xFFFFFFFFu;
 
@@ -154,12 +155,13 @@ __device__ __forceinline__ long long topw_slot_id(long long begin, int tid, int 
 // `avail` has a bit per slot still eligible (in range and not taken).  The
 // eligible slots are scanned once; a lane only rescans after both of its
 // heads were taken (rare: two of the warp's top-W in one lane).
-__device__ __forceinline__ void lane_best2(const float (&x)[kTopwPerThread], uint32_t avail, float& v1,
+template <int PER>
+__device__ __forceinline__ void lane_best2(const float (&x)[PER], uint32_t avail, float& v1,
                                            int& s1, float& v2, int& s2) {
     v1 = v2 = -INFINITY;
     s1 = s2 = -1;
 #pragma unroll
-    for (int s = 0; s < kTopwPerThread; ++s) {
+    for (int s = 0; s < PER; ++s) {
         if ((avail >> s) & 1u) {
             const float xs = x[s];
             if (s1 < 0 || xs > v1) {
@@ -188,12 +190,12 @@ __device__ __forceinline__ void warp_best(float& v, int& id) {
     }
 }
 
-template <int W, bool VEC>
+template <int W, bool VEC, int PER>
 __global__ void __launch_bounds__(kTopwThreads)
     topw_partial_kernel(const float* __restrict__ z, long long V, int splits, ExpTable tab,
                         float* __restrict__ part_v, int* __restrict__ part_id,
                         float* __restrict__ part_m, float2* __restrict__ part_s) {
-    constexpr int CH = kTopwThreads * kTopwPerThread;
+    constexpr int CH = kTopwThreads * PER;
     constexpr int NW = kTopwThreads / 32;
     __shared__ float s_thi[64], s_tlo[64];
     __shared__ float s_wv[NW][W];
@@ -212,10 +214,10 @@ __global__ void __launch_bounds__(kTopwThreads)
     const long long begin = static_cast<long long>(sp) * CH;
     const long long end = min(V, begin + CH);
 
-    float x[kTopwPerThread];
+    float x[PER];
     if (VEC) {
 #pragma unroll
-        for (int i = 0; i < kTopwPerThread / 4; ++i) {
+        for (int i = 0; i < PER / 4; ++i) {
             const long long e = begin + 4ll * (tid + kTopwThreads * i);
             float4 f = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             if (e < end) f = __ldg(reinterpret_cast<const float4*>(zr + e));
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kTopwThreads)
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < kTopwPerThread; ++i) {
+        for (int i = 0; i < PER; ++i) {
             const long long e = begin + tid + static_cast<long long>(kTopwThreads) * i;
             x[i] = (e < end) ? __ldg(zr + e) : -INFINITY;
         }
@@ -235,10 +237,10 @@ __global__ void __launch_bounds__(kTopwThreads)
     int nvalid = 0;
     if (VEC) {
         const long long g = (end - begin - 4ll * tid + 4ll * kTopwThreads - 1) / (4ll * kTopwThreads);
-        nvalid = 4 * static_cast<int>(max(0ll, min(static_cast<long long>(kTopwPerThread / 4), g)));
+        nvalid = 4 * static_cast<int>(max(0ll, min(static_cast<long long>(PER / 4), g)));
     } else {
         const long long g = (end - begin - tid + kTopwThreads - 1) / kTopwThreads;
-        nvalid = static_cast<int>(max(0ll, min(static_cast<long long>(kTopwPerThread), g)));
+        nvalid = static_cast<int>(max(0ll, min(static_cast<long long>(PER), g)));
     }
     uint32_t avail = (nvalid >= 32) ? 0xFFFFFFFFu : ((1u << nvalid) - 1u);
     float bv, bv2;
@@ -255,7 +257,7 @@ __global__ void __launch_bounds__(kTopwThreads)
         // instead of 0, far below the sum's rounding (the sum is >= 1)
         const float floor_v = mw - 87.0f;
 #pragma unroll
-        for (int i = 0; i < kTopwPerThread; ++i) {
+        for (int i = 0; i < PER; ++i) {
             float dh, dl;
             two_sum(fmaxf(x[i], floor_v), -mw, dh, dl);
             const ffloat y = ffexp_in_range(fmaxf(dh, -87.0f), dl, s_thi, s_tlo);
@@ -814,13 +816,20 @@ static cudaError_t set_expand_smem() {
     return done;
 }
 
-static int topw_splits(long long V) {
-    const long long CH = kTopwThreads * kTopwPerThread;
+static int topw_splits(long long V, int per) {
+    const long long CH = static_cast<long long>(kTopwThreads) * per;
     return static_cast<int>((V + CH - 1) / CH);
 }
 
+// Entries per thread: 32, or 16 when 32 would give fewer than four CTAs per
+// SM (few rows: shorter per-thread chains, more CTAs).
+static int topw_per_thread(long long rows, long long V) {
+    const long long ctas = rows * topw_splits(V, kTopwPerThread);
+    return (ctas < 4ll * device_sm_count()) ? kTopwPerThreadMin : kTopwPerThread;
+}
+
 size_t topw_workspace_bytes(long long rows, long long V, int W) {
-    const long long p = rows * topw_splits(V);
+    const long long p = rows * topw_splits(V, topw_per_thread(rows, V));
     size_t bytes = 0;
     bytes += align_up(rows * W * sizeof(int32_t));  // merged tables (tree build)
     bytes += align_up(rows * W * sizeof(double));
@@ -843,9 +852,9 @@ struct TopwParts {
     int splits;
 };
 
-static TopwParts carve_topw(char* base, long long rows, long long V, int W) {
+static TopwParts carve_topw(char* base, long long rows, long long V, int W, int per) {
     TopwParts t;
-    t.splits = topw_splits(V);
+    t.splits = topw_splits(V, per);
     const long long p = rows * t.splits;
     t.tok = reinterpret_cast<int32_t*>(base);
     base += align_up(rows * W * sizeof(int32_t));
@@ -864,23 +873,29 @@ static TopwParts carve_topw(char* base, long long rows, long long V, int W) {
 }
 
 template <int W>
-static cudaError_t launch_topw_partial(const float* z, long long rows, long long V, TopwParts& t,
+static cudaError_t launch_topw_partial(const float* z, long long rows, long long V, int per, TopwParts& t,
                                        cudaStream_t st) {
     const ExpTable& tab = exp_table();
     const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
     dim3 grid(t.splits, static_cast<unsigned>(rows));
-    if (vec)
-        return launch_kernel(topw_partial_kernel<W, true>, grid, dim3(kTopwThreads), 0, st, 0, z, V,
-                          t.splits, tab, t.v, t.id, t.m, t.s);
-    return launch_kernel(topw_partial_kernel<W, false>, grid, dim3(kTopwThreads), 0, st, 0, z, V, t.splits,
-                      tab, t.v, t.id, t.m, t.s);
+#define JT_TOPW_LAUNCH(VEC_, PER_)                                                                       \
+    return launch_kernel(topw_partial_kernel<W, VEC_, PER_>, grid, dim3(kTopwThreads), 0, st, 0, z, V, \
+                         t.splits, tab, t.v, t.id, t.m, t.s)
+    if (per == kTopwPerThreadMin) {
+        if (vec) JT_TOPW_LAUNCH(true, kTopwPerThreadMin);
+        JT_TOPW_LAUNCH(false, kTopwPerThreadMin);
+    }
+    if (vec) JT_TOPW_LAUNCH(true, kTopwPerThread);
+    JT_TOPW_LAUNCH(false, kTopwPerThread);
+#undef JT_TOPW_LAUNCH
 }
 
 template <int W>
 static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t* tok, double* lp,
                             double* lse, char* ws_parts, cudaStream_t st) {
-    TopwParts t = carve_topw(ws_parts, rows, V, W);
-    cudaError_t e = launch_topw_partial<W>(z, rows, V, t, st);
+    const int per = topw_per_thread(rows, V);
+    TopwParts t = carve_topw(ws_parts, rows, V, W, per);
+    cudaError_t e = launch_topw_partial<W>(z, rows, V, per, t, st);
     if (e != cudaSuccess) return e;
     const long long warps_per_block = 8;
     const unsigned blocks = static_cast<unsigned>((rows + warps_per_block - 1) / warps_per_block);
@@ -894,9 +909,10 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
                              int32_t* token, int32_t* depth, uint32_t* anc, char* ws_parts,
                              uint32_t* err, cudaStream_t st) {
     const long long rows = static_cast<long long>(nseq) * N;
-    TopwParts t = carve_topw(ws_parts, rows, V, W);
+    const int per = topw_per_thread(rows, V);
+    TopwParts t = carve_topw(ws_parts, rows, V, W, per);
     if (rows > 0) {
-        cudaError_t e = launch_topw_partial<W>(z, rows, V, t, st);
+        cudaError_t e = launch_topw_partial<W>(z, rows, V, per, t, st);
         if (e != cudaSuccess) return e;
         const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
         e = launch_kernel(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
