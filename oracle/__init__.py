@@ -50,8 +50,10 @@ def _load():
             lib.jto_verify_accept.argtypes = [P, P, P, P, i32, i32, i64, i32, dbl, P, P, P]
             lib.jto_verify_accept_stochastic.argtypes = [P, P, P, P, P, i32, i32, i64, P, P, P, P,
                                                          P, P, P, P]
+            lib.jto_tree_build_mixed.argtypes = [P, P, P, i32, i32, i32, i64, dbl, P, P, P, P, P, P, P]
             for f in (lib.jto_topw_lse, lib.jto_tree_expand, lib.jto_tree_build,
-                      lib.jto_tree_attn, lib.jto_verify_accept, lib.jto_verify_accept_stochastic):
+                      lib.jto_tree_attn, lib.jto_verify_accept, lib.jto_verify_accept_stochastic,
+                      lib.jto_tree_build_mixed):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -125,6 +127,24 @@ def tree_build(draft_logits, root_token, tree_off, W):
                                   _ptr(gap), _ptr(tok), _ptr(lp), _ptr(lse)), "tree_build")
     return dict(parent=parent, token=token, depth=depth, anc=anc, score=score, gap=gap,
                 tok=tok, lp=lp, lse=lse)
+
+
+def tree_build_mixed(draft_logits, root_token, tree_off, W, alpha):
+    """Tree build whose step from depth d to d+1 scores
+    (1 - alpha) * log-prob - alpha * entropy(draft row d), alpha in [0, 1).
+
+    Returns dict(parent, token, depth, anc, score, gap, entropy [nseq, N])."""
+    z = _c(draft_logits, np.float32)
+    nseq, N, V = z.shape
+    root_token, tree_off = _c(root_token, np.int32), _c(tree_off, np.int32)
+    total = int(tree_off[-1])
+    parent, token, depth, anc, score = _tree_outputs(total)
+    gap = np.empty(nseq, np.float64)
+    ent = np.empty((nseq, N), np.float64)
+    _check(_load().jto_tree_build_mixed(_ptr(z), _ptr(root_token), _ptr(tree_off), nseq, N, W, V,
+                                        float(alpha), _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc),
+                                        _ptr(score), _ptr(gap), _ptr(ent)), "tree_build_mixed")
+    return dict(parent=parent, token=token, depth=depth, anc=anc, score=score, gap=gap, entropy=ent)
 
 
 def tree_attn(q, k_cache, v_cache, block_table, prefix_len, tree_off, parent, scale, rows=None):
