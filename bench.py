@@ -176,18 +176,44 @@ def profiled_traffic(kernel_file):
 # --------------------------------------------------------------------------
 # CPU baseline: the oracle, as it stands, on a bounded sample
 # --------------------------------------------------------------------------
-def cpu_oracle_sample(wl, tree_parent, tree_token, target, attn_nodes):
+def oracle_build(wl, alpha):
+    """The oracle's tree build of the step: plain, or entropy-mixed scores."""
+    import oracle
+
+    if alpha == 0.0:
+        return oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"])
+    return oracle.tree_build_mixed(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"], alpha)
+
+
+def oracle_accept(wl, target, parent, token, uniforms):
+    """The oracle's acceptance rules of the step (greedy, margin, and the
+    temperature-1 rule when uniforms are given)."""
     import oracle
 
     c = wl.cfg
+    oracle.verify_accept(target, parent, token, wl.tree_off, c["N"], 0)
+    oracle.verify_accept(target, parent, token, wl.tree_off, c["N"], 1, math.log(c["t"]))
+    if uniforms is not None:
+        oracle.verify_accept_stochastic(target, wl.draft_logits, parent, token, wl.tree_off, c["N"],
+                                        uniforms[0], uniforms[1])
+
+
+def step_uniforms(cfg, rank, total):
+    """Seeded uniforms of the temperature-1 acceptance, one pair per node."""
+    u = np.random.default_rng(replica_seed(cfg, rank) + 1).random((2, total))
+    return u[0].copy(), u[1].copy()
+
+
+def cpu_oracle_sample(wl, tree_parent, tree_token, target, attn_nodes, alpha, uniforms):
+    import oracle
+
     t0 = time.perf_counter()
-    tr = oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, c["W"])
+    tr = oracle_build(wl, alpha)
     t1 = time.perf_counter()
     oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len, wl.tree_off,
                      tr["parent"], wl.scale, rows=attn_nodes)
     t2 = time.perf_counter()
-    oracle.verify_accept(target, tree_parent, tree_token, wl.tree_off, c["N"], 0)
-    oracle.verify_accept(target, tree_parent, tree_token, wl.tree_off, c["N"], 1, math.log(c["t"]))
+    oracle_accept(wl, target, tree_parent, tree_token, uniforms)
     t3 = time.perf_counter()
     # per-node cost of the whole step: build and accept per node of the
     # batch, attention per sampled node
@@ -200,6 +226,12 @@ def attn_sample_nodes(wl, k):
     return np.arange(0, wl.total, step, dtype=np.int32)[:k]
 
 
+def step_name(args):
+    build = "tree_build" if args.alpha == 0.0 else f"tree_build_mixed(alpha={args.alpha:g})"
+    return (build + " + tree_attn_paged + verify_accept(greedy) + verify_accept(margin t=0.8)"
+            + (" + verify_accept_stochastic(T=1)" if args.stochastic else ""))
+
+
 def run_reference(args, rank):
     """The oracle, as it stands, on the host cores.  One reference step is
     the attention of one tree node (rotating over the batch) plus a 1/B
@@ -210,15 +242,15 @@ def run_reference(args, rank):
         return
     import oracle
 
-    wl = wk.make(args.config)
+    wl = wk.make(args.config, seed=replica_seed(args.config, 0))
     c = wl.cfg
     t0 = time.perf_counter()
-    tr = oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, c["W"])
+    tr = oracle_build(wl, args.alpha)
     t_build = time.perf_counter() - t0
     target = wk.target_logits(wl, tr["parent"], tr["token"])
+    uniforms = step_uniforms(args.config, 0, wl.total) if args.stochastic else None
     t0 = time.perf_counter()
-    oracle.verify_accept(target, tr["parent"], tr["token"], wl.tree_off, c["N"], 0)
-    oracle.verify_accept(target, tr["parent"], tr["token"], wl.tree_off, c["N"], 1, math.log(c["t"]))
+    oracle_accept(wl, target, tr["parent"], tr["token"], uniforms)
     t_accept = time.perf_counter() - t0
 
     def attn_one(n):
@@ -240,9 +272,10 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_node,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": c["name"], "nseq": wl.nseq, "tree_nodes": wl.total},
+        "data": "synthetic", "config": {"workload": c["name"], "nseq": wl.nseq, "tree_nodes": wl.total,
+                                         "step": step_name(args)},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": f"tree build ({t_build:.2f} s) and both acceptance rules "
+                         "sample": f"tree build ({t_build:.2f} s) and the acceptance rules "
                                    f"({t_accept:.2f} s) over all {wl.total} nodes once, attention "
                                    f"of one node per step for {args.steps} steps ({wall:.1f} s); "
                                    f"single-threaded C, fp64"},
@@ -268,7 +301,11 @@ def main():
     ap.add_argument("--no-graph", action="store_true", help="launch every call eagerly")
     ap.add_argument("--stochastic", action="store_true",
                     help="add the temperature-1 acceptance (jt_verify_accept_stochastic) to the step")
+    ap.add_argument("--alpha", type=float, default=0.0,
+                    help="entropy weight of the tree build's step scores (jt_tree_build_mixed); 0 = plain")
     args = ap.parse_args()
+    if not 0.0 <= args.alpha <= 1.0:
+        raise SystemExit("--alpha must lie in [0, 1]")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -329,31 +366,38 @@ def main():
     acc = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(3)]
     path = [torch.empty((nseq, N + 1), dtype=torch.int32, device=dev) for _ in range(3)]
     bonus = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(3)]
-    ws_b = jt.workspace(jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, nseq, N, W, c["V"]), dev)
+    build_op = jt.JT_OP_TREE_BUILD_MIXED if args.alpha > 0 else jt.JT_OP_TREE_BUILD
+    ws_b = jt.workspace(jt.jt_workspace_size(build_op, nseq, N, W, c["V"]), dev)
+
+    def build(inp):
+        if args.alpha > 0:
+            jt.jt_tree_build_mixed(inp["draft"], inp["root"], inp["off"], W, args.alpha, total_nodes=total,
+                                   out=(parent, token, depth, anc), ws=ws_b)
+        else:
+            jt.jt_tree_build(inp["draft"], inp["root"], inp["off"], W, total_nodes=total,
+                             out=(parent, token, depth, anc), ws=ws_b)
     ws_a = jt.workspace(jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq, Hkv, D,
                                              max_pages, max_tree), dev)
     ws_v = [jt.workspace(jt.jt_workspace_size(jt.JT_OP_VERIFY_ACCEPT, nseq, 0, 0, 0, total), dev)
             for _ in range(3)]
 
     # target logits need the drafted tokens: build the tree once, then draw
-    jt.jt_tree_build(d["draft"], d["root"], d["off"], W, total_nodes=total,
-                     out=(parent, token, depth, anc), ws=ws_b)
+    build(d)
     jt.jt_check(ws_b)
     par_h, tok_h, dep_h = parent.cpu().numpy(), token.cpu().numpy(), depth.cpu().numpy()
     target_np = wk.target_logits(wl, par_h, tok_h)
     h["target"] = torch.from_numpy(target_np)
     d["target"] = h["target"].to(dev)
-    if args.stochastic:  # seeded uniforms of the temperature-1 acceptance, one pair per node
-        _u = np.random.default_rng(replica_seed(cfg, rank) + 1).random((2, total))
-        h["u_acc"], h["u_bon"] = torch.from_numpy(_u[0].copy()), torch.from_numpy(_u[1].copy())
+    uniforms = step_uniforms(cfg, rank, total) if args.stochastic else None
+    if uniforms is not None:
+        h["u_acc"], h["u_bon"] = torch.from_numpy(uniforms[0]), torch.from_numpy(uniforms[1])
         d["u_acc"], d["u_bon"] = h["u_acc"].to(dev), h["u_bon"].to(dev)
 
     stream = torch.cuda.current_stream()
     attn_ev = []
 
     def step(inp):
-        jt.jt_tree_build(inp["draft"], inp["root"], inp["off"], W, total_nodes=total,
-                         out=(parent, token, depth, anc), ws=ws_b)
+        build(inp)
         jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], inp["off"], anc,
                               scale=wl.scale, max_tree=max_tree, out=out, lse=lse, ws=ws_a)
         for i, rule in enumerate((jt.JT_RULE_GREEDY, jt.JT_RULE_MARGIN)):
@@ -482,9 +526,9 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nodes = attn_sample_nodes(wl, args.cpu_attn_nodes)
-        v, secs = cpu_oracle_sample(wl, par_h, tok_h, target_np, nodes)
+        v, secs = cpu_oracle_sample(wl, par_h, tok_h, target_np, nodes, args.alpha, uniforms)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"full tree build and both acceptance rules over all {total} nodes, "
+               "sample": f"full tree build and the step's acceptance rules over all {total} nodes, "
                          f"attention for {len(nodes)} of {total} nodes ({secs:.1f} s, "
                          f"single-threaded C, fp64)"}
 
@@ -501,8 +545,7 @@ def main():
             "config": {"workload": c["name"], "nseq": nseq, "tree_nodes": total,
                        "prefix_len": [int(x) for x in wl.prefix_len[:4]] + (["..."] if nseq > 4 else []),
                        "Hq": Hq, "Hkv": Hkv, "head_dim": D, "N": N, "W": W, "V": c["V"],
-                       "step": "tree_build + tree_attn_paged + verify_accept(greedy) + verify_accept(margin t=0.8)"
-                               + (" + verify_accept_stochastic(T=1)" if args.stochastic else ""),
+                       "step": step_name(args),
                        "l2": f"flushed before every step ({args.flush_mb} MiB write)",
                        "launch": "eager" if args.no_graph else "cuda_graph replay of the step",
                        "parallelism": f"replicas x{world}"},

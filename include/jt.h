@@ -79,7 +79,7 @@ typedef enum {
 typedef enum { JT_DTYPE_F32 = 0, JT_DTYPE_BF16 = 1 } jt_dtype;
 typedef enum { JT_RULE_GREEDY = 0, JT_RULE_MARGIN = 1 } jt_rule;
 typedef enum { JT_OP_TREE_BUILD = 0, JT_OP_TREE_ATTN = 1, JT_OP_VERIFY_ACCEPT = 2,
-               JT_OP_TREE_TOPW = 3 } jt_op;
+               JT_OP_TREE_TOPW = 3, JT_OP_TREE_BUILD_MIXED = 4 } jt_op;
 
 /* Limits of this build. */
 #define JT_MAX_TREE 256   /* B_b (bitset width) */
@@ -92,6 +92,7 @@ typedef enum { JT_OP_TREE_BUILD = 0, JT_OP_TREE_ATTN = 1, JT_OP_VERIFY_ACCEPT = 
  * op does not use are ignored; pass 0).  Depends on the current device's SM
  * count for JT_OP_TREE_ATTN.  Returns 0 for invalid sizes.
  *   TREE_BUILD:    nseq, N, W, V
+ *   TREE_BUILD_MIXED: nseq, N, W, V
  *   TREE_TOPW:     nseq*N rows given as nseq (N=1), W, V
  *   TREE_ATTN:     nseq, total_nodes, Hq, Hkv, D, max_pages, max_tree
  *   VERIFY_ACCEPT: nseq, total_nodes
@@ -122,6 +123,34 @@ jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
                         const int32_t* tree_off, int nseq, int N, int W, int64_t V,
                         int total_nodes, int32_t* parent, int32_t* token, int32_t* depth,
                         uint32_t* anc, void* ws, size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_tree_build_mixed -- jt_tree_build with entropy-mixed step scores
+ * ([JS-art] section 五: besides the cumulative probability, the authors
+ * score candidates by the information entropy at each position and by a
+ * weighted mix of the two).  Reading: the step from depth d to d+1 through
+ * token x adds
+ *     (1 - alpha) * lp_d(x) - alpha * H_d,
+ * H_d = lse_d - sum_v softmax(z_d)_v * z_d,v the natural-log entropy of
+ * draft row d (masked entries, z = -inf, add 0), evaluated in fp64 as
+ * ((1 - alpha) * lp) - (alpha * H); a candidate of probability 0 (lp =
+ * -inf) keeps -inf under every weight.
+ *   alpha: in [0, 1]; 0 gives exactly jt_tree_build's trees (the same
+ *          kernels run); 1 is the pure entropy score, under which every
+ *          node of a depth ties and the queue's tie-breaks (depth, then
+ *          token, then parent) decide.  Outside [0, 1]: JT_ERR_INVALID.
+ * Every step still adds a value <= 0; the expansion (queue key and
+ * tie-breaks), outputs, limits and error behaviour are those of
+ * jt_tree_build.  The entropy sum is accumulated in float-float (about
+ * 1e-12 relative), so trees equal the fp64 definition's except where two
+ * different candidate scores lie closer than that.
+ * Workspace: jt_workspace_size(JT_OP_TREE_BUILD_MIXED, nseq, N, W, V).
+ */
+jt_status jt_tree_build_mixed(const float* draft_logits, const int32_t* root_token,
+                              const int32_t* tree_off, int nseq, int N, int W, int64_t V,
+                              int total_nodes, double alpha, int32_t* parent, int32_t* token,
+                              int32_t* depth, uint32_t* anc, void* ws, size_t ws_bytes,
+                              jt_stream_t stream);
 
 /*
  * jt_tree_build_noalloc -- jt_tree_build with no caller workspace and no

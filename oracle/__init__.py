@@ -131,7 +131,8 @@ def tree_build(draft_logits, root_token, tree_off, W):
 
 def tree_build_mixed(draft_logits, root_token, tree_off, W, alpha):
     """Tree build whose step from depth d to d+1 scores
-    (1 - alpha) * log-prob - alpha * entropy(draft row d), alpha in [0, 1).
+    (1 - alpha) * log-prob - alpha * entropy(draft row d), alpha in [0, 1]
+    (1: pure entropy score); a candidate of probability 0 stays at -inf.
 
     Returns dict(parent, token, depth, anc, score, gap, entropy [nseq, N])."""
     z = _c(draft_logits, np.float32)

@@ -600,16 +600,18 @@ int jto_verify_accept_stochastic(const float* target_logits, const float* draft_
 /* entropy at each position, and a weighted mix of the cumulative            */
 /* probability and the entropy.  Reading: each step from depth d to d+1 adds */
 /* (1 - alpha) * lp_d(token) - alpha * H_d, with H_d the entropy (natural    */
-/* log) of draft row d and alpha in [0, 1); alpha = 0 is the plain build.    */
-/* Every step still adds a value <= 0 and siblings keep their log-prob       */
-/* order, so the best-first expansion is unchanged apart from the table.     */
+/* log) of draft row d and alpha in [0, 1]; alpha = 0 is the plain build    */
+/* and alpha = 1 the pure entropy score.  A candidate of probability 0       */
+/* (lp = -inf) keeps the score -inf under every weight.  Every step still    */
+/* adds a value <= 0; the best-first queue (with its tie-breaks) is the      */
+/* plain build's, fed the mixed table.                                       */
 /* ------------------------------------------------------------------------ */
 int jto_tree_build_mixed(const float* draft_logits, const int32_t* root_token, const int32_t* tree_off,
                          int nseq, int N, int W, int64_t V, double alpha,
                          int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc,
                          double* score, double* gap, double* entropy_out)
 {
-    if (!draft_logits || nseq < 0 || N < 0 || W < 1 || V < W || !(alpha >= 0.0) || !(alpha < 1.0))
+    if (!draft_logits || nseq < 0 || N < 0 || W < 1 || V < W || !(alpha >= 0.0) || !(alpha <= 1.0))
         return JTO_ERR_INVALID;
     int64_t rows = (int64_t)nseq * N;
     int32_t* tk = (int32_t*)malloc(sizeof(int32_t) * (size_t)(rows * W + 1));
@@ -619,13 +621,16 @@ int jto_tree_build_mixed(const float* draft_logits, const int32_t* root_token, c
     if (rc == JTO_OK) rc = jto_topw_lse(draft_logits, rows, V, W, tk, l, s);
     if (rc == JTO_OK) {
         for (int64_t r = 0; r < rows; ++r) {
-            /* H = -sum p log p = lse - sum p z, p = exp(z - lse), sum in order */
+            /* H = -sum p log p = lse - sum p z, p = exp(z - lse), sum in order;
+               a masked entry (z = -inf, p = 0) adds nothing (0 log 0 = 0) */
             const float* row = draft_logits + r * V;
             double pz = 0.0;
-            for (int64_t v = 0; v < V; ++v) pz += exp((double)row[v] - s[r]) * (double)row[v];
+            for (int64_t v = 0; v < V; ++v)
+                if (row[v] != -INFINITY) pz += exp((double)row[v] - s[r]) * (double)row[v];
             const double H = s[r] - pz;
             if (entropy_out) entropy_out[r] = H;
             for (int k = 0; k < W; ++k) {
+                if (l[r * W + k] == -INFINITY) continue; /* probability 0 stays -inf */
                 const double a = (1.0 - alpha) * l[r * W + k];
                 const double b = alpha * H;
                 l[r * W + k] = a - b;

@@ -1,0 +1,156 @@
+"""GPU parity of the entropy-mixed tree build (jt_tree_build_mixed) against
+the oracle ("加速AI思考…" section 五: candidates scored by per-position
+entropy and by a weighted mix of cumulative probability and entropy; each
+step adds (1 - alpha) * log-prob - alpha * H(draft row)).
+
+The trees must be bit-exact unless the oracle reports a decision gap below
+1e-9 (the kernel's entropy is float-float, ~1e-12 relative); alpha = 0 must
+give exactly jt_tree_build's trees.  At alpha = 1 every node of a depth ties
+exactly on both sides (each adds the same table values in the same order),
+so the gap is 0 by construction and the comparison is made without it, on
+rows whose entropies keep depths well apart."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import tree_speculative_decoding_jt_gb300 as jt
+from tree_speculative_decoding_jt_gb300 import workloads as wk
+from gpu_util import dev
+
+pytestmark = pytest.mark.gpu
+
+AMBIGUOUS_GAP = 1e-9
+
+
+def _got(z, root, off, W, alpha, total):
+    out = jt.jt_tree_build_mixed(dev(z), dev(root), dev(off), W, alpha, total_nodes=total)
+    torch.cuda.synchronize()
+    return [t.cpu().numpy() for t in out]
+
+
+def _compare(z, root, off, W, alpha):
+    want = oracle.tree_build_mixed(z, root, off, W, alpha)
+    if alpha == 1.0:
+        assert np.min(want["entropy"]) > 1e-6   # depths stay apart; exact ties within a depth
+    elif np.min(want["gap"]) < AMBIGUOUS_GAP:
+        pytest.skip(f"ambiguous: oracle decision gap {np.min(want['gap']):.3g} below rounding noise")
+    par, tk, dp, anc = _got(z, root, off, W, alpha, int(off[-1]))
+    np.testing.assert_array_equal(par, want["parent"])
+    np.testing.assert_array_equal(tk, want["token"])
+    np.testing.assert_array_equal(dp, want["depth"])
+    np.testing.assert_array_equal(anc.view(np.uint32), want["anc"])
+    return want
+
+
+@pytest.mark.parametrize("cfg,alpha", [(1, 0.3), (3, 0.5), (5, 0.2), (5, 0.7)])
+def test_mixed_bit_exact_full_configs(cfg, alpha):
+    wl = wk.make(cfg, with_draft=True)
+    _compare(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"], alpha)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_mixed_bit_exact_ragged_small(seed):
+    """Rows whose entropies differ widely (per-row logit scales from 0.2 to
+    4), so the mixed score reorders depths against the plain build."""
+    rng = np.random.default_rng(100 + seed)
+    nseq = int(rng.integers(1, 7))
+    N, W = int(rng.integers(1, 9)), int(rng.integers(1, 9))
+    V = int(rng.integers(W, 5000))
+    full = sum(W ** d for d in range(N + 1))
+    budgets = [int(rng.integers(1, min(full, 256) + 1)) for _ in range(nseq)]
+    scale = rng.uniform(0.2, 4.0, size=(nseq, N, 1))
+    z = (rng.standard_normal((nseq, N, V)) * scale).astype(np.float32)
+    root = rng.integers(0, V, size=nseq).astype(np.int32)
+    off = np.concatenate([[0], np.cumsum(budgets)]).astype(np.int32)
+    _compare(z, root, off, W, float(rng.uniform(0.05, 0.95)))
+
+
+def test_mixed_reorders_the_tree():
+    """A high-entropy first row and a peaked second row: with alpha > 0 the
+    mixed build must differ from the plain one (the oracle says how)."""
+    rng = np.random.default_rng(7)
+    V, N, W = 3000, 4, 3
+    z = rng.standard_normal((2, N, V)).astype(np.float32)
+    z[:, 0] *= 0.1
+    z[:, 1] *= 6.0
+    root = np.array([1, 2], np.int32)
+    off = np.array([0, 40, 100], np.int32)
+    plain = oracle.tree_build(z, root, off, W)
+    want = _compare(z, root, off, W, 0.6)
+    assert not np.array_equal(want["parent"], plain["parent"]) or \
+        not np.array_equal(want["token"], plain["token"])
+
+
+def test_alpha_zero_equals_plain_build():
+    wl = wk.make(5, with_draft=True)
+    got = _got(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"], 0.0, wl.total)
+    out = jt.jt_tree_build(dev(wl.draft_logits), dev(wl.root_token), dev(wl.tree_off), wl.cfg["W"],
+                           total_nodes=wl.total)
+    torch.cuda.synchronize()
+    for a, b in zip(got, out):
+        np.testing.assert_array_equal(a, b.cpu().numpy())
+
+
+def test_one_hot_rows_have_zero_entropy():
+    """Rows with a single finite logit: H = 0 and log-prob 0 for the only
+    candidate; -inf elsewhere (W = 1 keeps every candidate finite)."""
+    V, N = 600, 5
+    z = np.full((1, N, V), -np.inf, np.float32)
+    for d in range(N):
+        z[0, d, (37 * d + 11) % V] = 2.0 * d
+    root = np.array([0], np.int32)
+    off = np.array([0, N + 1], np.int32)
+    want = _compare(z, root, off, 1, 0.4)
+    np.testing.assert_array_equal(want["entropy"], 0.0)
+
+
+@pytest.mark.parametrize("cfg", [1, 5])
+def test_pure_entropy_full_configs(cfg):
+    wl = wk.make(cfg, with_draft=True)
+    _compare(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"], 1.0)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_pure_entropy_ragged_small(seed):
+    rng = np.random.default_rng(200 + seed)
+    nseq = int(rng.integers(1, 7))
+    N, W = int(rng.integers(1, 7)), int(rng.integers(2, 9))
+    V = int(rng.integers(W, 3000))
+    full = sum(W ** d for d in range(N + 1))
+    budgets = [int(rng.integers(1, min(full, 256) + 1)) for _ in range(nseq)]
+    z = (rng.standard_normal((nseq, N, V)) * rng.uniform(0.2, 3.0, size=(nseq, N, 1))).astype(np.float32)
+    root = rng.integers(0, V, size=nseq).astype(np.int32)
+    off = np.concatenate([[0], np.cumsum(budgets)]).astype(np.int32)
+    _compare(z, root, off, W, 1.0)
+
+
+@pytest.mark.parametrize("alpha", [0.0, 0.5, 1.0])
+def test_zero_probability_candidates_come_last(alpha):
+    """Rows with fewer finite logits than W: the extra candidates score
+    -inf under every weight and fill the tree only after every finite path."""
+    rng = np.random.default_rng(3)
+    V, W, N = 700, 5, 2
+    z = (rng.standard_normal((2, N, V)) * 2).astype(np.float32)
+    z[0, 0, :] = -np.inf
+    z[0, 0, [3, 90, 411]] = [0.2, 1.5, -0.7]
+    z[1, 1, :] = -np.inf
+    z[1, 1, 17] = 0.0
+    root = np.array([1, 2], np.int32)
+    off = np.array([0, 25, 45], np.int32)    # 19 and 11 finite nodes, then -inf ones
+    want = oracle.tree_build_mixed(z, root, off, W, alpha)
+    assert np.isinf(want["score"][19:25]).all() and np.isinf(want["score"][25 + 11:]).all()
+    par, tk, dp, anc = _got(z, root, off, W, alpha, 45)
+    np.testing.assert_array_equal(par, want["parent"])
+    np.testing.assert_array_equal(tk, want["token"])
+    np.testing.assert_array_equal(dp, want["depth"])
+    np.testing.assert_array_equal(anc.view(np.uint32), want["anc"])
+
+
+def test_invalid_alpha_is_refused():
+    z = dev(np.zeros((1, 2, 10), np.float32))
+    off = dev(np.array([0, 3], np.int32))
+    for alpha in (1.5, -0.1, float("nan")):
+        with pytest.raises(jt.JtError) as e:
+            jt.jt_tree_build_mixed(z, dev(np.array([1], np.int32)), off, 2, alpha, total_nodes=3)
+        assert e.value.status == -1

@@ -35,7 +35,7 @@ def test_entropy_matches_scipy():
     np.testing.assert_allclose(out["entropy"], scipy_entropy(p, axis=-1), rtol=1e-12, atol=1e-12)
 
 
-@pytest.mark.parametrize("alpha", [0.2, 0.5, 0.9])
+@pytest.mark.parametrize("alpha", [0.2, 0.5, 0.9, 1.0])
 def test_matches_exhaustive_enumeration(alpha):
     """Nodes 1..B-1 are the B-1 best paths under the mixed step scores
     (sorted by score desc, depth asc, token asc, parent index asc), for
@@ -79,6 +79,64 @@ def test_matches_exhaustive_enumeration(alpha):
 
 def test_alpha_outside_range_is_rejected():
     z = np.zeros((1, 1, 5), np.float32)
-    for a in (-0.1, 1.0, float("nan")):
+    for a in (-0.1, 1.0 + 1e-12, float("nan")):
         with pytest.raises(oracle.OracleError):
             oracle.tree_build_mixed(z, np.zeros(1, np.int32), np.array([0, 2], np.int32), 2, a)
+
+
+def test_masked_entries_add_nothing_to_the_entropy():
+    """Logits of -inf (probability 0) contribute 0 log 0 = 0: the entropy of
+    a row with masked entries is that of its finite part, and a row with one
+    finite entry has entropy 0."""
+    rng = np.random.default_rng(5)
+    z = _draft(rng, 1, 3, 120)
+    z[0, 0, ::3] = -np.inf
+    z[0, 1, :] = -np.inf
+    z[0, 1, 17] = 4.0
+    out = oracle.tree_build_mixed(z, np.zeros(1, np.int32), np.array([0, 4], np.int32), 1, 0.5)
+    fin = z[0, 0][np.isfinite(z[0, 0])].astype(np.float64)
+    np.testing.assert_allclose(out["entropy"][0, 0], scipy_entropy(np.exp(log_softmax(fin))), rtol=1e-12)
+    assert out["entropy"][0, 1] == 0.0
+    assert np.isfinite(out["entropy"]).all()
+
+
+def test_pure_entropy_is_breadth_first_by_token():
+    """alpha = 1: every node of depth d scores -(H_0 + ... + H_{d-1}) whatever
+    its tokens, so with all H_d > 0 the queue's tie-breaks alone order a
+    depth: the tree is breadth-first, a depth's nodes by (token asc, parent
+    asc).  Closed form, independent of the entropy values."""
+    rng = np.random.default_rng(11)
+    N, W, V = 3, 3, 40
+    z = _draft(rng, 1, N, V)
+    order = np.lexsort((np.arange(V)[None, :].repeat(N, 0), -z[0]), axis=-1)[:, :W]
+    full = 1 + W + W * W + W ** 3
+    out = oracle.tree_build_mixed(z, np.array([5], np.int32), np.array([0, full], np.int32), W, 1.0)
+    par, tok, dep = [0 - 1], [5], [0]
+    level = [0]
+    for d in range(N):
+        kids = sorted(((int(t), p) for p in level for t in order[d]), key=lambda c: (c[0], c[1]))
+        level = []
+        for t, p in kids:
+            level.append(len(tok))
+            par.append(p)
+            tok.append(t)
+            dep.append(d + 1)
+    np.testing.assert_array_equal(out["parent"], par)
+    np.testing.assert_array_equal(out["token"], tok)
+    np.testing.assert_array_equal(out["depth"], dep)
+
+
+def test_zero_probability_candidates_come_last():
+    """A row with fewer finite logits than W: the extra candidates have
+    probability 0 and score -inf under every weight, so they are popped
+    only once every finite path is in the tree."""
+    V, W = 10, 4
+    z = np.full((1, 2, V), -np.inf, np.float32)
+    z[0, 0, [2, 6]] = [1.0, 0.5]
+    z[0, 1, :] = np.linspace(0, 1, V, dtype=np.float32)
+    for alpha in (0.0, 0.5, 1.0):
+        out = oracle.tree_build_mixed(z, np.array([0], np.int32), np.array([0, 13], np.int32), W, alpha)
+        # nodes 1..10: the two finite depth-1 nodes and their 8 children
+        assert set(out["token"][1:3]) == {2, 6} and np.all(out["depth"][1:3] == 1)
+        assert np.all(out["depth"][3:11] == 2) and np.all(np.isin(out["parent"][3:11], [1, 2]))
+        assert np.all(out["score"][:11] > -np.inf) and np.all(out["score"][11:] == -np.inf)

@@ -21,13 +21,13 @@ from . import build as _build
 JT_OK, JT_ERR_INVALID, JT_ERR_UNSUPPORTED, JT_ERR_CUDA, JT_ERR_TIMEOUT, JT_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
 JT_DTYPE_F32, JT_DTYPE_BF16 = 0, 1
 JT_RULE_GREEDY, JT_RULE_MARGIN = 0, 1
-JT_OP_TREE_BUILD, JT_OP_TREE_ATTN, JT_OP_VERIFY_ACCEPT, JT_OP_TREE_TOPW = 0, 1, 2, 3
+JT_OP_TREE_BUILD, JT_OP_TREE_ATTN, JT_OP_VERIFY_ACCEPT, JT_OP_TREE_TOPW, JT_OP_TREE_BUILD_MIXED = 0, 1, 2, 3, 4
 JT_MAX_TREE, JT_MAX_W, JT_MAX_N, JT_PAGE_SIZE = 256, 8, 64, 16
 
 # every symbol include/jt.h declares
 EXPORTS = ("jt_workspace_size", "jt_tree_build", "jt_tree_topw", "jt_tree_expand",
            "jt_tree_attn_paged", "jt_verify_accept", "jt_check", "jt_status_str", "jt_version",
-           "jt_tree_build_noalloc", "jt_verify_accept_stochastic")
+           "jt_tree_build_noalloc", "jt_verify_accept_stochastic", "jt_tree_build_mixed")
 
 _lock = threading.Lock()
 _lib = None
@@ -58,6 +58,7 @@ def load(build_if_missing: bool = True):
         lib.jt_workspace_size.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, i32, i32, i32]
         lib.jt_workspace_size.restype = sz
         lib.jt_tree_build.argtypes = [P, P, P, i32, i32, i32, i64, i32, P, P, P, P, P, sz, P]
+        lib.jt_tree_build_mixed.argtypes = [P, P, P, i32, i32, i32, i64, i32, f64, P, P, P, P, P, sz, P]
         lib.jt_tree_topw.argtypes = [P, i64, i64, i32, P, P, P, P, sz, P]
         lib.jt_tree_build_noalloc.argtypes = [P, P, P, i32, i32, i32, i64, i32, P, P, P, P, i32, P]
         lib.jt_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz, P]
@@ -72,7 +73,7 @@ def load(build_if_missing: bool = True):
         lib.jt_version.argtypes = []
         for name in ("jt_tree_build", "jt_tree_topw", "jt_tree_expand", "jt_tree_attn_paged",
                      "jt_verify_accept", "jt_check", "jt_version", "jt_tree_build_noalloc",
-                     "jt_verify_accept_stochastic"):
+                     "jt_verify_accept_stochastic", "jt_tree_build_mixed"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -184,6 +185,35 @@ def jt_tree_build(draft_logits, root_token, tree_off, W, total_nodes=None, out=N
                            total_nodes, _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc),
                            _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "jt_tree_build")
+    return parent, token, depth, anc
+
+
+def jt_tree_build_mixed(draft_logits, root_token, tree_off, W, alpha, total_nodes=None, out=None, ws=None,
+                        stream=None):
+    """jt_tree_build whose step scores are (1 - alpha) * log-prob - alpha *
+    entropy(draft row), alpha in [0, 1] (1: pure entropy score).
+
+    Returns (parent, token, depth, anc) on the device."""
+    lib = load()
+    _need(draft_logits, "draft_logits", torch.float32)
+    _need(root_token, "root_token", torch.int32)
+    _need(tree_off, "tree_off", torch.int32)
+    nseq, N, V = draft_logits.shape
+    if total_nodes is None:
+        total_nodes = int(tree_off[-1].item())
+    dev = draft_logits.device
+    if out is None:
+        out = (torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty(total_nodes, dtype=torch.int32, device=dev),
+               torch.empty((total_nodes, 8), dtype=torch.int32, device=dev))
+    parent, token, depth, anc = out
+    if ws is None:
+        ws = workspace(jt_workspace_size(JT_OP_TREE_BUILD_MIXED, nseq, N, W, V), dev)
+    rc = lib.jt_tree_build_mixed(_ptr(draft_logits), _ptr(root_token), _ptr(tree_off), nseq, N, W, V,
+                                 total_nodes, float(alpha), _ptr(parent), _ptr(token), _ptr(depth),
+                                 _ptr(anc), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jt_tree_build_mixed")
     return parent, token, depth, anc
 
 

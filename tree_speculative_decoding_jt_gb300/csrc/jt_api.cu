@@ -37,8 +37,8 @@ static jt_status check_ws(void* ws, size_t ws_bytes, size_t need) {
     return JT_OK;
 }
 
-static size_t build_ws(int nseq, int N, int W, long long V) {
-    return kWsHeader + topw_workspace_bytes(static_cast<long long>(nseq) * N, V, W);
+static size_t build_ws(int nseq, int N, int W, long long V, bool ent = false) {
+    return kWsHeader + topw_workspace_bytes(static_cast<long long>(nseq) * N, V, W, ent);
 }
 
 }  // namespace jt
@@ -65,8 +65,9 @@ size_t jt_workspace_size(int op, int nseq, int N, int W, int64_t V, int total_no
                          int Hkv, int D, int max_pages, int max_tree) {
     switch (op) {
         case JT_OP_TREE_BUILD:
+        case JT_OP_TREE_BUILD_MIXED:
             if (nseq < 1 || N < 0 || N > JT_MAX_N || W < 1 || W > JT_MAX_W || V < W) return 0;
-            return build_ws(nseq, N, W, V);
+            return build_ws(nseq, N, W, V, op == JT_OP_TREE_BUILD_MIXED);
         case JT_OP_TREE_TOPW:
             if (nseq < 0 || W < 1 || W > JT_MAX_W || V < W) return 0;
             return build_ws(nseq, 1, W, V);
@@ -98,23 +99,32 @@ jt_status jt_tree_topw(const float* logits, int64_t rows, int64_t V, int W, int3
     return from_cuda(e);
 }
 
+jt_status jt_tree_build_mixed(const float* draft_logits, const int32_t* root_token,
+                              const int32_t* tree_off, int nseq, int N, int W, int64_t V,
+                              int total_nodes, double alpha, int32_t* parent, int32_t* token,
+                              int32_t* depth, uint32_t* anc, void* ws, size_t ws_bytes,
+                              jt_stream_t stream) {
+    if ((!draft_logits && N > 0) || !root_token || !tree_off || !parent || !token || !depth ||
+        !anc || nseq < 1 || nseq > 65535 || N < 0 || N > JT_MAX_N || W < 1 || W > JT_MAX_W ||
+        V < W || V > 0x7FFFFFFFll || total_nodes < nseq ||
+        static_cast<long long>(nseq) * N > 65535 || !(alpha >= 0.0 && alpha <= 1.0))
+        return JT_ERR_INVALID;
+    if (!aligned(anc, 16)) return JT_ERR_INVALID;
+    jt_status s = check_ws(ws, ws_bytes, build_ws(nseq, N, W, V, alpha != 0.0));
+    if (s != JT_OK) return s;
+    char* base = static_cast<char*>(ws);
+    cudaError_t e = tree_build_launch(draft_logits, root_token, tree_off, nseq, total_nodes, N, W, V, alpha,
+                                      parent, token, depth, anc, base + kWsHeader,
+                                      reinterpret_cast<uint32_t*>(base), stream);
+    return from_cuda(e);
+}
+
 jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
                         const int32_t* tree_off, int nseq, int N, int W, int64_t V, int total_nodes,
                         int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc, void* ws,
                         size_t ws_bytes, jt_stream_t stream) {
-    if ((!draft_logits && N > 0) || !root_token || !tree_off || !parent || !token || !depth ||
-        !anc || nseq < 1 || nseq > 65535 || N < 0 || N > JT_MAX_N || W < 1 || W > JT_MAX_W ||
-        V < W || V > 0x7FFFFFFFll || total_nodes < nseq ||
-        static_cast<long long>(nseq) * N > 65535)
-        return JT_ERR_INVALID;
-    if (!aligned(anc, 16)) return JT_ERR_INVALID;
-    jt_status s = check_ws(ws, ws_bytes, build_ws(nseq, N, W, V));
-    if (s != JT_OK) return s;
-    char* base = static_cast<char*>(ws);
-    cudaError_t e = tree_build_launch(draft_logits, root_token, tree_off, nseq, total_nodes, N, W, V, parent, token,
-                              depth, anc, base + kWsHeader, reinterpret_cast<uint32_t*>(base),
-                              stream);
-    return from_cuda(e);
+    return jt_tree_build_mixed(draft_logits, root_token, tree_off, nseq, N, W, V, total_nodes, 0.0, parent,
+                               token, depth, anc, ws, ws_bytes, stream);
 }
 
 jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_token,

@@ -22,13 +22,14 @@ struct WsHeader {
 constexpr size_t kWsHeader = kAlign;
 
 // tree_build.cu
-size_t topw_workspace_bytes(long long rows, long long V, int W);
+// ent: room for the entropy partials of the mixed build
+size_t topw_workspace_bytes(long long rows, long long V, int W, bool ent = false);
 cudaError_t tree_topw_launch(const float* z, long long rows, long long V, int W, int32_t* tok,
                              double* lp, double* lse, char* ws_parts, cudaStream_t st);
 cudaError_t tree_build_launch(const float* z, const int32_t* root_token, const int32_t* tree_off,
-                              int nseq, int total_nodes, int N, int W, long long V, int32_t* parent, int32_t* token,
-                              int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
-                              cudaStream_t st);
+                              int nseq, int total_nodes, int N, int W, long long V, double alpha,
+                              int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc, char* ws_parts,
+                              uint32_t* err, cudaStream_t st);
 cudaError_t tree_expand_launch(const int32_t* tok, const double* lp, const int32_t* root_token,
                                const int32_t* tree_off, int nseq, int total_nodes, int N, int W, int32_t* parent,
                                int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,

@@ -87,7 +87,7 @@ extern "C" jt_status jt_tree_build_noalloc(const float* draft_logits, const int3
     // it is read
     e = cudaMemsetAsync(base, 0, sizeof(WsHeader), stream);
     if (e == cudaSuccess)
-        e = tree_build_launch(draft_logits, root_token, tree_off, nseq, total_nodes, N, W, V, parent, token,
+        e = tree_build_launch(draft_logits, root_token, tree_off, nseq, total_nodes, N, W, V, 0.0, parent, token,
                               depth, anc, base + kWsHeader, reinterpret_cast<uint32_t*>(base), stream);
     if (e != cudaSuccess || !sync_check) return status_of(e);
     // synchronous check: wait for the stream, then read the error word

@@ -190,11 +190,14 @@ __device__ __forceinline__ void warp_best(float& v, int& id) {
     }
 }
 
-template <int W, bool VEC, int PER>
+// ENT: also sum exp(z - max) * z (float-float) for the row entropy
+// H = lse - sum p z of the entropy-mixed build.
+template <int W, bool VEC, int PER, bool ENT>
 __global__ void __launch_bounds__(kTopwThreads)
     topw_partial_kernel(const float* __restrict__ z, long long V, int splits, ExpTable tab,
                         float* __restrict__ part_v, int* __restrict__ part_id,
-                        float* __restrict__ part_m, float2* __restrict__ part_s) {
+                        float* __restrict__ part_m, float2* __restrict__ part_s,
+                        float2* __restrict__ part_t) {
     constexpr int CH = kTopwThreads * PER;
     constexpr int NW = kTopwThreads / 32;
     __shared__ float s_thi[64], s_tlo[64];
@@ -202,6 +205,7 @@ __global__ void __launch_bounds__(kTopwThreads)
     __shared__ int s_wi[NW][W];
     __shared__ float s_wmax[NW];
     __shared__ float2 s_wsum[NW];
+    __shared__ float2 s_wt[NW];
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const long long row = blockIdx.y;
@@ -250,7 +254,7 @@ __global__ void __launch_bounds__(kTopwThreads)
     // warp maximum, then this lane's share of sum exp(z - max) (float-float)
     const float mw = warp_max_f(bv);
     __syncthreads();  // exp table ready
-    float acc_hi = 0.0f, acc_lo = 0.0f;
+    float acc_hi = 0.0f, acc_lo = 0.0f, tac_hi = 0.0f, tac_lo = 0.0f;
     if (mw != -INFINITY) {
         // entries more than 87 below the maximum (and -inf padding) are
         // lifted to max - 87 (~87 after rounding): they then add ~1e-38 each
@@ -258,16 +262,27 @@ __global__ void __launch_bounds__(kTopwThreads)
         const float floor_v = mw - 87.0f;
 #pragma unroll
         for (int i = 0; i < PER; ++i) {
+            const float xc = fmaxf(x[i], floor_v);
             float dh, dl;
-            two_sum(fmaxf(x[i], floor_v), -mw, dh, dl);
+            two_sum(xc, -mw, dh, dl);
             const ffloat y = ffexp_in_range(fmaxf(dh, -87.0f), dl, s_thi, s_tlo);
             float sum, err;
             two_sum(acc_hi, y.hi, sum, err);
             acc_hi = sum;
             acc_lo = jt_add(acc_lo, jt_add(err, y.lo));
+            if (ENT) {  // y * xc as a float pair, summed the same way
+                const float ph = jt_mul(y.hi, xc);
+                const float pl = jt_fmaf(y.lo, xc, jt_fmaf(y.hi, xc, -ph));
+                two_sum(tac_hi, ph, sum, err);
+                tac_hi = sum;
+                tac_lo = jt_add(tac_lo, jt_add(err, pl));
+            }
         }
     }
     const ffloat Sw = warp_sum_ff(ff_norm(acc_hi, acc_lo));
+    ffloat Tw;
+    Tw.hi = Tw.lo = 0.0f;
+    if (ENT) Tw = warp_sum_ff(ff_norm(tac_hi, tac_lo));
 
     // warp top-W: W extraction rounds over the lanes' heads
 #pragma unroll
@@ -298,44 +313,53 @@ __global__ void __launch_bounds__(kTopwThreads)
     if (lane == 0) {
         s_wmax[warp] = mw;
         s_wsum[warp] = make_float2(Sw.hi, Sw.lo);
+        if (ENT) s_wt[warp] = make_float2(Tw.hi, Tw.lo);
     }
     __syncthreads();
     if (warp == 0) {
         // chunk max and sum: rescale each warp's sum to the chunk maximum
         float m = (lane < NW) ? s_wmax[lane] : -INFINITY;
         m = warp_max_f(m);
-        ffloat S;
-        S.hi = S.lo = 0.0f;
+        ffloat S, T;
+        S.hi = S.lo = T.hi = T.lo = 0.0f;
         if (lane < NW && m != -INFINITY) {
             const float mj = s_wmax[lane];
             if (mj != -INFINITY) {
                 float dh, dl;
                 two_sum(mj, -m, dh, dl);
+                const ffloat f = ffexp(dh, dl, s_thi, s_tlo);
                 ffloat Sj;
                 Sj.hi = s_wsum[lane].x;
                 Sj.lo = s_wsum[lane].y;
-                S = ff_mul(Sj, ffexp(dh, dl, s_thi, s_tlo));
+                S = ff_mul(Sj, f);
+                if (ENT) {
+                    ffloat Tj;
+                    Tj.hi = s_wt[lane].x;
+                    Tj.lo = s_wt[lane].y;
+                    T = ff_mul(Tj, f);
+                }
             }
         }
         S = warp_sum_ff(S);
+        if (ENT) T = warp_sum_ff(T);
         // chunk top-W from the warps' sorted lists (NW*W <= 64 entries; each
         // lane holds up to two, best first)
-        constexpr int PER = (NW * W + 31) / 32;
-        float hv[PER];
-        int hi[PER];
+        constexpr int PL = (NW * W + 31) / 32;
+        float hv[PL];
+        int hi[PL];
 #pragma unroll
-        for (int q = 0; q < PER; ++q) {
+        for (int q = 0; q < PL; ++q) {
             const int c = lane + 32 * q;
             hv[q] = (c < NW * W) ? s_wv[c / W][c % W] : -INFINITY;
             hi[q] = (c < NW * W) ? s_wi[c / W][c % W] : -1;
         }
-        if (PER == 2 && better(hv[PER - 1], hi[PER - 1], hv[0], hi[0])) {
+        if (PL == 2 && better(hv[PL - 1], hi[PL - 1], hv[0], hi[0])) {
             const float tv = hv[0];
             const int ti = hi[0];
-            hv[0] = hv[PER - 1];
-            hi[0] = hi[PER - 1];
-            hv[PER - 1] = tv;
-            hi[PER - 1] = ti;
+            hv[0] = hv[PL - 1];
+            hi[0] = hi[PL - 1];
+            hv[PL - 1] = tv;
+            hi[PL - 1] = ti;
         }
         const long long p = row * splits + sp;
 #pragma unroll
@@ -350,17 +374,18 @@ __global__ void __launch_bounds__(kTopwThreads)
             }
             if (id != -1 && id == mine) {  // pop this lane's head
 #pragma unroll
-                for (int q = 0; q + 1 < PER; ++q) {
+                for (int q = 0; q + 1 < PL; ++q) {
                     hv[q] = hv[q + 1];
                     hi[q] = hi[q + 1];
                 }
-                hv[PER - 1] = -INFINITY;
-                hi[PER - 1] = -1;
+                hv[PL - 1] = -INFINITY;
+                hi[PL - 1] = -1;
             }
         }
         if (lane == 0) {
             part_m[p] = m;
             part_s[p] = make_float2(S.hi, S.lo);
+            if (ENT) part_t[p] = make_float2(T.hi, T.lo);
         }
     }
 }
@@ -370,20 +395,23 @@ __global__ void __launch_bounds__(kTopwThreads)
 // rescaled with the table-driven exp, and log is one fp32 logf refined by a
 // Newton step (y = y0 + e - e^2/2 with 1 + e = S exp(-y0)), accurate to
 // ~1e-11; only the final assembly and lp = z - lse are fp64.
-template <int W>
+// ENT: also merge the sum exp(z - max) * z partials and return the row
+// entropy H = lse - sum p z.
+template <int W, bool ENT>
 __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
                                           const int* __restrict__ part_id,
                                           const float* __restrict__ part_m,
-                                          const float2* __restrict__ part_s, int splits,
+                                          const float2* __restrict__ part_s,
+                                          const float2* __restrict__ part_t, int splits,
                                           long long row, int lane, const float* tab_hi,
                                           const float* tab_lo, int (&tok)[W], double (&lp)[W],
-                                          double& lse) {
+                                          double& lse, double& H) {
     const long long base = row * splits;
     // every load of the row is issued up front (one memory round trip):
     // lane handles chunks s = lane + 32 r, r < kMergeR
     constexpr int kMergeR = 4;  // covers 128 chunks = 512k vocabulary entries
     float pm[kMergeR];
-    float2 ps[kMergeR];
+    float2 ps[kMergeR], pt[kMergeR];
     float pv[kMergeR][W];
     int pi[kMergeR][W];
 #pragma unroll
@@ -392,6 +420,7 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
         const bool in = s < splits;
         pm[r] = in ? part_m[base + s] : -INFINITY;
         ps[r] = in ? part_s[base + s] : make_float2(0.0f, 0.0f);
+        pt[r] = (ENT && in) ? part_t[base + s] : make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int k = 0; k < W; ++k) {
             pv[r][k] = in ? part_v[(base + s) * W + k] : -INFINITY;
@@ -403,18 +432,25 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
     for (int r = 0; r < kMergeR; ++r) M = fmaxf(M, pm[r]);
     for (int s = lane + 32 * kMergeR; s < splits; s += 32) M = fmaxf(M, part_m[base + s]);
     M = warp_max_f(M);
-    ffloat S;
-    S.hi = S.lo = 0.0f;
+    ffloat S, T;
+    S.hi = S.lo = T.hi = T.lo = 0.0f;
     if (M != -INFINITY) {
 #pragma unroll
         for (int r = 0; r < kMergeR; ++r) {
             if (pm[r] != -INFINITY) {
                 float dh, dl;
                 two_sum(pm[r], -M, dh, dl);
+                const ffloat f = ffexp(dh, dl, tab_hi, tab_lo);
                 ffloat Sj;
                 Sj.hi = ps[r].x;
                 Sj.lo = ps[r].y;
-                S = ff_add(S, ff_mul(Sj, ffexp(dh, dl, tab_hi, tab_lo)));
+                S = ff_add(S, ff_mul(Sj, f));
+                if (ENT) {
+                    ffloat Tj;
+                    Tj.hi = pt[r].x;
+                    Tj.lo = pt[r].y;
+                    T = ff_add(T, ff_mul(Tj, f));
+                }
             }
         }
         for (int s = lane + 32 * kMergeR; s < splits; s += 32) {
@@ -422,15 +458,24 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
             if (ms != -INFINITY) {
                 float dh, dl;
                 two_sum(ms, -M, dh, dl);
+                const ffloat f = ffexp(dh, dl, tab_hi, tab_lo);
                 const float2 q = part_s[base + s];
                 ffloat Sj;
                 Sj.hi = q.x;
                 Sj.lo = q.y;
-                S = ff_add(S, ff_mul(Sj, ffexp(dh, dl, tab_hi, tab_lo)));
+                S = ff_add(S, ff_mul(Sj, f));
+                if (ENT) {
+                    const float2 qt = part_t[base + s];
+                    ffloat Tj;
+                    Tj.hi = qt.x;
+                    Tj.lo = qt.y;
+                    T = ff_add(T, ff_mul(Tj, f));
+                }
             }
         }
     }
     S = warp_sum_ff(S);
+    if (ENT) T = warp_sum_ff(T);
     if (M == -INFINITY) {
         lse = -INFINITY;
     } else {
@@ -440,6 +485,11 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
         e = jt_add(e, -0.5f * e * e);
         lse = static_cast<double>(M) + (static_cast<double>(y0) + static_cast<double>(e));
     }
+
+    H = 0.0;
+    if (ENT && M != -INFINITY)
+        H = lse - (static_cast<double>(T.hi) + static_cast<double>(T.lo)) /
+                      (static_cast<double>(S.hi) + static_cast<double>(S.lo));
 
     TopList<W> L;
     L.init();
@@ -461,14 +511,15 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
 }
 
 // ---------------------------------------------------------------------------
-// Step 1b (jt_tree_topw only): one warp per row.
+// Step 1b: merge the partials, one warp per row.
 // ---------------------------------------------------------------------------
-template <int W>
+template <int W, bool ENT>
 __global__ void __launch_bounds__(256)
     topw_merge_kernel(const float* __restrict__ part_v, const int* __restrict__ part_id,
                       const float* __restrict__ part_m, const float2* __restrict__ part_s,
-                      int splits, long long rows, ExpTable tab, int32_t* __restrict__ tok_out,
-                      double* __restrict__ lp_out, double* __restrict__ lse_out) {
+                      const float2* __restrict__ part_t, int splits, long long rows, ExpTable tab,
+                      double alpha, int32_t* __restrict__ tok_out, double* __restrict__ lp_out,
+                      double* __restrict__ lse_out) {
     __shared__ float s_thi[64], s_tlo[64];
     if (threadIdx.x < 64) {
         s_thi[threadIdx.x] = tab.hi[threadIdx.x];
@@ -479,9 +530,33 @@ __global__ void __launch_bounds__(256)
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
     int tok[W];
-    double lp[W], lse;
-    merge_row<W>(part_v, part_id, part_m, part_s, splits, row, lane, s_thi, s_tlo, tok, lp, lse);
+    double lp[W], lse, H;
+    merge_row<W, ENT>(part_v, part_id, part_m, part_s, part_t, splits, row, lane, s_thi, s_tlo, tok, lp,
+                      lse, H);
     if (lane == 0) {
+        if (ENT) {
+            // entropy-mixed step score ((1 - alpha) * lp) - (alpha * H), each
+            // operation rounded on its own (no fused multiply-add), as the
+            // fp64 definition evaluates it; probability 0 stays at -inf
+#pragma unroll
+            for (int k = 0; k < W; ++k)
+                if (lp[k] != -INFINITY) lp[k] = __dsub_rn(__dmul_rn(1.0 - alpha, lp[k]), __dmul_rn(alpha, H));
+            // the expansion needs each row in queue-key order (score desc,
+            // token asc): equal scores (every candidate at alpha = 1, rare
+            // rounding collisions below it) go by token
+#pragma unroll
+            for (int i = 0; i + 1 < W; ++i)
+#pragma unroll
+                for (int j = 0; j + 1 < W - i; ++j)
+                    if (lp[j + 1] > lp[j] || (lp[j + 1] == lp[j] && tok[j + 1] < tok[j])) {
+                        const double tl = lp[j];
+                        lp[j] = lp[j + 1];
+                        lp[j + 1] = tl;
+                        const int tt = tok[j];
+                        tok[j] = tok[j + 1];
+                        tok[j + 1] = tt;
+                    }
+        }
 #pragma unroll
         for (int k = 0; k < W; ++k) {
             tok_out[row * W + k] = tok[k];
@@ -828,7 +903,7 @@ static int topw_per_thread(long long rows, long long V) {
     return (ctas < 4ll * device_sm_count()) ? kTopwPerThreadMin : kTopwPerThread;
 }
 
-size_t topw_workspace_bytes(long long rows, long long V, int W) {
+size_t topw_workspace_bytes(long long rows, long long V, int W, bool ent) {
     const long long p = rows * topw_splits(V, topw_per_thread(rows, V));
     size_t bytes = 0;
     bytes += align_up(rows * W * sizeof(int32_t));  // merged tables (tree build)
@@ -838,6 +913,7 @@ size_t topw_workspace_bytes(long long rows, long long V, int W) {
     bytes += align_up(p * W * sizeof(int));
     bytes += align_up(p * sizeof(float));
     bytes += align_up(p * sizeof(float2));
+    if (ent) bytes += align_up(p * sizeof(float2));  // entropy partials
     return bytes;
 }
 
@@ -849,6 +925,7 @@ struct TopwParts {
     int* id;
     float* m;
     float2* s;
+    float2* t;  // entropy partials (mixed build only)
     int splits;
 };
 
@@ -869,18 +946,20 @@ static TopwParts carve_topw(char* base, long long rows, long long V, int W, int 
     t.m = reinterpret_cast<float*>(base);
     base += align_up(p * sizeof(float));
     t.s = reinterpret_cast<float2*>(base);
+    base += align_up(p * sizeof(float2));
+    t.t = reinterpret_cast<float2*>(base);
     return t;
 }
 
-template <int W>
+template <int W, bool ENT>
 static cudaError_t launch_topw_partial(const float* z, long long rows, long long V, int per, TopwParts& t,
                                        cudaStream_t st) {
     const ExpTable& tab = exp_table();
     const bool vec = (V % 4 == 0) && ((reinterpret_cast<uintptr_t>(z) & 15u) == 0);
     dim3 grid(t.splits, static_cast<unsigned>(rows));
 #define JT_TOPW_LAUNCH(VEC_, PER_)                                                                       \
-    return launch_kernel(topw_partial_kernel<W, VEC_, PER_>, grid, dim3(kTopwThreads), 0, st, 0, z, V, \
-                         t.splits, tab, t.v, t.id, t.m, t.s)
+    return launch_kernel(topw_partial_kernel<W, VEC_, PER_, ENT>, grid, dim3(kTopwThreads), 0, st, 0, z, \
+                         V, t.splits, tab, t.v, t.id, t.m, t.s, t.t)
     if (per == kTopwPerThreadMin) {
         if (vec) JT_TOPW_LAUNCH(true, kTopwPerThreadMin);
         JT_TOPW_LAUNCH(false, kTopwPerThreadMin);
@@ -895,28 +974,34 @@ static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t
                             double* lse, char* ws_parts, cudaStream_t st) {
     const int per = topw_per_thread(rows, V);
     TopwParts t = carve_topw(ws_parts, rows, V, W, per);
-    cudaError_t e = launch_topw_partial<W>(z, rows, V, per, t, st);
+    cudaError_t e = launch_topw_partial<W, false>(z, rows, V, per, t, st);
     if (e != cudaSuccess) return e;
     const long long warps_per_block = 8;
     const unsigned blocks = static_cast<unsigned>((rows + warps_per_block - 1) / warps_per_block);
-    return launch_kernel(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
-                      t.splits, rows, exp_table(), tok, lp, lse);
+    return launch_kernel(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m,
+                         t.s, t.t, t.splits, rows, exp_table(), 0.0, tok, lp, lse);
 }
 
+// alpha > 0: entropy-mixed step scores (1 - alpha) * lp - alpha * H(row);
+// alpha == 0 runs the plain build's kernels.
 template <int W>
 static cudaError_t run_build(const float* z, const int32_t* root_token, const int32_t* tree_off,
-                             int nseq, int total_nodes, int N, long long V, int32_t* parent,
+                             int nseq, int total_nodes, int N, long long V, double alpha, int32_t* parent,
                              int32_t* token, int32_t* depth, uint32_t* anc, char* ws_parts,
                              uint32_t* err, cudaStream_t st) {
     const long long rows = static_cast<long long>(nseq) * N;
     const int per = topw_per_thread(rows, V);
     TopwParts t = carve_topw(ws_parts, rows, V, W, per);
     if (rows > 0) {
-        cudaError_t e = launch_topw_partial<W>(z, rows, V, per, t, st);
+        const bool ent = alpha != 0.0;
+        cudaError_t e = ent ? launch_topw_partial<W, true>(z, rows, V, per, t, st)
+                            : launch_topw_partial<W, false>(z, rows, V, per, t, st);
         if (e != cudaSuccess) return e;
         const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-        e = launch_kernel(topw_merge_kernel<W>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s,
-                       t.splits, rows, exp_table(), t.tok, t.lp, t.lse);
+        e = ent ? launch_kernel(topw_merge_kernel<W, true>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id,
+                                t.m, t.s, t.t, t.splits, rows, exp_table(), alpha, t.tok, t.lp, t.lse)
+                : launch_kernel(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id,
+                                t.m, t.s, t.t, t.splits, rows, exp_table(), 0.0, t.tok, t.lp, t.lse);
         if (e != cudaSuccess) return e;
     }
     cudaError_t ea = set_expand_smem<W>();
@@ -955,11 +1040,11 @@ cudaError_t tree_topw_launch(const float* z, long long rows, long long V, int W,
 }
 
 cudaError_t tree_build_launch(const float* z, const int32_t* root_token, const int32_t* tree_off,
-                              int nseq, int total_nodes, int N, int W, long long V, int32_t* parent, int32_t* token,
-                              int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
-                              cudaStream_t st) {
-    JT_DISPATCH_W(W, run_build<kW>(z, root_token, tree_off, nseq, total_nodes, N, V, parent, token, depth, anc,
-                                   ws_parts, err, st));
+                              int nseq, int total_nodes, int N, int W, long long V, double alpha,
+                              int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc, char* ws_parts,
+                              uint32_t* err, cudaStream_t st) {
+    JT_DISPATCH_W(W, run_build<kW>(z, root_token, tree_off, nseq, total_nodes, N, V, alpha, parent, token, depth,
+                                   anc, ws_parts, err, st));
 }
 
 cudaError_t tree_expand_launch(const int32_t* tok, const double* lp, const int32_t* root_token,
