@@ -51,9 +51,12 @@ def _load():
             lib.jto_verify_accept_stochastic.argtypes = [P, P, P, P, P, i32, i32, i64, P, P, P, P,
                                                          P, P, P, P]
             lib.jto_tree_build_mixed.argtypes = [P, P, P, i32, i32, i32, i64, dbl, P, P, P, P, P, P, P]
+            lib.jto_tree_expand_capped.argtypes = [P, P, P, P, P, P, i32, i32, i32, P, P, P, P, P, P]
+            lib.jto_tree_policy.argtypes = [P, i32, i32, i32, P, i32, i32, i32, i32, i32, i32, dbl, dbl,
+                                            dbl, P, P, P, P, P]
             for f in (lib.jto_topw_lse, lib.jto_tree_expand, lib.jto_tree_build,
                       lib.jto_tree_attn, lib.jto_verify_accept, lib.jto_verify_accept_stochastic,
-                      lib.jto_tree_build_mixed):
+                      lib.jto_tree_build_mixed, lib.jto_tree_expand_capped, lib.jto_tree_policy):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -107,6 +110,50 @@ def tree_expand(tok, lp, root_token, tree_off, N, W):
                                    N, W, _ptr(parent), _ptr(token), _ptr(depth), _ptr(anc),
                                    _ptr(score), _ptr(gap)), "tree_expand")
     return dict(parent=parent, token=token, depth=depth, anc=anc, score=score, gap=gap)
+
+
+def tree_expand_capped(tok, lp, root_token, tree_off, N, W, w_cap=None, n_cap=None):
+    """tree_expand with optional per-sequence caps: w_cap[b] candidates per
+    row, no children below depth n_cap[b]."""
+    tok, lp = _c(tok, np.int32), _c(lp, np.float64)
+    root_token, tree_off = _c(root_token, np.int32), _c(tree_off, np.int32)
+    wc = None if w_cap is None else _c(w_cap, np.int32)
+    nc = None if n_cap is None else _c(n_cap, np.int32)
+    nseq = len(root_token)
+    total = int(tree_off[-1])
+    parent, token, depth, anc, score = _tree_outputs(total)
+    gap = np.empty(nseq, np.float64)
+    _check(_load().jto_tree_expand_capped(_ptr(tok), _ptr(lp), _ptr(root_token), _ptr(tree_off),
+                                          _ptr(wc), _ptr(nc), nseq, N, W, _ptr(parent), _ptr(token),
+                                          _ptr(depth), _ptr(anc), _ptr(score), _ptr(gap)),
+           "tree_expand_capped")
+    return dict(parent=parent, token=token, depth=depth, anc=anc, score=score, gap=gap)
+
+
+POLICY_DEFAULTS = dict(b_min=16, b_max=256, node_cap=0, w_min=2, n_min=2, n_slack=3, beta=0.25,
+                       log_conf=float(np.log(0.5)), acc_thresh=3.0)
+
+
+def tree_policy(lp, accept_len, budget_state, acc_ema, **params):
+    """One step of the adaptive tree policy (see jt_oracle.c).  lp is the
+    per-depth table [nseq, N, W]; accept_len [nseq] (-1 = not observed) or
+    None.  Returns dict(tree_off, w_cap, n_cap, budget_state, acc_ema) with
+    the updated state (the inputs are not modified)."""
+    p = dict(POLICY_DEFAULTS)
+    p.update(params)
+    lp = _c(lp, np.float64)
+    nseq, N, W = lp.shape
+    acc = None if accept_len is None else _c(accept_len, np.int32)
+    bs = np.array(budget_state, dtype=np.int32, copy=True)
+    ema = np.array(acc_ema, dtype=np.float64, copy=True)
+    off = np.empty(nseq + 1, np.int32)
+    wc = np.empty(nseq, np.int32)
+    nc = np.empty(nseq, np.int32)
+    _check(_load().jto_tree_policy(_ptr(lp), nseq, N, W, _ptr(acc), p["b_min"], p["b_max"], p["node_cap"],
+                                   p["w_min"], p["n_min"], p["n_slack"], float(p["beta"]),
+                                   float(p["log_conf"]), float(p["acc_thresh"]), _ptr(bs), _ptr(ema),
+                                   _ptr(off), _ptr(wc), _ptr(nc)), "tree_policy")
+    return dict(tree_off=off, w_cap=wc, n_cap=nc, budget_state=bs, acc_ema=ema)
 
 
 def tree_build(draft_logits, root_token, tree_off, W):

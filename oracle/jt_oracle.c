@@ -175,17 +175,25 @@ static int cand_before(const jto_cand* a, const jto_cand* b)
  * difference between the popped candidate and the best remaining one over
  * all pops of sequence b (+inf if never two candidates): a decision closer
  * than rounding noise is reported, not hidden.
+ *
+ * Optional per-sequence caps (either pointer may be NULL = no cap): w_cap[b]
+ * in [1, W] keeps only the first w_cap[b] candidates of every row, n_cap[b]
+ * in [0, N] stops the tree at depth n_cap[b] (nodes of that depth get no
+ * children).  The budget must fit the capped full tree.
  */
-int jto_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
-                    const int32_t* tree_off, int nseq, int N, int W,
-                    int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc,
-                    double* score, double* gap)
+static int expand_impl(const int32_t* tok, const double* lp, const int32_t* root_token,
+                       const int32_t* tree_off, const int32_t* w_cap, const int32_t* n_cap,
+                       int nseq, int N, int W, int32_t* parent, int32_t* token, int32_t* depth,
+                       uint32_t* anc, double* score, double* gap)
 {
     if (!tok || !lp || !root_token || !tree_off || nseq < 0 || N < 0 || W < 1)
         return JTO_ERR_INVALID;
     for (int b = 0; b < nseq; ++b) {
         int B = tree_off[b + 1] - tree_off[b];
-        if (B < 1 || B > JTO_MAX_TREE || B > full_tree_nodes(N, W, JTO_MAX_TREE + 1))
+        int Wb = w_cap ? w_cap[b] : W;
+        int Nb = n_cap ? n_cap[b] : N;
+        if (Wb < 1 || Wb > W || Nb < 0 || Nb > N) return JTO_ERR_INVALID;
+        if (B < 1 || B > JTO_MAX_TREE || B > full_tree_nodes(Nb, Wb, JTO_MAX_TREE + 1))
             return JTO_ERR_INVALID;
     }
     /* every popped node pushes at most W candidates */
@@ -195,6 +203,8 @@ int jto_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_to
     for (int b = 0; b < nseq; ++b) {
         const int off = tree_off[b];
         const int B = tree_off[b + 1] - off;
+        const int Wb = w_cap ? w_cap[b] : W;
+        const int Nb = n_cap ? n_cap[b] : N;
         const int32_t* tk = tok + (int64_t)b * N * W;
         const double* lq = lp + (int64_t)b * N * W;
         double sc[JTO_MAX_TREE];
@@ -210,8 +220,8 @@ int jto_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_to
         dp[0] = 0;
         int count = 1;
         /* push the root's children */
-        if (N >= 1)
-            for (int k = 0; k < W; ++k) {
+        if (Nb >= 1)
+            for (int k = 0; k < Wb; ++k) {
                 jto_cand c = { sc[0] + lq[k], 1, tk[k], 0, 1 };
                 q[nq++] = c;
             }
@@ -239,8 +249,8 @@ int jto_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_to
             sc[n] = c.score;
             dp[n] = c.depth;
             /* push its children (row c.depth scores depth c.depth+1) */
-            if (c.depth < N)
-                for (int k = 0; k < W; ++k) {
+            if (c.depth < Nb)
+                for (int k = 0; k < Wb; ++k) {
                     jto_cand ch = { sc[n] + lq[(int64_t)c.depth * W + k], c.depth + 1,
                                     tk[(int64_t)c.depth * W + k], n, 1 };
                     q[nq++] = ch;
@@ -260,6 +270,24 @@ int jto_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_to
     }
     free(q);
     return JTO_OK;
+}
+
+int jto_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
+                    const int32_t* tree_off, int nseq, int N, int W,
+                    int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc,
+                    double* score, double* gap)
+{
+    return expand_impl(tok, lp, root_token, tree_off, NULL, NULL, nseq, N, W, parent, token, depth,
+                       anc, score, gap);
+}
+
+int jto_tree_expand_capped(const int32_t* tok, const double* lp, const int32_t* root_token,
+                           const int32_t* tree_off, const int32_t* w_cap, const int32_t* n_cap,
+                           int nseq, int N, int W, int32_t* parent, int32_t* token, int32_t* depth,
+                           uint32_t* anc, double* score, double* gap)
+{
+    return expand_impl(tok, lp, root_token, tree_off, w_cap, n_cap, nseq, N, W, parent, token, depth,
+                       anc, score, gap);
 }
 
 /* Full tree build: top-W/lse on every (sequence, depth) row, then expansion.
@@ -643,4 +671,91 @@ int jto_tree_build_mixed(const float* draft_logits, const int32_t* root_token, c
     free(l);
     free(s);
     return rc;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Adaptive per-request tree policy.                                         */
+/* [AS] section "逐步树策略：动态调整草稿树规模": two signals, the draft's      */
+/* top-1 confidence and the rolling acceptance history, set the depth, width */
+/* and node count of every request's tree; the tree grows when recent        */
+/* acceptance is high and the draft confident, and shrinks in the opposite   */
+/* case.  [JS-art] section 七: large budgets stop paying as the batch grows, */
+/* and budgets that follow the load are named as future work.               */
+/* Reading (the pages give no formula), per request b and step:              */
+/*   ema   <- (1 - beta) * ema + beta * accept_len[b]   (when observed, >= 0) */
+/*   conf  =  lp[b, 0, 0] >= log_conf    (log top-1 draft prob., depth 1)    */
+/*   hot   =  ema >= acc_thresh                                              */
+/*   ceil  =  b_max, or min(b_max, max(b_min, node_cap / nseq)) if node_cap  */
+/*   B     <- clamp(B, b_min, ceil); then 2B (<= ceil) if conf and hot,      */
+/*            B/2 (>= b_min) if neither, unchanged otherwise                 */
+/*   n_cap =  clamp(floor(ema) + n_slack, n_min, N), 0 <= n_slack <= N       */
+/*   w_cap =  conf ? W : w_min                                               */
+/*   emitted budget = min(B, nodes of the full w_cap-ary tree of depth n_cap) */
+/*   tree_off = exclusive prefix sum of the emitted budgets                  */
+/* Depth, width and node count each move with the signals (none shrinks    */
+/* when a signal rises), so the emitted budget is monotone in both.          */
+/* budget_state keeps the controller's B (not the emitted one).             */
+/* ------------------------------------------------------------------------ */
+int jto_tree_policy(const double* lp, int nseq, int N, int W, const int32_t* accept_len,
+                    int b_min, int b_max, int node_cap, int w_min, int n_min, int n_slack,
+                    double beta, double log_conf, double acc_thresh,
+                    int32_t* budget_state, double* acc_ema,
+                    int32_t* tree_off, int32_t* w_cap, int32_t* n_cap)
+{
+    if (!lp || !budget_state || !acc_ema || !tree_off || !w_cap || !n_cap || nseq < 1 || N < 1 ||
+        W < 1 || b_min < 1 || b_max < b_min || b_max > JTO_MAX_TREE || node_cap < 0 || w_min < 1 ||
+        w_min > W || n_min < 0 || n_min > N || n_slack < 0 || n_slack > N || !(beta > 0.0) ||
+        !(beta <= 1.0) ||
+        log_conf != log_conf || !(acc_thresh == acc_thresh))
+        return JTO_ERR_INVALID;
+    for (int b = 0; b < nseq; ++b) {
+        const int acc = accept_len ? accept_len[b] : -1;
+        if (acc < -1 || acc > N || !(acc_ema[b] >= 0.0) || acc_ema[b] == INFINITY)
+            return JTO_ERR_INVALID;
+    }
+    int ceil_b = b_max;
+    if (node_cap > 0) {
+        int per = node_cap / nseq;
+        if (per < b_min) per = b_min;
+        if (per < ceil_b) ceil_b = per;
+    }
+    tree_off[0] = 0;
+    for (int b = 0; b < nseq; ++b) {
+        double ema = acc_ema[b];
+        const int acc = accept_len ? accept_len[b] : -1;
+        if (acc >= 0) {
+            const double x = (1.0 - beta) * ema;
+            const double y = beta * (double)acc;
+            ema = x + y;
+        }
+        const int conf = lp[(int64_t)b * N * W] >= log_conf;
+        const int hot = ema >= acc_thresh;
+        int B = budget_state[b];
+        if (B < b_min) B = b_min;
+        if (B > ceil_b) B = ceil_b;
+        if (conf && hot) {
+            B = 2 * B;
+            if (B > ceil_b) B = ceil_b;
+        } else if (!conf && !hot) {
+            B = B / 2;
+            if (B < b_min) B = b_min;
+        }
+        int nc;
+        if (floor(ema) >= (double)N) {
+            nc = N;
+        } else {
+            nc = (int)floor(ema) + n_slack;
+            if (nc > N) nc = N;
+        }
+        if (nc < n_min) nc = n_min;
+        const int wc = conf ? W : w_min;
+        int64_t full = full_tree_nodes(nc, wc, JTO_MAX_TREE + 1);
+        const int emit = (int64_t)B < full ? B : (int)full;
+        budget_state[b] = B;
+        acc_ema[b] = ema;
+        w_cap[b] = wc;
+        n_cap[b] = nc;
+        tree_off[b + 1] = tree_off[b] + emit;
+    }
+    return JTO_OK;
 }
