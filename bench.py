@@ -176,13 +176,32 @@ def profiled_traffic(kernel_file):
 # --------------------------------------------------------------------------
 # CPU baseline: the oracle, as it stands, on a bounded sample
 # --------------------------------------------------------------------------
-def oracle_build(wl, alpha):
-    """The oracle's tree build of the step: plain, or entropy-mixed scores."""
+def held_policy(budgets, N, W):
+    """Adaptive-policy parameters that hold every request's budget: every
+    request is confident (log_conf = -inf) and none is accepting
+    (acc_thresh = +inf), so B never moves; width W, depth N.  The emitted
+    trees are then the fixed workload's, and the step measures the policy's
+    own cost in the loop."""
+    return dict(b_min=int(min(budgets)), b_max=int(max(budgets)), node_cap=0, w_min=W, n_min=N, n_slack=N,
+                beta=0.25, log_conf=-math.inf, acc_thresh=math.inf)
+
+
+def oracle_build(wl, alpha, adaptive=False):
+    """The oracle's tree build of the step: plain, entropy-mixed scores, or
+    the adaptive policy (held budgets) followed by the capped expansion."""
     import oracle
 
+    c = wl.cfg
+    if adaptive:
+        tb = oracle.tree_build(wl.draft_logits, wl.root_token,
+                               np.arange(wl.nseq + 1, dtype=np.int32), c["W"])
+        budgets = np.diff(wl.tree_off)
+        pol = oracle.tree_policy(tb["lp"], None, budgets, np.zeros(wl.nseq), **held_policy(budgets, c["N"], c["W"]))
+        return oracle.tree_expand_capped(tb["tok"], tb["lp"], wl.root_token, pol["tree_off"], c["N"], c["W"],
+                                         w_cap=pol["w_cap"], n_cap=pol["n_cap"])
     if alpha == 0.0:
-        return oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"])
-    return oracle.tree_build_mixed(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"], alpha)
+        return oracle.tree_build(wl.draft_logits, wl.root_token, wl.tree_off, c["W"])
+    return oracle.tree_build_mixed(wl.draft_logits, wl.root_token, wl.tree_off, c["W"], alpha)
 
 
 def oracle_accept(wl, target, parent, token, uniforms):
@@ -204,11 +223,11 @@ def step_uniforms(cfg, rank, total):
     return u[0].copy(), u[1].copy()
 
 
-def cpu_oracle_sample(wl, tree_parent, tree_token, target, attn_nodes, alpha, uniforms):
+def cpu_oracle_sample(wl, tree_parent, tree_token, target, attn_nodes, alpha, uniforms, adaptive):
     import oracle
 
     t0 = time.perf_counter()
-    tr = oracle_build(wl, alpha)
+    tr = oracle_build(wl, alpha, adaptive)
     t1 = time.perf_counter()
     oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len, wl.tree_off,
                      tr["parent"], wl.scale, rows=attn_nodes)
@@ -228,6 +247,8 @@ def attn_sample_nodes(wl, k):
 
 def step_name(args):
     build = "tree_build" if args.alpha == 0.0 else f"tree_build_mixed(alpha={args.alpha:g})"
+    if args.adaptive:
+        build = "tree_build_adaptive(policy fed the last greedy accept_len, holding each budget)"
     return (build + " + tree_attn_paged + verify_accept(greedy) + verify_accept(margin t=0.8)"
             + (" + verify_accept_stochastic(T=1)" if args.stochastic else ""))
 
@@ -245,7 +266,7 @@ def run_reference(args, rank):
     wl = wk.make(args.config, seed=replica_seed(args.config, 0))
     c = wl.cfg
     t0 = time.perf_counter()
-    tr = oracle_build(wl, args.alpha)
+    tr = oracle_build(wl, args.alpha, args.adaptive)
     t_build = time.perf_counter() - t0
     target = wk.target_logits(wl, tr["parent"], tr["token"])
     uniforms = step_uniforms(args.config, 0, wl.total) if args.stochastic else None
@@ -303,9 +324,14 @@ def main():
                     help="add the temperature-1 acceptance (jt_verify_accept_stochastic) to the step")
     ap.add_argument("--alpha", type=float, default=0.0,
                     help="entropy weight of the tree build's step scores (jt_tree_build_mixed); 0 = plain")
+    ap.add_argument("--adaptive", action="store_true",
+                    help="build through jt_tree_build_adaptive (top-W, policy, capped expansion), the "
+                         "policy fed each step's greedy accept_len and holding every budget")
     args = ap.parse_args()
     if not 0.0 <= args.alpha <= 1.0:
         raise SystemExit("--alpha must lie in [0, 1]")
+    if args.adaptive and args.alpha > 0:
+        raise SystemExit("--adaptive and --alpha do not combine")
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -356,21 +382,36 @@ def main():
     max_pages = wl.block_table.shape[1]
     log_t = math.log(c["t"])
 
-    # outputs and workspaces, allocated once
-    parent = torch.empty(total, dtype=torch.int32, device=dev)
+    # outputs and workspaces, allocated once (node arrays sized to the
+    # policy's capacity in adaptive mode)
+    budgets = np.diff(wl.tree_off)
+    cap = nseq * int(budgets.max()) if args.adaptive else total
+    parent = torch.empty(cap, dtype=torch.int32, device=dev)
     token = torch.empty_like(parent)
     depth = torch.empty_like(parent)
-    anc = torch.empty((total, 8), dtype=torch.int32, device=dev)
+    anc = torch.empty((cap, 8), dtype=torch.int32, device=dev)
     out = torch.empty_like(d["q"])
     lse = torch.empty((total, Hq), dtype=torch.float32, device=dev)
-    acc = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(3)]
+    acc = [torch.full((nseq,), -1, dtype=torch.int32, device=dev) for _ in range(3)]
     path = [torch.empty((nseq, N + 1), dtype=torch.int32, device=dev) for _ in range(3)]
     bonus = [torch.empty(nseq, dtype=torch.int32, device=dev) for _ in range(3)]
     build_op = jt.JT_OP_TREE_BUILD_MIXED if args.alpha > 0 else jt.JT_OP_TREE_BUILD
     ws_b = jt.workspace(jt.jt_workspace_size(build_op, nseq, N, W, c["V"]), dev)
 
+    if args.adaptive:
+        prm = jt.policy_params(**held_policy(budgets, N, W))
+        pol_state = (to_dev(budgets.astype(np.int32)), torch.zeros(nseq, dtype=torch.float64, device=dev))
+        pol_out = (torch.empty(nseq + 1, dtype=torch.int32, device=dev),
+                   torch.empty(nseq, dtype=torch.int32, device=dev), torch.empty(nseq, dtype=torch.int32, device=dev))
+
+    def offs(inp):
+        return pol_out[0] if args.adaptive else inp["off"]
+
     def build(inp):
-        if args.alpha > 0:
+        if args.adaptive:   # acc[0]: the previous step's greedy accepted lengths
+            jt.jt_tree_build_adaptive(inp["draft"], inp["root"], acc[0], pol_state[0], pol_state[1], W, prm,
+                                      capacity=cap, out=pol_out + (parent, token, depth, anc), ws=ws_b)
+        elif args.alpha > 0:
             jt.jt_tree_build_mixed(inp["draft"], inp["root"], inp["off"], W, args.alpha, total_nodes=total,
                                    out=(parent, token, depth, anc), ws=ws_b)
         else:
@@ -384,7 +425,9 @@ def main():
     # target logits need the drafted tokens: build the tree once, then draw
     build(d)
     jt.jt_check(ws_b)
-    par_h, tok_h, dep_h = parent.cpu().numpy(), token.cpu().numpy(), depth.cpu().numpy()
+    if args.adaptive:   # the held policy must reproduce the workload's offsets
+        assert np.array_equal(pol_out[0].cpu().numpy(), wl.tree_off), "adaptive policy moved a budget"
+    par_h, tok_h, dep_h = (t.cpu().numpy()[:total] for t in (parent, token, depth))
     target_np = wk.target_logits(wl, par_h, tok_h)
     h["target"] = torch.from_numpy(target_np)
     d["target"] = h["target"].to(dev)
@@ -398,13 +441,13 @@ def main():
 
     def step(inp):
         build(inp)
-        jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], inp["off"], anc,
+        jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], offs(inp), anc,
                               scale=wl.scale, max_tree=max_tree, out=out, lse=lse, ws=ws_a)
         for i, rule in enumerate((jt.JT_RULE_GREEDY, jt.JT_RULE_MARGIN)):
-            jt.jt_verify_accept(inp["target"], parent, token, inp["off"], N, rule=rule, log_t=log_t,
+            jt.jt_verify_accept(inp["target"], parent, token, offs(inp), N, rule=rule, log_t=log_t,
                                 out=(acc[i], path[i], bonus[i]), ws=ws_v[i])
         if args.stochastic:
-            jt.jt_verify_accept_stochastic(inp["target"], inp["draft"], parent, token, inp["off"], N,
+            jt.jt_verify_accept_stochastic(inp["target"], inp["draft"], parent, token, offs(inp), N,
                                            inp["u_acc"], inp["u_bon"], out=(acc[2], path[2], bonus[2]),
                                            ws=ws_v[2])
 
@@ -417,7 +460,7 @@ def main():
         jt.jt_check(ws)
 
     def attn_only(inp):
-        jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], inp["off"], anc,
+        jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], offs(inp), anc,
                               scale=wl.scale, max_tree=max_tree, out=out, lse=lse, ws=ws_a)
 
     # The step's kernels are replayed from a CUDA graph (as a serving engine
@@ -526,7 +569,7 @@ def main():
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         nodes = attn_sample_nodes(wl, args.cpu_attn_nodes)
-        v, secs = cpu_oracle_sample(wl, par_h, tok_h, target_np, nodes, args.alpha, uniforms)
+        v, secs = cpu_oracle_sample(wl, par_h, tok_h, target_np, nodes, args.alpha, uniforms, args.adaptive)
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"full tree build and the step's acceptance rules over all {total} nodes, "
                          f"attention for {len(nodes)} of {total} nodes ({secs:.1f} s, "
@@ -536,7 +579,8 @@ def main():
     # kernel (+ split combine when the plan splits the keys); two acceptances
     attn_split = jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq, Hkv, D,
                                       max_pages, max_tree) > 256
-    launches_per_step = 3 + (2 if attn_split else 1) + 2 + (1 if args.stochastic else 0)
+    launches_per_step = (3 + (2 if attn_split else 1) + 2 + (1 if args.stochastic else 0)
+                         + (1 if args.adaptive else 0))
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

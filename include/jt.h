@@ -38,6 +38,10 @@
  *  - anc: uint32 [total_nodes, 8], a 256-bit ancestor-or-self set per node:
  *    bit j of word w is set when local node 32*w + j is the node itself or
  *    one of its ancestors.
+ *  - total_nodes (host) is the capacity of the node-indexed arrays and must
+ *    be >= tree_off[nseq]; it may be larger (tree offsets written on the
+ *    device by jt_tree_policy, whose total the host does not know).  Rows at
+ *    or beyond tree_off[nseq] are neither read nor written.
  *
  * Sources (prose pages; no code is printed there):
  *  [JS-news] JetSpec news summary (mlqm.cn/news/158889): tree-causal
@@ -49,7 +53,9 @@
  *      expansion with a priority queue), section 七 (paged tree attention
  *      without a dense mask).
  *  [AS] "AdaptiveSpec：免训练推测解码方案提速56%的技术解析", section
- *      "逐步Margin规则": accept when p(draft)/p(top1) >= t.
+ *      "逐步Margin规则": accept when p(draft)/p(top1) >= t; section
+ *      "逐步树策略：动态调整草稿树规模": per-step tree size from the draft's
+ *      top-1 confidence and the rolling acceptance history.
  *  [SD] speculative-decoding overview, chooseai.io/news/6515, section
  *      "推测解码是什么：草稿模型先猜，目标模型验收" (rejection-sampling acceptance).
  */
@@ -79,7 +85,7 @@ typedef enum {
 typedef enum { JT_DTYPE_F32 = 0, JT_DTYPE_BF16 = 1 } jt_dtype;
 typedef enum { JT_RULE_GREEDY = 0, JT_RULE_MARGIN = 1 } jt_rule;
 typedef enum { JT_OP_TREE_BUILD = 0, JT_OP_TREE_ATTN = 1, JT_OP_VERIFY_ACCEPT = 2,
-               JT_OP_TREE_TOPW = 3, JT_OP_TREE_BUILD_MIXED = 4 } jt_op;
+               JT_OP_TREE_TOPW = 3, JT_OP_TREE_BUILD_MIXED = 4, JT_OP_TREE_POLICY = 5 } jt_op;
 
 /* Limits of this build. */
 #define JT_MAX_TREE 256   /* B_b (bitset width) */
@@ -93,6 +99,8 @@ typedef enum { JT_OP_TREE_BUILD = 0, JT_OP_TREE_ATTN = 1, JT_OP_VERIFY_ACCEPT = 
  * count for JT_OP_TREE_ATTN.  Returns 0 for invalid sizes.
  *   TREE_BUILD:    nseq, N, W, V
  *   TREE_BUILD_MIXED: nseq, N, W, V
+ *   TREE_POLICY:   (256 bytes: the header only; jt_tree_expand and
+ *                  jt_tree_expand_capped need the same)
  *   TREE_TOPW:     nseq*N rows given as nseq (N=1), W, V
  *   TREE_ATTN:     nseq, total_nodes, Hq, Hkv, D, max_pages, max_tree
  *   VERIFY_ACCEPT: nseq, total_nodes
@@ -109,7 +117,7 @@ size_t jt_workspace_size(int op, int nseq, int N, int W, int64_t V, int total_no
  *   root_token:   int32 [nseq], token of each root.
  *   tree_off:     int32 [nseq+1], budgets B_b as described above; the full
  *                 W-ary tree of depth N must hold at least B_b nodes.
- *   total_nodes:  tree_off[nseq] (host value; sizes the outputs).
+ *   total_nodes:  capacity >= tree_off[nseq] (host value; sizes the outputs).
  * Step 1 takes, per row, the top-W tokens (logit descending, token id
  * ascending) and lse = log sum exp(z).  Step 2 runs best-first expansion:
  * a queue of candidate nodes keyed by (cumulative log-prob descending, depth
@@ -197,6 +205,98 @@ jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* ro
                          const int32_t* tree_off, int nseq, int N, int W, int total_nodes,
                          int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc,
                          void* ws, size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_tree_expand_capped -- jt_tree_expand with per-sequence caps on the
+ * tree's width and depth ([AS] per-step tree policy: each request's tree
+ * gets its own depth, width and node count).
+ *   w_cap: int32 [nseq] or NULL; sequence b uses only the first w_cap[b]
+ *          candidates of every row (1 <= w_cap[b] <= W).
+ *   n_cap: int32 [nseq] or NULL; nodes of depth n_cap[b] get no children
+ *          (0 <= n_cap[b] <= N).
+ * The tree is then the best-first expansion of the capped full tree; B_b
+ * must fit it.  A cap out of range or a budget beyond the capped tree
+ * skips the sequence and raises JT_ERR_INVALID (device-side).  With both
+ * caps NULL this is jt_tree_expand.  Workspace: 256 bytes.
+ */
+jt_status jt_tree_expand_capped(const int32_t* tok, const double* lp, const int32_t* root_token,
+                                const int32_t* tree_off, const int32_t* w_cap, const int32_t* n_cap,
+                                int nseq, int N, int W, int total_nodes, int32_t* parent,
+                                int32_t* token, int32_t* depth, uint32_t* anc, void* ws,
+                                size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * Parameters of the adaptive tree policy (host struct, read at the call).
+ */
+typedef struct {
+    int32_t b_min;     /* budget floor, 1 <= b_min */
+    int32_t b_max;     /* budget ceiling, b_min <= b_max <= JT_MAX_TREE */
+    int32_t node_cap;  /* node budget of the whole batch, 0 = none; the
+                          per-request ceiling is then
+                          min(b_max, max(b_min, node_cap / nseq)) */
+    int32_t w_min;     /* width when the draft is not confident, 1..W */
+    int32_t n_min;     /* depth floor, 0..N */
+    int32_t n_slack;   /* depth beyond the rolling accepted length, 0..N */
+    double beta;       /* weight of the newest accepted length in the
+                          rolling average, 0 < beta <= 1 */
+    double log_conf;   /* confidence threshold on the log of the draft's
+                          top-1 probability at depth 1 (not NaN) */
+    double acc_thresh; /* threshold on the rolling accepted length, in
+                          tokens (not NaN) */
+} jt_policy_params;
+
+/*
+ * jt_tree_policy -- per-request tree size for the next step ([AS] section
+ * "逐步树策略：动态调整草稿树规模": the draft's top-1 confidence and the
+ * rolling acceptance history set depth, width and node count; the tree
+ * grows when both are high and shrinks in the opposite case; [JS-art]
+ * section 七: large budgets stop paying as the batch grows).  The pages
+ * give no formula; this is the rule, per request b:
+ *   ema   <- (1 - beta) * ema + beta * accept_len[b]   (if accept_len[b] >= 0)
+ *   conf  =  lp[b, 0, 0] >= log_conf;  hot = ema >= acc_thresh
+ *   B     <- clamp(B, b_min, ceil); then min(2B, ceil) if conf and hot,
+ *            max(B / 2, b_min) if neither, else unchanged
+ *   n_cap =  clamp(floor(ema) + n_slack, n_min, N);  w_cap = conf ? W : w_min
+ *   budget = min(B, nodes of the full w_cap-ary tree of depth n_cap)
+ *   tree_off = exclusive prefix sum of the budgets (tree_off[0] = 0)
+ * fp64 operations are rounded one at a time (no fused multiply-add).
+ *   lp:           fp64 [nseq, N, W], the per-depth table of jt_tree_topw.
+ *   accept_len:   int32 [nseq] or NULL: accepted length of each request's
+ *                 previous step (jt_verify_accept*), -1 = none observed.
+ *   budget_state: int32 [nseq], in/out: the controller's B (not clipped to
+ *                 the tree); initialise to the first budget wanted.
+ *   acc_ema:      fp64 [nseq], in/out: the rolling accepted length (>= 0,
+ *                 finite); initialise to a prior, e.g. acc_thresh.
+ *   tree_off:     int32 [nseq+1] out; w_cap, n_cap: int32 [nseq] out, for
+ *                 jt_tree_expand_capped.  tree_off[nseq] <= nseq * ceil.
+ * A request whose accept_len is outside [-1, N] or whose acc_ema is
+ * negative or not finite gets a root-only tree (budget 1, n_cap 0), keeps
+ * its state and raises JT_ERR_INVALID (device-side).  One CTA; N >= 1.
+ * Workspace: jt_workspace_size(JT_OP_TREE_POLICY, ...) = 256 bytes.
+ */
+jt_status jt_tree_policy(const double* lp, int nseq, int N, int W, const int32_t* accept_len,
+                         const jt_policy_params* params, int32_t* budget_state, double* acc_ema,
+                         int32_t* tree_off, int32_t* w_cap, int32_t* n_cap, void* ws,
+                         size_t ws_bytes, jt_stream_t stream);
+
+/*
+ * jt_tree_build_adaptive -- jt_tree_topw, jt_tree_policy and
+ * jt_tree_expand_capped in one call, with no host round trip: the budgets
+ * stay on the device.
+ *   capacity: host, >= nseq * ceil (ceil as in jt_tree_policy); sizes
+ *             parent/token/depth [capacity] and anc [capacity, 8] like
+ *             total_nodes elsewhere.  Pass it as total_nodes, and the
+ *             policy's ceiling as max_tree, to jt_tree_attn_paged.
+ * Other arguments as in jt_tree_build and jt_tree_policy (root_token
+ * [nseq]; tree_off, w_cap, n_cap are outputs).  Workspace:
+ * jt_workspace_size(JT_OP_TREE_BUILD, nseq, N, W, V).
+ */
+jt_status jt_tree_build_adaptive(const float* draft_logits, const int32_t* root_token, int nseq,
+                                 int N, int W, int64_t V, int capacity, const int32_t* accept_len,
+                                 const jt_policy_params* params, int32_t* budget_state,
+                                 double* acc_ema, int32_t* tree_off, int32_t* w_cap,
+                                 int32_t* n_cap, int32_t* parent, int32_t* token, int32_t* depth,
+                                 uint32_t* anc, void* ws, size_t ws_bytes, jt_stream_t stream);
 
 /*
  * jt_tree_attn_paged -- tree-causal attention over a paged KV cache

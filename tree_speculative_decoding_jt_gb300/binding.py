@@ -21,16 +21,40 @@ from . import build as _build
 JT_OK, JT_ERR_INVALID, JT_ERR_UNSUPPORTED, JT_ERR_CUDA, JT_ERR_TIMEOUT, JT_ERR_WORKSPACE = 0, -1, -2, -3, -4, -5
 JT_DTYPE_F32, JT_DTYPE_BF16 = 0, 1
 JT_RULE_GREEDY, JT_RULE_MARGIN = 0, 1
-JT_OP_TREE_BUILD, JT_OP_TREE_ATTN, JT_OP_VERIFY_ACCEPT, JT_OP_TREE_TOPW, JT_OP_TREE_BUILD_MIXED = 0, 1, 2, 3, 4
+(JT_OP_TREE_BUILD, JT_OP_TREE_ATTN, JT_OP_VERIFY_ACCEPT, JT_OP_TREE_TOPW, JT_OP_TREE_BUILD_MIXED,
+ JT_OP_TREE_POLICY) = 0, 1, 2, 3, 4, 5
 JT_MAX_TREE, JT_MAX_W, JT_MAX_N, JT_PAGE_SIZE = 256, 8, 64, 16
 
 # every symbol include/jt.h declares
 EXPORTS = ("jt_workspace_size", "jt_tree_build", "jt_tree_topw", "jt_tree_expand",
            "jt_tree_attn_paged", "jt_verify_accept", "jt_check", "jt_status_str", "jt_version",
-           "jt_tree_build_noalloc", "jt_verify_accept_stochastic", "jt_tree_build_mixed")
+           "jt_tree_build_noalloc", "jt_verify_accept_stochastic", "jt_tree_build_mixed",
+           "jt_tree_expand_capped", "jt_tree_policy", "jt_tree_build_adaptive")
 
 _lock = threading.Lock()
 _lib = None
+
+
+class PolicyParams(ctypes.Structure):
+    """jt_policy_params of include/jt.h (field order and types as there)."""
+    _fields_ = [("b_min", ctypes.c_int32), ("b_max", ctypes.c_int32), ("node_cap", ctypes.c_int32),
+                ("w_min", ctypes.c_int32), ("n_min", ctypes.c_int32), ("n_slack", ctypes.c_int32),
+                ("beta", ctypes.c_double), ("log_conf", ctypes.c_double), ("acc_thresh", ctypes.c_double)]
+
+
+def policy_params(b_min=16, b_max=256, node_cap=0, w_min=2, n_min=2, n_slack=3, beta=0.25,
+                  log_conf=-0.6931471805599453, acc_thresh=3.0) -> PolicyParams:
+    """Policy parameters with the defaults used by the tests and bench.py."""
+    return PolicyParams(b_min, b_max, node_cap, w_min, n_min, n_slack, float(beta), float(log_conf),
+                        float(acc_thresh))
+
+
+def policy_ceiling(params: PolicyParams, nseq: int) -> int:
+    """Per-request budget ceiling of the policy (min(b_max, max(b_min,
+    node_cap // nseq)) with a node cap, else b_max)."""
+    if params.node_cap > 0:
+        return min(params.b_max, max(params.b_min, params.node_cap // nseq))
+    return params.b_max
 
 
 class JtError(RuntimeError):
@@ -62,6 +86,11 @@ def load(build_if_missing: bool = True):
         lib.jt_tree_topw.argtypes = [P, i64, i64, i32, P, P, P, P, sz, P]
         lib.jt_tree_build_noalloc.argtypes = [P, P, P, i32, i32, i32, i64, i32, P, P, P, P, i32, P]
         lib.jt_tree_expand.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz, P]
+        lib.jt_tree_expand_capped.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, P, P, P, P, P, sz, P]
+        lib.jt_tree_policy.argtypes = [P, i32, i32, i32, P, ctypes.POINTER(PolicyParams), P, P, P, P, P, P,
+                                       sz, P]
+        lib.jt_tree_build_adaptive.argtypes = [P, P, i32, i32, i32, i64, i32, P, ctypes.POINTER(PolicyParams),
+                                               P, P, P, P, P, P, P, P, P, P, sz, P]
         lib.jt_tree_attn_paged.argtypes = [P, P, P, i32, P, i32, i32, P, P, P, i32, i32, i32, i32,
                                            i32, i32, i32, f32, P, P, P, sz, P]
         lib.jt_verify_accept.argtypes = [P, P, P, P, i32, i32, i64, i32, i32, f64, P, P, P, P, sz, P]
@@ -73,7 +102,8 @@ def load(build_if_missing: bool = True):
         lib.jt_version.argtypes = []
         for name in ("jt_tree_build", "jt_tree_topw", "jt_tree_expand", "jt_tree_attn_paged",
                      "jt_verify_accept", "jt_check", "jt_version", "jt_tree_build_noalloc",
-                     "jt_verify_accept_stochastic", "jt_tree_build_mixed"):
+                     "jt_verify_accept_stochastic", "jt_tree_build_mixed", "jt_tree_expand_capped",
+                     "jt_tree_policy", "jt_tree_build_adaptive"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -284,6 +314,98 @@ def jt_tree_expand(tok, lp, root_token, tree_off, total_nodes=None, ws=None, str
                             _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "jt_tree_expand")
     return parent, token, depth, anc
+
+
+def jt_tree_expand_capped(tok, lp, root_token, tree_off, w_cap=None, n_cap=None, total_nodes=None, ws=None,
+                          stream=None):
+    """jt_tree_expand with optional per-sequence width / depth caps
+    (int32 [nseq] device tensors)."""
+    lib = load()
+    _need(tok, "tok", torch.int32)
+    _need(lp, "lp", torch.float64)
+    _need(root_token, "root_token", torch.int32)
+    _need(tree_off, "tree_off", torch.int32)
+    for t, name in ((w_cap, "w_cap"), (n_cap, "n_cap")):
+        if t is not None:
+            _need(t, name, torch.int32)
+    nseq, N, W = tok.shape
+    if total_nodes is None:
+        total_nodes = int(tree_off[-1].item())
+    dev = tok.device
+    parent = torch.empty(total_nodes, dtype=torch.int32, device=dev)
+    token = torch.empty_like(parent)
+    depth = torch.empty_like(parent)
+    anc = torch.empty((total_nodes, 8), dtype=torch.int32, device=dev)
+    if ws is None:
+        ws = workspace(256, dev)
+    rc = lib.jt_tree_expand_capped(_ptr(tok), _ptr(lp), _ptr(root_token), _ptr(tree_off), _ptr(w_cap),
+                                   _ptr(n_cap), nseq, N, W, total_nodes, _ptr(parent), _ptr(token),
+                                   _ptr(depth), _ptr(anc), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jt_tree_expand_capped")
+    return parent, token, depth, anc
+
+
+def jt_tree_policy(lp, accept_len, budget_state, acc_ema, params=None, out=None, ws=None, stream=None):
+    """One step of the adaptive tree policy.  lp fp64 [nseq, N, W];
+    accept_len int32 [nseq] or None; budget_state int32 / acc_ema fp64
+    [nseq] are updated in place.  Returns (tree_off, w_cap, n_cap)."""
+    lib = load()
+    _need(lp, "lp", torch.float64)
+    _need(budget_state, "budget_state", torch.int32)
+    _need(acc_ema, "acc_ema", torch.float64)
+    if accept_len is not None:
+        _need(accept_len, "accept_len", torch.int32)
+    nseq, N, W = lp.shape
+    params = params or policy_params()
+    dev = lp.device
+    if out is None:
+        out = (torch.empty(nseq + 1, dtype=torch.int32, device=dev),
+               torch.empty(nseq, dtype=torch.int32, device=dev),
+               torch.empty(nseq, dtype=torch.int32, device=dev))
+    tree_off, w_cap, n_cap = out
+    if ws is None:
+        ws = workspace(jt_workspace_size(JT_OP_TREE_POLICY), dev)
+    rc = lib.jt_tree_policy(_ptr(lp), nseq, N, W, _ptr(accept_len), ctypes.byref(params), _ptr(budget_state),
+                            _ptr(acc_ema), _ptr(tree_off), _ptr(w_cap), _ptr(n_cap), _ptr(ws), ws.numel(),
+                            _stream(stream))
+    _check(rc, "jt_tree_policy")
+    return tree_off, w_cap, n_cap
+
+
+def jt_tree_build_adaptive(draft_logits, root_token, accept_len, budget_state, acc_ema, W, params=None,
+                           capacity=None, out=None, ws=None, stream=None):
+    """Top-W tables, adaptive policy and capped expansion in one call.
+    Returns (tree_off, w_cap, n_cap, parent, token, depth, anc); the node
+    arrays have `capacity` rows (default nseq * the policy's ceiling)."""
+    lib = load()
+    _need(draft_logits, "draft_logits", torch.float32)
+    _need(root_token, "root_token", torch.int32)
+    _need(budget_state, "budget_state", torch.int32)
+    _need(acc_ema, "acc_ema", torch.float64)
+    if accept_len is not None:
+        _need(accept_len, "accept_len", torch.int32)
+    nseq, N, V = draft_logits.shape
+    params = params or policy_params()
+    if capacity is None:
+        capacity = nseq * policy_ceiling(params, nseq)
+    dev = draft_logits.device
+    if out is None:
+        out = (torch.empty(nseq + 1, dtype=torch.int32, device=dev),
+               torch.empty(nseq, dtype=torch.int32, device=dev),
+               torch.empty(nseq, dtype=torch.int32, device=dev),
+               torch.empty(capacity, dtype=torch.int32, device=dev),
+               torch.empty(capacity, dtype=torch.int32, device=dev),
+               torch.empty(capacity, dtype=torch.int32, device=dev),
+               torch.empty((capacity, 8), dtype=torch.int32, device=dev))
+    tree_off, w_cap, n_cap, parent, token, depth, anc = out
+    if ws is None:
+        ws = workspace(jt_workspace_size(JT_OP_TREE_BUILD, nseq, N, W, V), dev)
+    rc = lib.jt_tree_build_adaptive(_ptr(draft_logits), _ptr(root_token), nseq, N, W, V, capacity,
+                                    _ptr(accept_len), ctypes.byref(params), _ptr(budget_state), _ptr(acc_ema),
+                                    _ptr(tree_off), _ptr(w_cap), _ptr(n_cap), _ptr(parent), _ptr(token),
+                                    _ptr(depth), _ptr(anc), _ptr(ws), ws.numel(), _stream(stream))
+    _check(rc, "jt_tree_build_adaptive")
+    return tree_off, w_cap, n_cap, parent, token, depth, anc
 
 
 def jt_tree_attn_paged(q, k_cache, v_cache, block_table, prefix_len, tree_off, anc, scale=None,

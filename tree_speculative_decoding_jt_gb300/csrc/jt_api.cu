@@ -81,6 +81,8 @@ size_t jt_workspace_size(int op, int nseq, int N, int W, int64_t V, int total_no
         case JT_OP_VERIFY_ACCEPT:
             if (nseq < 1 || total_nodes < 1) return 0;
             return accept_workspace_bytes(nseq, total_nodes);
+        case JT_OP_TREE_POLICY:
+            return kWsHeader;
         default:
             return 0;
     }
@@ -127,10 +129,11 @@ jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
                                token, depth, anc, ws, ws_bytes, stream);
 }
 
-jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
-                         const int32_t* tree_off, int nseq, int N, int W, int total_nodes,
-                         int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc, void* ws,
-                         size_t ws_bytes, jt_stream_t stream) {
+jt_status jt_tree_expand_capped(const int32_t* tok, const double* lp, const int32_t* root_token,
+                                const int32_t* tree_off, const int32_t* w_cap, const int32_t* n_cap,
+                                int nseq, int N, int W, int total_nodes, int32_t* parent,
+                                int32_t* token, int32_t* depth, uint32_t* anc, void* ws,
+                                size_t ws_bytes, jt_stream_t stream) {
     if ((N > 0 && (!tok || !lp)) || !root_token || !tree_off || !parent || !token || !depth ||
         !anc || nseq < 1 || nseq > 65535 || N < 0 || N > JT_MAX_N || W < 1 || W > JT_MAX_W ||
         total_nodes < nseq || !aligned(anc, 16))
@@ -138,8 +141,72 @@ jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* ro
     jt_status s = check_ws(ws, ws_bytes, kWsHeader);
     if (s != JT_OK) return s;
     char* base = static_cast<char*>(ws);
-    cudaError_t e = tree_expand_launch(tok, lp, root_token, tree_off, nseq, total_nodes, N, W, parent, token, depth, anc,
-                               reinterpret_cast<uint32_t*>(base), stream);
+    cudaError_t e = tree_expand_launch(tok, lp, root_token, tree_off, w_cap, n_cap, nseq, total_nodes, N, W,
+                                       parent, token, depth, anc, reinterpret_cast<uint32_t*>(base), stream);
+    return from_cuda(e);
+}
+
+jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
+                         const int32_t* tree_off, int nseq, int N, int W, int total_nodes,
+                         int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc, void* ws,
+                         size_t ws_bytes, jt_stream_t stream) {
+    return jt_tree_expand_capped(tok, lp, root_token, tree_off, nullptr, nullptr, nseq, N, W, total_nodes,
+                                 parent, token, depth, anc, ws, ws_bytes, stream);
+}
+
+// Host checks of the policy's parameters (jt_tree_policy's rules); returns
+// the per-request budget ceiling, or 0 when a parameter is out of range.
+static int policy_params_ok(const jt_policy_params* p, int nseq, int N, int W) {
+    if (!p || p->b_min < 1 || p->b_max < p->b_min || p->b_max > JT_MAX_TREE || p->node_cap < 0 ||
+        p->w_min < 1 || p->w_min > W || p->n_min < 0 || p->n_min > N || p->n_slack < 0 ||
+        p->n_slack > N || !(p->beta > 0.0) || !(p->beta <= 1.0) || p->log_conf != p->log_conf ||
+        p->acc_thresh != p->acc_thresh)
+        return 0;
+    int c = p->b_max;
+    if (p->node_cap > 0) {
+        const int per = p->node_cap / nseq;
+        c = per < p->b_min ? p->b_min : per;
+        if (c > p->b_max) c = p->b_max;
+    }
+    return c;
+}
+
+jt_status jt_tree_policy(const double* lp, int nseq, int N, int W, const int32_t* accept_len,
+                         const jt_policy_params* params, int32_t* budget_state, double* acc_ema,
+                         int32_t* tree_off, int32_t* w_cap, int32_t* n_cap, void* ws,
+                         size_t ws_bytes, jt_stream_t stream) {
+    if (!lp || !budget_state || !acc_ema || !tree_off || !w_cap || !n_cap || nseq < 1 ||
+        nseq > 65535 || N < 1 || N > JT_MAX_N || W < 1 || W > JT_MAX_W ||
+        policy_params_ok(params, nseq, N, W) == 0)
+        return JT_ERR_INVALID;
+    jt_status s = check_ws(ws, ws_bytes, kWsHeader);
+    if (s != JT_OK) return s;
+    cudaError_t e = tree_policy_launch(lp, nseq, N, W, accept_len, *params, budget_state, acc_ema, tree_off,
+                                       w_cap, n_cap, static_cast<uint32_t*>(ws), stream);
+    return from_cuda(e);
+}
+
+jt_status jt_tree_build_adaptive(const float* draft_logits, const int32_t* root_token, int nseq,
+                                 int N, int W, int64_t V, int capacity, const int32_t* accept_len,
+                                 const jt_policy_params* params, int32_t* budget_state,
+                                 double* acc_ema, int32_t* tree_off, int32_t* w_cap,
+                                 int32_t* n_cap, int32_t* parent, int32_t* token, int32_t* depth,
+                                 uint32_t* anc, void* ws, size_t ws_bytes, jt_stream_t stream) {
+    if (!draft_logits || !root_token || !budget_state || !acc_ema || !tree_off || !w_cap || !n_cap ||
+        !parent || !token || !depth || !anc || nseq < 1 || nseq > 65535 || N < 1 || N > JT_MAX_N ||
+        W < 1 || W > JT_MAX_W || V < W || V > 0x7FFFFFFFll || static_cast<long long>(nseq) * N > 65535 ||
+        !aligned(anc, 16))
+        return JT_ERR_INVALID;
+    const int ceil_b = policy_params_ok(params, nseq, N, W);
+    if (ceil_b == 0 || static_cast<long long>(capacity) < static_cast<long long>(nseq) * ceil_b)
+        return JT_ERR_INVALID;
+    jt_status s = check_ws(ws, ws_bytes, build_ws(nseq, N, W, V));
+    if (s != JT_OK) return s;
+    char* base = static_cast<char*>(ws);
+    cudaError_t e = tree_build_adaptive_launch(draft_logits, root_token, nseq, capacity, N, W, V, accept_len,
+                                               *params, budget_state, acc_ema, tree_off, w_cap, n_cap, parent,
+                                               token, depth, anc, base + kWsHeader,
+                                               reinterpret_cast<uint32_t*>(base), stream);
     return from_cuda(e);
 }
 

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/jt.h"
+
 namespace jt {
 
 constexpr size_t kAlign = 256;
@@ -30,10 +32,20 @@ cudaError_t tree_build_launch(const float* z, const int32_t* root_token, const i
                               int nseq, int total_nodes, int N, int W, long long V, double alpha,
                               int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc, char* ws_parts,
                               uint32_t* err, cudaStream_t st);
+// w_cap / n_cap: optional per-sequence width and depth caps (nullptr = none)
 cudaError_t tree_expand_launch(const int32_t* tok, const double* lp, const int32_t* root_token,
-                               const int32_t* tree_off, int nseq, int total_nodes, int N, int W, int32_t* parent,
-                               int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
+                               const int32_t* tree_off, const int32_t* w_cap, const int32_t* n_cap, int nseq,
+                               int total_nodes, int N, int W, int32_t* parent, int32_t* token, int32_t* depth,
+                               uint32_t* anc, uint32_t* err, cudaStream_t st);
+cudaError_t tree_policy_launch(const double* lp, int nseq, int N, int W, const int32_t* accept_len,
+                               const jt_policy_params& prm, int32_t* budget_state, double* acc_ema,
+                               int32_t* tree_off, int32_t* w_cap, int32_t* n_cap, uint32_t* err,
                                cudaStream_t st);
+cudaError_t tree_build_adaptive_launch(const float* z, const int32_t* root_token, int nseq, int capacity, int N,
+                                       int W, long long V, const int32_t* accept_len, const jt_policy_params& prm,
+                                       int32_t* budget_state, double* acc_ema, int32_t* tree_off, int32_t* w_cap,
+                                       int32_t* n_cap, int32_t* parent, int32_t* token, int32_t* depth,
+                                       uint32_t* anc, char* ws_parts, uint32_t* err, cudaStream_t st);
 
 // verify_accept.cu
 size_t accept_workspace_bytes(int nseq, int total_nodes);

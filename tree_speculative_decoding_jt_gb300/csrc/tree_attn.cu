@@ -545,6 +545,7 @@ __global__ void __launch_bounds__(128)
         static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE)
         return;  // reported by the main kernel
     const int node = n - off;
+    if (node >= B) return;  // spare capacity past the last tree
     const int valid_end = unit_valid_end(L, B, (node / p.npt) >> 1, p.npt);
     const long long rowid = static_cast<long long>(n) * p.Hq + h;
     float M = -INFINITY;

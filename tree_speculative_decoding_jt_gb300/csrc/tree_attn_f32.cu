@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(128)
         if (lane == 0) raise_error(err, DEVERR_INVALID);
         return;
     }
+    if (n - off >= B) return;  // spare capacity past the last tree
     const int kvh = h / (Hq / Hkv);
     const long long rowid = static_cast<long long>(n) * Hq + h;
     float qv[DPL], acc[DPL];

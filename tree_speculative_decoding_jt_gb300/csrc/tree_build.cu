@@ -8,20 +8,24 @@
 // children, push them, stop at B nodes).
 //
 // Kernels
-//   topw_partial_kernel  one CTA per (row, 4096-entry chunk): vectorised
-//                        coalesced loads, per-thread top-W in registers,
-//                        warp-shuffle merge; chunk max and the chunk's
-//                        sum of exp(z - max) from the table-driven fp32 exp
-//                        with float-float accumulation (fp64 per CTA).
+//   topw_partial_kernel  one CTA per (row, chunk of 256 x 16 or 32 entries):
+//                        vectorised coalesced loads, per-thread top-W in
+//                        registers, warp-shuffle merge; chunk max and the
+//                        chunk's sum of exp(z - max) from the table-driven
+//                        fp32 exp with float-float accumulation (and, for the
+//                        entropy-mixed build, the sum of exp(z - max) * z).
 //   topw_merge_kernel    one warp per row: merges the chunk partials into
-//                        top-W ids, log-probs and lse (fp64).
-//   expand_kernel        one CTA per sequence: merges its N rows, then one
-//                        warp runs the best-first expansion with a lazy
-//                        frontier (only a popped node's best child and a
-//                        popped child's next sibling are pushed, which pops
-//                        the same sequence as pushing all W children), then
-//                        all threads derive the 256-bit ancestor sets.
+//                        top-W ids, log-probs (or mixed step scores) and lse.
+//   expand_kernel        one CTA per sequence: builds the B-1 best nodes of
+//                        the (optionally width/depth-capped) full tree level
+//                        by level with rank-by-binary-search merges, then
+//                        derives the 256-bit ancestor sets.
+//   tree_policy_kernel   one CTA: the adaptive per-request budget, width and
+//                        depth caps and the tree offsets (AdaptiveSpec's
+//                        per-step tree policy).
 #include <float.h>
+
+#include <algorithm>
 
 #include "ffexp.cuh"
 #include "jt_common.cuh"
@@ -676,10 +680,13 @@ __device__ __forceinline__ int set_incl_scan(int v, int* s_warp) {
     return v;
 }
 
+// w_cap / n_cap (optional, per sequence): only the first w_cap[b] candidates
+// of every row are children, and nodes of depth n_cap[b] get none.
 template <int W>
 __global__ void __launch_bounds__(kExpandThreads, 1)
     expand_kernel(const int32_t* __restrict__ tok_in, const double* __restrict__ lp_in,
                   const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
+                  const int32_t* __restrict__ w_cap, const int32_t* __restrict__ n_cap,
                   int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
                   int32_t* __restrict__ depth, uint32_t* __restrict__ anc, uint32_t* err) {
     extern __shared__ __align__(16) unsigned char dsm[];
@@ -702,8 +709,10 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const int tid = threadIdx.x;
     const int off = tree_off[b];
     const int B = tree_off[b + 1] - off;
-    if (B < 1 || B > JT_MAX_TREE || B > full_tree_nodes(N, W, JT_MAX_TREE + 1) || off < 0 ||
-        off + B > total_nodes) {
+    const int Wb = w_cap ? w_cap[b] : W;
+    const int Nb = n_cap ? n_cap[b] : N;
+    if (Wb < 1 || Wb > W || Nb < 0 || Nb > N || B < 1 || B > JT_MAX_TREE ||
+        B > full_tree_nodes(Nb, Wb, JT_MAX_TREE + 1) || off < 0 || off + B > total_nodes) {
         if (tid == 0) raise_error(err, DEVERR_INVALID);
         return;
     }
@@ -717,7 +726,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     const int lane = tid & 31, warp = tid >> 5;
     int m = 0;            // size of the sorted set S (buffer cb)
     int cb = 0;
-    for (int d = 0; d < N && K > 0; ++d) {
+    for (int d = 0; d < Nb && K > 0; ++d) {
         unsigned long long* k1 = kb1(cb);
         unsigned long long* k2 = kb2(cb);
         short* par = pbuf(cb);
@@ -746,7 +755,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 #pragma unroll
                 for (int k = 0; k < W; ++k) {
                     ck[k] = double_order_key(__dadd_rn(su, s_lp[d * W + k]));
-                    if (c == k &&
+                    if (c == k && k < Wb &&
                         (!full || key_better(ck[k], make_k2(d + 1, s_tok[d * W + k], pos), t1, t2)))
                         ++c;
                 }
@@ -869,6 +878,96 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
 }
 
 constexpr size_t kExpandSmem = sizeof(unsigned long long) * 4 * kExpCap + sizeof(short) * 3 * kExpCap;
+
+// ---------------------------------------------------------------------------
+// Adaptive per-request tree policy (AdaptiveSpec, per-step tree policy: the
+// draft's top-1 confidence and the rolling acceptance history set the depth,
+// width and node count of each request's tree; it grows when both are high
+// and shrinks in the opposite case).  Per request b:
+//   ema  <- (1 - beta) * ema + beta * accept_len[b]      (when observed)
+//   conf =  lp[b, 0, 0] >= log_conf,  hot = ema >= acc_thresh
+//   B    <- clamp(B, b_min, ceil); 2B (<= ceil) if conf && hot, B/2 (>= b_min)
+//           if neither, else unchanged
+//   n_cap = clamp(floor(ema) + n_slack, n_min, N),  w_cap = conf ? W : w_min
+//   budget = min(B, full w_cap-ary tree of depth n_cap)
+// and tree_off = exclusive prefix sum of the budgets.  One CTA walks the
+// requests 1024 at a time with a block scan and a running carry.  fp64
+// operations are rounded one by one (no fused multiply-add), like the
+// definition, so every decision is reproducible bit for bit.
+// ---------------------------------------------------------------------------
+constexpr int kPolicyThreads = 1024;
+
+__global__ void __launch_bounds__(kPolicyThreads)
+    tree_policy_kernel(const double* __restrict__ lp, int nseq, int N, int W,
+                       const int32_t* __restrict__ accept_len, jt_policy_params prm, int ceil_b,
+                       int32_t* __restrict__ budget_state, double* __restrict__ acc_ema,
+                       int32_t* __restrict__ tree_off, int32_t* __restrict__ w_cap,
+                       int32_t* __restrict__ n_cap, uint32_t* err) {
+    __shared__ int s_warp[kPolicyThreads / 32];
+    __shared__ int s_carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_carry = 0;
+        tree_off[0] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < nseq; base += kPolicyThreads) {
+        const int b = base + tid;
+        int emit = 0;
+        if (b < nseq) {
+            double ema = acc_ema[b];
+            const int acc = accept_len ? accept_len[b] : -1;
+            if (acc < -1 || acc > N || !(ema >= 0.0) || ema == INFINITY) {
+                // invalid state: root-only tree, state left as it was
+                raise_error(err, DEVERR_INVALID);
+                emit = 1;
+                w_cap[b] = W;
+                n_cap[b] = 0;
+            } else {
+                if (acc >= 0)
+                    ema = __dadd_rn(__dmul_rn(1.0 - prm.beta, ema), __dmul_rn(prm.beta, static_cast<double>(acc)));
+                const bool conf = lp[static_cast<long long>(b) * N * W] >= prm.log_conf;
+                const bool hot = ema >= prm.acc_thresh;
+                int B = min(max(budget_state[b], prm.b_min), ceil_b);
+                if (conf && hot) B = min(2 * B, ceil_b);
+                else if (!conf && !hot) B = max(B / 2, prm.b_min);
+                const double fl = floor(ema);
+                int nc = (fl >= static_cast<double>(N)) ? N : min(static_cast<int>(fl) + prm.n_slack, N);
+                nc = max(nc, prm.n_min);
+                const int wc = conf ? W : prm.w_min;
+                emit = min(B, full_tree_nodes(nc, wc, JT_MAX_TREE + 1));
+                budget_state[b] = B;
+                acc_ema[b] = ema;
+                w_cap[b] = wc;
+                n_cap[b] = nc;
+            }
+        }
+        // inclusive block scan of emit
+        int v = emit;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(kFull, v, o);
+            if (lane >= o) v += t;
+        }
+        if (lane == 31) s_warp[warp] = v;
+        __syncthreads();
+        if (warp == 0) {
+            int w = s_warp[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(kFull, w, o);
+                if (lane >= o) w += t;
+            }
+            s_warp[lane] = w;
+        }
+        __syncthreads();
+        const int incl = v + (warp > 0 ? s_warp[warp - 1] : 0);
+        if (b < nseq) tree_off[b + 1] = s_carry + incl;
+        __syncthreads();
+        if (tid == 0) s_carry += s_warp[kPolicyThreads / 32 - 1];
+        __syncthreads();
+    }
+}
 
 // ---------------------------------------------------------------------------
 // Host launchers
@@ -1007,18 +1106,60 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
     return launch_kernel(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, t.tok, t.lp,
-                      root_token, tree_off, total_nodes, N, parent, token, depth, anc, err);
+                         root_token, tree_off, static_cast<const int32_t*>(nullptr),
+                         static_cast<const int32_t*>(nullptr), total_nodes, N, parent, token, depth, anc, err);
+}
+
+static int policy_ceiling(const jt_policy_params& prm, int nseq) {
+    int c = prm.b_max;
+    if (prm.node_cap > 0) c = std::min(c, std::max(prm.b_min, prm.node_cap / nseq));
+    return c;
+}
+
+cudaError_t tree_policy_launch(const double* lp, int nseq, int N, int W, const int32_t* accept_len,
+                               const jt_policy_params& prm, int32_t* budget_state, double* acc_ema,
+                               int32_t* tree_off, int32_t* w_cap, int32_t* n_cap, uint32_t* err,
+                               cudaStream_t st) {
+    return launch_kernel(tree_policy_kernel, dim3(1), dim3(kPolicyThreads), 0, st, 0, lp, nseq, N, W, accept_len,
+                         prm, policy_ceiling(prm, nseq), budget_state, acc_ema, tree_off, w_cap, n_cap, err);
+}
+
+// top-W tables -> policy (budgets, caps, tree_off) -> capped expansion
+template <int W>
+static cudaError_t run_build_adaptive(const float* z, const int32_t* root_token, int nseq, int capacity, int N,
+                                      long long V, const int32_t* accept_len, const jt_policy_params& prm,
+                                      int32_t* budget_state, double* acc_ema, int32_t* tree_off,
+                                      int32_t* w_cap, int32_t* n_cap, int32_t* parent, int32_t* token,
+                                      int32_t* depth, uint32_t* anc, char* ws_parts, uint32_t* err,
+                                      cudaStream_t st) {
+    const long long rows = static_cast<long long>(nseq) * N;
+    const int per = topw_per_thread(rows, V);
+    TopwParts t = carve_topw(ws_parts, rows, V, W, per);
+    cudaError_t e = launch_topw_partial<W, false>(z, rows, V, per, t, st);
+    if (e != cudaSuccess) return e;
+    const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
+    e = launch_kernel(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s, t.t,
+                      t.splits, rows, exp_table(), 0.0, t.tok, t.lp, t.lse);
+    if (e != cudaSuccess) return e;
+    e = tree_policy_launch(t.lp, nseq, N, W, accept_len, prm, budget_state, acc_ema, tree_off, w_cap, n_cap,
+                           err, st);
+    if (e != cudaSuccess) return e;
+    e = set_expand_smem<W>();
+    if (e != cudaSuccess) return e;
+    return launch_kernel(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, t.tok, t.lp,
+                         root_token, static_cast<const int32_t*>(tree_off), static_cast<const int32_t*>(w_cap),
+                         static_cast<const int32_t*>(n_cap), capacity, N, parent, token, depth, anc, err);
 }
 
 template <int W>
 static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_t* root_token,
-                              const int32_t* tree_off, int nseq, int total_nodes, int N, int32_t* parent,
-                              int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
-                              cudaStream_t st) {
+                              const int32_t* tree_off, const int32_t* w_cap, const int32_t* n_cap, int nseq,
+                              int total_nodes, int N, int32_t* parent, int32_t* token, int32_t* depth,
+                              uint32_t* anc, uint32_t* err, cudaStream_t st) {
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
     return launch_kernel(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, tok, lp,
-                      root_token, tree_off, total_nodes, N, parent, token, depth, anc, err);
+                         root_token, tree_off, w_cap, n_cap, total_nodes, N, parent, token, depth, anc, err);
 }
 
 #define JT_DISPATCH_W(W, CALL)           \
@@ -1048,11 +1189,21 @@ cudaError_t tree_build_launch(const float* z, const int32_t* root_token, const i
 }
 
 cudaError_t tree_expand_launch(const int32_t* tok, const double* lp, const int32_t* root_token,
-                               const int32_t* tree_off, int nseq, int total_nodes, int N, int W, int32_t* parent,
-                               int32_t* token, int32_t* depth, uint32_t* anc, uint32_t* err,
-                               cudaStream_t st) {
-    JT_DISPATCH_W(W, run_expand<kW>(tok, lp, root_token, tree_off, nseq, total_nodes, N, parent, token, depth,
-                                    anc, err, st));
+                               const int32_t* tree_off, const int32_t* w_cap, const int32_t* n_cap, int nseq,
+                               int total_nodes, int N, int W, int32_t* parent, int32_t* token, int32_t* depth,
+                               uint32_t* anc, uint32_t* err, cudaStream_t st) {
+    JT_DISPATCH_W(W, run_expand<kW>(tok, lp, root_token, tree_off, w_cap, n_cap, nseq, total_nodes, N, parent,
+                                    token, depth, anc, err, st));
+}
+
+cudaError_t tree_build_adaptive_launch(const float* z, const int32_t* root_token, int nseq, int capacity, int N,
+                                       int W, long long V, const int32_t* accept_len, const jt_policy_params& prm,
+                                       int32_t* budget_state, double* acc_ema, int32_t* tree_off, int32_t* w_cap,
+                                       int32_t* n_cap, int32_t* parent, int32_t* token, int32_t* depth,
+                                       uint32_t* anc, char* ws_parts, uint32_t* err, cudaStream_t st) {
+    JT_DISPATCH_W(W, run_build_adaptive<kW>(z, root_token, nseq, capacity, N, V, accept_len, prm, budget_state,
+                                            acc_ema, tree_off, w_cap, n_cap, parent, token, depth, anc, ws_parts,
+                                            err, st));
 }
 
 }  // namespace jt
