@@ -327,6 +327,10 @@ def main():
     ap.add_argument("--adaptive", action="store_true",
                     help="build through jt_tree_build_adaptive (top-W, policy, capped expansion), the "
                          "policy fed each step's greedy accept_len and holding every budget")
+    ap.add_argument("--serial", action="store_true",
+                    help="one stream: attention, then the acceptance rules (default: acceptance on side "
+                         "streams beside the attention)")
+    ap.add_argument("--attn-first", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if not 0.0 <= args.alpha <= 1.0:
         raise SystemExit("--alpha must lie in [0, 1]")
@@ -438,18 +442,47 @@ def main():
 
     stream = torch.cuda.current_stream()
     attn_ev = []
+    # The acceptance rules read the tree and the target logits, not the
+    # attention output: after the build they run on side streams beside the
+    # attention (joined before the step ends), unless --serial.
+    side = [torch.cuda.Stream(device=dev) for _ in range(3)]
 
-    def step(inp):
-        build(inp)
-        jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], offs(inp), anc,
-                              scale=wl.scale, max_tree=max_tree, out=out, lse=lse, ws=ws_a)
-        for i, rule in enumerate((jt.JT_RULE_GREEDY, jt.JT_RULE_MARGIN)):
-            jt.jt_verify_accept(inp["target"], parent, token, offs(inp), N, rule=rule, log_t=log_t,
+    def accepts(inp, i):
+        if i < 2:
+            jt.jt_verify_accept(inp["target"], parent, token, offs(inp), N,
+                                rule=(jt.JT_RULE_GREEDY, jt.JT_RULE_MARGIN)[i], log_t=log_t,
                                 out=(acc[i], path[i], bonus[i]), ws=ws_v[i])
-        if args.stochastic:
+        else:
             jt.jt_verify_accept_stochastic(inp["target"], inp["draft"], parent, token, offs(inp), N,
                                            inp["u_acc"], inp["u_bon"], out=(acc[2], path[2], bonus[2]),
                                            ws=ws_v[2])
+
+    n_acc = 3 if args.stochastic else 2
+
+    def attention(inp):
+        jt.jt_tree_attn_paged(inp["q"], inp["k"], inp["v"], inp["bt"], inp["plen"], offs(inp), anc,
+                              scale=wl.scale, max_tree=max_tree, out=out, lse=lse, ws=ws_a)
+
+    def step(inp):
+        build(inp)
+        if args.serial:
+            attention(inp)
+            for i in range(n_acc):
+                accepts(inp, i)
+            return
+        main = torch.cuda.current_stream()
+        built = torch.cuda.Event()
+        built.record(main)
+        if args.attn_first:
+            attention(inp)
+        for i in range(n_acc):
+            side[i].wait_event(built)
+            with torch.cuda.stream(side[i]):
+                accepts(inp, i)
+        if not args.attn_first:
+            attention(inp)
+        for i in range(n_acc):
+            main.wait_stream(side[i])
 
     flush = torch.empty(args.flush_mb * (1 << 20), dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -590,6 +623,8 @@ def main():
                        "prefix_len": [int(x) for x in wl.prefix_len[:4]] + (["..."] if nseq > 4 else []),
                        "Hq": Hq, "Hkv": Hkv, "head_dim": D, "N": N, "W": W, "V": c["V"],
                        "step": step_name(args),
+                       "schedule": ("one stream" if args.serial else
+                                    "acceptance on side streams beside the attention (after the build)"),
                        "l2": f"flushed before every step ({args.flush_mb} MiB write)",
                        "launch": "eager" if args.no_graph else "cuda_graph replay of the step",
                        "parallelism": f"replicas x{world}"},
