@@ -330,7 +330,6 @@ def main():
     ap.add_argument("--serial", action="store_true",
                     help="one stream: attention, then the acceptance rules (default: acceptance on side "
                          "streams beside the attention)")
-    ap.add_argument("--attn-first", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if not 0.0 <= args.alpha <= 1.0:
         raise SystemExit("--alpha must lie in [0, 1]")
@@ -470,17 +469,16 @@ def main():
             for i in range(n_acc):
                 accepts(inp, i)
             return
+        # acceptance first: its cluster kernels then find free SMs before the
+        # attention fills the GPU (the other order measured 83.7 vs 80.6 us)
         main = torch.cuda.current_stream()
         built = torch.cuda.Event()
         built.record(main)
-        if args.attn_first:
-            attention(inp)
         for i in range(n_acc):
             side[i].wait_event(built)
             with torch.cuda.stream(side[i]):
                 accepts(inp, i)
-        if not args.attn_first:
-            attention(inp)
+        attention(inp)
         for i in range(n_acc):
             main.wait_stream(side[i])
 
