@@ -605,7 +605,8 @@ def main():
         e2e_s = (time.perf_counter() - t0) / args.e2e_steps
         e2e_s = max_over_ranks([e2e_s], dev, world)[0]
         e2e = {"value": whole_job_rate(total, e2e_s, world), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps}
+               "d2h_bytes_per_step": int(d2h), "steps": args.e2e_steps,
+               "h2d_gbs": h2d / e2e_s / 1e9}
 
     # ---- roofline of the dominant kernel (the attention call)
     peaks, peak_src = load_peaks()
