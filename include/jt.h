@@ -395,6 +395,19 @@ jt_status jt_verify_accept_stochastic(const float* target_logits, const float* d
  */
 jt_status jt_check(void* ws, jt_stream_t stream);
 
+/*
+ * jt_selftest_wait_timeout -- diagnostic of the device-side failure path
+ * (no counterpart in the pages).  Launches one 32-thread CTA that waits,
+ * with the same bounded wait every kernel of the library uses, for an
+ * mbarrier phase that nothing completes.  After the library's wait limit
+ * (2 s) the wait gives up, raises the timeout flag in the workspace's error
+ * word and the kernel exits normally: the next jt_check(ws, stream) returns
+ * JT_ERR_TIMEOUT and the CUDA context stays usable.  No fault, trap or
+ * unbounded wait is involved.
+ *   ws: a workspace of at least 256 bytes (only its error word is used).
+ */
+jt_status jt_selftest_wait_timeout(void* ws, size_t ws_bytes, jt_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* jt_status_str(jt_status status);
 

@@ -29,7 +29,7 @@ JT_MAX_TREE, JT_MAX_W, JT_MAX_N, JT_PAGE_SIZE = 256, 8, 64, 16
 EXPORTS = ("jt_workspace_size", "jt_tree_build", "jt_tree_topw", "jt_tree_expand",
            "jt_tree_attn_paged", "jt_verify_accept", "jt_check", "jt_status_str", "jt_version",
            "jt_tree_build_noalloc", "jt_verify_accept_stochastic", "jt_tree_build_mixed",
-           "jt_tree_expand_capped", "jt_tree_policy", "jt_tree_build_adaptive")
+           "jt_tree_expand_capped", "jt_tree_policy", "jt_tree_build_adaptive", "jt_selftest_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -97,13 +97,14 @@ def load(build_if_missing: bool = True):
         lib.jt_verify_accept_stochastic.argtypes = [P, P, P, P, P, i32, i32, i64, i32, P, P, P, P, P,
                                                     P, sz, P]
         lib.jt_check.argtypes = [P, P]
+        lib.jt_selftest_wait_timeout.argtypes = [P, sz, P]
         lib.jt_status_str.argtypes = [i32]
         lib.jt_status_str.restype = ctypes.c_char_p
         lib.jt_version.argtypes = []
         for name in ("jt_tree_build", "jt_tree_topw", "jt_tree_expand", "jt_tree_attn_paged",
                      "jt_verify_accept", "jt_check", "jt_version", "jt_tree_build_noalloc",
                      "jt_verify_accept_stochastic", "jt_tree_build_mixed", "jt_tree_expand_capped",
-                     "jt_tree_policy", "jt_tree_build_adaptive"):
+                     "jt_tree_policy", "jt_tree_build_adaptive", "jt_selftest_wait_timeout"):
             getattr(lib, name).restype = i32
         _lib = lib
         return lib
@@ -481,3 +482,13 @@ def jt_verify_accept(target_logits, parent, token, tree_off, N, rule=JT_RULE_GRE
                               _ptr(ws), ws.numel(), _stream(stream))
     _check(rc, "jt_verify_accept")
     return acc, path, bonus
+
+
+def jt_selftest_wait_timeout(ws=None, stream=None):
+    """Run the bounded-wait timeout diagnostic; returns the workspace whose
+    error word it sets (read it with jt_check: JT_ERR_TIMEOUT)."""
+    lib = load()
+    if ws is None:
+        ws = workspace(256)
+    _check(lib.jt_selftest_wait_timeout(_ptr(ws), ws.numel(), _stream(stream)), "jt_selftest_wait_timeout")
+    return ws

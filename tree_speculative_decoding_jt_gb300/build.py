@@ -17,7 +17,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libjt.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["jt_api.cu", "tree_build.cu", "verify_accept.cu", "tree_attn.cu", "tree_attn_f32.cu", "jt_noalloc.cu", "verify_stochastic.cu"]
+SOURCES = ["jt_api.cu", "tree_build.cu", "verify_accept.cu", "tree_attn.cu", "tree_attn_f32.cu", "jt_noalloc.cu", "verify_stochastic.cu", "jt_selftest.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]

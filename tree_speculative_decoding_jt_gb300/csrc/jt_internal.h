@@ -82,6 +82,9 @@ cudaError_t tree_attn_f32_launch(const float* q, const float* k_cache, const flo
                                  int D, float scale, float* out, float* lse, uint32_t* err,
                                  cudaStream_t st);
 
+// jt_selftest.cu
+cudaError_t selftest_wait_timeout_launch(uint32_t* err, cudaStream_t st);
+
 int device_sm_count();
 
 }  // namespace jt
