@@ -88,10 +88,12 @@ def test_random_trees_match_oracle(rule, deep, V):
         _compare(z, parent, token, off, N, rule, math.log(t))
 
 
-@pytest.mark.parametrize("cfg", [1, 5])
+@pytest.mark.parametrize("cfg", [1, 2, 4, 5])
 @pytest.mark.parametrize("deep", [False, True])
 def test_config_trees_match_oracle(cfg, deep):
-    wl = wk.make(cfg)
+    """Full-size verify steps (config 4: 32 trees, 1.24 GB of target
+    logits), greedy and margin, against the oracle on every sequence."""
+    wl = wk.make(cfg, with_kv=False)
     tree = oracle_tree(wl)
     z = wk.target_logits(wl, tree["parent"], tree["token"], deep=deep)
     N = wl.cfg["N"]

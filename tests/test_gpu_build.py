@@ -82,7 +82,7 @@ def _build_and_compare(wl):
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
 def test_build_bit_exact_full_configs(cfg):
-    wl = wk.make(cfg, with_draft=True)
+    wl = wk.make(cfg, with_draft=True, with_kv=False)
     _build_and_compare(wl)
 
 

@@ -45,7 +45,7 @@ def _compare(z, root, off, W, alpha):
 
 @pytest.mark.parametrize("cfg,alpha", [(1, 0.3), (3, 0.5), (5, 0.2), (5, 0.7)])
 def test_mixed_bit_exact_full_configs(cfg, alpha):
-    wl = wk.make(cfg, with_draft=True)
+    wl = wk.make(cfg, with_draft=True, with_kv=False)
     _compare(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"], alpha)
 
 
@@ -83,7 +83,7 @@ def test_mixed_reorders_the_tree():
 
 
 def test_alpha_zero_equals_plain_build():
-    wl = wk.make(5, with_draft=True)
+    wl = wk.make(5, with_draft=True, with_kv=False)
     got = _got(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"], 0.0, wl.total)
     out = jt.jt_tree_build(dev(wl.draft_logits), dev(wl.root_token), dev(wl.tree_off), wl.cfg["W"],
                            total_nodes=wl.total)
@@ -107,7 +107,7 @@ def test_one_hot_rows_have_zero_entropy():
 
 @pytest.mark.parametrize("cfg", [1, 5])
 def test_pure_entropy_full_configs(cfg):
-    wl = wk.make(cfg, with_draft=True)
+    wl = wk.make(cfg, with_draft=True, with_kv=False)
     _compare(wl.draft_logits, wl.root_token, wl.tree_off, wl.cfg["W"], 1.0)
 
 

@@ -88,14 +88,16 @@ def _normal(rng, shape, std):
 
 
 def make(cfg_id=None, seed=None, *, overrides=None, poison=False, n_guard=2,
-         with_draft=True) -> Workload:
+         with_draft=True, with_kv=True) -> Workload:
     """Draw one workload.
 
     cfg_id: 1..5 picks a preset from CONFIGS; overrides replaces any preset
     field (e.g. smaller V or prefix for oracle-sized parity cases).  seed
     defaults to 1000 + cfg_id.  poison=True fills spare pool pages and the
     unused tail of every sequence's last page with NaN, so any read outside
-    the block table or past the tree shows up in the output.
+    the block table or past the tree shows up in the output.  with_kv=False
+    skips drawing q, K and V (they come last from the generator, so every
+    other field is unchanged) for cases that only need the draft side.
     """
     cfg = dict(CONFIGS[cfg_id]) if cfg_id is not None else {}
     if overrides:
@@ -140,6 +142,10 @@ def make(cfg_id=None, seed=None, *, overrides=None, poison=False, n_guard=2,
     draft = _normal(rng, (nseq, N, V), DRAFT_STD) if with_draft else None
     root_token = rng.integers(0, V, size=nseq).astype(np.int32)
 
+    if not with_kv:
+        return Workload(cfg=cfg, seed=seed, draft_logits=draft, root_token=root_token,
+                        tree_off=tree_off, prefix_len=prefix_len, block_table=block_table,
+                        k_cache=None, v_cache=None, q=None, scale=1.0 / math.sqrt(D), guard_pages=guard)
     std = cfg["qkv_std"]
     total = int(tree_off[-1])
     kf = _normal(rng, (n_pages, page, Hkv, D), std)
