@@ -35,8 +35,10 @@ def test_topw_lse_matches_oracle(V, W, rows):
     np.testing.assert_array_equal(tok.cpu().numpy(), otok)
     d = np.abs(lse.cpu().numpy() - olse)
     assert d.max() <= 1e-9, d
-    dl = np.abs(lp.cpu().numpy() - olp)
-    dl[np.isinf(olp)] = 0
+    got_lp = lp.cpu().numpy()
+    fin = np.isfinite(olp)
+    np.testing.assert_array_equal(np.isfinite(got_lp), fin)  # -inf (probability 0) on the same entries
+    dl = np.abs(got_lp[fin] - olp[fin])
     assert dl.max() <= 1e-9
 
 
