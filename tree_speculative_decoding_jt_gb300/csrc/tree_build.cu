@@ -574,9 +574,11 @@ __global__ void __launch_bounds__(256)
 // Step 2: best-first expansion, one CTA per sequence.
 //
 // The nodes best-first pops, in pop order, are exactly the B-1 best non-root
-// nodes of the full depth-N tree under the queue key, in key order: a child
-// never beats its parent (log-probs are <= 0, and depth breaks exact ties in
-// the parent's favour) and a later sibling never beats an earlier one.  So
+// nodes of the full depth-N tree (or of the tree cut at depth n_cap and
+// width w_cap) under the queue key, in key order: a child never beats its
+// parent (step scores -- log-probs, or the entropy-mixed scores -- are <= 0,
+// and depth breaks exact ties in the parent's favour) and a later sibling
+// never beats an earlier one (each table row is in queue-key order).  So
 // instead of B-1 dependent pops the CTA builds that set level by level.  S
 // holds the best candidates seen so far, sorted by key and cut to B-1.  At
 // level d every depth-d entry of S generates its children (depth d+1) that
