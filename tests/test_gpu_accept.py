@@ -111,3 +111,22 @@ def test_invalid_tree_is_flagged():
                         dev(np.array([0, 3], np.int32)), 2, ws=ws)
     with pytest.raises(jt.JtError):
         jt.jt_check(ws)
+
+
+def test_deepest_paths_at_maximum_depth():
+    """Chains of 64 drafted nodes whose target rows all pick the drafted
+    token: both rules accept the whole chain (accept_len 64, path of 65)."""
+    N, V, nseq = 64, 300, 3
+    rng = np.random.default_rng(64)
+    token = rng.integers(0, V, size=(nseq, N + 1)).astype(np.int32).reshape(-1)
+    parent = np.tile(np.arange(-1, N, dtype=np.int32), nseq)
+    off = (np.arange(nseq + 1) * (N + 1)).astype(np.int32)
+    z = rng.standard_normal((nseq * (N + 1), V)).astype(np.float32)
+    for b in range(nseq):
+        for c in range(1, N + 1):
+            row = off[b] + c - 1
+            z[row, token[off[b] + c]] = z[row].max() + 2.0
+    for rule in (0, 1):
+        acc, path, _ = _compare(z, parent, token, off, N, rule, math.log(0.8))
+        assert np.all(acc == N)
+        np.testing.assert_array_equal(path[:, -1], N)

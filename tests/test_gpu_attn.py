@@ -72,6 +72,16 @@ def test_bf16_matches_oracle_all_nodes(case):
     _check_bf16(*_run(wl, tree))
 
 
+def test_bf16_deep_tree_long_ancestor_chains():
+    """A tree about 64 deep (peaked draft rows: the top-1 log-prob near 0),
+    so nodes see up to 65 tree keys through their ancestor sets."""
+    wl = _small(21, 2, 32, 8, 128, [333, 64], (256, 200), N=64, W=2)
+    wl.draft_logits[:] *= np.float32(40.0 / np.sqrt(2))
+    tree = oracle_tree(wl)
+    assert tree["depth"].max() >= 48
+    _check_bf16(*_run(wl, tree))
+
+
 def test_bf16_peaky_scores():
     """Q scaled by 8: softmax far from uniform, exercises the rescaling."""
     wl = _small(11, 2, 32, 8, 128, [700, 40], (96, 200), q_mult=8.0)

@@ -80,6 +80,7 @@ def _build_and_compare(wl):
     np.testing.assert_array_equal(tk, want["token"])
     np.testing.assert_array_equal(dp, want["depth"])
     np.testing.assert_array_equal(anc.view(np.uint32), want["anc"])
+    return want
 
 
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4, 5])
@@ -119,3 +120,18 @@ def test_build_host_side_argument_errors():
     with pytest.raises(jt.JtError) as e:
         jt.jt_tree_build(z, dev(np.array([1], np.int32)), off, 2, total_nodes=3, ws=jt.workspace(256))
     assert e.value.status == -5  # workspace too small
+
+
+@pytest.mark.parametrize("N,W,budget,scale,depth", [(64, 1, 65, 1.4, 64), (64, 2, 256, 40.0, 64),
+                                                    (64, 8, 256, 40.0, 60), (64, 8, 256, 0.05, 2)])
+def test_build_bit_exact_maximum_depth_and_width(N, W, budget, scale, depth):
+    """The build's limits: depth 64, width 8, budget 256.  Peaked rows (a
+    large logit scale: the top-1 log-prob near 0) give trees about 64 deep;
+    near-uniform rows give wide, shallow ones; W = 1 is the full chain of
+    64 drafted nodes.  `depth`: the least deepest node the case reaches."""
+    o = dict(dtype="f32", nseq=2, Hq=4, Hkv=1, D=64, prefix=("fixed", 0), budgets=(budget,), N=N, W=W,
+             V=700, qkv_std=1.0)
+    wl = wk.make(1, seed=N + W, overrides=o, with_kv=False)
+    wl.draft_logits[:] *= np.float32(scale / np.sqrt(2))
+    want = _build_and_compare(wl)
+    assert want["depth"].max() >= depth
