@@ -248,6 +248,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     Bars* bars = reinterpret_cast<Bars*>(smem + SL::kBar);
 
+    pdl_wait();  // nothing is read before the previous kernel's writes are visible
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, g = blockIdx.y;
     const int mp = blockIdx.x / p.splits, sp = blockIdx.x % p.splits;
@@ -477,7 +478,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_before();
             mbar_arrive(&bars->p_full[x]);
         }
-        // epilogue
+        // epilogue (the split combine may be scheduled; it waits for this grid)
+        pdl_trigger();
         if (ok && mbar_wait_warp(&bars->o_final[x], 0, p.err, abort)) {
             tc_fence_after();
             const long long rowid = static_cast<long long>(off + node) * p.Hq + head;
@@ -529,6 +531,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 template <int D>
 __global__ void __launch_bounds__(128)
     tree_attn_combine_kernel(const AttnParams p, int total_nodes) {
+    pdl_wait();  // the partials are complete and visible
     const int lane = threadIdx.x & 31;
     const int n = blockIdx.x;
     const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
@@ -698,11 +701,11 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
         attr_done = true;
     }
     dim3 grid(((plan.mtiles + 1) / 2) * plan.splits, Hkv, nseq);
-    cudaError_t e = launch_kernel(tree_attn_tc_kernel<D>, grid, dim3(kAttnThreads), SL::kAlloc, st, 0, tq,
-                               tk, tv, prm);
+    cudaError_t e = launch_kernel_pdl(tree_attn_tc_kernel<D>, grid, dim3(kAttnThreads), SL::kAlloc, st, tq, tk,
+                                      tv, prm);
     if (e != cudaSuccess || plan.splits == 1) return e;
     dim3 cgrid(total_nodes, (Hq + 3) / 4);
-    return launch_kernel(tree_attn_combine_kernel<D>, cgrid, dim3(128), 0, st, 0, prm, total_nodes);
+    return launch_kernel_pdl(tree_attn_combine_kernel<D>, cgrid, dim3(128), 0, st, prm, total_nodes);
 }
 
 cudaError_t tree_attn_bf16_launch(const void* q, const void* k_cache, const void* v_cache,

@@ -283,6 +283,7 @@ __global__ void __launch_bounds__(kTopwThreads)
             }
         }
     }
+    pdl_trigger();  // the row merge may be scheduled; it waits for this grid's writes
     const ffloat Sw = warp_sum_ff(ff_norm(acc_hi, acc_lo));
     ffloat Tw;
     Tw.hi = Tw.lo = 0.0f;
@@ -530,6 +531,8 @@ __global__ void __launch_bounds__(256)
         s_tlo[threadIdx.x] = tab.lo[threadIdx.x];
     }
     __syncthreads();
+    pdl_wait();     // the partials are complete and visible
+    pdl_trigger();  // the expansion may be scheduled (it waits for this grid)
     const long long row = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -707,6 +710,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     __shared__ int s_cnt[kSetWarps][W];
     __shared__ int s_L[W];
 
+    pdl_wait();     // the tables are complete and visible
+    pdl_trigger();  // the next kernel may be scheduled (it waits for this grid)
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
     const int off = tree_off[b];
@@ -1079,8 +1084,8 @@ static cudaError_t run_topw(const float* z, long long rows, long long V, int32_t
     if (e != cudaSuccess) return e;
     const long long warps_per_block = 8;
     const unsigned blocks = static_cast<unsigned>((rows + warps_per_block - 1) / warps_per_block);
-    return launch_kernel(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m,
-                         t.s, t.t, t.splits, rows, exp_table(), 0.0, tok, lp, lse);
+    return launch_kernel_pdl(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, t.v, t.id, t.m, t.s,
+                             t.t, t.splits, rows, exp_table(), 0.0, tok, lp, lse);
 }
 
 // alpha > 0: entropy-mixed step scores (1 - alpha) * lp - alpha * H(row);
@@ -1099,17 +1104,17 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
                             : launch_topw_partial<W, false>(z, rows, V, per, t, st);
         if (e != cudaSuccess) return e;
         const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-        e = ent ? launch_kernel(topw_merge_kernel<W, true>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id,
-                                t.m, t.s, t.t, t.splits, rows, exp_table(), alpha, t.tok, t.lp, t.lse)
-                : launch_kernel(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id,
-                                t.m, t.s, t.t, t.splits, rows, exp_table(), 0.0, t.tok, t.lp, t.lse);
+        e = ent ? launch_kernel_pdl(topw_merge_kernel<W, true>, dim3(blocks), dim3(256), 0, st, t.v, t.id, t.m,
+                                    t.s, t.t, t.splits, rows, exp_table(), alpha, t.tok, t.lp, t.lse)
+                : launch_kernel_pdl(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, t.v, t.id, t.m,
+                                    t.s, t.t, t.splits, rows, exp_table(), 0.0, t.tok, t.lp, t.lse);
         if (e != cudaSuccess) return e;
     }
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    return launch_kernel(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, t.tok, t.lp,
-                         root_token, tree_off, static_cast<const int32_t*>(nullptr),
-                         static_cast<const int32_t*>(nullptr), total_nodes, N, parent, token, depth, anc, err);
+    return launch_kernel_pdl(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, t.tok, t.lp,
+                             root_token, tree_off, static_cast<const int32_t*>(nullptr),
+                             static_cast<const int32_t*>(nullptr), total_nodes, N, parent, token, depth, anc, err);
 }
 
 static int policy_ceiling(const jt_policy_params& prm, int nseq) {
@@ -1140,8 +1145,8 @@ static cudaError_t run_build_adaptive(const float* z, const int32_t* root_token,
     cudaError_t e = launch_topw_partial<W, false>(z, rows, V, per, t, st);
     if (e != cudaSuccess) return e;
     const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-    e = launch_kernel(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, 0, t.v, t.id, t.m, t.s, t.t,
-                      t.splits, rows, exp_table(), 0.0, t.tok, t.lp, t.lse);
+    e = launch_kernel_pdl(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, t.v, t.id, t.m, t.s,
+                          t.t, t.splits, rows, exp_table(), 0.0, t.tok, t.lp, t.lse);
     if (e != cudaSuccess) return e;
     e = tree_policy_launch(t.lp, nseq, N, W, accept_len, prm, budget_state, acc_ema, tree_off, w_cap, n_cap,
                            err, st);
@@ -1160,8 +1165,8 @@ static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_
                               uint32_t* anc, uint32_t* err, cudaStream_t st) {
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    return launch_kernel(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, tok, lp,
-                         root_token, tree_off, w_cap, n_cap, total_nodes, N, parent, token, depth, anc, err);
+    return launch_kernel_pdl(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, tok, lp,
+                             root_token, tree_off, w_cap, n_cap, total_nodes, N, parent, token, depth, anc, err);
 }
 
 #define JT_DISPATCH_W(W, CALL)           \
