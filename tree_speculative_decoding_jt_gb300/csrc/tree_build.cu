@@ -714,18 +714,20 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     pdl_trigger();  // the next kernel may be scheduled (it waits for this grid)
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
+    // The table loads do not depend on the offsets: issue both together.
+    for (int i = tid; i < N * W; i += kExpandThreads) {
+        s_tok[i] = tok_in[static_cast<long long>(b) * N * W + i];
+        s_lp[i] = lp_in[static_cast<long long>(b) * N * W + i];
+    }
     const int off = tree_off[b];
     const int B = tree_off[b + 1] - off;
     const int Wb = w_cap ? w_cap[b] : W;
     const int Nb = n_cap ? n_cap[b] : N;
+    // Uniform over the block: every thread returns or none does.
     if (Wb < 1 || Wb > W || Nb < 0 || Nb > N || B < 1 || B > JT_MAX_TREE ||
         B > full_tree_nodes(Nb, Wb, JT_MAX_TREE + 1) || off < 0 || off + B > total_nodes) {
         if (tid == 0) raise_error(err, DEVERR_INVALID);
         return;
-    }
-    for (int i = tid; i < N * W; i += kExpandThreads) {
-        s_tok[i] = tok_in[static_cast<long long>(b) * N * W + i];
-        s_lp[i] = lp_in[static_cast<long long>(b) * N * W + i];
     }
     __syncthreads();
 
