@@ -484,30 +484,63 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             tc_fence_after();
             const long long rowid = static_cast<long long>(off + node) * p.Hq + head;
             const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+            // Every QK_X MMA completed before o_final[X], so the Q_X tile is
+            // free: each warp stages its 32 rows there, one 128-byte piece
+            // of each row at a time (16-byte slots XOR-swizzled by row, so
+            // both the row-wise writes and the line-wise reads are free of
+            // bank conflicts), and 8 lanes then store each row's piece as
+            // one full 128-byte line.
+            uint8_t* stage = sQ + x * kTileBytes + (warp & 3) * 4096;
+            const int sub = lane & 7;  // 16-byte slot of the piece
+            const bool piece_f32 = p.splits > 1;
+            constexpr int kPiecesF32 = D / 32, kPiecesBf16 = D / 64;
+            const int pieces = piece_f32 ? kPiecesF32 : kPiecesBf16;
 #pragma unroll 1
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t v[32];
-                tmem_ld32(tO + q * 32, v);
-                tmem_wait_ld();
-                if (valid_row) {
-                    if (p.splits == 1) {
-                        uint4* dst = reinterpret_cast<uint4*>(p.out + rowid * D + q * 32);
+            for (int h = 0; h < pieces; ++h) {
+                uint4 slot[8];
+                if (piece_f32) {
+                    uint32_t v[32];
+                    tmem_ld32(tO + h * 32, v);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            dst[c] = make_uint4(
-                                pack_bf16x2(__uint_as_float(v[8 * c + 0]) * inv, __uint_as_float(v[8 * c + 1]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * c + 2]) * inv, __uint_as_float(v[8 * c + 3]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * c + 4]) * inv, __uint_as_float(v[8 * c + 5]) * inv),
-                                pack_bf16x2(__uint_as_float(v[8 * c + 6]) * inv, __uint_as_float(v[8 * c + 7]) * inv));
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(
-                            p.part_o + (rowid * p.splits + sp) * D + q * 32);
+                    for (int c = 0; c < 8; ++c) slot[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                } else {
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tO + h * 64, v0);
+                    tmem_ld32(tO + h * 64 + 32, v1);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            dst[c] = make_float4(__uint_as_float(v[4 * c]), __uint_as_float(v[4 * c + 1]),
-                                                 __uint_as_float(v[4 * c + 2]), __uint_as_float(v[4 * c + 3]));
+                    for (int c = 0; c < 4; ++c) {
+                        slot[c] = make_uint4(
+                            pack_bf16x2(__uint_as_float(v0[8 * c + 0]) * inv, __uint_as_float(v0[8 * c + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(v0[8 * c + 2]) * inv, __uint_as_float(v0[8 * c + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(v0[8 * c + 4]) * inv, __uint_as_float(v0[8 * c + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(v0[8 * c + 6]) * inv, __uint_as_float(v0[8 * c + 7]) * inv));
+                        slot[4 + c] = make_uint4(
+                            pack_bf16x2(__uint_as_float(v1[8 * c + 0]) * inv, __uint_as_float(v1[8 * c + 1]) * inv),
+                            pack_bf16x2(__uint_as_float(v1[8 * c + 2]) * inv, __uint_as_float(v1[8 * c + 3]) * inv),
+                            pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * inv, __uint_as_float(v1[8 * c + 5]) * inv),
+                            pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * inv, __uint_as_float(v1[8 * c + 7]) * inv));
                     }
                 }
+                uint4* my_row = reinterpret_cast<uint4*>(stage + lane * 128);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) my_row[c ^ (lane & 7)] = slot[c];
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rr = 4 * i + (lane >> 3);  // staged row this lane copies
+                    const long long rid = __shfl_sync(0xFFFFFFFFu, rowid, rr);
+                    const bool rvalid = __shfl_sync(0xFFFFFFFFu, valid_row, rr);
+                    const uint4 val = reinterpret_cast<const uint4*>(stage + rr * 128)[sub ^ (rr & 7)];
+                    if (rvalid) {
+                        if (piece_f32)
+                            reinterpret_cast<uint4*>(p.part_o + (rid * p.splits + sp) * D + h * 32)[sub] = val;
+                        else
+                            reinterpret_cast<uint4*>(p.out + rid * D + h * 64)[sub] = val;
+                    }
+                }
+                __syncwarp();  // the next piece overwrites the stage
             }
             if (valid_row) {
                 if (p.splits == 1) {
