@@ -64,6 +64,7 @@ def _small(seed, nseq, Hq, Hkv, D, prefix, budgets, N=6, W=3, dtype="bf16", q_mu
     (10, 1, 32, 8, 128, [1500], (100,)),           # 6 KV splits, the last one empty
     (11, 1, 32, 8, 64, [900], (37,)),              # 4 KV splits, D = 64
     (12, 1, 32, 8, 128, [700], (20,)),             # 3 KV splits, one query tile
+    (13, 1, 32, 8, 128, [7000], (30,)),            # 19 KV splits: three combine batches
 ])
 def test_bf16_matches_oracle_all_nodes(case):
     seed, nseq, Hq, Hkv, D, prefix, budgets = case
