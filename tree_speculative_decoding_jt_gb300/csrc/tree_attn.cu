@@ -248,27 +248,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     Bars* bars = reinterpret_cast<Bars*>(smem + SL::kBar);
 
-    pdl_wait();  // nothing is read before the previous kernel's writes are visible
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, g = blockIdx.y;
     const int mp = blockIdx.x / p.splits, sp = blockIdx.x % p.splits;
-    const int off = p.tree_off[b];
-    const int B = p.tree_off[b + 1] - off;
-    const int L = p.prefix_len[b];
-    const int m0 = 2 * mp;                    // query tile A; tile B = m0 + 1
-    if (m0 * p.npt >= B) return;              // pair past this sequence's tree
-    if (B > JT_MAX_TREE || L < 0 || off < 0 || off + B > p.total_nodes ||
-        static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE) {
-        if (tid == 0) raise_error(p.err, DEVERR_INVALID);
-        return;
-    }
-    const bool hasB = (m0 + 1) * p.npt < B;
-    const int n_end = min(B, (m0 + 2) * p.npt);
-    const int valid_end = L + n_end;
-    int t0;
-    const int nt = split_range(valid_end, p.splits, sp, t0);
-    if (nt == 0) return;  // empty split (the combine skips it too)
-
+    // Set-up that reads no global memory (barriers, TMEM, tensor-map
+    // prefetch) runs before the wait for the previous kernel, overlapping
+    // its tail when this grid is launched as its programmatic dependent.
     if (tid == 0) {
         mbar_init(&bars->q_full, 1);
         for (int s = 0; s < kStages; ++s) {
@@ -287,12 +272,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         bars->abort = 0;
         fence_mbar_init();
     }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
     if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     volatile int* abort = &bars->abort;
+
+    pdl_wait();  // no global memory is read before the previous kernel's writes are visible
+    const int off = p.tree_off[b];
+    const int B = p.tree_off[b + 1] - off;
+    const int L = p.prefix_len[b];
+    const int m0 = 2 * mp;                    // query tile A; tile B = m0 + 1
+    bool run = m0 * p.npt < B;                // else the pair lies past this sequence's tree
+    if (run && (B > JT_MAX_TREE || L < 0 || off < 0 || off + B > p.total_nodes ||
+                static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE)) {
+        if (tid == 0) raise_error(p.err, DEVERR_INVALID);
+        run = false;
+    }
+    const bool hasB = (m0 + 1) * p.npt < B;
+    const int n_end = min(B, (m0 + 2) * p.npt);
+    const int valid_end = L + n_end;
+    int t0 = 0;
+    const int nt = run ? split_range(valid_end, p.splits, sp, t0) : 0;
+    if (nt == 0) {  // nothing to do (or an empty split, which the combine skips too)
+        if (warp == 9) tmem_dealloc(tmem, 512);  // no tcgen05 operation was issued
+        return;
+    }
 
     uint8_t* sQ = smem + SL::kQ;
     uint8_t* sK = smem + SL::kK;
@@ -301,9 +312,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 8) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
             mbar_arrive_expect_tx(&bars->q_full, (hasB ? 2 : 1) * kTileBytes);
             for (int x = 0; x < (hasB ? 2 : 1); ++x)
                 for (int c = 0; c < SL::kChunks; ++c)
