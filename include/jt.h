@@ -10,6 +10,10 @@
  *    scratch array behind jt_tree_build_noalloc).
  *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream).  Outputs are valid once the stream reaches the call.
+ *    Some kernels are launched as programmatic dependents of the kernel
+ *    before them on the stream (they may become resident early); each one
+ *    waits for that kernel to finish before it reads or writes global
+ *    memory, so ordinary stream order holds whatever ran before.
  *  - Arguments checkable on the host (null pointers, sizes, limits, the
  *    workspace size) are checked before anything is enqueued; on failure the
  *    call returns JT_ERR_INVALID / JT_ERR_UNSUPPORTED / JT_ERR_WORKSPACE and
