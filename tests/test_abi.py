@@ -4,7 +4,6 @@ import ctypes
 import re
 import os
 
-import pytest
 
 import tree_speculative_decoding_jt_gb300 as jt
 from tree_speculative_decoding_jt_gb300 import binding

@@ -4,7 +4,6 @@ bf16 in, fp32 accumulate: max abs error <= 2e-2 and mean abs error <= 2e-3
 against the fp64 oracle (the task's stated tolerance); lse within 2e-2.
 fp32 inputs (CUDA-core path): max abs <= 1e-4.  Trees come from the oracle's
 build; every input from the seeded generators."""
-import math
 
 import numpy as np
 import pytest
