@@ -6,9 +6,16 @@ jt_tree_attn_paged (tree-causal attention over the paged bf16 KV cache, fed
 by the build's ancestor sets), then jt_verify_accept with the greedy rule
 and with the margin rule (t = 0.8).  Metric: tree-node tokens per second.
 
-Default workload: a Qwen3-8B-shaped attention layer (32 query / 8 KV heads,
-head dim 128, bf16), batch 1, prefix 4096, tree budget 256 (N=16, W=4),
-vocab 151936; pages randomly permuted in the pool.
+Default workload (--config 4): the KV-bandwidth-bound high-load case of a
+Qwen3-8B-shaped attention layer (32 query / 8 KV heads, head dim 128, bf16):
+32 sequences of prefix 32768, tree budget 64 (N=8, W=4), vocab 151936, pages
+randomly permuted in the pool (4.3 GB of K/V, far larger than L2).  The
+other workloads (--config 2: batch 1, prefix 4096, budget 256; 3: a ragged
+serving batch; 5: the full verify step of 8 sequences) run with --config.
+
+`value` is the whole verify step's rate (tree-node tokens per second of the
+step: build + attention + both acceptance rules); the attention call's own
+rate is `roofline.attn_tokens_per_s`.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl reference]
 
@@ -95,60 +102,97 @@ def attn_algorithmic(wl, depth):
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples while the timed region runs."""
+    """nvidia-smi clock/throttle samples around the timed region.
+
+    start() launches `nvidia-smi -lms PERIOD` and returns once its first
+    sample has arrived (so sampling is live before the region starts);
+    mark_start()/mark_end() bracket the timed region; stop() waits for one
+    more sample after the region, then ends the process and joins the
+    reader.  summary() reports the samples that fall inside the region,
+    widened by one period on each side (a region shorter than a period still
+    gets its nearest samples under load), beside the total count."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 100
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.thread = None
+        self.lines = []   # (host time, csv line)
+        self.t_start = self.t_end = None
 
-    def __enter__(self):
+    def start(self, wait_s=10.0):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
         except (FileNotFoundError, OSError):
             self.proc = None
+            return self
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        t0 = time.monotonic()
+        while not self.lines and time.monotonic() - t0 < wait_s and self.proc.poll() is None:
+            time.sleep(0.01)
         return self
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.monotonic(), line.strip()))
 
-    def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+    def mark_start(self):
+        self.t_start = time.monotonic()
+
+    def mark_end(self):
+        self.t_end = time.monotonic()
+
+    def stop(self, wait_s=3.0):
+        if self.proc is None:
+            return
+        t0 = time.monotonic()
+        end = self.t_end if self.t_end is not None else t0
+        while (not self.lines or self.lines[-1][0] <= end) and time.monotonic() - t0 < wait_s \
+                and self.proc.poll() is None:
+            time.sleep(0.01)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
+        pad = self.PERIOD_MS / 1000.0
+        t0 = (self.t_start or 0.0) - pad
+        t1 = (self.t_end or float("inf")) + pad
+        sm, mx, reasons, n_all = [], [], set(), 0
+        for t, line in self.lines:
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
+                a, b = float(f[1]), float(f[2])
             except ValueError:
                 continue
+            n_all += 1
+            if not t0 <= t <= t1:
+                continue
+            sm.append(a)
+            mx.append(b)
             for name, val in zip(names, f[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
+        out = {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+               "reasons": sorted(reasons), "samples": len(sm), "samples_total": n_all,
+               "window": f"timed region +/- {self.PERIOD_MS} ms (nvidia-smi -lms {self.PERIOD_MS})"}
         if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+            out["note"] = "no sample fell in the window"
+        return out
 
 
 def source_hash(paths):
@@ -158,17 +202,21 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_file):
-    """DRAM bytes per attention call from the committed ncu summary, or None
-    when absent or taken on a different version of the kernel source."""
+def profiled_traffic(kernel_file, workload):
+    """DRAM bytes of one main attention-kernel launch on `workload` from the
+    committed ncu summaries (profiles/traffic.json, one entry per workload),
+    or None when there is no capture for this workload or it was taken on a
+    different version of the kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     try:
         d = json.load(open(p))
-        if d.get("source_hash") != source_hash([kernel_file]):
-            return None
-        return d.get("attn_dram_bytes_per_call")
+        h = source_hash([kernel_file])
+        for e in d.get("entries", []):
+            if e.get("workload") == workload and e.get("source_hash") == h:
+                return e.get("dram_bytes_per_launch")
+        return None
     except (ValueError, OSError):
         return None
 
@@ -230,13 +278,15 @@ def host_cores():
         return os.cpu_count() or 1
 
 
-def cpu_oracle_sample(wl, attn_nodes, alpha, uniforms, adaptive, threads=1):
+def cpu_oracle_sample(wl, attn_k, alpha, uniforms, adaptive, threads=1, target_s=6.0):
     """The oracle, as it stands, on a bounded sample: the whole build and the
-    acceptance rules of the batch (single calls) and the attention of
-    `attn_nodes`; with threads > 1 the attention runs on `threads` host
-    threads, each over a disjoint node set of the same size as attn_nodes
-    (the C oracle runs outside the interpreter lock), and the attention
-    cost per node is the wall time over all of them."""
+    acceptance rules of the batch (single calls) and the attention of attn_k
+    nodes spread over the batch (attn_k = 0: as many as about target_s
+    seconds of one thread's work, from the time of two nodes); with threads
+    > 1 the attention runs on `threads` host threads, each over a disjoint
+    node set of that size (the C oracle runs outside the interpreter lock),
+    and the attention cost per node is the wall time over all of them.
+    Returns (tree-node tokens/s, seconds of oracle work, nodes per thread)."""
     import concurrent.futures
     import oracle
 
@@ -250,6 +300,12 @@ def cpu_oracle_sample(wl, attn_nodes, alpha, uniforms, adaptive, threads=1):
         oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len, wl.tree_off,
                          tr["parent"], wl.scale, rows=rows)
 
+    if attn_k <= 0:
+        tc = time.perf_counter()
+        attn(attn_sample_nodes(wl, 2))
+        per = (time.perf_counter() - tc) / 2
+        attn_k = int(max(4, min(512, target_s / max(per, 1e-6))))
+    attn_nodes = attn_sample_nodes(wl, attn_k)
     t1b = time.perf_counter()
     if threads <= 1:
         attn(attn_nodes)
@@ -266,7 +322,7 @@ def cpu_oracle_sample(wl, attn_nodes, alpha, uniforms, adaptive, threads=1):
     # per-node cost of the whole step: build and accept per node of the
     # batch, attention per sampled node
     per_node = (t1 - t0) / wl.total + (t2 - t1b) / n_attn + (t3 - t2) / wl.total
-    return 1.0 / per_node, (t1 - t0) + (t3 - t1b)
+    return 1.0 / per_node, (t1 - t0) + (t3 - t1b), len(attn_nodes)
 
 
 def attn_sample_nodes(wl, k):
@@ -282,6 +338,35 @@ def step_name(args):
             + (" + verify_accept_stochastic(T=1)" if args.stochastic else ""))
 
 
+def make_workload(args, seed):
+    """The seeded workload of --config; --nseq keeps only its first
+    sequences (a reduced shape for profiler captures, named as such)."""
+    if not args.nseq:
+        return wk.make(args.config, seed=seed)
+    c = wk.CONFIGS[args.config]
+    if not 1 <= args.nseq <= c["nseq"]:
+        raise SystemExit(f"--nseq must lie in [1, {c['nseq']}]")
+    budgets = c["budgets"] if len(c["budgets"]) == 1 else c["budgets"][:args.nseq]
+    name = f"{c['name']} (first {args.nseq} of {c['nseq']} sequences)"
+    return wk.make(args.config, seed=seed, overrides={"nseq": args.nseq, "budgets": budgets, "name": name})
+
+
+def config_dict(args, wl, world):
+    """The workload description both arms print (identical dicts for the
+    same command line)."""
+    c = wl.cfg
+    return {"workload": c["name"], "nseq": wl.nseq, "tree_nodes": wl.total,
+            "prefix_len": [int(x) for x in wl.prefix_len[:4]] + (["..."] if wl.nseq > 4 else []),
+            "Hq": c["Hq"], "Hkv": c["Hkv"], "head_dim": c["D"], "N": c["N"], "W": c["W"], "V": c["V"],
+            "step": step_name(args),
+            "l2": f"flushed before every step ({args.flush_mb} MiB write)",
+            "parallelism": f"replicas x{world}"}
+
+
+VALUE_IS = ("whole verify step: tree-node tokens per second of build + attention + acceptance "
+            "(attention alone: roofline.attn_tokens_per_s)")
+
+
 def run_reference(args, rank):
     """The oracle, as it stands, on the host cores.  One reference step is
     the attention of one tree node per host thread, run concurrently
@@ -295,7 +380,7 @@ def run_reference(args, rank):
     import concurrent.futures
     import oracle
 
-    wl = wk.make(args.config, seed=replica_seed(args.config, 0))
+    wl = make_workload(args, replica_seed(args.config, 0))
     c = wl.cfg
     t0 = time.perf_counter()
     tr = oracle_build(wl, args.alpha, args.adaptive)
@@ -314,12 +399,16 @@ def run_reference(args, rank):
     pool = concurrent.futures.ThreadPoolExecutor(threads)
     for i in range(min(args.warmup, 3)):
         list(pool.map(attn_one, [(i * threads + t) % wl.total for t in range(threads)]))
+    # K steps, or as many as fit in the time budget (a long-prefix node costs
+    # a fraction of a second of fp64 work per thread)
     times = []
     t_start = time.perf_counter()
     for i in range(args.steps):
         t0 = time.perf_counter()
         list(pool.map(attn_one, [((i * threads + t) * 37) % wl.total for t in range(threads)]))
         times.append(time.perf_counter() - t0)
+        if time.perf_counter() - t_start > args.ref_budget_s:
+            break
     wall = time.perf_counter() - t_start
     pool.shutdown()
     per_node = t_build / wl.total + t_accept / wl.total + statistics.mean(times) / threads
@@ -328,13 +417,13 @@ def run_reference(args, rank):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * per_node,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": c["name"], "nseq": wl.nseq, "tree_nodes": wl.total,
-                                         "step": step_name(args)},
+        "data": "synthetic", "value_is": VALUE_IS, "config": config_dict(args, wl, args.gpus),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                          "sample": f"tree build ({t_build:.2f} s) and the acceptance rules "
                                    f"({t_accept:.2f} s) over all {wl.total} nodes once (one thread), "
                                    f"attention of {threads} nodes per step on {threads} host threads "
-                                   f"for {args.steps} steps ({wall:.1f} s); C, fp64"},
+                                   f"for {len(times)} of {args.steps} steps ({wall:.1f} s, budget "
+                                   f"{args.ref_budget_s:g} s); C, fp64"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -348,10 +437,15 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--config", type=int, default=4)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--nseq", type=int, default=0,
+                    help="keep only the first NSEQ sequences of the workload (reduced shapes for profiling)")
     ap.add_argument("--e2e-steps", type=int, default=30)
-    ap.add_argument("--cpu-attn-nodes", type=int, default=48)
+    ap.add_argument("--cpu-attn-nodes", type=int, default=0,
+                    help="attention nodes per host thread in the CPU baseline (0: sized to the prefix)")
+    ap.add_argument("--ref-budget-s", type=float, default=90.0,
+                    help="--impl reference: stop after the step that crosses this many seconds")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--flush-mb", type=int, default=512)
     ap.add_argument("--no-graph", action="store_true", help="launch every call eagerly")
@@ -394,7 +488,7 @@ def main():
             dist.barrier()
 
     cfg = args.config
-    wl = wk.make(cfg, seed=replica_seed(cfg, rank))
+    wl = make_workload(args, replica_seed(cfg, rank))
     c = wl.cfg
     dev = torch.device("cuda", local_rank)
 
@@ -518,6 +612,9 @@ def main():
             main.wait_stream(side[i])
 
     flush = torch.empty(args.flush_mb * (1 << 20), dtype=torch.uint8, device=dev)
+    # clock sampling is live from the warm-up on, so the GPU is under load
+    # when the timed region starts
+    clocks = ClockSampler(local_rank).start()
     for _ in range(args.warmup):
         flush.zero_()
         step(d)
@@ -547,24 +644,26 @@ def main():
 
     # ---- timed region (inputs resident in HBM; L2 flushed before each step)
     evs = []
-    with ClockSampler(local_rank) as clocks:
-        barrier()
-        torch.cuda.synchronize()
-        t_wall0 = time.perf_counter()
-        for _ in range(args.steps):
-            flush.zero_()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            if g_step is not None:
-                g_step.replay()
-            else:
-                step(d)
-            e1.record(stream)
-            evs.append((e0, e1))
-        torch.cuda.synchronize()
-        barrier()
-        wall = time.perf_counter() - t_wall0
+    barrier()
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    t_wall0 = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        if g_step is not None:
+            g_step.replay()
+        else:
+            step(d)
+        e1.record(stream)
+        evs.append((e0, e1))
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t_wall0
+    clocks.mark_end()
+    clocks.stop()
     # the dominant kernel alone, same inputs, same L2 flush, for the roofline
     for _ in range(args.steps):
         flush.zero_()
@@ -626,7 +725,7 @@ def main():
         roof = {"bound": "hbm", "achieved": bytes_a / (attn_mean * 1e-3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu")
+    roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu", c["name"])
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
     roof["kernel"] = "jt_tree_attn_paged (tree_attn_tc_kernel + combine)"
     roof["algorithmic_bytes"] = int(bytes_a)
@@ -646,16 +745,15 @@ def main():
     # ---- CPU baseline (rank 0, N = 1)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        nodes = attn_sample_nodes(wl, args.cpu_attn_nodes)
-        v1, secs1 = cpu_oracle_sample(wl, nodes, args.alpha, uniforms, args.adaptive)
+        v1, secs1, k1 = cpu_oracle_sample(wl, args.cpu_attn_nodes, args.alpha, uniforms, args.adaptive)
         cores = min(host_cores(), 64)
-        vn, secsn = cpu_oracle_sample(wl, nodes, args.alpha, uniforms, args.adaptive, threads=cores)
+        vn, secsn, kn = cpu_oracle_sample(wl, k1, args.alpha, uniforms, args.adaptive, threads=cores)
         cpu = {"value": vn, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"full tree build and the step's acceptance rules over all {total} nodes "
-                         f"(one thread), attention for {len(nodes)} nodes on each of {cores} host threads "
+                         f"(one thread), attention for {kn} nodes on each of {cores} host threads "
                          f"({secsn:.1f} s; C, fp64)",
                "single_thread": {"value": v1, "cores": 1,
-                                 "sample": f"same, attention for {len(nodes)} of {total} nodes on one thread "
+                                 "sample": f"same, attention for {k1} of {total} nodes on one thread "
                                            f"({secs1:.1f} s)"}}
 
     # tree build: top-W partials, row merge, expansion; attention: main
@@ -669,15 +767,10 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "ms_per_step_median": ms_median, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": c["name"], "nseq": nseq, "tree_nodes": total,
-                       "prefix_len": [int(x) for x in wl.prefix_len[:4]] + (["..."] if nseq > 4 else []),
-                       "Hq": Hq, "Hkv": Hkv, "head_dim": D, "N": N, "W": W, "V": c["V"],
-                       "step": step_name(args),
-                       "schedule": ("one stream" if args.serial else
-                                    "acceptance on side streams beside the attention (after the build)"),
-                       "l2": f"flushed before every step ({args.flush_mb} MiB write)",
-                       "launch": "eager" if args.no_graph else "cuda_graph replay of the step",
-                       "parallelism": f"replicas x{world}"},
+            "value_is": VALUE_IS, "config": config_dict(args, wl, world),
+            "schedule": ("one stream" if args.serial else
+                         "acceptance on side streams beside the attention (after the build)"),
+            "launch": "eager" if args.no_graph else "cuda_graph replay of the step",
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -37,3 +37,27 @@ def oracle_tree(wl):
 def attn_errors(got, want):
     d = np.abs(got.astype(np.float64) - want)
     return float(d.max()), float(d.mean())
+
+
+def oracle_attn_threaded(wl, parent, rows, threads=None):
+    """The oracle's attention for the nodes in `rows`, spread over host
+    threads in contiguous chunks (the C oracle runs outside the interpreter
+    lock); returns (out, lse) in the order of `rows`."""
+    import concurrent.futures
+    import os
+
+    rows = np.asarray(rows, np.int32)
+    if threads is None:
+        try:
+            threads = len(os.sched_getaffinity(0))
+        except AttributeError:
+            threads = os.cpu_count() or 1
+    chunks = [c for c in np.array_split(rows, max(1, min(threads, len(rows)))) if len(c)]
+
+    def one(c):
+        return oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len, wl.tree_off,
+                                parent, wl.scale, rows=c)
+
+    with concurrent.futures.ThreadPoolExecutor(len(chunks)) as ex:
+        parts = list(ex.map(one, chunks))
+    return np.concatenate([p[0] for p in parts]), np.concatenate([p[1] for p in parts])

@@ -12,14 +12,14 @@ import torch
 import oracle
 import tree_speculative_decoding_jt_gb300 as jt
 from tree_speculative_decoding_jt_gb300 import workloads as wk
-from gpu_util import attn_errors, dev, kv_to_device, oracle_tree, to_np_bf16
+from gpu_util import attn_errors, dev, kv_to_device, oracle_attn_threaded, oracle_tree, to_np_bf16
 
 pytestmark = pytest.mark.gpu
 
 BF16_MAX, BF16_MEAN, LSE_TOL, F32_MAX = 2e-2, 2e-3, 2e-2, 1e-4
 
 
-def _run(wl, tree, rows=None, split_check=True):
+def _run(wl, tree, rows=None, threaded=False):
     q, k, v = kv_to_device(wl)
     out, lse = jt.jt_tree_attn_paged(q, k, v, dev(wl.block_table), dev(wl.prefix_len),
                                      dev(wl.tree_off), dev(tree["anc"].view(np.int32)),
@@ -27,8 +27,12 @@ def _run(wl, tree, rows=None, split_check=True):
     torch.cuda.synchronize()
     got = to_np_bf16(out) if out.dtype == torch.bfloat16 else out.cpu().numpy()
     got_lse = lse.cpu().numpy()
-    want, want_lse = oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len,
-                                      wl.tree_off, tree["parent"], wl.scale, rows=rows)
+    del q, k, v, out, lse
+    if threaded:
+        want, want_lse = oracle_attn_threaded(wl, tree["parent"], rows)
+    else:
+        want, want_lse = oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len,
+                                          wl.tree_off, tree["parent"], wl.scale, rows=rows)
     if rows is not None:
         got, got_lse = got[rows], got_lse[rows]
     return got, got_lse, want, want_lse
@@ -127,12 +131,13 @@ def test_f32_config1_full():
     assert np.abs(got_lse - want_lse).max() <= F32_MAX
 
 
-def _sample_rows(wl, k_per_seq=3):
-    rows = []
-    for b in range(wl.nseq):
-        o, e = int(wl.tree_off[b]), int(wl.tree_off[b + 1])
-        rows += sorted({o, e - 1, o + (e - o) // 2})[:k_per_seq]
-    return np.array(rows, np.int32)
+def _whole_sequences(wl, seqs):
+    """Every node of the listed sequences (global node indices)."""
+    return np.concatenate([np.arange(wl.tree_off[b], wl.tree_off[b + 1], dtype=np.int32) for b in seqs])
+
+
+def _longest(wl, candidates):
+    return max(candidates, key=lambda b: (int(wl.prefix_len[b]), -b))
 
 
 def test_bf16_drafter_tree_only_all_nodes():
@@ -143,20 +148,42 @@ def test_bf16_drafter_tree_only_all_nodes():
     _check_bf16(*_run(wl, tree))
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 5])
-def test_bf16_full_configs_sampled(cfg):
-    wl = wk.make(cfg)
+def test_bf16_config2_every_node():
+    """Batch 1, prefix 4096, B = 256: all 256 nodes x 32 heads (the KV range
+    is split over several CTAs and merged by the combine)."""
+    wl = wk.make(2)
     tree = oracle_tree(wl)
-    rows = _sample_rows(wl) if cfg != 2 else np.arange(0, 256, 5, dtype=np.int32)
-    _check_bf16(*_run(wl, tree, rows=rows))
+    _check_bf16(*_run(wl, tree, rows=_whole_sequences(wl, [0]), threaded=True))
+
+
+def test_bf16_config3_whole_sequences():
+    """The ragged serving batch: every node and head of the longest-prefix
+    sequence with B = 128 and of the longest-prefix one with B = 256."""
+    wl = wk.make(3)
+    tree = oracle_tree(wl)
+    budgets = np.diff(wl.tree_off)
+    seqs = [_longest(wl, [b for b in range(wl.nseq) if budgets[b] == 128]),
+            _longest(wl, [b for b in range(wl.nseq) if budgets[b] == 256])]
+    _check_bf16(*_run(wl, tree, rows=_whole_sequences(wl, seqs), threaded=True))
+
+
+def test_bf16_config5_whole_sequences():
+    """The verify-step batch (B = 256, prefixes 2k-16k): every node and head
+    of the longest- and of the shortest-prefix sequence."""
+    wl = wk.make(5)
+    tree = oracle_tree(wl)
+    order = np.argsort(wl.prefix_len, kind="stable")
+    seqs = [int(order[-1]), int(order[0])]
+    _check_bf16(*_run(wl, tree, rows=_whole_sequences(wl, seqs), threaded=True))
 
 
 @pytest.mark.slow
-def test_bf16_config4_sampled():
+def test_bf16_config4_whole_sequences():
+    """32 sequences of prefix 32768, B = 64: all 64 nodes x 32 heads of the
+    first and of the last sequence."""
     wl = wk.make(4)
     tree = oracle_tree(wl)
-    rows = np.array([0, 63, 64 * 17 + 5, 64 * 31 + 63], np.int32)
-    _check_bf16(*_run(wl, tree, rows=rows))
+    _check_bf16(*_run(wl, tree, rows=_whole_sequences(wl, [0, wl.nseq - 1]), threaded=True))
 
 
 def test_host_side_argument_errors():

@@ -4,7 +4,11 @@ oracle's fp64, so decisions taken within rounding of their thresholds may
 differ:
   * a sequence whose acceptance tests all lie further than 1e-4 from their
     thresholds must give the same accept_len and path (the oracle reports
-    that margin); closer sequences are counted as ambiguous and must be rare;
+    that margin); closer sequences are counted as ambiguous, their count is
+    printed, and at most 5 % of a case's sequences may be ambiguous (with
+    fewer than 20 sequences: none).  1e-4 bounds the kernel's fp32 error in
+    min(1, r/q): a softmax over at most 151936 entries and a residual
+    rewrite per rejection, each a few fp32 roundings relative;
   * its bonus must be a valid draw from the oracle's final residual r: the
     kernel's token x has r(x) > 0 and its CDF bin contains the uniform
     within 1e-4; when the uniform lies further than 1e-4 inside the
@@ -24,7 +28,10 @@ MARGIN = 1e-4
 CDF_TOL = 1e-4
 
 
-def _compare(target, draft, parent, token, off, N, ua, ub, min_clear=0.8):
+MAX_AMBIGUOUS = 0.05
+
+
+def _compare(target, draft, parent, token, off, N, ua, ub):
     want_acc, want_path, want_bonus, margin, fr, fu = oracle.verify_accept_stochastic(
         target, draft, parent, token, off, N, ua, ub, with_residual=True)
     acc, path, bonus = jt.jt_verify_accept_stochastic(dev(target), dev(draft), dev(parent), dev(token),
@@ -32,7 +39,9 @@ def _compare(target, draft, parent, token, off, N, ua, ub, min_clear=0.8):
     torch.cuda.synchronize()
     acc, path, bonus = acc.cpu().numpy(), path.cpu().numpy(), bonus.cpu().numpy()
     clear = margin > MARGIN
-    assert clear.mean() >= min_clear, f"too many ambiguous sequences: {clear.mean()}"
+    n_amb = int((~clear).sum())
+    print(f"stochastic parity: {n_amb} of {len(clear)} sequences ambiguous (a test within {MARGIN} of its threshold)")
+    assert n_amb <= int(MAX_AMBIGUOUS * len(clear)), f"{n_amb} of {len(clear)} sequences ambiguous"
     np.testing.assert_array_equal(acc[clear], want_acc[clear])
     np.testing.assert_array_equal(path[clear], want_path[clear])
     V = target.shape[1]
@@ -104,8 +113,7 @@ def test_full_vocabulary_verify_step():
     target = wk.target_logits(wl, tree["parent"], tree["token"], deep=True)
     rng = np.random.default_rng(55)
     ua, ub = _uniforms(rng, wl.total)
-    _compare(target, wl.draft_logits, tree["parent"], tree["token"], wl.tree_off, wl.cfg["N"], ua, ub,
-             min_clear=0.75)
+    _compare(target, wl.draft_logits, tree["parent"], tree["token"], wl.tree_off, wl.cfg["N"], ua, ub)
 
 
 def test_root_only_tree_draws_from_the_target_row():
@@ -117,7 +125,7 @@ def test_root_only_tree_draws_from_the_target_row():
     token = np.array([5, 6, 7], np.int32)
     off = np.array([0, 1, 2, 3], np.int32)
     ua, ub = _uniforms(rng, 3)
-    acc = _compare(target, draft, parent, token, off, 2, ua, ub, min_clear=0.6)
+    acc = _compare(target, draft, parent, token, off, 2, ua, ub)
     assert np.all(acc == 0)
 
 

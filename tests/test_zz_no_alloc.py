@@ -23,7 +23,7 @@ def test_oversized_build_is_refused_on_the_host():
     nseq, N, W, V = 1024, 16, 4, 151936         # 16384 rows: well past 4 MiB of tables
     need = jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, nseq, N, W, V)
     assert need > SCRATCH_BYTES
-    fake = ctypes.c_void_p(4096)                  # never dereferenced: refused before any CUDA call
+    fake = ctypes.c_void_p(4096)                  # never dereferenced: refused before any device work is enqueued
     rc = lib.jt_tree_build_noalloc(fake, fake, fake, nseq, N, W, V, nseq * 16, fake, fake, fake,
                                    fake, 1, None)
     assert rc == JT_ERR_WORKSPACE

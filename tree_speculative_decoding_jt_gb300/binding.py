@@ -10,6 +10,7 @@ GPU or without the built library the calls fail.
 from __future__ import annotations
 
 import ctypes
+import functools
 import math
 import os
 import threading
@@ -144,6 +145,31 @@ def _check(rc, where):
         raise JtError(rc, where)
 
 
+def _tensors(obj):
+    if isinstance(obj, torch.Tensor):
+        yield obj
+    elif isinstance(obj, (tuple, list)):
+        for o in obj:
+            yield from _tensors(o)
+
+
+def _on_tensor_device(fn):
+    """Run a binding call with its tensors' device current.  The library
+    launches on the current device (its stream, its per-device set-up and
+    fixed scratch), so a call whose tensors live on another device than the
+    current one is moved there; tensors on different devices are refused."""
+    @functools.wraps(fn)
+    def wrapper(*args, **kwargs):
+        devs = {t.device for t in _tensors(list(args) + list(kwargs.values())) if t.is_cuda}
+        if len(devs) > 1:
+            raise ValueError(f"{fn.__name__}: tensors on several devices ({sorted(map(str, devs))})")
+        if not devs:
+            return fn(*args, **kwargs)
+        with torch.cuda.device(devs.pop()):
+            return fn(*args, **kwargs)
+    return wrapper
+
+
 def jt_workspace_size(op, nseq=0, N=0, W=0, V=0, total_nodes=0, Hq=0, Hkv=0, D=0, max_pages=0,
                       max_tree=0) -> int:
     return int(load().jt_workspace_size(op, nseq, N, W, V, total_nodes, Hq, Hkv, D, max_pages,
@@ -157,6 +183,7 @@ def workspace(nbytes: int, device=None) -> torch.Tensor:
     return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
 
 
+@_on_tensor_device
 def jt_verify_accept_stochastic(target_logits, draft_logits, parent, token, tree_off, N, u_accept,
                                 u_bonus, out=None, ws=None, stream=None):
     """Temperature-1 tree acceptance by rejection sampling with the caller's
@@ -186,11 +213,13 @@ def jt_verify_accept_stochastic(target_logits, draft_logits, parent, token, tree
     return acc, path, bonus
 
 
+@_on_tensor_device
 def jt_check(ws: torch.Tensor, stream=None) -> None:
     """Synchronise and raise if a kernel flagged a device-side error in ws."""
     _check(load().jt_check(_ptr(ws), _stream(stream)), "jt_check")
 
 
+@_on_tensor_device
 def jt_tree_build(draft_logits, root_token, tree_off, W, total_nodes=None, out=None, ws=None,
                   stream=None):
     """Best-first draft tree from per-depth draft logits [nseq, N, V] (fp32).
@@ -219,6 +248,7 @@ def jt_tree_build(draft_logits, root_token, tree_off, W, total_nodes=None, out=N
     return parent, token, depth, anc
 
 
+@_on_tensor_device
 def jt_tree_build_mixed(draft_logits, root_token, tree_off, W, alpha, total_nodes=None, out=None, ws=None,
                         stream=None):
     """jt_tree_build whose step scores are (1 - alpha) * log-prob - alpha *
@@ -248,6 +278,7 @@ def jt_tree_build_mixed(draft_logits, root_token, tree_off, W, alpha, total_node
     return parent, token, depth, anc
 
 
+@_on_tensor_device
 def jt_tree_build_noalloc(draft_logits, root_token, tree_off, W, total_nodes=None, out=None,
                           sync_check=True, stream=None):
     """jt_tree_build with the library's fixed device scratch instead of a
@@ -275,6 +306,7 @@ def jt_tree_build_noalloc(draft_logits, root_token, tree_off, W, total_nodes=Non
     return parent, token, depth, anc
 
 
+@_on_tensor_device
 def jt_tree_topw(logits, W, ws=None, stream=None):
     """Top-W ids (int32), log-probs and lse (fp64) of every row of [..., V] fp32."""
     lib = load()
@@ -293,6 +325,7 @@ def jt_tree_topw(logits, W, ws=None, stream=None):
     return tok, lp, lse
 
 
+@_on_tensor_device
 def jt_tree_expand(tok, lp, root_token, tree_off, total_nodes=None, ws=None, stream=None):
     """Best-first expansion from given tables tok [nseq,N,W] int32, lp fp64."""
     lib = load()
@@ -317,6 +350,7 @@ def jt_tree_expand(tok, lp, root_token, tree_off, total_nodes=None, ws=None, str
     return parent, token, depth, anc
 
 
+@_on_tensor_device
 def jt_tree_expand_capped(tok, lp, root_token, tree_off, w_cap=None, n_cap=None, total_nodes=None, ws=None,
                           stream=None):
     """jt_tree_expand with optional per-sequence width / depth caps
@@ -346,6 +380,7 @@ def jt_tree_expand_capped(tok, lp, root_token, tree_off, w_cap=None, n_cap=None,
     return parent, token, depth, anc
 
 
+@_on_tensor_device
 def jt_tree_policy(lp, accept_len, budget_state, acc_ema, params=None, out=None, ws=None, stream=None):
     """One step of the adaptive tree policy.  lp fp64 [nseq, N, W];
     accept_len int32 [nseq] or None; budget_state int32 / acc_ema fp64
@@ -373,6 +408,7 @@ def jt_tree_policy(lp, accept_len, budget_state, acc_ema, params=None, out=None,
     return tree_off, w_cap, n_cap
 
 
+@_on_tensor_device
 def jt_tree_build_adaptive(draft_logits, root_token, accept_len, budget_state, acc_ema, W, params=None,
                            capacity=None, out=None, ws=None, stream=None):
     """Top-W tables, adaptive policy and capped expansion in one call.
@@ -409,6 +445,7 @@ def jt_tree_build_adaptive(draft_logits, root_token, accept_len, budget_state, a
     return tree_off, w_cap, n_cap, parent, token, depth, anc
 
 
+@_on_tensor_device
 def jt_tree_attn_paged(q, k_cache, v_cache, block_table, prefix_len, tree_off, anc, scale=None,
                        max_tree=None, out=None, lse=None, ws=None, stream=None, with_lse=True):
     """Tree-causal attention over a paged KV cache.
@@ -455,6 +492,7 @@ def jt_tree_attn_paged(q, k_cache, v_cache, block_table, prefix_len, tree_off, a
     return out, lse
 
 
+@_on_tensor_device
 def jt_verify_accept(target_logits, parent, token, tree_off, N, rule=JT_RULE_GREEDY, t=None,
                      log_t=None, out=None, ws=None, stream=None):
     """Tree acceptance: returns (accept_len [nseq], path [nseq, N+1], bonus [nseq])."""
@@ -484,6 +522,7 @@ def jt_verify_accept(target_logits, parent, token, tree_off, N, rule=JT_RULE_GRE
     return acc, path, bonus
 
 
+@_on_tensor_device
 def jt_selftest_wait_timeout(ws=None, stream=None):
     """Run the bounded-wait timeout diagnostic; returns the workspace whose
     error word it sets (read it with jt_check: JT_ERR_TIMEOUT)."""

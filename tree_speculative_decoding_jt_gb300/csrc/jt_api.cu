@@ -9,16 +9,14 @@
 namespace jt {
 
 int device_sm_count() {
-    static int cached_dev = -1, cached_sms = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev != cached_dev) {
-        int sms = 0;
-        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached_sms = sms;
-        cached_dev = dev;
-    }
-    return cached_sms;
+    static PerDeviceCache cache;
+    return cache.get([] {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return 0;
+        return sms;
+    });
 }
 
 static jt_status from_cuda(cudaError_t e) {

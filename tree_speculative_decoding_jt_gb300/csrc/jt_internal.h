@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/jt.h"
 
 namespace jt {
@@ -86,5 +88,38 @@ cudaError_t tree_attn_f32_launch(const float* q, const float* k_cache, const flo
 cudaError_t selftest_wait_timeout_launch(uint32_t* err, cudaStream_t st);
 
 int device_sm_count();
+
+// One-time set-up remembered per device.  Kernel attributes
+// (cudaFuncSetAttribute) and occupancy answers belong to the device that was
+// current when they were set or asked, so a process that drives several
+// devices must redo them on each; get() runs `compute` the first time the
+// current device asks (per key) and returns the stored value afterwards.
+// Thread-safe.  Where no device can be named the value is computed afresh.
+constexpr int kMaxDevices = 64;
+class PerDeviceCache {
+  public:
+    template <typename F>
+    int get(F compute, long long key = 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return compute();
+        std::lock_guard<std::mutex> lk(mu_);
+        Slot& s = slot_[dev];
+        if (!s.set || s.key != key) {
+            s.val = compute();
+            s.key = key;
+            s.set = true;
+        }
+        return s.val;
+    }
+
+  private:
+    struct Slot {
+        bool set = false;
+        long long key = 0;
+        int val = 0;
+    };
+    std::mutex mu_;
+    Slot slot_[kMaxDevices];
+};
 
 }  // namespace jt

@@ -75,7 +75,7 @@ extern "C" jt_status jt_tree_build_noalloc(const float* draft_logits, const int3
         return JT_ERR_INVALID;
     if (reinterpret_cast<uintptr_t>(anc) % 16 != 0) return JT_ERR_INVALID;
     // scratch the build needs; beyond the fixed array the call is refused
-    // before anything touches the device
+    // before any device work is enqueued
     const size_t need = kWsHeader + topw_workspace_bytes(static_cast<long long>(nseq) * N, V, W);
     if (need > JT_NOALLOC_SCRATCH_BYTES) return JT_ERR_WORKSPACE;
 

@@ -734,13 +734,12 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
     prm.scale_log2 = scale * 1.4426950408889634f;
 
     using SL = SmemLayout<D>;
-    static bool attr_done = false;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(tree_attn_tc_kernel<D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    static PerDeviceCache attr;  // the shared-memory opt-in is per device
+    const cudaError_t ea = static_cast<cudaError_t>(attr.get([] {
+        return static_cast<int>(cudaFuncSetAttribute(tree_attn_tc_kernel<D>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc));
+    }));
+    if (ea != cudaSuccess) return ea;
     dim3 grid(((plan.mtiles + 1) / 2) * plan.splits, Hkv, nseq);
     cudaError_t e = launch_kernel_pdl(tree_attn_tc_kernel<D>, grid, dim3(kAttnThreads), SL::kAlloc, st, tq, tk,
                                       tv, prm);

@@ -990,13 +990,15 @@ static const ExpTable& exp_table() {
     return tab;
 }
 
-// One-time (per process) attribute set-up; the first call should come before
-// any stream capture.
+// One-time attribute set-up per device; the first call on a device should
+// come before any stream capture.
 template <int W>
 static cudaError_t set_expand_smem() {
-    static cudaError_t done = cudaFuncSetAttribute(
-        expand_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kExpandSmem));
-    return done;
+    static PerDeviceCache done;
+    return static_cast<cudaError_t>(done.get([] {
+        return static_cast<int>(cudaFuncSetAttribute(expand_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     static_cast<int>(kExpandSmem)));
+    }));
 }
 
 static int topw_splits(long long V, int per) {

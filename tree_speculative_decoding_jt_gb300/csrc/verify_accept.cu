@@ -217,11 +217,10 @@ __global__ void __launch_bounds__(kAccThreads)
     cl.sync();  // rank 0's shared memory stays alive until every rank is done with it
 }
 
-// Largest cluster size (16, 8, 4, 2, 1) the device can schedule for this kernel.
+// Largest cluster size (16, 8, 4, 2, 1) the current device can schedule for
+// this kernel (asked once per device).
 template <bool VEC>
-static int accept_cluster_size() {
-    static int cached = 0;
-    if (cached) return cached;
+static int accept_cluster_size_uncached() {
     cudaFuncSetAttribute(accept_cluster_kernel<VEC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     for (int cs = 16; cs >= 1; cs >>= 1) {
         cudaLaunchConfig_t cfg = {};
@@ -236,14 +235,17 @@ static int accept_cluster_size() {
         cfg.numAttrs = 1;
         int nclusters = 0;
         if (cudaOccupancyMaxActiveClusters(&nclusters, accept_cluster_kernel<VEC>, &cfg) == cudaSuccess &&
-            nclusters > 0) {
-            cached = cs;
+            nclusters > 0)
             return cs;
-        }
         cudaGetLastError();
     }
-    cached = 1;
     return 1;
+}
+
+template <bool VEC>
+static int accept_cluster_size() {
+    static PerDeviceCache cache;
+    return cache.get(accept_cluster_size_uncached<VEC>);
 }
 
 template <bool VEC>

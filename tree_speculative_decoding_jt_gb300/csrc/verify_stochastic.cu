@@ -337,13 +337,8 @@ cudaError_t verify_stochastic_launch(const float* z, const float* zd, const int3
                                      const double* u_bonus, int32_t* accept_len, int32_t* path,
                                      int32_t* bonus, char* ws, cudaStream_t st) {
     uint32_t* err = reinterpret_cast<uint32_t*>(ws);
-    static long long cached_v = -1;
-    static int cached_cs = 0;
-    if (V != cached_v) {
-        cached_cs = stochastic_cluster_size(V);
-        cached_v = V;
-    }
-    const int cs = cached_cs;
+    static PerDeviceCache cache;  // per device and vocabulary size
+    const int cs = cache.get([V] { return stochastic_cluster_size(V); }, V);
     if (cs == 0) return cudaErrorNotSupported;
     const long long chunk = (V + cs - 1) / cs;
     const size_t smem = static_cast<size_t>(chunk) * 2 * sizeof(float);
