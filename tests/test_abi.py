@@ -45,3 +45,19 @@ def test_host_side_checks_need_no_gpu():
     assert jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, 8, 16, 4, 151936) > 0
     assert jt.jt_workspace_size(jt.JT_OP_TREE_BUILD, 8, 16, 9, 151936) == 0
     assert jt.jt_workspace_size(jt.JT_OP_VERIFY_ACCEPT, 8, 0, 0, 0, 2048) > 0
+
+
+def test_checks_variant_builds_and_exports_every_symbol():
+    """The debug variant (-DJT_CHECKS device-side input checks, -DJT_NVTX
+    ranges) builds for sm_103a and exports the same entry points."""
+    from tree_speculative_decoding_jt_gb300 import build as b
+
+    path = b.build(variant="checks")
+    assert path.endswith("libjt_checks.so") and os.path.exists(path)
+    raw = ctypes.CDLL(path)
+    for name in _declared():
+        assert hasattr(raw, name), name
+    # the host-side checks answer the same way in the variant
+    raw.jt_tree_topw.restype = ctypes.c_int
+    assert raw.jt_tree_topw(None, ctypes.c_int64(1), ctypes.c_int64(10), 2, None, None, None, None,
+                            ctypes.c_size_t(0), None) == -1

@@ -64,17 +64,25 @@ class JtError(RuntimeError):
         super().__init__(f"{where}: {jt_status_str(status)}")
 
 
+def library_variant() -> str:
+    """The library variant this process loads: JT_LIB_VARIANT ("" = the
+    default build, "checks" = extra device-side input checks and NVTX
+    ranges)."""
+    return os.environ.get("JT_LIB_VARIANT", "")
+
+
 def library_path() -> str:
-    return _build.LIB
+    return _build.lib_path(library_variant())
 
 
 def load(build_if_missing: bool = True):
-    """Load libjt.so (building it with nvcc first if it is missing or stale)."""
+    """Load libjt (building it with nvcc first if it is missing or stale)."""
     global _lib
     with _lock:
         if _lib is not None:
             return _lib
-        path = _build.build() if build_if_missing else _build.LIB
+        variant = library_variant()
+        path = _build.build(variant=variant) if build_if_missing else _build.lib_path(variant)
         if not os.path.exists(path):
             raise RuntimeError(f"libjt.so not found at {path}; run tree_speculative_decoding_jt_gb300.build")
         lib = ctypes.CDLL(path)

@@ -88,6 +88,7 @@ size_t jt_workspace_size(int op, int nseq, int N, int W, int64_t V, int total_no
 
 jt_status jt_tree_topw(const float* logits, int64_t rows, int64_t V, int W, int32_t* tok,
                        double* lp, double* lse, void* ws, size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_tree_topw");
     if (!logits || !tok || !lp || !lse || rows < 0 || W < 1 || W > JT_MAX_W || V < W ||
         V > 0x7FFFFFFFll || rows > 65535)
         return JT_ERR_INVALID;
@@ -104,6 +105,7 @@ jt_status jt_tree_build_mixed(const float* draft_logits, const int32_t* root_tok
                               int total_nodes, double alpha, int32_t* parent, int32_t* token,
                               int32_t* depth, uint32_t* anc, void* ws, size_t ws_bytes,
                               jt_stream_t stream) {
+    JT_RANGE("jt_tree_build_mixed");
     if ((!draft_logits && N > 0) || !root_token || !tree_off || !parent || !token || !depth ||
         !anc || nseq < 1 || nseq > 65535 || N < 0 || N > JT_MAX_N || W < 1 || W > JT_MAX_W ||
         V < W || V > 0x7FFFFFFFll || total_nodes < nseq ||
@@ -123,6 +125,7 @@ jt_status jt_tree_build(const float* draft_logits, const int32_t* root_token,
                         const int32_t* tree_off, int nseq, int N, int W, int64_t V, int total_nodes,
                         int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc, void* ws,
                         size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_tree_build");
     return jt_tree_build_mixed(draft_logits, root_token, tree_off, nseq, N, W, V, total_nodes, 0.0, parent,
                                token, depth, anc, ws, ws_bytes, stream);
 }
@@ -132,6 +135,7 @@ jt_status jt_tree_expand_capped(const int32_t* tok, const double* lp, const int3
                                 int nseq, int N, int W, int total_nodes, int32_t* parent,
                                 int32_t* token, int32_t* depth, uint32_t* anc, void* ws,
                                 size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_tree_expand_capped");
     if ((N > 0 && (!tok || !lp)) || !root_token || !tree_off || !parent || !token || !depth ||
         !anc || nseq < 1 || nseq > 65535 || N < 0 || N > JT_MAX_N || W < 1 || W > JT_MAX_W ||
         total_nodes < nseq || !aligned(anc, 16))
@@ -148,6 +152,7 @@ jt_status jt_tree_expand(const int32_t* tok, const double* lp, const int32_t* ro
                          const int32_t* tree_off, int nseq, int N, int W, int total_nodes,
                          int32_t* parent, int32_t* token, int32_t* depth, uint32_t* anc, void* ws,
                          size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_tree_expand");
     return jt_tree_expand_capped(tok, lp, root_token, tree_off, nullptr, nullptr, nseq, N, W, total_nodes,
                                  parent, token, depth, anc, ws, ws_bytes, stream);
 }
@@ -173,6 +178,7 @@ jt_status jt_tree_policy(const double* lp, int nseq, int N, int W, const int32_t
                          const jt_policy_params* params, int32_t* budget_state, double* acc_ema,
                          int32_t* tree_off, int32_t* w_cap, int32_t* n_cap, void* ws,
                          size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_tree_policy");
     if (!lp || !budget_state || !acc_ema || !tree_off || !w_cap || !n_cap || nseq < 1 ||
         nseq > 65535 || N < 1 || N > JT_MAX_N || W < 1 || W > JT_MAX_W ||
         policy_params_ok(params, nseq, N, W) == 0)
@@ -190,6 +196,7 @@ jt_status jt_tree_build_adaptive(const float* draft_logits, const int32_t* root_
                                  double* acc_ema, int32_t* tree_off, int32_t* w_cap,
                                  int32_t* n_cap, int32_t* parent, int32_t* token, int32_t* depth,
                                  uint32_t* anc, void* ws, size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_tree_build_adaptive");
     if (!draft_logits || !root_token || !budget_state || !acc_ema || !tree_off || !w_cap || !n_cap ||
         !parent || !token || !depth || !anc || nseq < 1 || nseq > 65535 || N < 1 || N > JT_MAX_N ||
         W < 1 || W > JT_MAX_W || V < W || V > 0x7FFFFFFFll || static_cast<long long>(nseq) * N > 65535 ||
@@ -214,6 +221,7 @@ jt_status jt_tree_attn_paged(const void* q, const void* k_cache, const void* v_c
                              const uint32_t* anc, int nseq, int total_nodes, int max_tree, int Hq,
                              int Hkv, int D, int page_size, float scale, void* out, float* lse,
                              void* ws, size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_tree_attn_paged");
     if (!q || !k_cache || !v_cache || !block_table || !prefix_len || !tree_off || !anc || !out ||
         nseq < 1 || nseq > 65535 || total_nodes < nseq || max_tree < 1 ||
         max_tree > JT_MAX_TREE || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || max_pages < 1 ||
@@ -253,6 +261,7 @@ jt_status jt_verify_accept(const float* target_logits, const int32_t* parent,
                            int64_t V, int total_nodes, int rule, double log_t,
                            int32_t* accept_len, int32_t* path, int32_t* bonus, void* ws,
                            size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_verify_accept");
     if (!target_logits || !parent || !token || !tree_off || !accept_len || !path || !bonus ||
         nseq < 1 || nseq > 8192 || N < 0 || N > JT_MAX_TREE || V < 1 || V > 0x7FFFFFFFll ||
         total_nodes < nseq || (rule != JT_RULE_GREEDY && rule != JT_RULE_MARGIN) ||
@@ -271,6 +280,7 @@ jt_status jt_verify_accept_stochastic(const float* target_logits, const float* d
                                       int total_nodes, const double* u_accept, const double* u_bonus,
                                       int32_t* accept_len, int32_t* path, int32_t* bonus, void* ws,
                                       size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_verify_accept_stochastic");
     if (!target_logits || (!draft_logits && N > 0) || !parent || !token || !tree_off || !u_accept ||
         !u_bonus || !accept_len || !path || !bonus || nseq < 1 || nseq > 8192 || N < 0 ||
         N > JT_MAX_TREE || V < 1 || V > 0x7FFFFFFFll || total_nodes < nseq)
@@ -284,6 +294,7 @@ jt_status jt_verify_accept_stochastic(const float* target_logits, const float* d
 }
 
 jt_status jt_check(void* ws, jt_stream_t stream) {
+    JT_RANGE("jt_check");
     if (!ws) return JT_ERR_WORKSPACE;
     cudaError_t e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return JT_ERR_CUDA;

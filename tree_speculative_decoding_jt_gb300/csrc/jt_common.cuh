@@ -33,6 +33,20 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t code) {
     if (err) atomicOr(err, code);
 }
 
+// Extra device-side validation of input contents, compiled in with
+// -DJT_CHECKS (the "checks" build of the library): a failed check sets
+// DEVERR_INVALID in the error word, which jt_check reports as
+// JT_ERR_INVALID; the kernel carries on and nothing traps.  Compiled out by
+// default.
+#ifdef JT_CHECKS
+#define JT_DCHECK(cond, err)                                         \
+    do {                                                             \
+        if (!(cond)) ::jt::raise_error((err), ::jt::DEVERR_INVALID); \
+    } while (0)
+#else
+#define JT_DCHECK(cond, err) ((void)0)
+#endif
+
 // cudaLaunchKernelEx with, when cluster_x > 0, a (cluster_x, 1, 1)
 // thread-block cluster.
 template <typename... KArgs, typename... Args>

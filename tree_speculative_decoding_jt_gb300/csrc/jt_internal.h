@@ -10,6 +10,24 @@
 
 #include "../../include/jt.h"
 
+// NVTX ranges around every extern "C" entry point, compiled in with
+// -DJT_NVTX (header-only NVTX v3: nothing is linked, and the ranges cost a
+// branch when no profiler is attached); compiled out by default.
+#ifdef JT_NVTX
+#include <nvtx3/nvToolsExt.h>
+namespace jt {
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+}  // namespace jt
+#define JT_RANGE(name) ::jt::NvtxRange jt_nvtx_range_(name)
+#else
+#define JT_RANGE(name) ((void)0)
+#endif
+
 namespace jt {
 
 constexpr size_t kAlign = 256;

@@ -24,7 +24,6 @@ static __device__ __align__(256) char g_noalloc_scratch[JT_NOALLOC_SCRATCH_BYTES
 
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 char* g_scratch_ptr[kMaxDevices] = {};
 
@@ -67,6 +66,7 @@ extern "C" jt_status jt_tree_build_noalloc(const float* draft_logits, const int3
                                            int total_nodes, int32_t* parent, int32_t* token,
                                            int32_t* depth, uint32_t* anc, int sync_check,
                                            jt_stream_t stream) {
+    JT_RANGE("jt_tree_build_noalloc");
     // the same argument rules as jt_tree_build
     if ((!draft_logits && N > 0) || !root_token || !tree_off || !parent || !token || !depth ||
         !anc || nseq < 1 || nseq > 65535 || N < 0 || N > JT_MAX_N || W < 1 || W > JT_MAX_W ||

@@ -30,6 +30,7 @@ cudaError_t selftest_wait_timeout_launch(uint32_t* err, cudaStream_t st) {
 using namespace jt;
 
 extern "C" jt_status jt_selftest_wait_timeout(void* ws, size_t ws_bytes, jt_stream_t stream) {
+    JT_RANGE("jt_selftest_wait_timeout");
     if (!ws || ws_bytes < kWsHeader || (reinterpret_cast<uintptr_t>(ws) % kAlign) != 0) return JT_ERR_WORKSPACE;
     const cudaError_t e = selftest_wait_timeout_launch(static_cast<uint32_t*>(ws), stream);
     if (e == cudaSuccess) return JT_OK;

@@ -718,6 +718,8 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     for (int i = tid; i < N * W; i += kExpandThreads) {
         s_tok[i] = tok_in[static_cast<long long>(b) * N * W + i];
         s_lp[i] = lp_in[static_cast<long long>(b) * N * W + i];
+        // a NaN draft logit makes its row's lse (so every lp) NaN
+        JT_DCHECK(s_lp[i] == s_lp[i] && s_tok[i] >= 0, err);
     }
     const int off = tree_off[b];
     const int B = tree_off[b + 1] - off;
@@ -863,6 +865,7 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
             pn = -1;
             tn = root_token[b];
             dn = 0;
+            JT_DCHECK(tn >= 0, err);
         } else {
             pn = parf[n - 1] + 1;
             tn = k2_token(k2f[n - 1]);

@@ -110,6 +110,8 @@ __global__ void __launch_bounds__(kAccThreads)
                 for (int q = 0; q < kAccChunk / 128; ++q) {
                     const long long e = begin + 4ll * (lane + 32 * q);
                     if (e < end) {
+                        JT_DCHECK(f[q].x == f[q].x && f[q].y == f[q].y && f[q].z == f[q].z && f[q].w == f[q].w,
+                                  err);
                         best = max(best, pack_argmax_key(f[q].x, e));
                         best = max(best, pack_argmax_key(f[q].y, e + 1));
                         best = max(best, pack_argmax_key(f[q].z, e + 2));
@@ -117,8 +119,11 @@ __global__ void __launch_bounds__(kAccThreads)
                     }
                 }
             } else {
-                for (long long e = begin + lane; e < end; e += 32)
-                    best = max(best, pack_argmax_key(__ldg(zr + e), e));
+                for (long long e = begin + lane; e < end; e += 32) {
+                    const float v = __ldg(zr + e);
+                    JT_DCHECK(v == v, err);  // a NaN logit has no place in the argmax order
+                    best = max(best, pack_argmax_key(v, e));
+                }
             }
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) best = max(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
@@ -127,6 +132,7 @@ __global__ void __launch_bounds__(kAccThreads)
         if (lvl == 0 && rank == 0) {
             s_par[tid] = my_par;
             s_tok[tid] = my_tok;
+            JT_DCHECK(tid != 0 || my_par == -1, err);  // node 0 is the root
         }
         cl.sync();
         // ---- phase 2 (rank 0): combine the ranks' keys, test the children

@@ -157,10 +157,12 @@ __global__ void __launch_bounds__(kStThreads)
             const float zv = zr[i];
             r[i] = zv;
             mp = fmaxf(mp, zv);
+            JT_DCHECK(zv == zv, err);  // a NaN logit leaves the softmax undefined
             if (has_children) {
                 const float dv = dr[i];
                 q[i] = dv;
                 mq = fmaxf(mq, dv);
+                JT_DCHECK(dv == dv, err);
             }
         }
         block_max2(mp, mq, sh);
