@@ -11,4 +11,4 @@ from .binding import (  # noqa: F401
     PolicyParams, jt_check, jt_status_str, jt_tree_attn_paged, jt_tree_build, jt_tree_build_adaptive,
     jt_tree_build_mixed, jt_tree_build_noalloc, jt_tree_expand, jt_tree_expand_capped, jt_tree_policy,
     jt_tree_topw, jt_selftest_wait_timeout, jt_verify_accept, jt_verify_accept_stochastic, jt_version, jt_workspace_size,
-    library_path, load, policy_ceiling, policy_params, workspace)
+    library_path, library_variant, load, policy_ceiling, policy_params, workspace)

@@ -61,7 +61,7 @@ struct AttnParams {
     float* part_o;   // [total*Hq*splits, D] when splits > 1
     float2* part_ml; // [total*Hq*splits]: running max (log2 units), sum
     uint32_t* err;
-    int max_pages, nseq, total_nodes, Hq, G, npt, splits;
+    int max_pages, num_pages, nseq, total_nodes, Hq, G, npt, splits;
     float scale_log2;
 };
 
@@ -143,31 +143,66 @@ __device__ __forceinline__ void mask_srow(SRow& s, const uint32_t (&a)[8], int r
     }
 }
 
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Packed fp32 pair arithmetic (one instruction per two lanes of data on
+// sm_100 and later): (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), and the sum.
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b0, float b1, float c0,
+                                      float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+    asm("{\n\t.reg .b64 a, b, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t"
+        "add.rn.f32x2 d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ float max_srow(const SRow& s) {
-    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
     for (int q = 0; q < 4; ++q)
 #pragma unroll
-        for (int c = 0; c < 32; ++c) m4[c & 3] = fmaxf(m4[c & 3], __uint_as_float(s.c[q][c]));
-    return fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+        for (int c = 0; c < 32; c += 4) {
+            m0 = fmax3(m0, __uint_as_float(s.c[q][c]), __uint_as_float(s.c[q][c + 1]));
+            m1 = fmax3(m1, __uint_as_float(s.c[q][c + 2]), __uint_as_float(s.c[q][c + 3]));
+        }
+    return fmaxf(m0, m1);
 }
 
 // P = exp2(s * sl2 - m), packed to bf16 pairs into the first 64 columns of
-// the S region (the scores are already in registers); row sums into l4.
-__device__ __forceinline__ void exp_store_srow(const SRow& s, uint32_t tS, float sl2, float m,
-                                               float (&l4)[4]) {
+// the S region (the scores are already in registers); returns the row sum.
+// Per pair of scores: one packed FMA, two ex2, one packed add, one convert.
+__device__ __forceinline__ float exp_store_srow(const SRow& s, uint32_t tS, float sl2, float m) {
+    float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint32_t pk[16];
 #pragma unroll
         for (int c2 = 0; c2 < 16; ++c2) {
-            const float e0 = ex2_approx(fmaf(__uint_as_float(s.c[q][2 * c2]), sl2, -m));
-            const float e1 = ex2_approx(fmaf(__uint_as_float(s.c[q][2 * c2 + 1]), sl2, -m));
-            l4[c2 & 3] += e0 + e1;
+            float x0, x1;
+            ffma2(x0, x1, __uint_as_float(s.c[q][2 * c2]), __uint_as_float(s.c[q][2 * c2 + 1]), sl2, sl2, -m, -m);
+            const float e0 = ex2_approx(x0);
+            const float e1 = ex2_approx(x1);
+            if (c2 & 1)
+                fadd2(b0, b1, b0, b1, e0, e1);
+            else
+                fadd2(a0, a1, a0, a1, e0, e1);
             pk[c2] = pack_bf16x2(e0, e1);
         }
         tmem_st16(tS + 16 * q, pk);
     }
+    return (a0 + a1) + (b0 + b1);
 }
 
 // Tile range [t0, t0 + count) of split sp for a unit whose needed keys end
@@ -237,7 +272,7 @@ __device__ __forceinline__ int bt_group(const AttnParams& p, int b, int t0, int 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1)
+__global__ void __maxnreg__(200)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
@@ -335,6 +370,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const int nvalid = min(kTileN, valid_end - slot0);
             const int npg = (nvalid + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
             const int pid = __shfl_sync(0xFFFFFFFFu, bt_cur, ((j & 3) << 3) + (lane & 7));
+            JT_DCHECK(lane >= npg || (pid >= 0 && pid < p.num_pages), p.err);  // block-table entry in the pool
             const uint32_t bytes = npg * SL::kChunks * (JT_PAGE_SIZE * 128);
             // K of tile j: its slot is free once QK^T of tile j-kStages is done
             if (j >= kStages && !mbar_wait_warp(&bars->k_empty[st], empty_parity, p.err, abort)) break;
@@ -435,6 +471,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
         for (int w = 0; w < 8; ++w)
             a[w] = valid_row ? p.anc[static_cast<long long>(off + node) * 8 + w] : 0u;
+#ifdef JT_CHECKS
+        if (valid_row) {  // a node's set holds the node itself and only nodes before it
+            bool ok_set = true;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                const int lo = 32 * w;
+                const uint32_t allowed = node >= lo + 31 ? 0xFFFFFFFFu : (node < lo ? 0u : (2u << (node - lo)) - 1u);
+                if (a[w] & ~allowed) ok_set = false;
+                if (node >= lo && node < lo + 32 && !((a[w] >> (node - lo)) & 1u)) ok_set = false;
+            }
+            JT_DCHECK(ok_set, p.err);
+        }
+#endif
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + 256 * x + lane_off, tO = tS + 128;
         const float sl2 = p.scale_log2;
@@ -465,9 +514,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             // P = exp2(s*scale*log2e - m), written over S (bf16 pairs)
             const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-            float l4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            exp_store_srow(sr, tS, sl2, m_use, l4);
-            l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+            l_run += exp_store_srow(sr, tS, sl2, m_use);
             if (__any_sync(0xFFFFFFFFu, resc)) {
                 // O_X from the earlier tiles, rescaled before PV_X(j) adds to it
                 // (S_X(j) done implies PV_X(j-1) done: O_X is current)
@@ -725,6 +772,7 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
     }
     prm.err = err;
     prm.max_pages = max_pages;
+    prm.num_pages = num_pages;
     prm.nseq = nseq;
     prm.total_nodes = total_nodes;
     prm.Hq = Hq;
