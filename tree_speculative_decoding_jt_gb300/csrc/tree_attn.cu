@@ -186,21 +186,23 @@ __device__ __forceinline__ float max_srow(const SRow& s) {
 __device__ __forceinline__ float exp_store_srow(const SRow& s, uint32_t tS, float sl2, float m) {
     float a0 = 0.0f, a1 = 0.0f, b0 = 0.0f, b1 = 0.0f;
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        uint32_t pk[16];
+    for (int q = 0; q < 8; ++q) {
+        uint32_t pk[8];
 #pragma unroll
-        for (int c2 = 0; c2 < 16; ++c2) {
+        for (int c = 0; c < 8; ++c) {
+            const int c2 = (q & 1) * 8 + c;
             float x0, x1;
-            ffma2(x0, x1, __uint_as_float(s.c[q][2 * c2]), __uint_as_float(s.c[q][2 * c2 + 1]), sl2, sl2, -m, -m);
+            ffma2(x0, x1, __uint_as_float(s.c[q >> 1][2 * c2]), __uint_as_float(s.c[q >> 1][2 * c2 + 1]), sl2, sl2,
+                  -m, -m);
             const float e0 = ex2_approx(x0);
             const float e1 = ex2_approx(x1);
-            if (c2 & 1)
+            if (c & 1)
                 fadd2(b0, b1, b0, b1, e0, e1);
             else
                 fadd2(a0, a1, a0, a1, e0, e1);
-            pk[c2] = pack_bf16x2(e0, e1);
+            pk[c] = pack_bf16x2(e0, e1);
         }
-        tmem_st16(tS + 16 * q, pk);
+        tmem_st8(tS + 8 * q, pk);
     }
     return (a0 + a1) + (b0 + b1);
 }
@@ -272,7 +274,7 @@ __device__ __forceinline__ int bt_group(const AttnParams& p, int b, int t0, int 
 }
 
 template <int D>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kAttnThreads, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                         const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
