@@ -63,11 +63,11 @@ def _small(seed, nseq, Hq, Hkv, D, prefix, budgets, N=6, W=3, dtype="bf16", q_mu
     (6, 2, 16, 8, 128, [64, 257], (48, 90)),       # G = 2
     (7, 2, 64, 8, 128, [100, 50], (20, 40)),       # G = 8
     (8, 2, 32, 8, 64, [500, 33], (77, 12)),        # D = 64
-    (9, 1, 32, 2, 128, [2000], (256,)),            # few KV heads: 9 KV splits
-    (10, 1, 32, 8, 128, [1500], (100,)),           # 6 KV splits, the last one empty
-    (11, 1, 32, 8, 64, [900], (37,)),              # 4 KV splits, D = 64
-    (12, 1, 32, 8, 128, [700], (20,)),             # 3 KV splits, one query tile
-    (13, 1, 32, 8, 128, [7000], (30,)),            # 19 KV splits: three combine batches
+    (9, 1, 32, 2, 128, [2000], (256,)),            # G = 16: 16 query-tile pairs per KV head
+    (10, 1, 32, 8, 128, [1500], (100,)),           # units cut into 1-2 tile pieces across CTAs
+    (11, 1, 32, 8, 64, [900], (37,)),              # the same with D = 64
+    (12, 1, 32, 8, 128, [700], (20,)),             # one query tile per unit (tile B absent)
+    (13, 1, 32, 8, 128, [7000], (30,)),            # each unit merged from ~3 CTAs' partials
 ])
 def test_bf16_matches_oracle_all_nodes(case):
     seed, nseq, Hq, Hkv, D, prefix, budgets = case
@@ -195,6 +195,32 @@ def test_host_side_argument_errors():
         jt.jt_tree_attn_paged(q[:, :, :96].contiguous(), k[..., :96].contiguous(),
                               v[..., :96].contiguous(), bt, pl, off, anc, max_tree=4)
     assert e.value.status == -2
-    with pytest.raises(jt.JtError) as e:   # workspace too small for a KV split
+    with pytest.raises(jt.JtError) as e:   # workspace too small for the plan and the partials
         jt.jt_tree_attn_paged(q, k, v, bt, pl, off, anc, max_tree=4, ws=jt.workspace(256))
     assert e.value.status == -5
+
+
+def test_repeated_calls_on_one_workspace_and_stale_merge_counts():
+    """Units cut across CTAs are merged by the CTA that finishes last, counted
+    in the workspace with the number of the call: repeated calls on one
+    workspace give identical outputs, and counts left behind by an earlier
+    call (planted here: call number 0 with a count of 7) are ignored."""
+    wl = _small(31, 2, 32, 8, 128, [2500, 900], (200, 64))
+    tree = oracle_tree(wl)
+    q, k, v = kv_to_device(wl)
+    args = (q, k, v, dev(wl.block_table), dev(wl.prefix_len), dev(wl.tree_off), dev(tree["anc"].view(np.int32)))
+    ws = jt.workspace(jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, wl.nseq, 0, 0, 0, wl.total, 32, 8, 128,
+                                           wl.block_table.shape[1], 200))
+    outs = []
+    for i in range(4):
+        if i == 2:   # stale counts right after the header
+            cnt = ws[256:256 + 8 * torch.cuda.get_device_properties(0).multi_processor_count].view(torch.int64)
+            cnt.fill_(7)
+        out, lse = jt.jt_tree_attn_paged(*args, scale=wl.scale, max_tree=200, ws=ws)
+        jt.jt_check(ws)
+        outs.append((to_np_bf16(out), lse.cpu().numpy()))
+    for o, l in outs[1:]:
+        assert np.array_equal(o, outs[0][0]) and np.array_equal(l, outs[0][1])
+    want, want_lse = oracle.tree_attn(wl.q, wl.k_cache, wl.v_cache, wl.block_table, wl.prefix_len, wl.tree_off,
+                                      tree["parent"], wl.scale)
+    _check_bf16(outs[0][0], outs[0][1], want, want_lse)

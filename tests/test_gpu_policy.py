@@ -173,7 +173,7 @@ def test_adaptive_build_matches_oracle_over_steps(seed):
 
 
 def test_attention_and_acceptance_over_device_offsets_with_spare_capacity():
-    """The adaptive build's offsets feed jt_tree_attn_paged (bf16, split KV)
+    """The adaptive build's offsets feed jt_tree_attn_paged (bf16, units cut across CTAs)
     and jt_verify_accept with total_nodes = capacity: the trees' rows match
     the oracle and the spare rows past the last tree are never written."""
     nseq, N, W, V = 3, 6, 3, 500

@@ -35,11 +35,9 @@ inline size_t align_up(size_t n) { return (n + kAlign - 1) / kAlign * kAlign; }
 
 // Workspace header (first kAlign bytes of every workspace).
 struct WsHeader {
-    uint32_t err;       // device error flags (DEVERR_*)
-    uint32_t bar_count; // grid barrier arrivals
-    uint32_t bar_gen;   // grid barrier generation
-    uint32_t active[2]; // accept: sequences still walking, per level parity
-    uint32_t pad[3];
+    uint32_t err;                // device error flags (DEVERR_*)
+    uint32_t reserved;
+    unsigned long long tickets;  // attention: CTA arrivals over all calls (call number = tickets / grid)
 };
 constexpr size_t kWsHeader = kAlign;
 
@@ -83,7 +81,8 @@ cudaError_t verify_stochastic_launch(const float* z, const float* zd, const int3
 
 // tree_attn.cu / tree_attn_f32.cu
 struct AttnPlan {
-    int splits;      // KV splits per (sequence, kv head, row tile)
+    int grid;        // CTAs of the bf16 kernel (one per SM; 0 on the fp32 path)
+    int nseq;
     int mtiles;      // row tiles per (sequence, kv head) at max_tree
     int rows_per_tile_nodes;  // tree nodes per 128-row tile (128 / G)
 };

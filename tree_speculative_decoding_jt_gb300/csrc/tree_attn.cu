@@ -9,23 +9,35 @@
 // pages' own kernel (SM90, CuTe DSL, shared-memory mask staging) is prior
 // art; this is a Blackwell design.
 //
-// Work unit (one CTA): sequence b, KV head g, two 128-row query tiles A and
-// B (each = 128/G tree nodes x the G query heads of that KV head: GQA heads
-// share K/V because they are stacked in the MMA's M dimension), and a
-// contiguous range of 128-key tiles of the logical key sequence (prefix +
-// tree tail).  Both query tiles consume every K/V tile, halving the paged TMA
-// traffic per FLOP.  Keys past the last node of tile B are never loaded
-// (ancestors have smaller indices).  Several key ranges of one unit (KV
-// split) are merged by tree_attn_combine_kernel.
+// Work.  A unit is (sequence b, KV head g, query-tile pair mp): two 128-row
+// query tiles A = 2mp and B = 2mp+1 (each = 128/G tree nodes x the G query
+// heads of KV head g, which share K/V because they are stacked in the MMA's
+// M dimension; B is absent when the tree ends inside A) against the 128-key
+// tiles 0..T_u-1 of the sequence's logical keys (prefix + tree through the
+// last node of tile B; ancestors have smaller indices, so no later key is
+// ever visible).  Units are laid end to end in (b, g, mp) order and the
+// T_total key tiles of all units are cut into one equal range of
+// P = ceil(T_total / grid) tiles per CTA, one CTA per SM: every SM gets the
+// same tile count whatever the prefix lengths, so there is no tail wave and
+// no straggler.  A CTA walks the pieces of units in its range; a unit cut
+// by a range boundary leaves fp32 partials (O, running max, sum) from each
+// CTA that holds a piece of it, and the CTA that finishes its piece last
+// merges them (an atomic count per cut unit, tagged with the call's number
+// so that counts left by earlier calls never need clearing; no CTA ever
+// waits for another).  Only the first and the last piece of a CTA can be
+// cut, so two partial slots per CTA suffice.  Each CTA derives the whole
+// plan from prefix_len and tree_off on the device, so sequence lengths never
+// visit the host.
 //
 // Warp roles (320 threads):
 //   warps 0-3 / 4-7  softmax + epilogue of query tile A / B, one query row
 //                    per thread (TMEM lane);
-//   warp 8           TMA producer: both Q tiles once, then per KV tile one
-//                    16-row box per 16-token page for K and for V (128-byte
-//                    swizzle); page ids are held in registers, loaded two
-//                    groups of four tiles ahead; zero-fills V rows past the
-//                    last needed slot of the final tile;
+//   warp 8           planner, then TMA producer: per piece the Q tiles, then
+//                    per KV tile one 16-row box per 16-token page for K and
+//                    for V (128-byte swizzle); page ids are held in
+//                    registers, loaded two groups of four tiles ahead; zero-
+//                    fills V rows past the last needed slot of a unit's
+//                    final tile;
 //   warp 9           TMEM allocator and single-thread MMA issuer.
 // TMEM (512 columns): per query tile X, S_X (128 fp32 columns) and O_X (D
 // fp32 columns).  Per KV tile j: S_X = Q_X K^T (SS MMA, K-major operands,
@@ -36,6 +48,9 @@
 // softmax B works and the other way round.  MMAs from one thread execute in
 // issue order, so QK_X(j+1) overwrites S_X only after PV_X(j) has read P_X,
 // and the completion of QK_X(j+1) tells softmax X that O_X holds PV_X(j).
+// Across pieces the barrier phases run on (global tile and piece counters);
+// the next piece's first PV_X overwrites O_X only after softmax X has read
+// it out, because softmax X reads O_X before it releases that PV.
 // Online softmax in the log2 domain, two passes over S in TMEM (row max,
 // then exp and P), lazy rescaling of O (only when the running max grows by
 // more than 2^8).  All waits are bounded in time.
@@ -49,7 +64,7 @@ constexpr int kStages = 2;   // K ring and V ring depth
 constexpr int kTileN = 128;  // keys per KV tile
 constexpr int kTileM = 128;  // query rows per query tile
 constexpr float kRescaleLog2 = 8.0f;
-constexpr int kMaxSplits = 32;
+constexpr int kMaxMergeIn = 4;  // other pieces whose (m, l) a merging row loads in one batch
 
 struct AttnParams {
     const int32_t* block_table;
@@ -58,10 +73,13 @@ struct AttnParams {
     const uint32_t* anc;
     __nv_bfloat16* out;
     float* lse;
-    float* part_o;   // [total*Hq*splits, D] when splits > 1
-    float2* part_ml; // [total*Hq*splits]: running max (log2 units), sum
+    float* part_o;    // [2 * grid][2][128][D]: partial O of the pieces of cut units
+    float2* part_ml;  // [2 * grid][2][128]: their running max (log2 units) and sum
+    int* plan;        // [2 + nseq + 1]: T_total, P, then each sequence's first global tile
+    unsigned long long* tickets;    // CTA arrivals over all calls (workspace header)
+    unsigned long long* merge_cnt;  // [grid]: (call number << 32) | pieces done, per cut unit
     uint32_t* err;
-    int max_pages, num_pages, nseq, total_nodes, Hq, G, npt, splits;
+    int max_pages, num_pages, nseq, total_nodes, Hq, Hkv, G, npt;
     float scale_log2;
 };
 
@@ -73,25 +91,251 @@ struct SmemLayout {
     static constexpr int kQ = 0;                      // Q_A, Q_B
     static constexpr int kK = kQ + 2 * kTileBytes;
     static constexpr int kV = kK + kStages * kTileBytes;
-    static constexpr int kBar = kV + kStages * kTileBytes;
-    static constexpr int kBytes = kBar + 256;
+    static constexpr int kStage = kV + kStages * kTileBytes;  // epilogue staging, 4 KB per softmax warp
+    static constexpr int kBar = kStage + 8 * 4096;
+    static constexpr int kBytes = kBar + 512;
     static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
 };
 
 struct Bars {
     uint64_t q_full;
+    uint64_t q_empty;
     uint64_t k_full[kStages];
     uint64_t v_full[kStages];
     uint64_t k_empty[kStages];
     uint64_t v_empty[kStages];
+    uint64_t v_last[kStages];
     uint64_t s_full[2];
     uint64_t p_full[2];
     uint64_t o_final[2];
-    uint64_t v_last;
     uint64_t mma_final;
     uint32_t tmem_base;
     int abort;
+    // the CTA's start position, published by the planner
+    int w_b, w_g, w_mp, w_t, w_quota, w_P;
+    uint32_t call_id;  // this call's number (+1) on this workspace
+    int merge_flag;    // this CTA finished the last piece of a cut unit
 };
+
+// ---------------------------------------------------------------------------
+// The work plan (shared by the main kernel's roles and the combine)
+// ---------------------------------------------------------------------------
+struct SeqInfo {
+    int L, B, off;
+    int np;  // query-tile pairs (0: no tree, or contents out of range)
+};
+
+__device__ __forceinline__ SeqInfo load_seq(const AttnParams& p, int b) {
+    SeqInfo s;
+    s.off = p.tree_off[b];
+    s.B = p.tree_off[b + 1] - s.off;
+    s.L = p.prefix_len[b];
+    const bool ok = s.B >= 0 && s.B <= JT_MAX_TREE && s.L >= 0 && s.off >= 0 && s.off + s.B <= p.total_nodes &&
+                    static_cast<long long>(s.L) + s.B <= static_cast<long long>(p.max_pages) * JT_PAGE_SIZE;
+    s.np = ok ? ((s.B + p.npt - 1) / p.npt + 1) / 2 : (s.B == 0 ? 0 : -1);
+    return s;
+}
+
+// Keys needed by pair mp: through the last node of its second tile.
+__device__ __forceinline__ int unit_end(const SeqInfo& s, int mp, int npt) {
+    return s.L + min(s.B, (2 * mp + 2) * npt);
+}
+__device__ __forceinline__ int unit_tiles(const SeqInfo& s, int mp, int npt) {
+    return (unit_end(s, mp, npt) + kTileN - 1) / kTileN;
+}
+// Key tiles of all pairs of one KV head.
+__device__ __forceinline__ int head_tiles(const SeqInfo& s, int npt) {
+    int t = 0;
+    for (int mp = 0; mp < s.np; ++mp) t += unit_tiles(s, mp, npt);
+    return t;
+}
+
+// One piece: key tiles [t0, t0 + nt) of unit (b, g, mp), which has T tiles.
+// slot: the partial slot the piece writes, or -1 when it is the whole unit.
+struct Piece {
+    SeqInfo s;
+    int b, g, mp, t0, nt, T, slot;
+    int gpos;  // global tile index of the piece's first tile
+};
+
+// Walks the pieces of this CTA's tile range in order.  Every role runs its
+// own copy over the same start position, so all roles see the same pieces.
+struct Walker {
+    SeqInfo s;
+    int b, g, mp, t, remaining, piece, gpos;
+
+    __device__ __forceinline__ void init(const AttnParams& p, const Bars* bars) {
+        b = bars->w_b;
+        g = bars->w_g;
+        mp = bars->w_mp;
+        t = bars->w_t;
+        remaining = bars->w_quota;
+        gpos = static_cast<int>(blockIdx.x) * bars->w_P;
+        piece = 0;
+        if (remaining > 0) s = load_seq(p, b);
+    }
+
+    __device__ __forceinline__ bool next(const AttnParams& p, Piece& pc) {
+        if (remaining <= 0) return false;
+        const int T = unit_tiles(s, mp, p.npt);
+        const int nt = min(T - t, remaining);
+        pc.s = s;
+        pc.b = b;
+        pc.g = g;
+        pc.mp = mp;
+        pc.t0 = t;
+        pc.nt = nt;
+        pc.T = T;
+        pc.slot = (t == 0 && nt == T) ? -1 : 2 * static_cast<int>(blockIdx.x) + (piece == 0 ? 0 : 1);
+        pc.gpos = gpos;
+        gpos += nt;
+        remaining -= nt;
+        t += nt;
+        ++piece;
+        if (t == T && remaining > 0) {  // on to the next unit in (b, g, mp) order
+            t = 0;
+            if (++mp >= s.np) {
+                mp = 0;
+                if (++g >= p.Hkv) {
+                    g = 0;
+                    do {
+                        ++b;
+                        s = load_seq(p, b);
+                    } while (s.np <= 0 && b + 1 < p.nseq);
+                }
+            }
+        }
+        return true;
+    }
+};
+
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+// The planner (one warp): the total tile count, this CTA's range and the
+// unit and tile its range starts at.  CTA 0 also records the plan for the
+// combine (T_total, P and each sequence's first global tile) and reports
+// sequences whose offsets or lengths are out of range.
+__device__ void plan_cta(const AttnParams& p, Bars* bars, int lane) {
+    const int H = p.Hkv;
+    const bool rec = blockIdx.x == 0;
+    long long total = 0;
+    for (int base = 0; base < p.nseq; base += 32) {
+        const int b = base + lane;
+        int t = 0;
+        if (b < p.nseq) {
+            const SeqInfo s = load_seq(p, b);
+            if (s.np < 0) {
+                if (rec) raise_error(p.err, DEVERR_INVALID);
+            } else {
+                t = H * head_tiles(s, p.npt);
+            }
+        }
+        total += warp_sum(t);
+    }
+    if (total > 0x7FFFFFFFll) {  // beyond the int tile arithmetic: refuse the launch's work
+        if (rec && lane == 0) raise_error(p.err, DEVERR_INVALID);
+        total = 0;
+    }
+    const int T_total = static_cast<int>(total);
+    const int P = T_total > 0 ? (T_total + gridDim.x - 1) / gridDim.x : 0;
+    const long long start = static_cast<long long>(blockIdx.x) * P;
+    int quota = (start < T_total) ? static_cast<int>(min(static_cast<long long>(P), T_total - start)) : 0;
+    if (rec && lane == 0) {
+        p.plan[0] = T_total;
+        p.plan[1] = P;
+    }
+    // second pass: the sequence holding tile `start` (and, on CTA 0, every
+    // sequence's first global tile)
+    int found_b = -1, found_rel = 0;
+    int acc = 0;
+    for (int base = 0; base < p.nseq && (rec || found_b < 0); base += 32) {
+        const int b = base + lane;
+        int t = 0;
+        if (b < p.nseq) {
+            const SeqInfo s = load_seq(p, b);
+            if (s.np > 0) t = H * head_tiles(s, p.npt);
+        }
+        int incl = t;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += u;
+        }
+        const int excl = acc + incl - t;
+        if (rec && b < p.nseq) p.plan[2 + b] = excl;
+        const bool here = t > 0 && start >= excl && start < excl + t;
+        const unsigned m = __ballot_sync(0xFFFFFFFFu, here);
+        if (m && found_b < 0) {
+            const int src = __ffs(m) - 1;
+            found_b = base + src;
+            found_rel = static_cast<int>(start) - __shfl_sync(0xFFFFFFFFu, excl, src);
+        }
+        acc += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+    if (rec && lane == 0) p.plan[2 + p.nseq] = acc;
+    if (found_b < 0) quota = 0;
+    if (lane == 0) {
+        int g = 0, mp = 0, t = 0;
+        if (quota > 0) {
+            const SeqInfo s = load_seq(p, found_b);
+            const int ht = head_tiles(s, p.npt);
+            g = found_rel / ht;
+            int r = found_rel - g * ht;
+            while (mp < s.np - 1 && r >= unit_tiles(s, mp, p.npt)) {
+                r -= unit_tiles(s, mp, p.npt);
+                ++mp;
+            }
+            t = r;
+        }
+        bars->w_b = found_b;
+        bars->w_g = g;
+        bars->w_mp = mp;
+        bars->w_t = t;
+        bars->w_quota = quota;
+        bars->w_P = P;
+    }
+}
+
+// The CTAs holding the pieces of the unit that starts at global tile U and
+// has T tiles (range length P): c0 .. c0 + n - 1; slot of piece k.
+struct CutUnit {
+    int c0, n, slot0;
+    __device__ __forceinline__ CutUnit(int U, int T, int P) {
+        c0 = U / P;
+        n = (U + T - 1) / P - c0 + 1;
+        slot0 = 2 * c0 + (U == c0 * P ? 0 : 1);
+    }
+    __device__ __forceinline__ int slot(int k) const { return k == 0 ? slot0 : 2 * (c0 + k); }
+};
+
+__device__ __forceinline__ void named_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Stage this warp's 32 rows' 128-byte pieces (slot[8] = this thread's row)
+// through shared memory (16-byte slots XOR-swizzled by row: conflict-free
+// both ways) and store each row's piece as one full line: dst(rr) gives the
+// destination of staged row rr (nullptr: skip).
+template <typename Dst>
+__device__ __forceinline__ void stage_store(uint8_t* stage, int lane, const uint4 (&slot)[8], Dst dst) {
+    uint4* my_row = reinterpret_cast<uint4*>(stage + lane * 128);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) my_row[c ^ (lane & 7)] = slot[c];
+    __syncwarp();
+    const int sub = lane & 7;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + (lane >> 3);  // staged row this lane copies
+        const uint4 val = reinterpret_cast<const uint4*>(stage + rr * 128)[sub ^ (rr & 7)];
+        uint4* d = dst(rr);
+        if (d) d[sub] = val;
+    }
+    __syncwarp();  // the next piece overwrites the stage
+}
 
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
@@ -207,22 +451,6 @@ __device__ __forceinline__ float exp_store_srow(const SRow& s, uint32_t tS, floa
     return (a0 + a1) + (b0 + b1);
 }
 
-// Tile range [t0, t0 + count) of split sp for a unit whose needed keys end
-// at valid_end; returns the count.
-__device__ __forceinline__ int split_range(int valid_end, int splits, int sp, int& t0) {
-    const int T = (valid_end + kTileN - 1) / kTileN;
-    const int tps = (T + splits - 1) / splits;
-    t0 = sp * tps;
-    const int t1 = min(T, t0 + tps);
-    return max(0, t1 - t0);
-}
-
-// Keys needed by the unit of query-tile pair mp: through the last node of
-// its second tile.
-__device__ __forceinline__ int unit_valid_end(int L, int B, int mp, int npt) {
-    return L + min(B, (2 * mp + 2) * npt);
-}
-
 // Operand descriptors are built once (dq: Q tile, dk / dv: K / V stage) and
 // stepped by adding the byte offset / 16 to the start-address field (the
 // field cannot carry: shared memory addresses stay below 256 KB).  The whole
@@ -262,14 +490,13 @@ __device__ __forceinline__ void commit_warp(uint64_t* bar) {
     __syncwarp();
 }
 
-// Page ids of 4 consecutive tiles (group g4): lane l holds page l%8 of tile
-// 4*g4 + l/8 of the unit.
-__device__ __forceinline__ int bt_group(const AttnParams& p, int b, int t0, int nt, int valid_end,
-                                        int g4, int lane) {
+// Page ids of 4 consecutive tiles (group g4) of a piece: lane l holds page
+// l%8 of tile 4*g4 + l/8 of the piece.
+__device__ __forceinline__ int bt_group(const AttnParams& p, const Piece& pc, int valid_end, int g4, int lane) {
     const int tile = 4 * g4 + (lane >> 3);
-    const int slot = (t0 + tile) * kTileN + (lane & 7) * JT_PAGE_SIZE;
-    return (tile < nt && slot < valid_end)
-               ? p.block_table[static_cast<long long>(b) * p.max_pages + slot / JT_PAGE_SIZE]
+    const int slot = (pc.t0 + tile) * kTileN + (lane & 7) * JT_PAGE_SIZE;
+    return (tile < pc.nt && slot < valid_end)
+               ? p.block_table[static_cast<long long>(pc.b) * p.max_pages + slot / JT_PAGE_SIZE]
                : 0;
 }
 
@@ -286,25 +513,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     Bars* bars = reinterpret_cast<Bars*>(smem + SL::kBar);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.z, g = blockIdx.y;
-    const int mp = blockIdx.x / p.splits, sp = blockIdx.x % p.splits;
     // Set-up that reads no global memory (barriers, TMEM, tensor-map
     // prefetch) runs before the wait for the previous kernel, overlapping
     // its tail when this grid is launched as its programmatic dependent.
     if (tid == 0) {
         mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
             mbar_init(&bars->v_full[s], 1);
             mbar_init(&bars->k_empty[s], 1);
             mbar_init(&bars->v_empty[s], 1);
+            mbar_init(&bars->v_last[s], 1);
         }
         for (int x = 0; x < 2; ++x) {
             mbar_init(&bars->s_full[x], 1);
             mbar_init(&bars->p_full[x], 128);
             mbar_init(&bars->o_final[x], 1);
         }
-        mbar_init(&bars->v_last, 1);
         mbar_init(&bars->mma_final, 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -315,29 +541,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tma_prefetch_desc(&tm_v);
     }
     if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
+    pdl_wait();  // no global memory is read before the previous kernel's writes are visible
+    if (warp == 8) plan_cta(p, bars, lane);
+    if (tid == 0)  // every CTA of a call draws one ticket before anything can fail
+        bars->call_id = static_cast<uint32_t>(atomicAdd(p.tickets, 1ull) / gridDim.x) + 1u;
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
     volatile int* abort = &bars->abort;
-
-    pdl_wait();  // no global memory is read before the previous kernel's writes are visible
-    const int off = p.tree_off[b];
-    const int B = p.tree_off[b + 1] - off;
-    const int L = p.prefix_len[b];
-    const int m0 = 2 * mp;                    // query tile A; tile B = m0 + 1
-    bool run = m0 * p.npt < B;                // else the pair lies past this sequence's tree
-    if (run && (B > JT_MAX_TREE || L < 0 || off < 0 || off + B > p.total_nodes ||
-                static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE)) {
-        if (tid == 0) raise_error(p.err, DEVERR_INVALID);
-        run = false;
-    }
-    const bool hasB = (m0 + 1) * p.npt < B;
-    const int n_end = min(B, (m0 + 2) * p.npt);
-    const int valid_end = L + n_end;
-    int t0 = 0;
-    const int nt = run ? split_range(valid_end, p.splits, sp, t0) : 0;
-    if (nt == 0) {  // nothing to do (or an empty split, which the combine skips too)
+    if (bars->w_quota <= 0) {  // no tiles for this CTA
         if (warp == 9) tmem_dealloc(tmem, 512);  // no tcgen05 operation was issued
         return;
     }
@@ -345,227 +558,291 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* sQ = smem + SL::kQ;
     uint8_t* sK = smem + SL::kK;
     uint8_t* sV = smem + SL::kV;
+    const int npt = p.npt;
 
     if (warp == 8) {
         // ------------------------------------------------------------ TMA
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&bars->q_full, (hasB ? 2 : 1) * kTileBytes);
-            for (int x = 0; x < (hasB ? 2 : 1); ++x)
-                for (int c = 0; c < SL::kChunks; ++c)
-                    tma_load_3d(sQ + x * kTileBytes + c * SL::kChunkBytes, &tm_q, &bars->q_full,
-                                c * 64, g * p.G, off + (m0 + x) * p.npt);
-        }
-        // page ids held in registers, loaded two groups of four tiles ahead
-        int bt_cur = bt_group(p, b, t0, nt, valid_end, 0, lane);
-        int bt_nxt = bt_group(p, b, t0, nt, valid_end, 1, lane);
-        int bt_nn = bt_group(p, b, t0, nt, valid_end, 2, lane);
-        int issued = 0;
-        for (int j = 0; j < nt; ++j) {
-            const int st = j % kStages;
-            const uint32_t empty_parity = ((j / kStages) & 1) ^ 1;
-            if (j > 0 && (j & 3) == 0) {
-                bt_cur = bt_nxt;
-                bt_nxt = bt_nn;
-                bt_nn = bt_group(p, b, t0, nt, valid_end, (j >> 2) + 2, lane);
+        Walker w;
+        w.init(p, bars);
+        Piece pc;
+        int jj = 0, npc = 0, q_pending = 0;
+        int k_iss = 0, v_iss = 0;  // K / V tiles whose copies have been issued
+        int vl[kStages] = {0, 0};
+        while (!*abort && w.next(p, pc)) {
+            const bool hasB = (2 * pc.mp + 1) * npt < pc.s.B;
+            const int valid_end = unit_end(pc.s, pc.mp, npt);
+            // Q of this piece: the Q tiles are free once every QK of the
+            // previous piece has completed
+            if (npc > 0 && !mbar_wait_warp(&bars->q_empty, (npc - 1) & 1, p.err, abort)) break;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&bars->q_full, (hasB ? 2 : 1) * kTileBytes);
+                for (int x = 0; x < (hasB ? 2 : 1); ++x)
+                    for (int c = 0; c < SL::kChunks; ++c)
+                        tma_load_3d(sQ + x * kTileBytes + c * SL::kChunkBytes, &tm_q, &bars->q_full, c * 64,
+                                    pc.g * p.G, pc.s.off + (2 * pc.mp + x) * npt);
             }
-            const int slot0 = (t0 + j) * kTileN;
-            const int nvalid = min(kTileN, valid_end - slot0);
-            const int npg = (nvalid + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
-            const int pid = __shfl_sync(0xFFFFFFFFu, bt_cur, ((j & 3) << 3) + (lane & 7));
-            JT_DCHECK(lane >= npg || (pid >= 0 && pid < p.num_pages), p.err);  // block-table entry in the pool
-            const uint32_t bytes = npg * SL::kChunks * (JT_PAGE_SIZE * 128);
-            // K of tile j: its slot is free once QK^T of tile j-kStages is done
-            if (j >= kStages && !mbar_wait_warp(&bars->k_empty[st], empty_parity, p.err, abort)) break;
-            if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], bytes);
-            __syncwarp();
-            if (lane < npg)
-                for (int c = 0; c < SL::kChunks; ++c)
-                    tma_load_4d(sK + st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128),
-                                &tm_k, &bars->k_full[st], c * 64, g, 0, pid);
-            // V of tile j: free once PV of tile j-kStages is done
-            if (j >= kStages && !mbar_wait_warp(&bars->v_empty[st], empty_parity, p.err, abort)) break;
-            if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], bytes);
-            __syncwarp();
-            if (lane < npg)
-                for (int c = 0; c < SL::kChunks; ++c)
-                    tma_load_4d(sV + st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128),
-                                &tm_v, &bars->v_full[st], c * 64, g, 0, pid);
-            issued = j + 1;
-            if (j == nt - 1) {
-                // final tile: once its V has landed, zero rows past the last
-                // needed slot (stale or foreign data; P is 0 there but
-                // 0 * NaN would not be), then release it to the MMA warp
-                if (!mbar_wait_warp(&bars->v_full[st], (j / kStages) & 1, p.err, abort)) break;
-                uint8_t* vt = sV + st * kTileBytes;
-                const int n16 = (kTileN - nvalid) * 8;  // 16-byte pieces per column block
-                for (int c = 0; c < SL::kChunks; ++c)
-                    for (int idx = lane; idx < n16; idx += 32)
-                        reinterpret_cast<uint4*>(vt + c * SL::kChunkBytes + (nvalid + (idx >> 3)) * 128)[idx & 7] =
-                            make_uint4(0u, 0u, 0u, 0u);
-                fence_proxy_async_smem();
+            q_pending = npc + 1;
+            // page ids held in registers, loaded two groups of four tiles ahead
+            int bt_cur = bt_group(p, pc, valid_end, 0, lane);
+            int bt_nxt = bt_group(p, pc, valid_end, 1, lane);
+            int bt_nn = bt_group(p, pc, valid_end, 2, lane);
+            bool ok = true;
+            for (int j = 0; j < pc.nt; ++j, ++jj) {
+                const int st = jj % kStages;
+                const uint32_t empty_parity = ((jj / kStages) & 1) ^ 1;
+                if (j > 0 && (j & 3) == 0) {
+                    bt_cur = bt_nxt;
+                    bt_nxt = bt_nn;
+                    bt_nn = bt_group(p, pc, valid_end, (j >> 2) + 2, lane);
+                }
+                const int slot0 = (pc.t0 + j) * kTileN;
+                const int nvalid = min(kTileN, valid_end - slot0);
+                const int npg = (nvalid + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
+                const int pid = __shfl_sync(0xFFFFFFFFu, bt_cur, ((j & 3) << 3) + (lane & 7));
+                JT_DCHECK(lane >= npg || (pid >= 0 && pid < p.num_pages), p.err);  // block-table entry in the pool
+                const uint32_t bytes = npg * SL::kChunks * (JT_PAGE_SIZE * 128);
+                // K of tile jj: its slot is free once QK^T of tile jj-kStages is done
+                if (jj >= kStages && !mbar_wait_warp(&bars->k_empty[st], empty_parity, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&bars->k_full[st], bytes);
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bars->v_last);
+                if (lane < npg)
+                    for (int c = 0; c < SL::kChunks; ++c)
+                        tma_load_4d(sK + st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128),
+                                    &tm_k, &bars->k_full[st], c * 64, pc.g, 0, pid);
+                k_iss = jj + 1;
+                // V of tile jj: free once PV of tile jj-kStages is done
+                if (jj >= kStages && !mbar_wait_warp(&bars->v_empty[st], empty_parity, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+                __syncwarp();
+                if (lane < npg)
+                    for (int c = 0; c < SL::kChunks; ++c)
+                        tma_load_4d(sV + st * kTileBytes + c * SL::kChunkBytes + lane * (JT_PAGE_SIZE * 128),
+                                    &tm_v, &bars->v_full[st], c * 64, pc.g, 0, pid);
+                v_iss = jj + 1;
+                if (pc.t0 + j == pc.T - 1) {
+                    // the unit's final tile: once its V has landed, zero the
+                    // rows past the last needed slot (stale or foreign data;
+                    // P is 0 there but 0 * NaN would not be), then release
+                    // it to the MMA warp
+                    if (!mbar_wait_warp(&bars->v_full[st], (jj / kStages) & 1, p.err, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* vt = sV + st * kTileBytes;
+                    const int n16 = (kTileN - nvalid) * 8;  // 16-byte pieces per column block
+                    for (int c = 0; c < SL::kChunks; ++c)
+                        for (int idx = lane; idx < n16; idx += 32)
+                            reinterpret_cast<uint4*>(vt + c * SL::kChunkBytes + (nvalid + (idx >> 3)) * 128)[idx & 7] =
+                                make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bars->v_last[st]);
+                    ++vl[st];
+                }
             }
+            if (!ok) break;
+            ++npc;
         }
         // on abort: let copies already in flight land before the CTA exits
         if (*abort) {
-            for (int j = max(0, issued - kStages); j < issued; ++j) {
+            for (int j = max(0, k_iss - kStages); j < k_iss; ++j)
                 mbar_wait(&bars->k_full[j % kStages], (j / kStages) & 1, p.err, nullptr);
+            for (int j = max(0, v_iss - kStages); j < v_iss; ++j)
                 mbar_wait(&bars->v_full[j % kStages], (j / kStages) & 1, p.err, nullptr);
-            }
+            if (q_pending > 0) mbar_wait(&bars->q_full, (q_pending - 1) & 1, p.err, nullptr);
         }
     } else if (warp == 9) {
         // ------------------------------------------------------------ MMA
         // the whole warp runs this loop (uniform control flow, operands in
         // uniform registers); one elected lane issues every tcgen05 op
-        using SLm = SmemLayout<D>;
         const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
         const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
-        const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), SLm::kChunkBytes, 1024);
-        constexpr uint32_t kTileStep = SLm::kTileBytes >> 4;  // one tile / stage in 16-byte units
-        const int nx = hasB ? 2 : 1;
-        bool ok = mbar_wait_warp(&bars->q_full, 0, p.err, abort) &&
-                  mbar_wait_warp(&bars->k_full[0], 0, p.err, abort);
-        if (ok) {
+        const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), SL::kChunkBytes, 1024);
+        constexpr uint32_t kTileStep = SL::kTileBytes >> 4;  // one tile / stage in 16-byte units
+        Walker w;
+        w.init(p, bars);
+        Piece pc;
+        int jj = 0, npc = 0;
+        int cnt[2] = {0, 0};  // tiles handed to each query tile's softmax so far
+        int vl[kStages] = {0, 0};
+        bool ok = true;
+        while (ok && w.next(p, pc)) {
+            const int nx = ((2 * pc.mp + 1) * npt < pc.s.B) ? 2 : 1;
+            ok = mbar_wait_warp(&bars->q_full, npc & 1, p.err, abort) &&
+                 mbar_wait_warp(&bars->k_full[jj % kStages], (jj / kStages) & 1, p.err, abort);
+            if (!ok) break;
             tc_fence_after();
             for (int x = 0; x < nx; ++x) {
-                issue_qk<D>(tmem + 256 * x, dq0 + x * kTileStep, dk0);
+                issue_qk<D>(tmem + 256 * x, dq0 + x * kTileStep, dk0 + (jj % kStages) * kTileStep);
                 commit_warp(&bars->s_full[x]);
             }
-            commit_warp(&bars->k_empty[0]);
-        }
-        for (int j = 0; ok && j < nt; ++j) {
-            const int st = j % kStages;
-            const bool more = j + 1 < nt;
-            for (int x = 0; ok && x < nx; ++x) {
-                ok = mbar_wait_warp(&bars->p_full[x], j & 1, p.err, abort);
-                if (ok && x == 0)
-                    ok = (j == nt - 1) ? mbar_wait_warp(&bars->v_last, 0, p.err, abort)
-                                       : mbar_wait_warp(&bars->v_full[st], (j / kStages) & 1, p.err, abort);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv<D>(tmem + 256 * x, dv0 + st * kTileStep, j > 0);
-                if (x == nx - 1) commit_warp(&bars->v_empty[st]);
-                if (!more) {
-                    commit_warp(&bars->o_final[x]);
-                } else {
-                    if (x == 0) ok = mbar_wait_warp(&bars->k_full[(j + 1) % kStages],
-                                                    ((j + 1) / kStages) & 1, p.err, abort);
+            commit_warp(&bars->k_empty[jj % kStages]);
+            if (pc.nt == 1) commit_warp(&bars->q_empty);  // the piece's last QK is issued
+            for (int j = 0; ok && j < pc.nt; ++j, ++jj) {
+                const int st = jj % kStages;
+                const bool more = j + 1 < pc.nt;
+                const bool unit_final = pc.t0 + j == pc.T - 1;
+                for (int x = 0; ok && x < nx; ++x) {
+                    ok = mbar_wait_warp(&bars->p_full[x], cnt[x] & 1, p.err, abort);
+                    if (ok && x == 0)
+                        ok = unit_final ? mbar_wait_warp(&bars->v_last[st], vl[st] & 1, p.err, abort)
+                                        : mbar_wait_warp(&bars->v_full[st], (jj / kStages) & 1, p.err, abort);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_qk<D>(tmem + 256 * x, dq0 + x * kTileStep, dk0 + ((j + 1) % kStages) * kTileStep);
-                    commit_warp(&bars->s_full[x]);
-                    if (x == nx - 1) commit_warp(&bars->k_empty[(j + 1) % kStages]);
+                    issue_pv<D>(tmem + 256 * x, dv0 + st * kTileStep, j > 0);
+                    if (x == nx - 1) commit_warp(&bars->v_empty[st]);
+                    if (!more) {
+                        commit_warp(&bars->o_final[x]);
+                    } else {
+                        const int st1 = (jj + 1) % kStages;
+                        if (x == 0) ok = mbar_wait_warp(&bars->k_full[st1], ((jj + 1) / kStages) & 1, p.err, abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_qk<D>(tmem + 256 * x, dq0 + x * kTileStep, dk0 + st1 * kTileStep);
+                        commit_warp(&bars->s_full[x]);
+                        if (x == nx - 1) commit_warp(&bars->k_empty[st1]);
+                    }
+                    ++cnt[x];
                 }
+                if (unit_final) ++vl[st];
+                if (ok && j == pc.nt - 2) commit_warp(&bars->q_empty);  // the piece's last QK is issued
             }
+            ++npc;
         }
         // every MMA issued above completes before TMEM is released
         commit_warp(&bars->mma_final);
         mbar_wait_warp(&bars->mma_final, 0, p.err, nullptr);
-    } else if (warp < 4 || hasB) {
+    } else {
         // ---------------------------------------------- softmax of tile X
         const int x = warp >> 2;
         const int r = tid & 127;  // query row = TMEM lane
-        const int node = (m0 + x) * p.npt + r / p.G;
-        const int head = g * p.G + r % p.G;
-        const bool valid_row = node < n_end;
-        uint32_t a[8];
-#pragma unroll
-        for (int w = 0; w < 8; ++w)
-            a[w] = valid_row ? p.anc[static_cast<long long>(off + node) * 8 + w] : 0u;
-#ifdef JT_CHECKS
-        if (valid_row) {  // a node's set holds the node itself and only nodes before it
-            bool ok_set = true;
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const int lo = 32 * w;
-                const uint32_t allowed = node >= lo + 31 ? 0xFFFFFFFFu : (node < lo ? 0u : (2u << (node - lo)) - 1u);
-                if (a[w] & ~allowed) ok_set = false;
-                if (node >= lo && node < lo + 32 && !((a[w] >> (node - lo)) & 1u)) ok_set = false;
-            }
-            JT_DCHECK(ok_set, p.err);
-        }
-#endif
         const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + 256 * x + lane_off, tO = tS + 128;
         const float sl2 = p.scale_log2;
-        float m_run = -INFINITY, l_run = 0.0f;
+        uint8_t* stage = smem + SL::kStage + warp * 4096;
+        Walker w;
+        w.init(p, bars);
+        Piece pc;
+        int cnt = 0, nfin = 0;
         bool ok = true;
-        for (int j = 0; j < nt && ok; ++j) {
-            if (!mbar_wait_warp(&bars->s_full[x], j & 1, p.err, abort)) { ok = false; break; }
-            tc_fence_after();
-            const int slot0 = (t0 + j) * kTileN;
-            const bool tail = slot0 + kTileN > L;
-            SRow sr;
-            load_srow(tS, sr);
-            if (tail) mask_srow(sr, a, slot0 - L);  // tiles inside the prefix need no mask
-            const float mx = max_srow(sr);
-            const float mx_s = mx * sl2;
-            bool resc = false;
-            float factor = 1.0f;
-            if (mx_s > m_run + kRescaleLog2 || m_run == -INFINITY) {
-                const float m_new = fmaxf(m_run, mx_s);
-                if (m_run != -INFINITY) {
-                    factor = ex2_approx(m_run - m_new);
-                    resc = j > 0;
-                } else {
-                    factor = 0.0f;
-                }
-                l_run *= factor;
-                m_run = m_new;
-            }
-            // P = exp2(s*scale*log2e - m), written over S (bf16 pairs)
-            const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
-            l_run += exp_store_srow(sr, tS, sl2, m_use);
-            if (__any_sync(0xFFFFFFFFu, resc)) {
-                // O_X from the earlier tiles, rescaled before PV_X(j) adds to it
-                // (S_X(j) done implies PV_X(j-1) done: O_X is current)
-#pragma unroll 1
-                for (int q = 0; q < D / 32; ++q) {
-                    uint32_t v[32];
-                    tmem_ld32(tO + q * 32, v);
-                    tmem_wait_ld();
+        while (ok && w.next(p, pc)) {
+            if (x == 1 && (2 * pc.mp + 1) * npt >= pc.s.B) continue;  // tile B absent from this unit
+            const int L = pc.s.L;
+            const int n_end = min(pc.s.B, (2 * pc.mp + 2) * npt);
+            const int node = (2 * pc.mp + x) * npt + r / p.G;
+            const int head = pc.g * p.G + r % p.G;
+            const bool valid_row = node < n_end;
+            uint32_t a[8];
 #pragma unroll
-                    for (int c = 0; c < 32; ++c)
-                        v[c] = __float_as_uint(__uint_as_float(v[c]) * (resc ? factor : 1.0f));
-                    tmem_st32(tO + q * 32, v);
+            for (int k = 0; k < 8; ++k)
+                a[k] = valid_row ? p.anc[static_cast<long long>(pc.s.off + node) * 8 + k] : 0u;
+#ifdef JT_CHECKS
+            if (valid_row) {  // a node's set holds the node itself and only nodes before it
+                bool ok_set = true;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int lo = 32 * k;
+                    const uint32_t allowed =
+                        node >= lo + 31 ? 0xFFFFFFFFu : (node < lo ? 0u : (2u << (node - lo)) - 1u);
+                    if (a[k] & ~allowed) ok_set = false;
+                    if (node >= lo && node < lo + 32 && !((a[k] >> (node - lo)) & 1u)) ok_set = false;
                 }
+                JT_DCHECK(ok_set, p.err);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(&bars->p_full[x]);
-        }
-        // epilogue (the split combine may be scheduled; it waits for this grid)
-        pdl_trigger();
-        if (ok && mbar_wait_warp(&bars->o_final[x], 0, p.err, abort)) {
-            tc_fence_after();
-            const long long rowid = static_cast<long long>(off + node) * p.Hq + head;
-            const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-            // Every QK_X MMA completed before o_final[X], so the Q_X tile is
-            // free: each warp stages its 32 rows there, one 128-byte piece
-            // of each row at a time (16-byte slots XOR-swizzled by row, so
-            // both the row-wise writes and the line-wise reads are free of
-            // bank conflicts), and 8 lanes then store each row's piece as
-            // one full 128-byte line.
-            uint8_t* stage = sQ + x * kTileBytes + (warp & 3) * 4096;
-            const int sub = lane & 7;  // 16-byte slot of the piece
-            const bool piece_f32 = p.splits > 1;
-            constexpr int kPiecesF32 = D / 32, kPiecesBf16 = D / 64;
-            const int pieces = piece_f32 ? kPiecesF32 : kPiecesBf16;
+#endif
+            float m_run = -INFINITY, l_run = 0.0f;
+            for (int j = 0; j < pc.nt; ++j, ++cnt) {
+                if (!mbar_wait_warp(&bars->s_full[x], cnt & 1, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int slot0 = (pc.t0 + j) * kTileN;
+                SRow sr;
+                load_srow(tS, sr);
+                if (slot0 + kTileN > L) mask_srow(sr, a, slot0 - L);  // tiles inside the prefix need no mask
+                const float mx = max_srow(sr);
+                const float mx_s = mx * sl2;
+                bool resc = false;
+                float factor = 1.0f;
+                if (mx_s > m_run + kRescaleLog2 || m_run == -INFINITY) {
+                    const float m_new = fmaxf(m_run, mx_s);
+                    if (m_run != -INFINITY) {
+                        factor = ex2_approx(m_run - m_new);
+                        resc = j > 0;
+                    } else {
+                        factor = 0.0f;
+                    }
+                    l_run *= factor;
+                    m_run = m_new;
+                }
+                // P = exp2(s*scale*log2e - m), written over S (bf16 pairs)
+                const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+                l_run += exp_store_srow(sr, tS, sl2, m_use);
+                if (__any_sync(0xFFFFFFFFu, resc)) {
+                    // O_X from the earlier tiles, rescaled before PV_X(j) adds to it
+                    // (S_X(j) done implies PV_X(j-1) done: O_X is current)
 #pragma unroll 1
-            for (int h = 0; h < pieces; ++h) {
-                uint4 slot[8];
-                if (piece_f32) {
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t v[32];
+                        tmem_ld32(tO + q * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            v[c] = __float_as_uint(__uint_as_float(v[c]) * (resc ? factor : 1.0f));
+                        tmem_st32(tO + q * 32, v);
+                    }
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(&bars->p_full[x]);
+            }
+            if (!ok) break;
+            // epilogue of the piece (after the CTA's last piece the combine may
+            // be scheduled; it waits for this grid)
+            if (w.remaining <= 0) pdl_trigger();
+            if (!mbar_wait_warp(&bars->o_final[x], nfin & 1, p.err, abort)) {
+                ok = false;
+                break;
+            }
+            ++nfin;
+            tc_fence_after();
+            const long long rowid = static_cast<long long>(pc.s.off + node) * p.Hq + head;
+            const bool partial = pc.slot >= 0;
+            const long long prow = (static_cast<long long>(pc.slot) * 2 + x) * kTileM + r;  // partial row
+            const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+            // Each warp stages its 32 output rows in its own 4 KB of shared
+            // memory, one 128-byte piece of each row at a time, and stores
+            // full lines (stage_store).
+            if (partial) {
+#pragma unroll 1
+                for (int h = 0; h < D / 32; ++h) {
                     uint32_t v[32];
                     tmem_ld32(tO + h * 32, v);
                     tmem_wait_ld();
+                    uint4 slot[8];
 #pragma unroll
                     for (int c = 0; c < 8; ++c) slot[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                } else {
+                    stage_store(stage, lane, slot, [&](int rr) {
+                        const long long pr = __shfl_sync(0xFFFFFFFFu, prow, rr);
+                        return reinterpret_cast<uint4*>(p.part_o + pr * D + h * 32);
+                    });
+                }
+                p.part_ml[prow] = make_float2(m_run, l_run);
+            } else {
+#pragma unroll 1
+                for (int h = 0; h < D / 64; ++h) {
                     uint32_t v0[32], v1[32];
                     tmem_ld32(tO + h * 64, v0);
                     tmem_ld32(tO + h * 64 + 32, v1);
                     tmem_wait_ld();
+                    uint4 slot[8];
 #pragma unroll
                     for (int c = 0; c < 4; ++c) {
                         slot[c] = make_uint4(
@@ -579,33 +856,143 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * inv, __uint_as_float(v1[8 * c + 5]) * inv),
                             pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * inv, __uint_as_float(v1[8 * c + 7]) * inv));
                     }
+                    stage_store(stage, lane, slot, [&](int rr) {
+                        const long long rid = __shfl_sync(0xFFFFFFFFu, rowid, rr);
+                        const bool rvalid = __shfl_sync(0xFFFFFFFFu, valid_row, rr);
+                        return rvalid ? reinterpret_cast<uint4*>(p.out + rid * D + h * 64) : nullptr;
+                    });
                 }
-                uint4* my_row = reinterpret_cast<uint4*>(stage + lane * 128);
+                if (valid_row && p.lse) p.lse[rowid] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+            }
+            if (partial) {
+                // count this piece done; the CTA that completes the unit
+                // merges every piece's partial rows (its own included)
+                const int nthr = ((2 * pc.mp + 1) * npt < pc.s.B) ? 256 : 128;
+                const CutUnit cu(pc.gpos - pc.t0, pc.T, bars->w_P);
+                __threadfence();  // this thread's partial rows are visible GPU-wide
+                named_sync(1, nthr);
+                if (tid == 0) {
+                    const uint32_t cid = bars->call_id;
+                    unsigned long long* ctr = p.merge_cnt + cu.c0;
+                    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), assumed, nv;
+                    do {  // a count from an earlier call restarts at this call's first piece
+                        assumed = old;
+                        nv = ((assumed >> 32) == cid) ? assumed + 1ull
+                                                      : ((static_cast<unsigned long long>(cid) << 32) | 1ull);
+                        old = atomicCAS(ctr, assumed, nv);
+                    } while (old != assumed);
+                    bars->merge_flag = static_cast<int>(nv & 0xFFFFFFFFull) == cu.n;
+                    __threadfence();  // the other pieces' rows are read after this count
+                }
+                named_sync(1, nthr);
+                if (bars->merge_flag) {  // uniform over the piece's warps
+                    // merge this row over the unit's pieces: M = max m_k,
+                    // O = sum 2^(m_k - M) O_k / sum 2^(m_k - M) l_k.  This
+                    // CTA's own piece is still in TMEM (O_X) and registers
+                    // (m_run, l_run); the other pieces come from L2, each
+                    // half row (64 columns) one batch of 16 loads in flight.
+                    const int own = static_cast<int>(blockIdx.x) - cu.c0;
+                    float mk[kMaxMergeIn], lk[kMaxMergeIn];
+                    float M = m_run;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) my_row[c ^ (lane & 7)] = slot[c];
-                __syncwarp();
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rr = 4 * i + (lane >> 3);  // staged row this lane copies
-                    const long long rid = __shfl_sync(0xFFFFFFFFu, rowid, rr);
-                    const bool rvalid = __shfl_sync(0xFFFFFFFFu, valid_row, rr);
-                    const uint4 val = reinterpret_cast<const uint4*>(stage + rr * 128)[sub ^ (rr & 7)];
-                    if (rvalid) {
-                        if (piece_f32)
-                            reinterpret_cast<uint4*>(p.part_o + (rid * p.splits + sp) * D + h * 32)[sub] = val;
-                        else
-                            reinterpret_cast<uint4*>(p.out + rid * D + h * 64)[sub] = val;
+                    for (int i = 0; i < kMaxMergeIn; ++i) {  // every other piece's (m, l) in one round trip
+                        const int k = i < own ? i : i + 1;
+                        mk[i] = -INFINITY;
+                        lk[i] = 0.0f;
+                        if (k < cu.n) {
+                            const float2 ml = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]);
+                            mk[i] = ml.x;
+                            lk[i] = ml.y;
+                        }
                     }
+                    for (int k0 = kMaxMergeIn; k0 + 1 < cu.n; ++k0) {  // beyond the unrolled pieces (rare)
+                        const int k = k0 < own ? k0 : k0 + 1;
+                        M = fmaxf(M, __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).x);
+                    }
+#pragma unroll
+                    for (int i = 0; i < kMaxMergeIn; ++i) M = fmaxf(M, mk[i]);
+                    // weights and sums in piece order, whichever CTA merges,
+                    // so that every call rounds the same way
+                    const float w_own = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - M);
+#pragma unroll
+                    for (int i = 0; i < kMaxMergeIn; ++i) mk[i] = (mk[i] == -INFINITY) ? 0.0f : exp2f(mk[i] - M);
+                    auto weight_of = [&](int k) {  // piece k's weight (k != own)
+                        const int i = k < own ? k : k - 1;
+                        float w = mk[0];
+#pragma unroll
+                        for (int j = 1; j < kMaxMergeIn; ++j)
+                            if (j == i) w = mk[j];
+                        if (i >= kMaxMergeIn) {
+                            const float ms = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).x;
+                            w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
+                        }
+                        return w;
+                    };
+                    auto sum_of = [&](int k) {  // piece k's row sum (k != own)
+                        const int i = k < own ? k : k - 1;
+                        float l = lk[0];
+#pragma unroll
+                        for (int j = 1; j < kMaxMergeIn; ++j)
+                            if (j == i) l = lk[j];
+                        if (i >= kMaxMergeIn) l = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).y;
+                        return l;
+                    };
+                    float lsum = 0.0f;
+                    for (int k = 0; k < cu.n; ++k) lsum += (k == own) ? w_own * l_run : weight_of(k) * sum_of(k);
+                    const float minv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+#pragma unroll 1
+                    for (int h = 0; h < D / 64; ++h) {
+                        uint32_t packed[32];  // the 64 output columns of this staged piece, bf16 pairs
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {
+                            const int col = h * 64 + half * 32;
+                            float acc[32];
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) acc[c] = 0.0f;
+#pragma unroll 1
+                            for (int k = 0; k < cu.n; ++k) {
+                                if (k == own) {  // this CTA's piece, from TMEM (k is the same for the whole warp)
+                                    uint32_t v[32];
+                                    tmem_ld32(tO + col, v);
+                                    tmem_wait_ld();
+#pragma unroll
+                                    for (int c = 0; c < 32; ++c) acc[c] += w_own * __uint_as_float(v[c]);
+                                } else {
+                                    const long long pr = (static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r;
+                                    const float wgt = weight_of(k);
+                                    const float4* po = reinterpret_cast<const float4*>(p.part_o + pr * D + col);
+                                    float4 q[8];
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c) q[c] = __ldcg(po + c);
+#pragma unroll
+                                    for (int c = 0; c < 8; ++c) {
+                                        acc[4 * c + 0] += wgt * q[c].x;
+                                        acc[4 * c + 1] += wgt * q[c].y;
+                                        acc[4 * c + 2] += wgt * q[c].z;
+                                        acc[4 * c + 3] += wgt * q[c].w;
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                packed[half * 16 + c] = pack_bf16x2(acc[2 * c] * minv, acc[2 * c + 1] * minv);
+                        }
+                        uint4 slot[8];
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            slot[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                        stage_store(stage, lane, slot, [&](int rr) {
+                            const long long rid = __shfl_sync(0xFFFFFFFFu, rowid, rr);
+                            const bool rvalid = __shfl_sync(0xFFFFFFFFu, valid_row, rr);
+                            return rvalid ? reinterpret_cast<uint4*>(p.out + rid * D + h * 64) : nullptr;
+                        });
+                    }
+                    if (valid_row && p.lse) p.lse[rowid] = (M + log2f(lsum)) * 0.6931471805599453f;
                 }
-                __syncwarp();  // the next piece overwrites the stage
             }
-            if (valid_row) {
-                if (p.splits == 1) {
-                    if (p.lse) p.lse[rowid] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
-                } else {
-                    p.part_ml[rowid * p.splits + sp] = make_float2(m_run, l_run);
-                }
-            }
+            // O_X has been read (tcgen05.wait::ld above) before this thread
+            // arrives on p_full[X] for the next piece's first tile, which is
+            // what lets the MMA warp overwrite O_X
         }
     }
 
@@ -615,56 +1002,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
-}
-
-// Merge the KV-split partials of every (node, head) row.  One warp per row.
-template <int D>
-__global__ void __launch_bounds__(128)
-    tree_attn_combine_kernel(const AttnParams p, int total_nodes) {
-    pdl_wait();  // the partials are complete and visible
-    const int lane = threadIdx.x & 31;
-    const int n = blockIdx.x;
-    const int h = blockIdx.y * 4 + (threadIdx.x >> 5);
-    if (n >= total_nodes || h >= p.Hq) return;
-    int lo = 0, hi = p.nseq;  // sequence of node n
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (p.tree_off[mid] <= n) lo = mid; else hi = mid;
-    }
-    const int b = lo, off = p.tree_off[b];
-    const int B = p.tree_off[b + 1] - off;
-    const int L = p.prefix_len[b];
-    if (B < 1 || B > JT_MAX_TREE || L < 0 || off < 0 || off + B > p.total_nodes ||
-        static_cast<long long>(L) + B > static_cast<long long>(p.max_pages) * JT_PAGE_SIZE)
-        return;  // reported by the main kernel
-    const int node = n - off;
-    if (node >= B) return;  // spare capacity past the last tree
-    const int valid_end = unit_valid_end(L, B, (node / p.npt) >> 1, p.npt);
-    const long long rowid = static_cast<long long>(n) * p.Hq + h;
-    float M = -INFINITY;
-    int ns = 0;
-    for (int s = 0; s < p.splits; ++s) {
-        int t0;
-        if (split_range(valid_end, p.splits, s, t0) == 0) break;
-        M = fmaxf(M, p.part_ml[rowid * p.splits + s].x);
-        ns = s + 1;
-    }
-    float acc[D / 32];
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) acc[k] = 0.0f;
-    float lsum = 0.0f;
-    for (int s = 0; s < ns; ++s) {
-        const float2 ml = p.part_ml[rowid * p.splits + s];
-        const float wgt = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - M);
-        lsum += wgt * ml.y;
-        const float* po = p.part_o + (rowid * p.splits + s) * D;
-#pragma unroll
-        for (int k = 0; k < D / 32; ++k) acc[k] += wgt * po[lane + 32 * k];
-    }
-    const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
-#pragma unroll
-    for (int k = 0; k < D / 32; ++k) p.out[rowid * D + lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
-    if (lane == 0 && p.lse) p.lse[rowid] = (M + log2f(lsum)) * 0.6931471805599453f;
 }
 
 // ---------------------------------------------------------------------------
@@ -689,31 +1026,35 @@ static PFN_encodeTiled_t get_encode_fn() {
 }
 
 AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int dtype) {
+    (void)Hkv;
+    (void)max_pages;
     AttnPlan pl;
     const int G = Hq / Hkv;
     pl.rows_per_tile_nodes = kTileM / G;
     pl.mtiles = (max_tree + pl.rows_per_tile_nodes - 1) / pl.rows_per_tile_nodes;
-    pl.splits = 1;
-    if (dtype == JT_DTYPE_BF16) {
-        const long long units = static_cast<long long>(nseq) * Hkv * ((pl.mtiles + 1) / 2);
-        const int sms = device_sm_count();
-        const int tmax = (max_pages * JT_PAGE_SIZE + kTileN - 1) / kTileN;
-        if (units > 0 && units < sms) {
-            int s = static_cast<int>(sms / units);
-            s = min(s, max(1, tmax / 2));
-            pl.splits = max(1, min(s, kMaxSplits));
-        }
-    }
+    pl.grid = 0;
+    pl.nseq = nseq;
+    if (dtype == JT_DTYPE_BF16) pl.grid = device_sm_count();  // one CTA per SM, every one the same tile count
     return pl;
 }
 
+// Workspace of the bf16 path after the header: the merge counts of cut
+// units (one per CTA; like the header they must be zero before the
+// workspace's first use, and stay valid across calls), the plan (T_total, P,
+// the first global tile of each sequence), then two partial slots per CTA.
+static size_t attn_cnt_bytes(const AttnPlan& p) { return align_up(static_cast<size_t>(p.grid) * 8); }
+static size_t attn_plan_bytes(const AttnPlan& p) { return align_up(static_cast<size_t>(p.nseq + 3) * sizeof(int)); }
+static size_t attn_ml_bytes(const AttnPlan& p) {
+    return align_up(static_cast<size_t>(2) * p.grid * 2 * kTileM * sizeof(float2));
+}
+
 size_t attn_workspace_bytes(const AttnPlan& p, int total_nodes, int Hq, int D) {
+    (void)total_nodes;
+    (void)Hq;
     size_t b = kWsHeader;
-    if (p.splits > 1) {
-        const size_t rows = static_cast<size_t>(total_nodes) * Hq * p.splits;
-        b += align_up(rows * D * sizeof(float));
-        b += align_up(rows * sizeof(float2));
-    }
+    if (p.grid > 0)
+        b += attn_cnt_bytes(p) + attn_plan_bytes(p) + attn_ml_bytes(p) +
+             align_up(static_cast<size_t>(2) * p.grid * 2 * kTileM * D * sizeof(float));
     return b;
 }
 
@@ -726,6 +1067,7 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
                                char* ws_parts, uint32_t* err, cudaStream_t st) {
     PFN_encodeTiled_t enc = get_encode_fn();
     if (!enc) return cudaErrorNotSupported;
+    if (plan.grid < 1) return cudaErrorInvalidValue;
     const int G = Hq / Hkv;
     CUtensorMap tq, tk, tv;
     {
@@ -765,22 +1107,24 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
     prm.anc = anc;
     prm.out = static_cast<__nv_bfloat16*>(out);
     prm.lse = lse;
-    prm.part_o = nullptr;
-    prm.part_ml = nullptr;
-    if (plan.splits > 1) {
-        const size_t rows = static_cast<size_t>(total_nodes) * Hq * plan.splits;
-        prm.part_o = reinterpret_cast<float*>(ws_parts);
-        prm.part_ml = reinterpret_cast<float2*>(ws_parts + align_up(rows * D * sizeof(float)));
-    }
+    char* w = ws_parts;
+    prm.merge_cnt = reinterpret_cast<unsigned long long*>(w);
+    w += attn_cnt_bytes(plan);
+    prm.plan = reinterpret_cast<int*>(w);
+    w += attn_plan_bytes(plan);
+    prm.part_ml = reinterpret_cast<float2*>(w);
+    w += attn_ml_bytes(plan);
+    prm.part_o = reinterpret_cast<float*>(w);
+    prm.tickets = &reinterpret_cast<WsHeader*>(err)->tickets;
     prm.err = err;
     prm.max_pages = max_pages;
     prm.num_pages = num_pages;
     prm.nseq = nseq;
     prm.total_nodes = total_nodes;
     prm.Hq = Hq;
+    prm.Hkv = Hkv;
     prm.G = G;
     prm.npt = plan.rows_per_tile_nodes;
-    prm.splits = plan.splits;
     prm.scale_log2 = scale * 1.4426950408889634f;
 
     using SL = SmemLayout<D>;
@@ -790,12 +1134,8 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc));
     }));
     if (ea != cudaSuccess) return ea;
-    dim3 grid(((plan.mtiles + 1) / 2) * plan.splits, Hkv, nseq);
-    cudaError_t e = launch_kernel_pdl(tree_attn_tc_kernel<D>, grid, dim3(kAttnThreads), SL::kAlloc, st, tq, tk,
-                                      tv, prm);
-    if (e != cudaSuccess || plan.splits == 1) return e;
-    dim3 cgrid(total_nodes, (Hq + 3) / 4);
-    return launch_kernel_pdl(tree_attn_combine_kernel<D>, cgrid, dim3(128), 0, st, prm, total_nodes);
+    return launch_kernel_pdl(tree_attn_tc_kernel<D>, dim3(plan.grid), dim3(kAttnThreads), SL::kAlloc, st, tq, tk,
+                             tv, prm);
 }
 
 cudaError_t tree_attn_bf16_launch(const void* q, const void* k_cache, const void* v_cache,

@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(kTopwThreads)
 // ~1e-11; only the final assembly and lp = z - lse are fp64.
 // ENT: also merge the sum exp(z - max) * z partials and return the row
 // entropy H = lse - sum p z.
-template <int W, bool ENT>
+template <int W, bool ENT, int R = 4>
 __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
                                           const int* __restrict__ part_id,
                                           const float* __restrict__ part_m,
@@ -412,9 +412,10 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
                                           const float* tab_lo, int (&tok)[W], double (&lp)[W],
                                           double& lse, double& H) {
     const long long base = row * splits;
-    // every load of the row is issued up front (one memory round trip):
-    // lane handles chunks s = lane + 32 r, r < kMergeR
-    constexpr int kMergeR = 4;  // covers 128 chunks = 512k vocabulary entries
+    // the row's first 32 * R chunk loads are issued up front (one memory
+    // round trip): lane handles chunks s = lane + 32 r, r < R; any further
+    // chunks (R = 4 covers 512k vocabulary entries) are read in a loop
+    constexpr int kMergeR = R;
     float pm[kMergeR];
     float2 ps[kMergeR], pt[kMergeR];
     float pv[kMergeR][W];
@@ -515,8 +516,33 @@ __device__ __forceinline__ void merge_row(const float* __restrict__ part_v,
     }
 }
 
+// Entropy-mixed step scores of one merged row: ((1 - alpha) * lp) - (alpha *
+// H), each operation rounded on its own (no fused multiply-add), as the fp64
+// definition evaluates it; probability 0 stays at -inf.  The expansion needs
+// each row in queue-key order (score desc, token asc): equal scores (every
+// candidate at alpha = 1, rare rounding collisions below it) go by token.
+template <int W>
+__device__ __forceinline__ void mixed_scores(int (&tok)[W], double (&lp)[W], double H, double alpha) {
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+        if (lp[k] != -INFINITY) lp[k] = __dsub_rn(__dmul_rn(1.0 - alpha, lp[k]), __dmul_rn(alpha, H));
+#pragma unroll
+    for (int i = 0; i + 1 < W; ++i)
+#pragma unroll
+        for (int j = 0; j + 1 < W - i; ++j)
+            if (lp[j + 1] > lp[j] || (lp[j + 1] == lp[j] && tok[j + 1] < tok[j])) {
+                const double tl = lp[j];
+                lp[j] = lp[j + 1];
+                lp[j + 1] = tl;
+                const int tt = tok[j];
+                tok[j] = tok[j + 1];
+                tok[j + 1] = tt;
+            }
+}
+
 // ---------------------------------------------------------------------------
-// Step 1b: merge the partials, one warp per row.
+// Step 1b: merge the partials, one warp per row (the adaptive build and
+// jt_tree_topw; the plain and mixed builds merge inside the expansion).
 // ---------------------------------------------------------------------------
 template <int W, bool ENT>
 __global__ void __launch_bounds__(256)
@@ -541,29 +567,7 @@ __global__ void __launch_bounds__(256)
     merge_row<W, ENT>(part_v, part_id, part_m, part_s, part_t, splits, row, lane, s_thi, s_tlo, tok, lp,
                       lse, H);
     if (lane == 0) {
-        if (ENT) {
-            // entropy-mixed step score ((1 - alpha) * lp) - (alpha * H), each
-            // operation rounded on its own (no fused multiply-add), as the
-            // fp64 definition evaluates it; probability 0 stays at -inf
-#pragma unroll
-            for (int k = 0; k < W; ++k)
-                if (lp[k] != -INFINITY) lp[k] = __dsub_rn(__dmul_rn(1.0 - alpha, lp[k]), __dmul_rn(alpha, H));
-            // the expansion needs each row in queue-key order (score desc,
-            // token asc): equal scores (every candidate at alpha = 1, rare
-            // rounding collisions below it) go by token
-#pragma unroll
-            for (int i = 0; i + 1 < W; ++i)
-#pragma unroll
-                for (int j = 0; j + 1 < W - i; ++j)
-                    if (lp[j + 1] > lp[j] || (lp[j + 1] == lp[j] && tok[j + 1] < tok[j])) {
-                        const double tl = lp[j];
-                        lp[j] = lp[j + 1];
-                        lp[j + 1] = tl;
-                        const int tt = tok[j];
-                        tok[j] = tok[j + 1];
-                        tok[j + 1] = tt;
-                    }
-        }
+        if (ENT) mixed_scores<W>(tok, lp, H, alpha);
 #pragma unroll
         for (int k = 0; k < W; ++k) {
             tok_out[row * W + k] = tok[k];
@@ -687,9 +691,21 @@ __device__ __forceinline__ int set_incl_scan(int v, int* s_warp) {
 
 // w_cap / n_cap (optional, per sequence): only the first w_cap[b] candidates
 // of every row are children, and nodes of depth n_cap[b] get none.
-template <int W>
+// The top-W partials of a build whose rows the expansion merges itself.
+struct MergeIn {
+    const float* v;
+    const int* id;
+    const float* m;
+    const float2* s;
+    const float2* t;
+    int splits;
+    double alpha;
+    ExpTable tab;
+};
+
+template <int W, int MODE>  // MODE 0: tok_in / lp_in given; 1: merge the partials; 2: merge, mixed scores
 __global__ void __launch_bounds__(kExpandThreads, 1)
-    expand_kernel(const int32_t* __restrict__ tok_in, const double* __restrict__ lp_in,
+    expand_kernel(const int32_t* __restrict__ tok_in, const double* __restrict__ lp_in, const MergeIn mi,
                   const int32_t* __restrict__ root_token, const int32_t* __restrict__ tree_off,
                   const int32_t* __restrict__ w_cap, const int32_t* __restrict__ n_cap,
                   int total_nodes, int N, int32_t* __restrict__ parent, int32_t* __restrict__ token,
@@ -710,16 +726,41 @@ __global__ void __launch_bounds__(kExpandThreads, 1)
     __shared__ int s_cnt[kSetWarps][W];
     __shared__ int s_L[W];
 
-    pdl_wait();     // the tables are complete and visible
-    pdl_trigger();  // the next kernel may be scheduled (it waits for this grid)
+    __shared__ float s_thi[MODE ? 64 : 1], s_tlo[MODE ? 64 : 1];
     const int b = blockIdx.x;
     const int tid = threadIdx.x;
-    // The table loads do not depend on the offsets: issue both together.
-    for (int i = tid; i < N * W; i += kExpandThreads) {
-        s_tok[i] = tok_in[static_cast<long long>(b) * N * W + i];
-        s_lp[i] = lp_in[static_cast<long long>(b) * N * W + i];
-        // a NaN draft logit makes its row's lse (so every lp) NaN
-        JT_DCHECK(s_lp[i] == s_lp[i] && s_tok[i] >= 0, err);
+    if (MODE && tid < 64) {
+        s_thi[tid] = mi.tab.hi[tid];
+        s_tlo[tid] = mi.tab.lo[tid];
+    }
+    pdl_wait();     // the tables (or partials) are complete and visible
+    pdl_trigger();  // the next kernel may be scheduled (it waits for this grid)
+    if (MODE) {
+        // the N top-W rows of this sequence from the partials, one warp each
+        __syncthreads();  // exp table ready
+        for (int d = tid >> 5; d < N; d += kExpandThreads / 32) {
+            int tk[W];
+            double lp[W], lse, H;
+            merge_row<W, MODE == 2, 1>(mi.v, mi.id, mi.m, mi.s, mi.t, mi.splits, static_cast<long long>(b) * N + d,
+                                       tid & 31, s_thi, s_tlo, tk, lp, lse, H);
+            if ((tid & 31) == 0) {
+                if (MODE == 2) mixed_scores<W>(tk, lp, H, mi.alpha);
+#pragma unroll
+                for (int k = 0; k < W; ++k) {
+                    s_tok[d * W + k] = tk[k];
+                    s_lp[d * W + k] = lp[k];
+                    JT_DCHECK(lp[k] == lp[k] && tk[k] >= 0, err);  // a NaN draft logit makes the row NaN
+                }
+            }
+        }
+    } else {
+        // The table loads do not depend on the offsets: issue both together.
+        for (int i = tid; i < N * W; i += kExpandThreads) {
+            s_tok[i] = tok_in[static_cast<long long>(b) * N * W + i];
+            s_lp[i] = lp_in[static_cast<long long>(b) * N * W + i];
+            // a NaN draft logit makes its row's lse (so every lp) NaN
+            JT_DCHECK(s_lp[i] == s_lp[i] && s_tok[i] >= 0, err);
+        }
     }
     const int off = tree_off[b];
     const int B = tree_off[b + 1] - off;
@@ -995,13 +1036,19 @@ static const ExpTable& exp_table() {
 
 // One-time attribute set-up per device; the first call on a device should
 // come before any stream capture.
-template <int W>
+template <int W, int MODE = 0>
 static cudaError_t set_expand_smem() {
     static PerDeviceCache done;
     return static_cast<cudaError_t>(done.get([] {
-        return static_cast<int>(cudaFuncSetAttribute(expand_kernel<W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        return static_cast<int>(cudaFuncSetAttribute(expand_kernel<W, MODE>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                      static_cast<int>(kExpandSmem)));
     }));
+}
+
+static MergeIn no_merge() {
+    MergeIn mi = {};
+    return mi;
 }
 
 static int topw_splits(long long V, int per) {
@@ -1105,23 +1152,36 @@ static cudaError_t run_build(const float* z, const int32_t* root_token, const in
     const long long rows = static_cast<long long>(nseq) * N;
     const int per = topw_per_thread(rows, V);
     TopwParts t = carve_topw(ws_parts, rows, V, W, per);
+    const bool ent = alpha != 0.0;
     if (rows > 0) {
-        const bool ent = alpha != 0.0;
         cudaError_t e = ent ? launch_topw_partial<W, true>(z, rows, V, per, t, st)
                             : launch_topw_partial<W, false>(z, rows, V, per, t, st);
         if (e != cudaSuccess) return e;
-        const unsigned blocks = static_cast<unsigned>((rows + 7) / 8);
-        e = ent ? launch_kernel_pdl(topw_merge_kernel<W, true>, dim3(blocks), dim3(256), 0, st, t.v, t.id, t.m,
-                                    t.s, t.t, t.splits, rows, exp_table(), alpha, t.tok, t.lp, t.lse)
-                : launch_kernel_pdl(topw_merge_kernel<W, false>, dim3(blocks), dim3(256), 0, st, t.v, t.id, t.m,
-                                    t.s, t.t, t.splits, rows, exp_table(), 0.0, t.tok, t.lp, t.lse);
-        if (e != cudaSuccess) return e;
     }
-    cudaError_t ea = set_expand_smem<W>();
+    // the expansion merges each sequence's rows from the partials itself
+    // (one launch fewer on the critical path)
+    MergeIn mi;
+    mi.v = t.v;
+    mi.id = t.id;
+    mi.m = t.m;
+    mi.s = t.s;
+    mi.t = t.t;
+    mi.splits = t.splits;
+    mi.alpha = alpha;
+    mi.tab = exp_table();
+    const int32_t* none = nullptr;
+    if (ent) {
+        cudaError_t ea = set_expand_smem<W, 2>();
+        if (ea != cudaSuccess) return ea;
+        return launch_kernel_pdl(expand_kernel<W, 2>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, none,
+                                 static_cast<const double*>(nullptr), mi, root_token, tree_off, none, none,
+                                 total_nodes, N, parent, token, depth, anc, err);
+    }
+    cudaError_t ea = set_expand_smem<W, 1>();
     if (ea != cudaSuccess) return ea;
-    return launch_kernel_pdl(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, t.tok, t.lp,
-                             root_token, tree_off, static_cast<const int32_t*>(nullptr),
-                             static_cast<const int32_t*>(nullptr), total_nodes, N, parent, token, depth, anc, err);
+    return launch_kernel_pdl(expand_kernel<W, 1>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, none,
+                             static_cast<const double*>(nullptr), mi, root_token, tree_off, none, none, total_nodes,
+                             N, parent, token, depth, anc, err);
 }
 
 static int policy_ceiling(const jt_policy_params& prm, int nseq) {
@@ -1160,8 +1220,8 @@ static cudaError_t run_build_adaptive(const float* z, const int32_t* root_token,
     if (e != cudaSuccess) return e;
     e = set_expand_smem<W>();
     if (e != cudaSuccess) return e;
-    return launch_kernel(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, t.tok, t.lp,
-                         root_token, static_cast<const int32_t*>(tree_off), static_cast<const int32_t*>(w_cap),
+    return launch_kernel(expand_kernel<W, 0>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, 0, t.tok, t.lp,
+                         no_merge(), root_token, static_cast<const int32_t*>(tree_off), static_cast<const int32_t*>(w_cap),
                          static_cast<const int32_t*>(n_cap), capacity, N, parent, token, depth, anc, err);
 }
 
@@ -1172,8 +1232,9 @@ static cudaError_t run_expand(const int32_t* tok, const double* lp, const int32_
                               uint32_t* anc, uint32_t* err, cudaStream_t st) {
     cudaError_t ea = set_expand_smem<W>();
     if (ea != cudaSuccess) return ea;
-    return launch_kernel_pdl(expand_kernel<W>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, tok, lp,
-                             root_token, tree_off, w_cap, n_cap, total_nodes, N, parent, token, depth, anc, err);
+    return launch_kernel_pdl(expand_kernel<W, 0>, dim3(nseq), dim3(kExpandThreads), kExpandSmem, st, tok, lp,
+                             no_merge(), root_token, tree_off, w_cap, n_cap, total_nodes, N, parent, token, depth,
+                             anc, err);
 }
 
 #define JT_DISPATCH_W(W, CALL)           \
