@@ -324,9 +324,9 @@ jt_status jt_tree_build_adaptive(const float* draft_logits, const int32_t* root_
  * boundary is merged from fp32 partials in the workspace by the CTA that
  * finishes its piece last.  Workspace: jt_workspace_size(JT_OP_TREE_ATTN,
  * nseq, 0, 0, 0, total_nodes, Hq, Hkv, D, max_pages, max_tree) = 256 +
- * 8 * SMs + O(nseq) + 2 * SMs * 256 * (D + 2) * 4 bytes (about 40 MB at
+ * 16 * SMs + O(nseq) + 2 * SMs * 256 * (D + 2) * 4 bytes (about 40 MB at
  * D = 128 on 152 SMs), sized for the current device and serving that device
- * only.  Its first 256 + 8 * SMs bytes (rounded up to 256; the header and
+ * only.  Its first 256 + 16 * SMs bytes (rounded up to 256; the header and
  * the merge counts) must be zero before its first use, like every header;
  * they stay valid from call to call (counts carry the number of the call
  * that wrote them), so they never need clearing again.

@@ -214,7 +214,7 @@ def test_repeated_calls_on_one_workspace_and_stale_merge_counts():
     outs = []
     for i in range(4):
         if i == 2:   # stale counts right after the header
-            cnt = ws[256:256 + 8 * torch.cuda.get_device_properties(0).multi_processor_count].view(torch.int64)
+            cnt = ws[256:256 + 16 * torch.cuda.get_device_properties(0).multi_processor_count].view(torch.int64)
             cnt.fill_(7)
         out, lse = jt.jt_tree_attn_paged(*args, scale=wl.scale, max_tree=200, ws=ws)
         jt.jt_check(ws)

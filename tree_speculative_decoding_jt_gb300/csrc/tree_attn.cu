@@ -77,7 +77,7 @@ struct AttnParams {
     float2* part_ml;  // [2 * grid][2][128]: their running max (log2 units) and sum
     int* plan;        // [2 + nseq + 1]: T_total, P, then each sequence's first global tile
     unsigned long long* tickets;    // CTA arrivals over all calls (workspace header)
-    unsigned long long* merge_cnt;  // [grid]: (call number << 32) | pieces done, per cut unit
+    unsigned long long* merge_cnt;  // [grid][2]: (call number << 32) | pieces done, per cut unit and query tile
     uint32_t* err;
     int max_pages, num_pages, nseq, total_nodes, Hq, Hkv, G, npt;
     float scale_log2;
@@ -114,7 +114,7 @@ struct Bars {
     // the CTA's start position, published by the planner
     int w_b, w_g, w_mp, w_t, w_quota, w_P;
     uint32_t call_id;  // this call's number (+1) on this workspace
-    int merge_flag;    // this CTA finished the last piece of a cut unit
+    int merge_flag[2];  // per query tile: this CTA finished the last piece of a cut unit
 };
 
 // ---------------------------------------------------------------------------
@@ -866,14 +866,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             if (partial) {
                 // count this piece done; the CTA that completes the unit
-                // merges every piece's partial rows (its own included)
-                const int nthr = ((2 * pc.mp + 1) * npt < pc.s.B) ? 256 : 128;
+                // merges every piece's partial rows (its own included).  Each
+                // query tile's four warps do this on their own (barrier 1 + X,
+                // count and flag per tile), so neither tile's warps ever wait
+                // for the other's.
                 const CutUnit cu(pc.gpos - pc.t0, pc.T, bars->w_P);
                 __threadfence();  // this thread's partial rows are visible GPU-wide
-                named_sync(1, nthr);
-                if (tid == 0) {
+                named_sync(1 + x, 128);
+                if (r == 0) {
                     const uint32_t cid = bars->call_id;
-                    unsigned long long* ctr = p.merge_cnt + cu.c0;
+                    unsigned long long* ctr = p.merge_cnt + 2 * cu.c0 + x;
                     unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), assumed, nv;
                     do {  // a count from an earlier call restarts at this call's first piece
                         assumed = old;
@@ -881,11 +883,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                                       : ((static_cast<unsigned long long>(cid) << 32) | 1ull);
                         old = atomicCAS(ctr, assumed, nv);
                     } while (old != assumed);
-                    bars->merge_flag = static_cast<int>(nv & 0xFFFFFFFFull) == cu.n;
+                    bars->merge_flag[x] = static_cast<int>(nv & 0xFFFFFFFFull) == cu.n;
                     __threadfence();  // the other pieces' rows are read after this count
                 }
-                named_sync(1, nthr);
-                if (bars->merge_flag) {  // uniform over the piece's warps
+                named_sync(1 + x, 128);
+                if (bars->merge_flag[x]) {  // uniform over the tile's warps
                     // merge this row over the unit's pieces: M = max m_k,
                     // O = sum 2^(m_k - M) O_k / sum 2^(m_k - M) l_k.  This
                     // CTA's own piece is still in TMEM (O_X) and registers
@@ -1042,7 +1044,7 @@ AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int d
 // units (one per CTA; like the header they must be zero before the
 // workspace's first use, and stay valid across calls), the plan (T_total, P,
 // the first global tile of each sequence), then two partial slots per CTA.
-static size_t attn_cnt_bytes(const AttnPlan& p) { return align_up(static_cast<size_t>(p.grid) * 8); }
+static size_t attn_cnt_bytes(const AttnPlan& p) { return align_up(static_cast<size_t>(p.grid) * 2 * 8); }
 static size_t attn_plan_bytes(const AttnPlan& p) { return align_up(static_cast<size_t>(p.nseq + 3) * sizeof(int)); }
 static size_t attn_ml_bytes(const AttnPlan& p) {
     return align_up(static_cast<size_t>(2) * p.grid * 2 * kTileM * sizeof(float2));
