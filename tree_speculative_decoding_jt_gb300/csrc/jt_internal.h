@@ -81,10 +81,12 @@ cudaError_t verify_stochastic_launch(const float* z, const float* zd, const int3
 
 // tree_attn.cu / tree_attn_f32.cu
 struct AttnPlan {
-    int grid;        // CTAs of the bf16 kernel (one per SM; 0 on the fp32 path)
+    int grid;        // CTAs of the bf16 kernel (0 on the fp32 path)
     int nseq;
     int mtiles;      // row tiles per (sequence, kv head) at max_tree
     int rows_per_tile_nodes;  // tree nodes per 128-row tile (128 / G)
+    int splits;      // > 0: split mode, one CTA per (unit, key split); 0: equal tile ranges per SM
+    int npairs;      // query-tile pairs per (sequence, KV head) at max_tree
 };
 AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int dtype);
 size_t attn_workspace_bytes(const AttnPlan& p, int total_nodes, int Hq, int D);

@@ -27,7 +27,10 @@
 // waits for another).  Only the first and the last piece of a CTA can be
 // cut, so two partial slots per CTA suffice.  Each CTA derives the whole
 // plan from prefix_len and tree_off on the device, so sequence lengths never
-// visit the host.
+// visit the host.  With few units (a batch of one: every unit would be cut
+// into many pieces whose merge lands on one CTA's critical path) the launch
+// runs in split mode instead: one CTA per (unit, key split), the splits'
+// partials merged by tree_attn_combine_kernel, one warp per query row.
 //
 // Warp roles (320 threads):
 //   warps 0-3 / 4-7  softmax + epilogue of query tile A / B, one query row
@@ -54,6 +57,8 @@
 // Online softmax in the log2 domain, two passes over S in TMEM (row max,
 // then exp and P), lazy rescaling of O (only when the running max grows by
 // more than 2^8).  All waits are bounded in time.
+#include <algorithm>
+
 #include "jt_common.cuh"
 #include "jt_internal.h"
 
@@ -80,6 +85,7 @@ struct AttnParams {
     unsigned long long* merge_cnt;  // [grid][2]: (call number << 32) | pieces done, per cut unit and query tile
     uint32_t* err;
     int max_pages, num_pages, nseq, total_nodes, Hq, Hkv, G, npt;
+    int splits, npairs;  // split mode (splits > 0): CTA c = unit c / splits, key split c % splits
     float scale_log2;
 };
 
@@ -297,6 +303,43 @@ __device__ void plan_cta(const AttnParams& p, Bars* bars, int lane) {
         bars->w_t = t;
         bars->w_quota = quota;
         bars->w_P = P;
+    }
+}
+
+// Split mode: unit u = blockIdx.x / splits of the dense (b, g, mp) layout
+// (npairs pairs per KV head), key split blockIdx.x % splits of ceil(T /
+// splits) tiles.  CTAs whose pair lies past the sequence's tree, or whose
+// split is empty, get no tiles.
+__device__ __forceinline__ int split_tiles(int T, int splits) { return (T + splits - 1) / splits; }
+
+__device__ void plan_cta_split(const AttnParams& p, Bars* bars, int lane) {
+    const int c = blockIdx.x;
+    const int u = c / p.splits, sp = c % p.splits;
+    const int b = u / (p.Hkv * p.npairs);
+    const int rem = u % (p.Hkv * p.npairs);
+    int quota = 0, t0 = 0;
+    if (b < p.nseq) {
+        const SeqInfo s = load_seq(p, b);
+        if (s.np < 0 && c == 0 && lane == 0) raise_error(p.err, DEVERR_INVALID);
+        // CTA 0 also reports the other sequences' bad contents
+        if (c == 0)
+            for (int bb = lane; bb < p.nseq; bb += 32)
+                if (bb != b && load_seq(p, bb).np < 0) raise_error(p.err, DEVERR_INVALID);
+        const int mp = rem % p.npairs;
+        if (mp < s.np) {
+            const int T = unit_tiles(s, mp, p.npt);
+            const int tps = split_tiles(T, p.splits);
+            t0 = sp * tps;
+            quota = max(0, min(T, t0 + tps) - t0);
+        }
+    }
+    if (lane == 0) {
+        bars->w_b = b;
+        bars->w_g = rem / p.npairs;
+        bars->w_mp = rem % p.npairs;
+        bars->w_t = t0;
+        bars->w_quota = quota;
+        bars->w_P = 0;
     }
 }
 
@@ -542,7 +585,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
     if (warp == 9) tmem_alloc(&bars->tmem_base, 512);
     pdl_wait();  // no global memory is read before the previous kernel's writes are visible
-    if (warp == 8) plan_cta(p, bars, lane);
+    if (warp == 8) {
+        if (p.splits > 0)
+            plan_cta_split(p, bars, lane);
+        else
+            plan_cta(p, bars, lane);
+    }
     if (tid == 0)  // every CTA of a call draws one ticket before anything can fail
         bars->call_id = static_cast<uint32_t>(atomicAdd(p.tickets, 1ull) / gridDim.x) + 1u;
     tc_fence_before();
@@ -864,7 +912,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 if (valid_row && p.lse) p.lse[rowid] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
             }
-            if (partial) {
+            if (partial && p.splits == 0) {
                 // count this piece done; the CTA that completes the unit
                 // merges every piece's partial rows (its own included).  Each
                 // query tile's four warps do this on their own (barrier 1 + X,
@@ -1006,6 +1054,76 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     }
 }
 
+// Split mode: merge the key splits of every unit cut into more than one.
+// Grid (units, 32): blockIdx.y picks 8 of the unit's 256 query rows, one
+// warp per row; lane k holds split k's (m, l), each lane D/32 columns of O.
+constexpr int kCombineThreads = 256;
+constexpr int kCombineRowBlocks = 2 * kTileM / (kCombineThreads / 32);
+
+template <int D>
+__global__ void __launch_bounds__(kCombineThreads)
+    tree_attn_combine_kernel(const AttnParams p) {
+    constexpr int kCols = D / 32;
+    pdl_wait();  // the partials are complete and visible
+    const int u = blockIdx.x;
+    const int b = u / (p.Hkv * p.npairs);
+    const int rem = u % (p.Hkv * p.npairs);
+    const int g = rem / p.npairs, mp = rem % p.npairs;
+    if (b >= p.nseq) return;
+    const SeqInfo s = load_seq(p, b);
+    if (mp >= s.np) return;
+    const int T = unit_tiles(s, mp, p.npt);
+    const int tps = split_tiles(T, p.splits);
+    const int nsp = (T + tps - 1) / tps;  // non-empty splits
+    if (nsp <= 1) return;                 // the whole unit was one split: written directly
+    const int row = blockIdx.y * (kCombineThreads / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    const int x = row / kTileM, r = row % kTileM;
+    if (x == 1 && (2 * mp + 1) * p.npt >= s.B) return;  // tile B absent
+    const int node = (2 * mp + x) * p.npt + r / p.G;
+    if (node >= min(s.B, (2 * mp + 2) * p.npt)) return;
+    const int head = g * p.G + r % p.G;
+    auto prow = [&](int k) {  // partial row of split k (slot 2 * CTA)
+        return (static_cast<long long>(2 * (u * p.splits + k)) * 2 + x) * kTileM + r;
+    };
+    // lane k: split k's running max and sum (nsp <= 32)
+    const float2 ml = (lane < nsp) ? p.part_ml[prow(lane)] : make_float2(-INFINITY, 0.0f);
+    float M = ml.x;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
+    const float w = (ml.x == -INFINITY) ? 0.0f : exp2f(ml.x - M);
+    float lsum = w * ml.y;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) lsum += __shfl_xor_sync(0xFFFFFFFFu, lsum, o);
+    float acc[kCols];
+#pragma unroll
+    for (int q = 0; q < kCols; ++q) acc[q] = 0.0f;
+    for (int k0 = 0; k0 < nsp; k0 += 8) {  // eight splits' loads in flight
+        float v[8][kCols];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int k = k0 + i;
+            const float* po = p.part_o + prow(k < nsp ? k : 0) * D + lane * kCols;
+#pragma unroll
+            for (int q = 0; q < kCols; ++q) v[i][q] = (k < nsp) ? po[q] : 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float wk = __shfl_sync(0xFFFFFFFFu, w, (k0 + i) & 31);
+            if (k0 + i < nsp)
+#pragma unroll
+                for (int q = 0; q < kCols; ++q) acc[q] += wk * v[i][q];
+        }
+    }
+    const float inv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+    const long long rowid = static_cast<long long>(s.off + node) * p.Hq + head;
+    __nv_bfloat16* dst = p.out + rowid * D + lane * kCols;
+#pragma unroll
+    for (int q = 0; q < kCols; q += 2)
+        *reinterpret_cast<uint32_t*>(dst + q) = pack_bf16x2(acc[q] * inv, acc[q + 1] * inv);
+    if (lane == 0 && p.lse) p.lse[rowid] = (M + log2f(lsum)) * 0.6931471805599453f;
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -1028,15 +1146,32 @@ static PFN_encodeTiled_t get_encode_fn() {
 }
 
 AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int dtype) {
-    (void)Hkv;
-    (void)max_pages;
     AttnPlan pl;
     const int G = Hq / Hkv;
     pl.rows_per_tile_nodes = kTileM / G;
     pl.mtiles = (max_tree + pl.rows_per_tile_nodes - 1) / pl.rows_per_tile_nodes;
     pl.grid = 0;
     pl.nseq = nseq;
-    if (dtype == JT_DTYPE_BF16) pl.grid = device_sm_count();  // one CTA per SM, every one the same tile count
+    pl.npairs = (pl.mtiles + 1) / 2;
+    pl.splits = 0;
+    if (dtype == JT_DTYPE_BF16) {
+        const int sms = device_sm_count();
+        pl.grid = sms;  // one CTA per SM, every one the same tile count
+        // Few units (at most half the SMs): split mode, each unit's keys split
+        // over sms / units CTAs (at most one split per two key tiles) and
+        // merged by the combine kernel.
+        const long long units = static_cast<long long>(nseq) * Hkv * pl.npairs;
+        const int tmax = (max_pages * JT_PAGE_SIZE + kTileN - 1) / kTileN;
+        if (units > 0 && 2 * units <= sms) {
+            int sp = static_cast<int>(sms / units);
+            sp = std::min(sp, std::max(1, tmax / 2));
+            sp = std::min(sp, 32);
+            if (sp >= 2) {
+                pl.splits = sp;
+                pl.grid = static_cast<int>(units) * sp;
+            }
+        }
+    }
     return pl;
 }
 
@@ -1127,6 +1262,8 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
     prm.Hkv = Hkv;
     prm.G = G;
     prm.npt = plan.rows_per_tile_nodes;
+    prm.splits = plan.splits;
+    prm.npairs = plan.npairs;
     prm.scale_log2 = scale * 1.4426950408889634f;
 
     using SL = SmemLayout<D>;
@@ -1136,8 +1273,11 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
                                                      cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc));
     }));
     if (ea != cudaSuccess) return ea;
-    return launch_kernel_pdl(tree_attn_tc_kernel<D>, dim3(plan.grid), dim3(kAttnThreads), SL::kAlloc, st, tq, tk,
-                             tv, prm);
+    cudaError_t e = launch_kernel_pdl(tree_attn_tc_kernel<D>, dim3(plan.grid), dim3(kAttnThreads), SL::kAlloc, st,
+                                      tq, tk, tv, prm);
+    if (e != cudaSuccess || plan.splits == 0) return e;
+    return launch_kernel_pdl(tree_attn_combine_kernel<D>, dim3(plan.grid / plan.splits, kCombineRowBlocks),
+                             dim3(kCombineThreads), 0, st, prm);
 }
 
 cudaError_t tree_attn_bf16_launch(const void* q, const void* k_cache, const void* v_cache,
