@@ -351,6 +351,18 @@ def make_workload(args, seed):
     return wk.make(args.config, seed=seed, overrides={"nseq": args.nseq, "budgets": budgets, "name": name})
 
 
+def attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, sms):
+    """Whether jt_tree_attn_paged runs in split mode (a second, combine
+    kernel): the library's rule -- at most half as many (sequence, KV head,
+    query-tile pair) units as SMs, and at least two key splits each."""
+    npt = 128 // (Hq // Hkv)
+    units = nseq * Hkv * ((-(-max_tree // npt) + 1) // 2)
+    tmax = -(-max_pages * 16 // 128)
+    if units <= 0 or 2 * units > sms:
+        return False
+    return min(sms // units, max(1, tmax // 2), 32) >= 2
+
+
 def config_dict(args, wl, world):
     """The workload description both arms print (identical dicts for the
     same command line)."""
@@ -756,12 +768,12 @@ def main():
                                  "sample": f"same, attention for {k1} of {total} nodes on one thread "
                                            f"({secs1:.1f} s)"}}
 
-    # tree build: top-W partials, row merge, expansion; attention: main
-    # kernel (+ split combine when the plan splits the keys); two acceptances
-    attn_split = jt.jt_workspace_size(jt.JT_OP_TREE_ATTN, nseq, 0, 0, 0, total, Hq, Hkv, D,
-                                      max_pages, max_tree) > 256
-    launches_per_step = (3 + (2 if attn_split else 1) + 2 + (1 if args.stochastic else 0)
-                         + (1 if args.adaptive else 0))
+    # our kernels per step: the build (top-W partials, then the expansion
+    # with the row merge; the adaptive build: partials, row merge, policy,
+    # capped expansion), the attention (one kernel; plus the combine in
+    # split mode), the acceptance rules
+    split = attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, torch.cuda.get_device_properties(dev).multi_processor_count)
+    launches_per_step = ((4 if args.adaptive else 2) + (2 if split else 1) + 2 + (1 if args.stochastic else 0))
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -64,3 +64,13 @@ def test_both_arms_describe_the_same_workload():
     a = bench.config_dict(args, wl, 1)
     b = bench.config_dict(args, wk.make(3, with_kv=False, with_draft=False), 1)
     assert a == b and a["workload"] == wk.CONFIGS[3]["name"] and a["nseq"] == 16
+
+
+def test_split_mode_rule_matches_the_workloads():
+    """bench.py's launch count follows the library's plan: split mode only
+    when the units are at most half the SMs (batch 1)."""
+    sms = 152
+    assert bench.attn_split_mode(1, 32, 8, 256, 273, sms)          # config 2: 32 units
+    assert not bench.attn_split_mode(32, 32, 8, 64, 2053, sms)     # config 4: 256 units
+    assert not bench.attn_split_mode(16, 32, 8, 256, 514, sms)     # config 3: 512 units at max_tree
+    assert not bench.attn_split_mode(1, 32, 8, 256, 2, sms)        # too few key tiles to split
