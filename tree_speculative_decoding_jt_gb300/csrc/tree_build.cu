@@ -149,6 +149,73 @@ __device__ __forceinline__ float warp_max_f(float x) {
 //   sum: per warp, exp(z - warp max) summed in float-float from the
 //   table-driven exp; warp 0 rescales the warp sums to the chunk maximum.
 // ---------------------------------------------------------------------------
+// Packed fp32 pairs: one instruction computes two independent lanes of
+// data on sm_100 and later, each lane rounded exactly like the scalar
+// operation (round to nearest, no fusion beyond what is written).
+struct F2 {
+    float x, y;
+};
+__device__ __forceinline__ F2 f2(float a, float b) { return F2{a, b}; }
+__device__ __forceinline__ F2 f2(float a) { return F2{a, a}; }
+#define JT_F2_OP(NAME, INSTR)                                                                                     \
+    __device__ __forceinline__ F2 NAME(F2 a, F2 b) {                                                              \
+        F2 d;                                                                                                     \
+        asm("{\n\t.reg .b64 a, b, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\t" INSTR             \
+            " d, a, b;\n\tmov.b64 {%0, %1}, d;\n\t}"                                                           \
+            : "=f"(d.x), "=f"(d.y)                                                                                \
+            : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));                                                            \
+        return d;                                                                                                 \
+    }
+JT_F2_OP(add2, "add.rn.f32x2")
+JT_F2_OP(sub2, "sub.rn.f32x2")
+JT_F2_OP(mul2, "mul.rn.f32x2")
+#undef JT_F2_OP
+__device__ __forceinline__ F2 fma2(F2 a, F2 b, F2 c) {
+    F2 d;
+    asm("{\n\t.reg .b64 a, b, c, d;\n\tmov.b64 a, {%2, %3};\n\tmov.b64 b, {%4, %5};\n\tmov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\tmov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+// Error-free sum of two pairs (two_sum on each lane).
+__device__ __forceinline__ void two_sum2(F2 a, F2 b, F2& s, F2& e) {
+    s = add2(a, b);
+    const F2 bb = sub2(s, a);
+    e = add2(sub2(a, sub2(s, bb)), sub2(b, bb));
+}
+
+// ffexp_in_range (ffexp.cuh: Tang's table-driven exp with error-free
+// transforms) on two entries at once: the same operations, each lane
+// rounded as there, with the negated reduction constants folded into the
+// multiplications (exact).
+__device__ __forceinline__ void ffexp_pair(F2 xh, F2 xl, const float* tab_hi, const float* tab_lo, F2& yh,
+                                           F2& yl) {
+    const F2 tk = fma2(xh, f2(kExpInvL), f2(kRoundMagic));
+    const F2 kf = sub2(tk, f2(kRoundMagic));
+    const int k0 = static_cast<int>(__float_as_uint(tk.x)) - 0x4B400000;
+    const int k1 = static_cast<int>(__float_as_uint(tk.y)) - 0x4B400000;
+    const F2 r1 = fma2(kf, f2(-kExpC1), xh);  // exact
+    const F2 rh = fma2(kf, f2(-kExpC2), r1);  // exact
+    const F2 rl = fma2(kf, f2(-kExpC3), xl);
+    const F2 rc = add2(rh, rl);
+    F2 p = fma2(rc, f2(1.0f / 120.0f), f2(1.0f / 24.0f));
+    p = fma2(rc, p, f2(1.0f / 6.0f));
+    p = fma2(rc, p, f2(0.5f));
+    p = mul2(mul2(rc, rc), p);
+    const F2 q = add2(rl, p);
+    const F2 th = f2(tab_hi[k0 & 63], tab_hi[k1 & 63]), tl = f2(tab_lo[k0 & 63], tab_lo[k1 & 63]);
+    const F2 prod = mul2(th, rh);
+    const F2 perr = fma2(th, rh, sub2(f2(0.0f), prod));
+    const F2 small = fma2(th, q, add2(fma2(tl, rh, tl), perr));
+    const F2 sm = add2(th, prod);  // |th| > |prod|: Fast2Sum
+    const F2 e = add2(sub2(th, sm), prod);
+    const F2 sc = f2(jt_pow2i(k0 >> 6), jt_pow2i(k1 >> 6));
+    yh = mul2(sm, sc);
+    yl = mul2(add2(e, small), sc);
+}
+
 template <bool VEC>
 __device__ __forceinline__ long long topw_slot_id(long long begin, int tid, int s) {
     return VEC ? begin + 4ll * (tid + kTopwThreads * (s >> 2)) + (s & 3)
@@ -264,8 +331,28 @@ __global__ void __launch_bounds__(kTopwThreads)
         // lifted to max - 87 (~87 after rounding): they then add ~1e-38 each
         // instead of 0, far below the sum's rounding (the sum is >= 1)
         const float floor_v = mw - 87.0f;
+        if (!ENT) {
+            // two entries per step on packed fp32 pairs, two running sums
+            // (even and odd slots) joined in float-float at the end
+            F2 ah = f2(0.0f), al = f2(0.0f);
 #pragma unroll
-        for (int i = 0; i < PER; ++i) {
+            for (int i = 0; i < PER; i += 2) {
+                const F2 xc = f2(fmaxf(x[i], floor_v), fmaxf(x[i + 1], floor_v));
+                F2 dh, dl;
+                two_sum2(xc, f2(-mw), dh, dl);
+                F2 yh, yl;
+                ffexp_pair(f2(fmaxf(dh.x, -87.0f), fmaxf(dh.y, -87.0f)), dl, s_thi, s_tlo, yh, yl);
+                F2 sum, err;
+                two_sum2(ah, yh, sum, err);
+                ah = sum;
+                al = add2(al, add2(err, yl));
+            }
+            const ffloat sa = ff_add(ff_norm(ah.x, al.x), ff_norm(ah.y, al.y));
+            acc_hi = sa.hi;
+            acc_lo = sa.lo;
+        }
+#pragma unroll
+        for (int i = 0; ENT && i < PER; ++i) {
             const float xc = fmaxf(x[i], floor_v);
             float dh, dl;
             two_sum(xc, -mw, dh, dl);
