@@ -351,16 +351,23 @@ def make_workload(args, seed):
     return wk.make(args.config, seed=seed, overrides={"nseq": args.nseq, "budgets": budgets, "name": name})
 
 
-def attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, sms):
+def attn_kernel(D):
+    """The attention kernel the library picks: the CTA-pair kernel for head
+    dim 128 when JT_ATTN_KERNEL=pair, else the single-SM kernel."""
+    return "pair" if D == 128 and os.environ.get("JT_ATTN_KERNEL") == "pair" else "single"
+
+
+def attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, slots):
     """Whether jt_tree_attn_paged runs in split mode (a second, combine
     kernel): the library's rule -- at most half as many (sequence, KV head,
-    query-tile pair) units as SMs, and at least two key splits each."""
+    query-tile pair) units as work slots (one per SM, or one per resident CTA
+    pair: SMs / 2), and at least two key splits each."""
     npt = 128 // (Hq // Hkv)
     units = nseq * Hkv * ((-(-max_tree // npt) + 1) // 2)
     tmax = -(-max_pages * 16 // 128)
-    if units <= 0 or 2 * units > sms:
+    if units <= 0 or 2 * units > slots:
         return False
-    return min(sms // units, max(1, tmax // 2), 32) >= 2
+    return min(slots // units, max(1, tmax // 2), 32) >= 2
 
 
 def config_dict(args, wl, world):
@@ -739,7 +746,8 @@ def main():
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu", c["name"])
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
-    roof["kernel"] = "jt_tree_attn_paged (tree_attn_tc_kernel + combine)"
+    roof["kernel"] = ("jt_tree_attn_paged (" + ("tree_attn_pair_kernel" if attn_kernel(c["D"]) == "pair"
+                                                 else "tree_attn_tc_kernel") + " + combine in split mode)")
     roof["algorithmic_bytes"] = int(bytes_a)
     roof["algorithmic_flops"] = int(flops_a)
     roof["attn_ms"] = attn_mean
@@ -772,7 +780,9 @@ def main():
     # with the row merge; the adaptive build: partials, row merge, policy,
     # capped expansion), the attention (one kernel; plus the combine in
     # split mode), the acceptance rules
-    split = attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, torch.cuda.get_device_properties(dev).multi_processor_count)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    kern = attn_kernel(c["D"])
+    split = attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, sms // 2 if kern == "pair" else sms)
     launches_per_step = ((4 if args.adaptive else 2) + (2 if split else 1) + 2 + (1 if args.stochastic else 0))
     if rank == 0:
         line = {

@@ -74,3 +74,8 @@ def test_split_mode_rule_matches_the_workloads():
     assert not bench.attn_split_mode(32, 32, 8, 64, 2053, sms)     # config 4: 256 units
     assert not bench.attn_split_mode(16, 32, 8, 256, 514, sms)     # config 3: 512 units at max_tree
     assert not bench.attn_split_mode(1, 32, 8, 256, 2, sms)        # too few key tiles to split
+    # the CTA-pair kernel has one work slot per two SMs
+    assert bench.attn_split_mode(1, 32, 8, 256, 273, sms // 2)     # config 2: 32 units, 2 splits
+    assert bench.attn_split_mode(2, 32, 8, 256, 273, sms)           # 64 units: split on 152 slots,
+    assert not bench.attn_split_mode(2, 32, 8, 256, 273, sms // 2)  # not on 76
+    assert bench.attn_kernel(128) in ("pair", "single") and bench.attn_kernel(64) == "single"

@@ -73,7 +73,7 @@ size_t jt_workspace_size(int op, int nseq, int N, int W, int64_t V, int total_no
             if (nseq < 1 || total_nodes < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv || D < 1 ||
                 max_pages < 1 || max_tree < 1 || max_tree > JT_MAX_TREE)
                 return 0;
-            const AttnPlan pl = attn_plan(nseq, Hkv, Hq, max_tree, max_pages, JT_DTYPE_BF16);
+            const AttnPlan pl = attn_plan(nseq, Hkv, Hq, D, max_tree, max_pages, JT_DTYPE_BF16);
             return attn_workspace_bytes(pl, total_nodes, Hq, D);
         }
         case JT_OP_VERIFY_ACCEPT:
@@ -238,7 +238,7 @@ jt_status jt_tree_attn_paged(const void* q, const void* k_cache, const void* v_c
     } else {
         if (D != 32 && D != 64 && D != 96 && D != 128) return JT_ERR_UNSUPPORTED;
     }
-    const AttnPlan pl = attn_plan(nseq, Hkv, Hq, max_tree, max_pages, dtype);
+    const AttnPlan pl = attn_plan(nseq, Hkv, Hq, D, max_tree, max_pages, dtype);
     jt_status s = check_ws(ws, ws_bytes, attn_workspace_bytes(pl, total_nodes, Hq, D));
     if (s != JT_OK) return s;
     char* base = static_cast<char*>(ws);

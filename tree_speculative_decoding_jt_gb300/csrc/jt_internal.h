@@ -82,13 +82,15 @@ cudaError_t verify_stochastic_launch(const float* z, const float* zd, const int3
 // tree_attn.cu / tree_attn_f32.cu
 struct AttnPlan {
     int grid;        // CTAs of the bf16 kernel (0 on the fp32 path)
+    int work;        // work slots: one per CTA, or one per CTA pair (pair != 0)
+    int pair;        // the CTA-pair kernel (D = 128): two CTAs per work slot
     int nseq;
     int mtiles;      // row tiles per (sequence, kv head) at max_tree
     int rows_per_tile_nodes;  // tree nodes per 128-row tile (128 / G)
-    int splits;      // > 0: split mode, one CTA per (unit, key split); 0: equal tile ranges per SM
+    int splits;      // > 0: split mode, one work slot per (unit, key split); 0: equal tile ranges per slot
     int npairs;      // query-tile pairs per (sequence, KV head) at max_tree
 };
-AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int dtype);
+AttnPlan attn_plan(int nseq, int Hkv, int Hq, int D, int max_tree, int max_pages, int dtype);
 size_t attn_workspace_bytes(const AttnPlan& p, int total_nodes, int Hq, int D);
 cudaError_t tree_attn_bf16_launch(const void* q, const void* k_cache, const void* v_cache,
                                   const int32_t* block_table, int max_pages, int num_pages,

@@ -58,6 +58,8 @@
 // then exp and P), lazy rescaling of O (only when the running max grows by
 // more than 2^8).  All waits are bounded in time.
 #include <algorithm>
+#include <cstdlib>
+#include <cstring>
 
 #include "jt_common.cuh"
 #include "jt_internal.h"
@@ -164,19 +166,22 @@ struct Piece {
     int gpos;  // global tile index of the piece's first tile
 };
 
-// Walks the pieces of this CTA's tile range in order.  Every role runs its
-// own copy over the same start position, so all roles see the same pieces.
+// Walks the pieces of one work slot's tile range in order.  Every role runs
+// its own copy over the same start position, so all roles see the same
+// pieces.  A work slot is one CTA of the single-SM kernel, or one CTA pair.
 struct Walker {
     SeqInfo s;
-    int b, g, mp, t, remaining, piece, gpos;
+    int b, g, mp, t, remaining, piece, gpos, work;
 
-    __device__ __forceinline__ void init(const AttnParams& p, const Bars* bars) {
+    template <typename BarsT>
+    __device__ __forceinline__ void init(const AttnParams& p, const BarsT* bars, int work_slot) {
         b = bars->w_b;
         g = bars->w_g;
         mp = bars->w_mp;
         t = bars->w_t;
         remaining = bars->w_quota;
-        gpos = static_cast<int>(blockIdx.x) * bars->w_P;
+        work = work_slot;
+        gpos = work * bars->w_P;
         piece = 0;
         if (remaining > 0) s = load_seq(p, b);
     }
@@ -192,7 +197,7 @@ struct Walker {
         pc.t0 = t;
         pc.nt = nt;
         pc.T = T;
-        pc.slot = (t == 0 && nt == T) ? -1 : 2 * static_cast<int>(blockIdx.x) + (piece == 0 ? 0 : 1);
+        pc.slot = (t == 0 && nt == T) ? -1 : 2 * work + (piece == 0 ? 0 : 1);
         pc.gpos = gpos;
         gpos += nt;
         remaining -= nt;
@@ -221,13 +226,14 @@ __device__ __forceinline__ int warp_sum(int v) {
     return v;
 }
 
-// The planner (one warp): the total tile count, this CTA's range and the
-// unit and tile its range starts at.  CTA 0 also records the plan for the
-// combine (T_total, P and each sequence's first global tile) and reports
-// sequences whose offsets or lengths are out of range.
-__device__ void plan_cta(const AttnParams& p, Bars* bars, int lane) {
+// The planner (one warp): the total tile count, the range of work slot
+// `work` (of nwork) and the unit and tile that range starts at.  With rec
+// set (one CTA of work slot 0) it also records the plan (T_total, P and each
+// sequence's first global tile) and reports sequences whose offsets or
+// lengths are out of range.
+template <typename BarsT>
+__device__ void plan_cta(const AttnParams& p, BarsT* bars, int lane, int work, int nwork, bool rec) {
     const int H = p.Hkv;
-    const bool rec = blockIdx.x == 0;
     long long total = 0;
     for (int base = 0; base < p.nseq; base += 32) {
         const int b = base + lane;
@@ -247,8 +253,8 @@ __device__ void plan_cta(const AttnParams& p, Bars* bars, int lane) {
         total = 0;
     }
     const int T_total = static_cast<int>(total);
-    const int P = T_total > 0 ? (T_total + gridDim.x - 1) / gridDim.x : 0;
-    const long long start = static_cast<long long>(blockIdx.x) * P;
+    const int P = T_total > 0 ? (T_total + nwork - 1) / nwork : 0;
+    const long long start = static_cast<long long>(work) * P;
     int quota = (start < T_total) ? static_cast<int>(min(static_cast<long long>(P), T_total - start)) : 0;
     if (rec && lane == 0) {
         p.plan[0] = T_total;
@@ -306,23 +312,23 @@ __device__ void plan_cta(const AttnParams& p, Bars* bars, int lane) {
     }
 }
 
-// Split mode: unit u = blockIdx.x / splits of the dense (b, g, mp) layout
-// (npairs pairs per KV head), key split blockIdx.x % splits of ceil(T /
-// splits) tiles.  CTAs whose pair lies past the sequence's tree, or whose
-// split is empty, get no tiles.
+// Split mode: work slot c holds unit u = c / splits of the dense (b, g, mp)
+// layout (npairs pairs per KV head), key split c % splits of ceil(T /
+// splits) tiles.  Slots whose pair lies past the sequence's tree, or whose
+// split is empty, get no tiles.  rec: report bad sequence contents.
 __device__ __forceinline__ int split_tiles(int T, int splits) { return (T + splits - 1) / splits; }
 
-__device__ void plan_cta_split(const AttnParams& p, Bars* bars, int lane) {
-    const int c = blockIdx.x;
+template <typename BarsT>
+__device__ void plan_cta_split(const AttnParams& p, BarsT* bars, int lane, int c, bool rec) {
     const int u = c / p.splits, sp = c % p.splits;
     const int b = u / (p.Hkv * p.npairs);
     const int rem = u % (p.Hkv * p.npairs);
     int quota = 0, t0 = 0;
     if (b < p.nseq) {
         const SeqInfo s = load_seq(p, b);
-        if (s.np < 0 && c == 0 && lane == 0) raise_error(p.err, DEVERR_INVALID);
-        // CTA 0 also reports the other sequences' bad contents
-        if (c == 0)
+        if (s.np < 0 && rec && lane == 0) raise_error(p.err, DEVERR_INVALID);
+        // the recording CTA also reports the other sequences' bad contents
+        if (rec)
             for (int bb = lane; bb < p.nseq; bb += 32)
                 if (bb != b && load_seq(p, bb).np < 0) raise_error(p.err, DEVERR_INVALID);
         const int mp = rem % p.npairs;
@@ -467,6 +473,21 @@ __device__ __forceinline__ float max_srow(const SRow& s) {
     return fmaxf(m0, m1);
 }
 
+// The same maximum over eight independent chains (a shorter dependency
+// chain, for kernels with registers to spare).
+__device__ __forceinline__ float max_srow8(const SRow& s) {
+    float m[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m[i] = fmaxf(__uint_as_float(s.c[i >> 1][(i & 1) * 16]), __uint_as_float(s.c[i >> 1][(i & 1) * 16 + 1]));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int c = 2; c < 16; c += 2)
+            m[i] = fmax3(m[i], __uint_as_float(s.c[i >> 1][(i & 1) * 16 + c]),
+                         __uint_as_float(s.c[i >> 1][(i & 1) * 16 + c + 1]));
+    return fmaxf(fmax3(m[0], m[1], m[2]), fmax3(fmax3(m[3], m[4], m[5]), m[6], m[7]));
+}
+
 // P = exp2(s * sl2 - m), packed to bf16 pairs into the first 64 columns of
 // the S region (the scores are already in registers); returns the row sum.
 // Per pair of scores: one packed FMA, two ex2, one packed add, one convert.
@@ -543,6 +564,209 @@ __device__ __forceinline__ int bt_group(const AttnParams& p, const Piece& pc, in
                : 0;
 }
 
+// Call numbers for the merge counts.  Every CTA of a call draws from the
+// workspace's ticket counter: the recording CTA (the first of work slot 0)
+// draws kTicketQuantum - (CTAs - 1) tickets and every other CTA one, so a
+// call draws exactly kTicketQuantum tickets whatever its grid, and all its
+// CTAs compute the same number, ticket / kTicketQuantum + 1.
+constexpr unsigned long long kTicketQuantum = 1ull << 24;
+
+__device__ __forceinline__ uint32_t draw_call_id(unsigned long long* tickets, bool first, unsigned ctas) {
+    const unsigned long long t = atomicAdd(tickets, first ? kTicketQuantum - (ctas - 1u) : 1ull);
+    return static_cast<uint32_t>(t / kTicketQuantum) + 1u;
+}
+
+// Output of one piece for this thread's query row (tile X, row r): the
+// normalised bf16 row and its lse when the piece is a whole unit, else the
+// fp32 partial row; when this work slot completes a cut unit, the merge of
+// all its pieces.  O_X is read from TMEM at tO (complete: the caller has
+// waited for the piece's last PV).  The four softmax warps of tile X call
+// this together; bar_id is their named barrier.
+template <int D, typename BarsT>
+__device__ __forceinline__ void piece_output(const AttnParams& p, const Piece& pc, BarsT* bars, int work, int x,
+                                             int r, int lane, int node, int head, bool valid_row, uint32_t tO,
+                                             uint8_t* stage, float m_run, float l_run, int bar_id) {
+    const long long rowid = static_cast<long long>(pc.s.off + node) * p.Hq + head;
+    const bool partial = pc.slot >= 0;
+    const long long prow = (static_cast<long long>(pc.slot) * 2 + x) * kTileM + r;  // partial row
+    const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
+    // Each warp stages its 32 output rows in its own 4 KB of shared
+    // memory, one 128-byte piece of each row at a time, and stores
+    // full lines (stage_store).
+    if (partial) {
+#pragma unroll 1
+        for (int h = 0; h < D / 32; ++h) {
+            uint32_t v[32];
+            tmem_ld32(tO + h * 32, v);
+            tmem_wait_ld();
+            uint4 slot[8];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) slot[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+            stage_store(stage, lane, slot, [&](int rr) {
+                const long long pr = __shfl_sync(0xFFFFFFFFu, prow, rr);
+                return reinterpret_cast<uint4*>(p.part_o + pr * D + h * 32);
+            });
+        }
+        p.part_ml[prow] = make_float2(m_run, l_run);
+    } else {
+#pragma unroll 1
+        for (int h = 0; h < D / 64; ++h) {
+            uint32_t v0[32], v1[32];
+            tmem_ld32(tO + h * 64, v0);
+            tmem_ld32(tO + h * 64 + 32, v1);
+            tmem_wait_ld();
+            uint4 slot[8];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                slot[c] = make_uint4(
+                    pack_bf16x2(__uint_as_float(v0[8 * c + 0]) * inv, __uint_as_float(v0[8 * c + 1]) * inv),
+                    pack_bf16x2(__uint_as_float(v0[8 * c + 2]) * inv, __uint_as_float(v0[8 * c + 3]) * inv),
+                    pack_bf16x2(__uint_as_float(v0[8 * c + 4]) * inv, __uint_as_float(v0[8 * c + 5]) * inv),
+                    pack_bf16x2(__uint_as_float(v0[8 * c + 6]) * inv, __uint_as_float(v0[8 * c + 7]) * inv));
+                slot[4 + c] = make_uint4(
+                    pack_bf16x2(__uint_as_float(v1[8 * c + 0]) * inv, __uint_as_float(v1[8 * c + 1]) * inv),
+                    pack_bf16x2(__uint_as_float(v1[8 * c + 2]) * inv, __uint_as_float(v1[8 * c + 3]) * inv),
+                    pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * inv, __uint_as_float(v1[8 * c + 5]) * inv),
+                    pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * inv, __uint_as_float(v1[8 * c + 7]) * inv));
+            }
+            stage_store(stage, lane, slot, [&](int rr) {
+                const long long rid = __shfl_sync(0xFFFFFFFFu, rowid, rr);
+                const bool rvalid = __shfl_sync(0xFFFFFFFFu, valid_row, rr);
+                return rvalid ? reinterpret_cast<uint4*>(p.out + rid * D + h * 64) : nullptr;
+            });
+        }
+        if (valid_row && p.lse) p.lse[rowid] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
+    }
+    if (partial && p.splits == 0) {
+        // count this piece done; the CTA that completes the unit
+        // merges every piece's partial rows (its own included).  Each
+        // query tile's four warps do this on their own (named barrier
+        // bar_id, count and flag per tile), so neither tile's warps ever
+        // wait for the other's.
+        const CutUnit cu(pc.gpos - pc.t0, pc.T, bars->w_P);
+        __threadfence();  // this thread's partial rows are visible GPU-wide
+        named_sync(bar_id, 128);
+        if (r == 0) {
+            const uint32_t cid = bars->call_id;
+            unsigned long long* ctr = p.merge_cnt + 2 * cu.c0 + x;
+            unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), assumed, nv;
+            do {  // a count from an earlier call restarts at this call's first piece
+                assumed = old;
+                nv = ((assumed >> 32) == cid) ? assumed + 1ull
+                                              : ((static_cast<unsigned long long>(cid) << 32) | 1ull);
+                old = atomicCAS(ctr, assumed, nv);
+            } while (old != assumed);
+            bars->merge_flag[x] = static_cast<int>(nv & 0xFFFFFFFFull) == cu.n;
+            __threadfence();  // the other pieces' rows are read after this count
+        }
+        named_sync(bar_id, 128);
+        if (bars->merge_flag[x]) {  // uniform over the tile's warps
+            // merge this row over the unit's pieces: M = max m_k,
+            // O = sum 2^(m_k - M) O_k / sum 2^(m_k - M) l_k.  This
+            // CTA's own piece is still in TMEM (O_X) and registers
+            // (m_run, l_run); the other pieces come from L2, each
+            // half row (64 columns) one batch of 16 loads in flight.
+            const int own = work - cu.c0;
+            float mk[kMaxMergeIn], lk[kMaxMergeIn];
+            float M = m_run;
+#pragma unroll
+            for (int i = 0; i < kMaxMergeIn; ++i) {  // every other piece's (m, l) in one round trip
+                const int k = i < own ? i : i + 1;
+                mk[i] = -INFINITY;
+                lk[i] = 0.0f;
+                if (k < cu.n) {
+                    const float2 ml = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]);
+                    mk[i] = ml.x;
+                    lk[i] = ml.y;
+                }
+            }
+            for (int k0 = kMaxMergeIn; k0 + 1 < cu.n; ++k0) {  // beyond the unrolled pieces (rare)
+                const int k = k0 < own ? k0 : k0 + 1;
+                M = fmaxf(M, __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).x);
+            }
+#pragma unroll
+            for (int i = 0; i < kMaxMergeIn; ++i) M = fmaxf(M, mk[i]);
+            // weights and sums in piece order, whichever CTA merges,
+            // so that every call rounds the same way
+            const float w_own = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - M);
+#pragma unroll
+            for (int i = 0; i < kMaxMergeIn; ++i) mk[i] = (mk[i] == -INFINITY) ? 0.0f : exp2f(mk[i] - M);
+            auto weight_of = [&](int k) {  // piece k's weight (k != own)
+                const int i = k < own ? k : k - 1;
+                float w = mk[0];
+#pragma unroll
+                for (int j = 1; j < kMaxMergeIn; ++j)
+                    if (j == i) w = mk[j];
+                if (i >= kMaxMergeIn) {
+                    const float ms = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).x;
+                    w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
+                }
+                return w;
+            };
+            auto sum_of = [&](int k) {  // piece k's row sum (k != own)
+                const int i = k < own ? k : k - 1;
+                float l = lk[0];
+#pragma unroll
+                for (int j = 1; j < kMaxMergeIn; ++j)
+                    if (j == i) l = lk[j];
+                if (i >= kMaxMergeIn) l = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).y;
+                return l;
+            };
+            float lsum = 0.0f;
+            for (int k = 0; k < cu.n; ++k) lsum += (k == own) ? w_own * l_run : weight_of(k) * sum_of(k);
+            const float minv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
+#pragma unroll 1
+            for (int h = 0; h < D / 64; ++h) {
+                uint32_t packed[32];  // the 64 output columns of this staged piece, bf16 pairs
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    const int col = h * 64 + half * 32;
+                    float acc[32];
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) acc[c] = 0.0f;
+#pragma unroll 1
+                    for (int k = 0; k < cu.n; ++k) {
+                        if (k == own) {  // this CTA's piece, from TMEM (k is the same for the whole warp)
+                            uint32_t v[32];
+                            tmem_ld32(tO + col, v);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int c = 0; c < 32; ++c) acc[c] += w_own * __uint_as_float(v[c]);
+                        } else {
+                            const long long pr = (static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r;
+                            const float wgt = weight_of(k);
+                            const float4* po = reinterpret_cast<const float4*>(p.part_o + pr * D + col);
+                            float4 q[8];
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) q[c] = __ldcg(po + c);
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                acc[4 * c + 0] += wgt * q[c].x;
+                                acc[4 * c + 1] += wgt * q[c].y;
+                                acc[4 * c + 2] += wgt * q[c].z;
+                                acc[4 * c + 3] += wgt * q[c].w;
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int c = 0; c < 16; ++c)
+                        packed[half * 16 + c] = pack_bf16x2(acc[2 * c] * minv, acc[2 * c + 1] * minv);
+                }
+                uint4 slot[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    slot[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
+                stage_store(stage, lane, slot, [&](int rr) {
+                    const long long rid = __shfl_sync(0xFFFFFFFFu, rowid, rr);
+                    const bool rvalid = __shfl_sync(0xFFFFFFFFu, valid_row, rr);
+                    return rvalid ? reinterpret_cast<uint4*>(p.out + rid * D + h * 64) : nullptr;
+                });
+            }
+            if (valid_row && p.lse) p.lse[rowid] = (M + log2f(lsum)) * 0.6931471805599453f;
+        }
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -556,6 +780,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     Bars* bars = reinterpret_cast<Bars*>(smem + SL::kBar);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int work = blockIdx.x;  // one work slot per CTA
     // Set-up that reads no global memory (barriers, TMEM, tensor-map
     // prefetch) runs before the wait for the previous kernel, overlapping
     // its tail when this grid is launched as its programmatic dependent.
@@ -587,12 +812,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     pdl_wait();  // no global memory is read before the previous kernel's writes are visible
     if (warp == 8) {
         if (p.splits > 0)
-            plan_cta_split(p, bars, lane);
+            plan_cta_split(p, bars, lane, blockIdx.x, blockIdx.x == 0);
         else
-            plan_cta(p, bars, lane);
+            plan_cta(p, bars, lane, blockIdx.x, gridDim.x, blockIdx.x == 0);
     }
-    if (tid == 0)  // every CTA of a call draws one ticket before anything can fail
-        bars->call_id = static_cast<uint32_t>(atomicAdd(p.tickets, 1ull) / gridDim.x) + 1u;
+    if (tid == 0)  // every CTA of a call draws its tickets before anything can fail
+        bars->call_id = draw_call_id(p.tickets, blockIdx.x == 0, gridDim.x);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -611,7 +836,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 8) {
         // ------------------------------------------------------------ TMA
         Walker w;
-        w.init(p, bars);
+        w.init(p, bars, work);
         Piece pc;
         int jj = 0, npc = 0, q_pending = 0;
         int k_iss = 0, v_iss = 0;  // K / V tiles whose copies have been issued
@@ -714,7 +939,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), SL::kChunkBytes, 1024);
         constexpr uint32_t kTileStep = SL::kTileBytes >> 4;  // one tile / stage in 16-byte units
         Walker w;
-        w.init(p, bars);
+        w.init(p, bars, work);
         Piece pc;
         int jj = 0, npc = 0;
         int cnt[2] = {0, 0};  // tiles handed to each query tile's softmax so far
@@ -775,7 +1000,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const float sl2 = p.scale_log2;
         uint8_t* stage = smem + SL::kStage + warp * 4096;
         Walker w;
-        w.init(p, bars);
+        w.init(p, bars, work);
         Piece pc;
         int cnt = 0, nfin = 0;
         bool ok = true;
@@ -861,185 +1086,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             ++nfin;
             tc_fence_after();
-            const long long rowid = static_cast<long long>(pc.s.off + node) * p.Hq + head;
-            const bool partial = pc.slot >= 0;
-            const long long prow = (static_cast<long long>(pc.slot) * 2 + x) * kTileM + r;  // partial row
-            const float inv = (l_run > 0.0f) ? 1.0f / l_run : 0.0f;
-            // Each warp stages its 32 output rows in its own 4 KB of shared
-            // memory, one 128-byte piece of each row at a time, and stores
-            // full lines (stage_store).
-            if (partial) {
-#pragma unroll 1
-                for (int h = 0; h < D / 32; ++h) {
-                    uint32_t v[32];
-                    tmem_ld32(tO + h * 32, v);
-                    tmem_wait_ld();
-                    uint4 slot[8];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) slot[c] = make_uint4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                    stage_store(stage, lane, slot, [&](int rr) {
-                        const long long pr = __shfl_sync(0xFFFFFFFFu, prow, rr);
-                        return reinterpret_cast<uint4*>(p.part_o + pr * D + h * 32);
-                    });
-                }
-                p.part_ml[prow] = make_float2(m_run, l_run);
-            } else {
-#pragma unroll 1
-                for (int h = 0; h < D / 64; ++h) {
-                    uint32_t v0[32], v1[32];
-                    tmem_ld32(tO + h * 64, v0);
-                    tmem_ld32(tO + h * 64 + 32, v1);
-                    tmem_wait_ld();
-                    uint4 slot[8];
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        slot[c] = make_uint4(
-                            pack_bf16x2(__uint_as_float(v0[8 * c + 0]) * inv, __uint_as_float(v0[8 * c + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(v0[8 * c + 2]) * inv, __uint_as_float(v0[8 * c + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(v0[8 * c + 4]) * inv, __uint_as_float(v0[8 * c + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(v0[8 * c + 6]) * inv, __uint_as_float(v0[8 * c + 7]) * inv));
-                        slot[4 + c] = make_uint4(
-                            pack_bf16x2(__uint_as_float(v1[8 * c + 0]) * inv, __uint_as_float(v1[8 * c + 1]) * inv),
-                            pack_bf16x2(__uint_as_float(v1[8 * c + 2]) * inv, __uint_as_float(v1[8 * c + 3]) * inv),
-                            pack_bf16x2(__uint_as_float(v1[8 * c + 4]) * inv, __uint_as_float(v1[8 * c + 5]) * inv),
-                            pack_bf16x2(__uint_as_float(v1[8 * c + 6]) * inv, __uint_as_float(v1[8 * c + 7]) * inv));
-                    }
-                    stage_store(stage, lane, slot, [&](int rr) {
-                        const long long rid = __shfl_sync(0xFFFFFFFFu, rowid, rr);
-                        const bool rvalid = __shfl_sync(0xFFFFFFFFu, valid_row, rr);
-                        return rvalid ? reinterpret_cast<uint4*>(p.out + rid * D + h * 64) : nullptr;
-                    });
-                }
-                if (valid_row && p.lse) p.lse[rowid] = (m_run + __log2f(l_run)) * 0.6931471805599453f;
-            }
-            if (partial && p.splits == 0) {
-                // count this piece done; the CTA that completes the unit
-                // merges every piece's partial rows (its own included).  Each
-                // query tile's four warps do this on their own (barrier 1 + X,
-                // count and flag per tile), so neither tile's warps ever wait
-                // for the other's.
-                const CutUnit cu(pc.gpos - pc.t0, pc.T, bars->w_P);
-                __threadfence();  // this thread's partial rows are visible GPU-wide
-                named_sync(1 + x, 128);
-                if (r == 0) {
-                    const uint32_t cid = bars->call_id;
-                    unsigned long long* ctr = p.merge_cnt + 2 * cu.c0 + x;
-                    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(ctr), assumed, nv;
-                    do {  // a count from an earlier call restarts at this call's first piece
-                        assumed = old;
-                        nv = ((assumed >> 32) == cid) ? assumed + 1ull
-                                                      : ((static_cast<unsigned long long>(cid) << 32) | 1ull);
-                        old = atomicCAS(ctr, assumed, nv);
-                    } while (old != assumed);
-                    bars->merge_flag[x] = static_cast<int>(nv & 0xFFFFFFFFull) == cu.n;
-                    __threadfence();  // the other pieces' rows are read after this count
-                }
-                named_sync(1 + x, 128);
-                if (bars->merge_flag[x]) {  // uniform over the tile's warps
-                    // merge this row over the unit's pieces: M = max m_k,
-                    // O = sum 2^(m_k - M) O_k / sum 2^(m_k - M) l_k.  This
-                    // CTA's own piece is still in TMEM (O_X) and registers
-                    // (m_run, l_run); the other pieces come from L2, each
-                    // half row (64 columns) one batch of 16 loads in flight.
-                    const int own = static_cast<int>(blockIdx.x) - cu.c0;
-                    float mk[kMaxMergeIn], lk[kMaxMergeIn];
-                    float M = m_run;
-#pragma unroll
-                    for (int i = 0; i < kMaxMergeIn; ++i) {  // every other piece's (m, l) in one round trip
-                        const int k = i < own ? i : i + 1;
-                        mk[i] = -INFINITY;
-                        lk[i] = 0.0f;
-                        if (k < cu.n) {
-                            const float2 ml = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]);
-                            mk[i] = ml.x;
-                            lk[i] = ml.y;
-                        }
-                    }
-                    for (int k0 = kMaxMergeIn; k0 + 1 < cu.n; ++k0) {  // beyond the unrolled pieces (rare)
-                        const int k = k0 < own ? k0 : k0 + 1;
-                        M = fmaxf(M, __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).x);
-                    }
-#pragma unroll
-                    for (int i = 0; i < kMaxMergeIn; ++i) M = fmaxf(M, mk[i]);
-                    // weights and sums in piece order, whichever CTA merges,
-                    // so that every call rounds the same way
-                    const float w_own = (m_run == -INFINITY) ? 0.0f : exp2f(m_run - M);
-#pragma unroll
-                    for (int i = 0; i < kMaxMergeIn; ++i) mk[i] = (mk[i] == -INFINITY) ? 0.0f : exp2f(mk[i] - M);
-                    auto weight_of = [&](int k) {  // piece k's weight (k != own)
-                        const int i = k < own ? k : k - 1;
-                        float w = mk[0];
-#pragma unroll
-                        for (int j = 1; j < kMaxMergeIn; ++j)
-                            if (j == i) w = mk[j];
-                        if (i >= kMaxMergeIn) {
-                            const float ms = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).x;
-                            w = (ms == -INFINITY) ? 0.0f : exp2f(ms - M);
-                        }
-                        return w;
-                    };
-                    auto sum_of = [&](int k) {  // piece k's row sum (k != own)
-                        const int i = k < own ? k : k - 1;
-                        float l = lk[0];
-#pragma unroll
-                        for (int j = 1; j < kMaxMergeIn; ++j)
-                            if (j == i) l = lk[j];
-                        if (i >= kMaxMergeIn) l = __ldcg(&p.part_ml[(static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r]).y;
-                        return l;
-                    };
-                    float lsum = 0.0f;
-                    for (int k = 0; k < cu.n; ++k) lsum += (k == own) ? w_own * l_run : weight_of(k) * sum_of(k);
-                    const float minv = (lsum > 0.0f) ? 1.0f / lsum : 0.0f;
-#pragma unroll 1
-                    for (int h = 0; h < D / 64; ++h) {
-                        uint32_t packed[32];  // the 64 output columns of this staged piece, bf16 pairs
-#pragma unroll
-                        for (int half = 0; half < 2; ++half) {
-                            const int col = h * 64 + half * 32;
-                            float acc[32];
-#pragma unroll
-                            for (int c = 0; c < 32; ++c) acc[c] = 0.0f;
-#pragma unroll 1
-                            for (int k = 0; k < cu.n; ++k) {
-                                if (k == own) {  // this CTA's piece, from TMEM (k is the same for the whole warp)
-                                    uint32_t v[32];
-                                    tmem_ld32(tO + col, v);
-                                    tmem_wait_ld();
-#pragma unroll
-                                    for (int c = 0; c < 32; ++c) acc[c] += w_own * __uint_as_float(v[c]);
-                                } else {
-                                    const long long pr = (static_cast<long long>(cu.slot(k)) * 2 + x) * kTileM + r;
-                                    const float wgt = weight_of(k);
-                                    const float4* po = reinterpret_cast<const float4*>(p.part_o + pr * D + col);
-                                    float4 q[8];
-#pragma unroll
-                                    for (int c = 0; c < 8; ++c) q[c] = __ldcg(po + c);
-#pragma unroll
-                                    for (int c = 0; c < 8; ++c) {
-                                        acc[4 * c + 0] += wgt * q[c].x;
-                                        acc[4 * c + 1] += wgt * q[c].y;
-                                        acc[4 * c + 2] += wgt * q[c].z;
-                                        acc[4 * c + 3] += wgt * q[c].w;
-                                    }
-                                }
-                            }
-#pragma unroll
-                            for (int c = 0; c < 16; ++c)
-                                packed[half * 16 + c] = pack_bf16x2(acc[2 * c] * minv, acc[2 * c + 1] * minv);
-                        }
-                        uint4 slot[8];
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            slot[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2], packed[4 * c + 3]);
-                        stage_store(stage, lane, slot, [&](int rr) {
-                            const long long rid = __shfl_sync(0xFFFFFFFFu, rowid, rr);
-                            const bool rvalid = __shfl_sync(0xFFFFFFFFu, valid_row, rr);
-                            return rvalid ? reinterpret_cast<uint4*>(p.out + rid * D + h * 64) : nullptr;
-                        });
-                    }
-                    if (valid_row && p.lse) p.lse[rowid] = (M + log2f(lsum)) * 0.6931471805599453f;
-                }
-            }
+            piece_output<D>(p, pc, bars, work, x, r, lane, node, head, valid_row, tO, stage, m_run, l_run, 1 + x);
             // O_X has been read (tcgen05.wait::ld above) before this thread
             // arrives on p_full[X] for the next piece's first tile, which is
             // what lets the MMA warp overwrite O_X
@@ -1051,6 +1098,483 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (warp == 9) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
+    }
+}
+
+// ===========================================================================
+// CTA-pair kernel (D = 128)
+//
+// The two CTAs of a cluster (a pair, on two SMs) run one work slot: CTA
+// rank X takes query tile X of each unit, and one tcgen05.mma.cta_group::2
+// of M = 256 covers both tiles, issued by CTA 0 (the leader).  Each CTA
+// holds its half of every K tile (keys 64X..64X+63, all 128 dims) and of
+// every V tile (all 128 keys, dims 64X..64X+63); the MMA reads B's halves
+// from both CTAs, so a unit's K/V cross HBM and shared memory once while
+// each SM's tensor core does the MMAs of its own 128 rows.  Against the
+// single-SM kernel this halves the shared-memory reads per MMA (the K/V
+// operand is split) and leaves room in TMEM for three S buffers: per CTA
+// S0, S1, S2 (128 columns each) and O (128).  MMAs from one thread run in
+// issue order, and QK(t) may overwrite S(t mod 3) only after PV(t-3) has
+// read P(t-3) from it, so with three buffers QK(j+1) and QK(j+2) are not
+// queued behind PV(j-1): the tensor core scores the next tiles while
+// softmax works on tile j.
+//
+// Warp roles (224 threads per CTA):
+//   warps 0-3  softmax + epilogue of this CTA's query tile, one row per
+//              thread (TMEM lane);
+//   warp 4     planner, then TMA producer of this CTA's Q tile and K halves
+//              (the leader's barriers count both CTAs' bytes);
+//   warp 5     TMEM allocation; in the leader, the single-thread MMA issuer;
+//   warp 6     TMA producer of this CTA's V halves.
+// Issue order per piece: QK(0), QK(1), QK(2), then per tile j: PV(j),
+// QK(j+3) (later, after PV(j+1) or PV(j+2), when its K lands late).  Per
+// tile the eight softmax warps of the pair arrive on the leader's
+// p_full[j mod 3].  Every PV commits one phase of o_done, and every softmax
+// warp waits for PV(t-1) before it releases P(t) (and before rescaling O):
+// that keeps o_done within one phase of each waiter's count, and neither
+// CTA's softmax more than one tile ahead of the other's.
+// ===========================================================================
+constexpr int kPairThreads = 224;
+constexpr int kPairKStages = 6;  // K ring depth (half tiles): a K slot frees at QK, early
+constexpr int kPairVStages = 4;  // V ring depth (half tiles): a V slot frees at PV
+
+struct PairSmem {
+    static constexpr int kQChunk = kTileM * 128;  // 128 query rows x 64 dims
+    static constexpr int kQBytes = 2 * kQChunk;
+    static constexpr int kKChunk = 64 * 128;      // 64 keys x 64 dims
+    static constexpr int kKHalf = 2 * kKChunk;    // this CTA's 64 keys x 128 dims
+    static constexpr int kVHalf = kTileN * 128;   // 128 keys x this CTA's 64 dims
+    static constexpr int kQ = 0;
+    static constexpr int kK = kQ + kQBytes;
+    static constexpr int kV = kK + kPairKStages * kKHalf;
+    static constexpr int kStage = kV + kPairVStages * kVHalf;  // epilogue staging, 4 KB per softmax warp
+    static constexpr int kBar = kStage + 4 * 4096;
+    static constexpr int kBytes = kBar + 512;
+    static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024
+};
+
+struct PairBars {
+    uint64_t q_full;                // leader: both CTAs' Q tiles have landed
+    uint64_t q_empty;               // every QK of the piece has completed
+    uint64_t k_full[kPairKStages];   // leader: both halves of the stage's K tile have landed
+    uint64_t k_empty[kPairKStages];  // QK of the stage's tile has completed
+    uint64_t v_full[kPairVStages];   // leader: both halves of the stage's V tile have landed
+    uint64_t v_empty[kPairVStages];  // PV of the stage's tile has completed
+    uint64_t v_own[kPairVStages];    // this CTA's half of a unit-final V tile has landed
+    uint64_t v_last[kPairVStages];   // leader: both halves of a unit-final V tile are zero-filled
+    uint64_t s_full[3];             // S buffer X holds QK of its latest tile
+    uint64_t p_full[3];             // leader: P of the tile in S buffer X, from the pair's 8 softmax warps
+    uint64_t o_done;                // one phase per PV
+    uint64_t mma_final;             // every MMA of the pair has completed
+    uint32_t tmem_base;
+    int abort;
+    int w_b, w_g, w_mp, w_t, w_quota, w_P;
+    uint32_t call_id;
+    int merge_flag[2];
+};
+static_assert(sizeof(PairBars) <= 512, "barrier block");
+
+__device__ __forceinline__ void commit_pair_warp(uint64_t* bar) {
+    if (elect_one()) mma_commit_pair(bar);
+    __syncwarp();
+}
+
+// S (+)= Q K^T over the pair: 8 MMAs of M = 256, N = 128, K = 16.
+__device__ __forceinline__ void issue_qk_pair(uint32_t tS, uint64_t dq, uint64_t dk) {
+    constexpr uint32_t idesc = idesc_bf16_f32(2 * kTileM, kTileN, false);
+    if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t qo = ((kk >> 2) * PairSmem::kQChunk + (kk & 3) * 32) >> 4;
+            const uint32_t ko = ((kk >> 2) * PairSmem::kKChunk + (kk & 3) * 32) >> 4;
+            mma_ss_pair(tS, dq + qo, dk + ko, idesc, kk > 0 ? 1u : 0u);
+        }
+    }
+    __syncwarp();
+}
+
+// O (+)= P V over the pair, P (bf16 pairs) in the first 64 columns of an S
+// buffer: 8 MMAs of M = 256, N = 128, K = 16.
+__device__ __forceinline__ void issue_pv_pair(uint32_t tO, uint32_t tP, uint64_t dv, bool accumulate) {
+    constexpr uint32_t idesc = idesc_bf16_f32(2 * kTileM, 128, true);
+    if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < kTileN / 16; ++kk)
+            mma_ts_pair(tO, tP + kk * 8, dv + kk * ((16 * 128) >> 4), idesc, (accumulate || kk > 0) ? 1u : 0u);
+    }
+    __syncwarp();
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+    tree_attn_pair_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                          const __grid_constant__ CUtensorMap tm_v, const AttnParams p) {
+    constexpr int D = 128;
+    using SL = PairSmem;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    PairBars* bars = reinterpret_cast<PairBars*>(smem + SL::kBar);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: the leader, which issues the pair's MMAs
+    const int work = static_cast<int>(blockIdx.x >> 1), nwork = static_cast<int>(gridDim.x >> 1);
+    if (tid == 0) {
+        mbar_init(&bars->q_full, 1);
+        mbar_init(&bars->q_empty, 1);
+        for (int s = 0; s < kPairKStages; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->k_empty[s], 1);
+        }
+        for (int s = 0; s < kPairVStages; ++s) {
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->v_empty[s], 1);
+            mbar_init(&bars->v_own[s], 1);
+            mbar_init(&bars->v_last[s], 2);
+        }
+        for (int x = 0; x < 3; ++x) {
+            mbar_init(&bars->s_full[x], 1);
+            mbar_init(&bars->p_full[x], 8);
+        }
+        mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->mma_final, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == 5) tmem_alloc_pair(&bars->tmem_base, 512);
+    cluster_sync();  // both CTAs' barriers exist before any copy, commit or arrive crosses the pair
+    pdl_wait();
+    if (warp == 4) {
+        const bool rec = work == 0 && rank == 0;
+        if (p.splits > 0)
+            plan_cta_split(p, bars, lane, work, rec);
+        else
+            plan_cta(p, bars, lane, work, nwork, rec);
+    }
+    if (tid == 0) bars->call_id = draw_call_id(p.tickets, work == 0 && rank == 0, gridDim.x);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    volatile int* abort = &bars->abort;
+    const bool has_work = bars->w_quota > 0;  // the same in both CTAs: one plan per work slot
+
+    uint8_t* sQ = smem + SL::kQ;
+    uint8_t* sK = smem + SL::kK;
+    uint8_t* sV = smem + SL::kV;
+    const int npt = p.npt;
+
+    if (!has_work) {
+        // nothing issued: both CTAs go straight to the teardown
+    } else if (warp == 4 || warp == 6) {
+        // ------------------------------------------------------------ TMA
+        // warp 4: Q and K, warp 6: V.  Each walks the pieces on its own, so
+        // K copies run ahead of V's (a K slot frees at QK, a V slot at PV).
+        const bool kw = warp == 4;
+        const int nst = kw ? kPairKStages : kPairVStages;
+        Walker w;
+        w.init(p, bars, work);
+        Piece pc;
+        int jj = 0, npc = 0, q_pending = 0;
+        int iss = 0;  // tiles whose copies this warp has issued
+        int vo[kPairVStages] = {0, 0, 0, 0};
+        const uint32_t lead_q = cluster_map(&bars->q_full, 0);
+        bool ok = true;
+        while (ok && !*abort && w.next(p, pc)) {
+            const int valid_end = unit_end(pc.s, pc.mp, npt);
+            if (kw) {
+                // Q of this piece (this CTA's tile; the peer's tile may lie
+                // past the tree: its rows are then never written out)
+                if (npc > 0 && !mbar_wait_warp(&bars->q_empty, (npc - 1) & 1, p.err, abort)) break;
+                if (lane == 0) {
+                    if (rank == 0) mbar_arrive_expect_tx(&bars->q_full, 2 * SL::kQBytes);
+                    for (int c = 0; c < 2; ++c)
+                        tma_load_3d_pair(sQ + c * SL::kQChunk, &tm_q, lead_q, c * 64, pc.g * p.G,
+                                         pc.s.off + (2 * pc.mp + static_cast<int>(rank)) * npt);
+                }
+                q_pending = npc + 1;
+            }
+            int bt_cur = bt_group(p, pc, valid_end, 0, lane);
+            int bt_nxt = bt_group(p, pc, valid_end, 1, lane);
+            int bt_nn = bt_group(p, pc, valid_end, 2, lane);
+            for (int j = 0; j < pc.nt; ++j, ++jj) {
+                const int st = jj % nst;
+                const uint32_t empty_parity = ((jj / nst) & 1) ^ 1;
+                if (j > 0 && (j & 3) == 0) {
+                    bt_cur = bt_nxt;
+                    bt_nxt = bt_nn;
+                    bt_nn = bt_group(p, pc, valid_end, (j >> 2) + 2, lane);
+                }
+                const int slot0 = (pc.t0 + j) * kTileN;
+                const int nvalid = min(kTileN, valid_end - slot0);
+                const int npg = (nvalid + JT_PAGE_SIZE - 1) / JT_PAGE_SIZE;
+                const int pid = __shfl_sync(0xFFFFFFFFu, bt_cur, ((j & 3) << 3) + (lane & 7));
+                JT_DCHECK(lane >= npg || (pid >= 0 && pid < p.num_pages), p.err);  // block-table entry in the pool
+                const uint32_t bytes = npg * 2 * (JT_PAGE_SIZE * 128);  // both CTAs' halves
+                if (kw) {
+                    // K: this CTA's 64 keys (pages 4X..4X+3 of the tile), both
+                    // 64-dim chunks; the slot frees once QK of tile jj - nst is done
+                    if (jj >= nst && !mbar_wait_warp(&bars->k_empty[st], empty_parity, p.err, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    if (lane == 0 && rank == 0) mbar_arrive_expect_tx(&bars->k_full[st], bytes);
+                    __syncwarp();
+                    if (lane < npg && (lane >> 2) == static_cast<int>(rank)) {
+                        const uint32_t lead = cluster_map(&bars->k_full[st], 0);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_4d_pair(sK + st * SL::kKHalf + c * SL::kKChunk + (lane & 3) * (JT_PAGE_SIZE * 128),
+                                             &tm_k, lead, c * 64, pc.g, 0, pid);
+                    }
+                    iss = jj + 1;
+                    continue;
+                }
+                // V: this CTA's 64 dims of every key; the slot frees once PV
+                // of tile jj - nst is done
+                if (jj >= nst && !mbar_wait_warp(&bars->v_empty[st], empty_parity, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* vt = sV + st * SL::kVHalf;
+                if (pc.t0 + j != pc.T - 1) {
+                    if (lane == 0 && rank == 0) mbar_arrive_expect_tx(&bars->v_full[st], bytes);
+                    __syncwarp();
+                    if (lane < npg)
+                        tma_load_4d_pair(vt + lane * (JT_PAGE_SIZE * 128), &tm_v, cluster_map(&bars->v_full[st], 0),
+                                         static_cast<int>(rank) * 64, pc.g, 0, pid);
+                } else {
+                    // the unit's final tile: each CTA lands its half on its
+                    // own barrier, zeroes the rows past the last needed slot
+                    // (stale or foreign data: P is 0 there but 0 * NaN would
+                    // not be) and reports to the leader's v_last; the
+                    // leader's v_full phase of this tile completes empty
+                    if (lane == 0) {
+                        if (rank == 0) mbar_arrive(&bars->v_full[st]);
+                        mbar_arrive_expect_tx(&bars->v_own[st], npg * (JT_PAGE_SIZE * 128));
+                    }
+                    __syncwarp();
+                    if (lane < npg)
+                        tma_load_4d(vt + lane * (JT_PAGE_SIZE * 128), &tm_v, &bars->v_own[st],
+                                    static_cast<int>(rank) * 64, pc.g, 0, pid);
+                    if (!mbar_wait_warp(&bars->v_own[st], vo[st] & 1, p.err, abort)) {
+                        ok = false;
+                        break;
+                    }
+                    ++vo[st];
+                    const int n16 = (kTileN - nvalid) * 8;  // 16-byte pieces
+                    for (int idx = lane; idx < n16; idx += 32)
+                        reinterpret_cast<uint4*>(vt + (nvalid + (idx >> 3)) * 128)[idx & 7] = make_uint4(0u, 0u, 0u, 0u);
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(cluster_map(&bars->v_last[st], 0));
+                }
+                iss = jj + 1;
+            }
+            if (!ok) break;
+            ++npc;
+        }
+        // on abort: the leader lets the copies it counted land before the
+        // pair exits (the peer's copies report to the leader's barriers)
+        if (*abort && rank == 0) {
+            uint64_t* full = kw ? bars->k_full : bars->v_full;
+            for (int j = max(0, iss - nst); j < iss; ++j) mbar_wait(&full[j % nst], (j / nst) & 1, p.err, nullptr);
+            if (kw && q_pending > 0) mbar_wait(&bars->q_full, (q_pending - 1) & 1, p.err, nullptr);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA
+        if (rank == 0) {
+            const uint64_t dq0 = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+            const uint64_t dk0 = smem_desc_sw128(smem_u32(sK), 16, 1024);
+            const uint64_t dv0 = smem_desc_sw128(smem_u32(sV), SL::kVHalf, 1024);
+            Walker w;
+            w.init(p, bars, work);
+            Piece pc;
+            int jj = 0, npc = 0;
+            int vl[kPairVStages] = {0, 0, 0, 0};
+            bool ok = true;
+            while (ok && w.next(p, pc)) {
+                ok = mbar_wait_warp(&bars->q_full, npc & 1, p.err, abort);
+                const int j0 = jj;
+                int issued = 0;  // QKs of this piece issued
+                // QK of the piece's next tile; block: wait for its K, else
+                // return false when K has not landed yet
+                auto qk_next = [&](bool block) -> bool {
+                    const int t = j0 + issued, st = t % kPairKStages;
+                    const uint32_t par = (t / kPairKStages) & 1;
+                    if (block) {
+                        if (!mbar_wait_warp(&bars->k_full[st], par, p.err, abort)) {
+                            ok = false;
+                            return false;
+                        }
+                    } else if (!__all_sync(0xFFFFFFFFu, mbar_try_wait(&bars->k_full[st], par))) {
+                        return false;
+                    }
+                    tc_fence_after();
+                    issue_qk_pair(tmem + 128 * (t % 3), dq0, dk0 + st * (SL::kKHalf >> 4));
+                    commit_pair_warp(&bars->s_full[t % 3]);
+                    commit_pair_warp(&bars->k_empty[st]);
+                    if (++issued == pc.nt) commit_pair_warp(&bars->q_empty);  // the piece's last QK
+                    return true;
+                };
+                while (ok && issued < min(3, pc.nt)) qk_next(true);
+                for (int j = 0; ok && j < pc.nt; ++j, ++jj) {
+                    const int st = jj % kPairVStages, b = jj % 3;
+                    const bool unit_final = pc.t0 + j == pc.T - 1;
+                    ok = mbar_wait_warp(&bars->p_full[b], (jj / 3) & 1, p.err, abort);
+                    if (ok)
+                        ok = unit_final ? mbar_wait_warp(&bars->v_last[st], vl[st] & 1, p.err, abort)
+                                        : mbar_wait_warp(&bars->v_full[st], (jj / kPairVStages) & 1, p.err, abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv_pair(tmem + 384, tmem + 128 * b, dv0 + st * (SL::kVHalf >> 4), j > 0);
+                    commit_pair_warp(&bars->o_done);
+                    commit_pair_warp(&bars->v_empty[st]);
+                    if (unit_final) ++vl[st];
+                    // S(j mod 3) is free for QK(j + 3) once PV(j) is issued.
+                    // QK(j + 1) must be on its way before P(j + 1) is awaited;
+                    // later QKs go now only if their K has landed, so that a
+                    // late K never holds back the next PV
+                    while (ok && issued < min(j + 4, pc.nt))
+                        if (!qk_next(issued > j + 1 ? false : true)) break;
+                }
+                ++npc;
+            }
+            commit_pair_warp(&bars->mma_final);
+        }
+        // both CTAs: every MMA of the pair has completed before TMEM is released
+        mbar_wait_warp(&bars->mma_final, 0, p.err, nullptr);
+    } else {
+        // ------------------------------------------- softmax of this CTA's tile
+        const int x = static_cast<int>(rank);
+        const int r = tid;  // query row = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tO = tmem + 384 + lane_off;
+        const float sl2 = p.scale_log2;
+        uint8_t* stage = smem + SL::kStage + warp * 4096;
+        const uint32_t lead_p[3] = {cluster_map(&bars->p_full[0], 0), cluster_map(&bars->p_full[1], 0),
+                                    cluster_map(&bars->p_full[2], 0)};
+        Walker w;
+        w.init(p, bars, work);
+        Piece pc;
+        int cnt = 0;  // tiles of this work slot so far (the pair's global tile count)
+        bool ok = true;
+        while (ok && w.next(p, pc)) {
+            const bool active = (2 * pc.mp + x) * npt < pc.s.B;  // this CTA's query tile exists
+            const int L = pc.s.L;
+            const int n_end = min(pc.s.B, (2 * pc.mp + 2) * npt);
+            const int node = (2 * pc.mp + x) * npt + r / p.G;
+            const int head = pc.g * p.G + r % p.G;
+            const bool valid_row = node < n_end;
+            uint32_t a[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                a[k] = valid_row ? p.anc[static_cast<long long>(pc.s.off + node) * 8 + k] : 0u;
+#ifdef JT_CHECKS
+            if (valid_row) {  // a node's set holds the node itself and only nodes before it
+                bool ok_set = true;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int lo = 32 * k;
+                    const uint32_t allowed =
+                        node >= lo + 31 ? 0xFFFFFFFFu : (node < lo ? 0u : (2u << (node - lo)) - 1u);
+                    if (a[k] & ~allowed) ok_set = false;
+                    if (node >= lo && node < lo + 32 && !((a[k] >> (node - lo)) & 1u)) ok_set = false;
+                }
+                JT_DCHECK(ok_set, p.err);
+            }
+#endif
+            float m_run = -INFINITY, l_run = 0.0f;
+            for (int j = 0; j < pc.nt; ++j, ++cnt) {
+                const int b = cnt % 3;
+                const uint32_t tS = tmem + 128 * b + lane_off;
+                if (!mbar_wait_warp(&bars->s_full[b], (cnt / 3) & 1, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (active) {
+                    const int slot0 = (pc.t0 + j) * kTileN;
+                    SRow sr;
+                    load_srow(tS, sr);
+                    if (slot0 + kTileN > L) mask_srow(sr, a, slot0 - L);  // tiles inside the prefix need no mask
+                    const float mx = max_srow8(sr);
+                    const float mx_s = mx * sl2;
+                    bool resc = false;
+                    float factor = 1.0f;
+                    if (mx_s > m_run + kRescaleLog2 || m_run == -INFINITY) {
+                        const float m_new = fmaxf(m_run, mx_s);
+                        if (m_run != -INFINITY) {
+                            factor = ex2_approx(m_run - m_new);
+                            resc = j > 0;
+                        } else {
+                            factor = 0.0f;
+                        }
+                        l_run *= factor;
+                        m_run = m_new;
+                    }
+                    // P = exp2(s*scale*log2e - m), written over S (bf16 pairs)
+                    const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
+                    l_run += exp_store_srow(sr, tS, sl2, m_use);
+                    if (j > 0) {
+                        // PV(cnt - 1) has completed (awaited below) before O
+                        // is rescaled
+                        if (!mbar_wait_warp(&bars->o_done, (cnt - 1) & 1, p.err, abort)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        if (__any_sync(0xFFFFFFFFu, resc)) {
+#pragma unroll 1
+                            for (int q = 0; q < D / 32; ++q) {
+                                uint32_t v[32];
+                                tmem_ld32(tO + q * 32, v);
+                                tmem_wait_ld();
+#pragma unroll
+                                for (int c = 0; c < 32; ++c)
+                                    v[c] = __float_as_uint(__uint_as_float(v[c]) * (resc ? factor : 1.0f));
+                                tmem_st32(tO + q * 32, v);
+                            }
+                        }
+                    }
+                    tmem_wait_st();
+                }
+                // every warp, active or not, sees PV(cnt - 1) complete before
+                // it releases P(cnt) (observed above on an active tile j > 0,
+                // else here)
+                if (cnt > 0 && !(active && j > 0) && !mbar_wait_warp(&bars->o_done, (cnt - 1) & 1, p.err, abort)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(lead_p[b]);
+            }
+            if (!ok || !active) continue;
+            // epilogue of the piece (after the last piece the combine may be
+            // scheduled; it waits for this grid): PV(cnt - 1), the piece's
+            // last, has completed (PV(cnt - 2) was observed above)
+            if (w.remaining <= 0) pdl_trigger();
+            if (!mbar_wait_warp(&bars->o_done, (cnt - 1) & 1, p.err, abort)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            piece_output<D>(p, pc, bars, work, x, r, lane, node, head, valid_row, tO, stage, m_run, l_run, 1);
+            // O has been read (tcgen05.wait::ld) before this thread releases
+            // P of the next piece's first tile, whose PV overwrites O
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // no copy, arrive or MMA of the pair targets either CTA any more
+    if (warp == 5) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
     }
 }
 
@@ -1145,44 +1669,88 @@ static PFN_encodeTiled_t get_encode_fn() {
     return fn;
 }
 
-AttnPlan attn_plan(int nseq, int Hkv, int Hq, int max_tree, int max_pages, int dtype) {
+// Whether D = 128 calls run the CTA-pair kernel: when the environment
+// variable JT_ATTN_KERNEL is "pair"; otherwise the single-SM kernel (which
+// D = 64 always uses).
+static bool pair_kernel_selected() {
+    const char* v = std::getenv("JT_ATTN_KERNEL");
+    return v && std::strcmp(v, "pair") == 0;
+}
+
+// Work slots of the CTA-pair kernel on the current device: the clusters of
+// two CTAs that can be resident at once (one CTA per SM).
+static int pair_work_slots() {
+    static PerDeviceCache cache;
+    return cache.get([] {
+        const int fallback = device_sm_count() / 2;
+        if (cudaFuncSetAttribute(tree_attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 PairSmem::kAlloc) != cudaSuccess)
+            return fallback;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * std::max(1, fallback));
+        cfg.blockDim = dim3(kPairThreads);
+        cfg.dynamicSmemBytes = PairSmem::kAlloc;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, tree_attn_pair_kernel, &cfg) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            return fallback;
+        }
+        return n;
+    });
+}
+
+AttnPlan attn_plan(int nseq, int Hkv, int Hq, int D, int max_tree, int max_pages, int dtype) {
     AttnPlan pl;
     const int G = Hq / Hkv;
     pl.rows_per_tile_nodes = kTileM / G;
     pl.mtiles = (max_tree + pl.rows_per_tile_nodes - 1) / pl.rows_per_tile_nodes;
     pl.grid = 0;
+    pl.work = 0;
+    pl.pair = 0;
     pl.nseq = nseq;
     pl.npairs = (pl.mtiles + 1) / 2;
     pl.splits = 0;
     if (dtype == JT_DTYPE_BF16) {
-        const int sms = device_sm_count();
-        pl.grid = sms;  // one CTA per SM, every one the same tile count
-        // Few units (at most half the SMs): split mode, each unit's keys split
-        // over sms / units CTAs (at most one split per two key tiles) and
-        // merged by the combine kernel.
+        pl.pair = (D == 128 && pair_kernel_selected()) ? 1 : 0;
+        // one work slot per SM (single-SM kernel) or per resident CTA pair,
+        // every one the same tile count
+        const int slots = pl.pair ? pair_work_slots() : device_sm_count();
+        pl.work = slots;
+        // Few units (at most half the slots): split mode, each unit's keys
+        // split over slots / units work slots (at most one split per two key
+        // tiles) and merged by the combine kernel.
         const long long units = static_cast<long long>(nseq) * Hkv * pl.npairs;
         const int tmax = (max_pages * JT_PAGE_SIZE + kTileN - 1) / kTileN;
-        if (units > 0 && 2 * units <= sms) {
-            int sp = static_cast<int>(sms / units);
+        if (units > 0 && 2 * units <= slots) {
+            int sp = static_cast<int>(slots / units);
             sp = std::min(sp, std::max(1, tmax / 2));
             sp = std::min(sp, 32);
             if (sp >= 2) {
                 pl.splits = sp;
-                pl.grid = static_cast<int>(units) * sp;
+                pl.work = static_cast<int>(units) * sp;
             }
         }
+        pl.grid = pl.pair ? 2 * pl.work : pl.work;
     }
     return pl;
 }
 
 // Workspace of the bf16 path after the header: the merge counts of cut
-// units (one per CTA; like the header they must be zero before the
+// units (two per work slot; like the header they must be zero before the
 // workspace's first use, and stay valid across calls), the plan (T_total, P,
-// the first global tile of each sequence), then two partial slots per CTA.
-static size_t attn_cnt_bytes(const AttnPlan& p) { return align_up(static_cast<size_t>(p.grid) * 2 * 8); }
+// the first global tile of each sequence), then two partial slots per work
+// slot.
+static size_t attn_cnt_bytes(const AttnPlan& p) { return align_up(static_cast<size_t>(p.work) * 2 * 8); }
 static size_t attn_plan_bytes(const AttnPlan& p) { return align_up(static_cast<size_t>(p.nseq + 3) * sizeof(int)); }
 static size_t attn_ml_bytes(const AttnPlan& p) {
-    return align_up(static_cast<size_t>(2) * p.grid * 2 * kTileM * sizeof(float2));
+    return align_up(static_cast<size_t>(2) * p.work * 2 * kTileM * sizeof(float2));
 }
 
 size_t attn_workspace_bytes(const AttnPlan& p, int total_nodes, int Hq, int D) {
@@ -1191,7 +1759,7 @@ size_t attn_workspace_bytes(const AttnPlan& p, int total_nodes, int Hq, int D) {
     size_t b = kWsHeader;
     if (p.grid > 0)
         b += attn_cnt_bytes(p) + attn_plan_bytes(p) + attn_ml_bytes(p) +
-             align_up(static_cast<size_t>(2) * p.grid * 2 * kTileM * D * sizeof(float));
+             align_up(static_cast<size_t>(2) * p.work * 2 * kTileM * D * sizeof(float));
     return b;
 }
 
@@ -1266,17 +1834,30 @@ static cudaError_t launch_bf16(const void* q, const void* k_cache, const void* v
     prm.npairs = plan.npairs;
     prm.scale_log2 = scale * 1.4426950408889634f;
 
-    using SL = SmemLayout<D>;
-    static PerDeviceCache attr;  // the shared-memory opt-in is per device
-    const cudaError_t ea = static_cast<cudaError_t>(attr.get([] {
-        return static_cast<int>(cudaFuncSetAttribute(tree_attn_tc_kernel<D>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc));
-    }));
-    if (ea != cudaSuccess) return ea;
-    cudaError_t e = launch_kernel_pdl(tree_attn_tc_kernel<D>, dim3(plan.grid), dim3(kAttnThreads), SL::kAlloc, st,
-                                      tq, tk, tv, prm);
+    cudaError_t e;
+    if (plan.pair) {
+        if (D != 128) return cudaErrorInvalidValue;
+        static PerDeviceCache attr;  // the shared-memory opt-in is per device
+        const cudaError_t ea = static_cast<cudaError_t>(attr.get([] {
+            return static_cast<int>(cudaFuncSetAttribute(
+                tree_attn_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, PairSmem::kAlloc));
+        }));
+        if (ea != cudaSuccess) return ea;
+        e = launch_kernel_pdl(tree_attn_pair_kernel, dim3(plan.grid), dim3(kPairThreads), PairSmem::kAlloc, st, tq,
+                              tk, tv, prm);
+    } else {
+        using SL = SmemLayout<D>;
+        static PerDeviceCache attr;
+        const cudaError_t ea = static_cast<cudaError_t>(attr.get([] {
+            return static_cast<int>(cudaFuncSetAttribute(tree_attn_tc_kernel<D>,
+                                                         cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc));
+        }));
+        if (ea != cudaSuccess) return ea;
+        e = launch_kernel_pdl(tree_attn_tc_kernel<D>, dim3(plan.grid), dim3(kAttnThreads), SL::kAlloc, st, tq, tk,
+                              tv, prm);
+    }
     if (e != cudaSuccess || plan.splits == 0) return e;
-    return launch_kernel_pdl(tree_attn_combine_kernel<D>, dim3(plan.grid / plan.splits, kCombineRowBlocks),
+    return launch_kernel_pdl(tree_attn_combine_kernel<D>, dim3(plan.work / plan.splits, kCombineRowBlocks),
                              dim3(kCombineThreads), 0, st, prm);
 }
 
