@@ -151,9 +151,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Wait for the phase with the given parity to complete.  Bounded: after
 // kWaitLimitNs the error word gets DEVERR_TIMEOUT, *abort is set and false is
 // returned.  Also gives up early (false) when *abort is already set.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
-                                          volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __forceinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity, uint32_t* err, volatile int* abort) {
     const unsigned long long t0 = globaltimer_ns();
     for (;;) {
         if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
@@ -166,13 +164,16 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
     }
 }
 
-// Warp-uniform variant: every lane polls, and the warp succeeds only if all
-// lanes saw the phase complete (so warp-collective code after it is never
-// entered by a partial warp).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err,
+                                          volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, err, abort);
+}
+
 __device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, uint32_t* err,
                                                volatile int* abort) {
-    const bool ok = mbar_wait(bar, parity, err, abort);
-    return __all_sync(0xFFFFFFFFu, ok);
+    if (__all_sync(0xFFFFFFFFu, mbar_try_wait(bar, parity))) return true;  // warp-uniform fast path
+    return __all_sync(0xFFFFFFFFu, mbar_wait_slow(bar, parity, err, abort));
 }
 
 
