@@ -202,11 +202,11 @@ def source_hash(paths):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_file, workload):
+def profiled_traffic(kernel_file, workload, kernel=None):
     """DRAM bytes of one main attention-kernel launch on `workload` from the
-    committed ncu summaries (profiles/traffic.json, one entry per workload),
-    or None when there is no capture for this workload or it was taken on a
-    different version of the kernel source."""
+    committed ncu summaries (profiles/traffic.json, one entry per workload
+    and kernel), or None when there is no capture for this workload and
+    kernel or it was taken on a different version of the kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -214,7 +214,8 @@ def profiled_traffic(kernel_file, workload):
         d = json.load(open(p))
         h = source_hash([kernel_file])
         for e in d.get("entries", []):
-            if e.get("workload") == workload and e.get("source_hash") == h:
+            if (e.get("workload") == workload and e.get("source_hash") == h
+                    and (kernel is None or e.get("kernel") == kernel)):
                 return e.get("dram_bytes_per_launch")
         return None
     except (ValueError, OSError):
@@ -744,7 +745,9 @@ def main():
         roof = {"bound": "hbm", "achieved": bytes_a / (attn_mean * 1e-3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu", c["name"])
+    roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu", c["name"],
+                                       "tree_attn_pair_kernel" if attn_kernel(c["D"]) == "pair"
+                                       else f"tree_attn_tc_kernel<{c['D']}>")
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
     roof["kernel"] = ("jt_tree_attn_paged (" + ("tree_attn_pair_kernel" if attn_kernel(c["D"]) == "pair"
                                                  else "tree_attn_tc_kernel") + " + combine in split mode)")

@@ -40,14 +40,17 @@ def test_traffic_is_looked_up_per_workload_and_source(tmp_path, monkeypatch):
     (tmp_path / "profiles").mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     h = bench.source_hash(["k.cu"])
-    entries = [{"workload": "a", "source_hash": h, "dram_bytes_per_launch": 111},
-               {"workload": "b", "source_hash": "0" * 16, "dram_bytes_per_launch": 222}]
+    entries = [{"workload": "a", "kernel": "k1", "source_hash": h, "dram_bytes_per_launch": 111},
+               {"workload": "a", "kernel": "k2", "source_hash": h, "dram_bytes_per_launch": 333},
+               {"workload": "b", "kernel": "k1", "source_hash": "0" * 16, "dram_bytes_per_launch": 222}]
     (tmp_path / "profiles" / "traffic.json").write_text(json.dumps({"entries": entries}))
-    assert bench.profiled_traffic("k.cu", "a") == 111
+    assert bench.profiled_traffic("k.cu", "a", "k1") == 111
+    assert bench.profiled_traffic("k.cu", "a", "k2") == 333   # per kernel
+    assert bench.profiled_traffic("k.cu", "a", "k3") is None
     assert bench.profiled_traffic("k.cu", "b") is None        # taken on another source
     assert bench.profiled_traffic("k.cu", "c") is None        # no capture of this workload
     kern.write_text("kernel v2")
-    assert bench.profiled_traffic("k.cu", "a") is None        # the kernel changed since
+    assert bench.profiled_traffic("k.cu", "a", "k1") is None  # the kernel changed since
 
 
 def test_committed_traffic_entries_are_keyed():
@@ -56,6 +59,7 @@ def test_committed_traffic_entries_are_keyed():
     names = {c["name"] for c in wk.CONFIGS.values()}
     for e in d["entries"]:
         assert e["workload"] in names and len(e["source_hash"]) == 16 and e["dram_bytes_per_launch"] > 0
+        assert e["kernel"] in ("tree_attn_tc_kernel<128>", "tree_attn_pair_kernel")
 
 
 def test_both_arms_describe_the_same_workload():
