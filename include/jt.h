@@ -318,18 +318,24 @@ jt_status jt_tree_build_adaptive(const float* draft_logits, const int32_t* root_
  *   anc:      the ancestor-or-self sets of the tree (see above).
  *   max_tree: max_b B_b (host value; an upper bound used for sizing).
  *   page_size: must be JT_PAGE_SIZE.  scale: softmax scale (e.g. 1/sqrt(D)).
- * The bf16 path runs one CTA per SM; the key tiles of all (sequence, KV head,
- * query-tile pair) units are split into equal ranges, one per CTA, planned
- * on the device from prefix_len and tree_off.  A unit cut by a range
- * boundary is merged from fp32 partials in the workspace by the CTA that
- * finishes its piece last.  Workspace: jt_workspace_size(JT_OP_TREE_ATTN,
- * nseq, 0, 0, 0, total_nodes, Hq, Hkv, D, max_pages, max_tree) = 256 +
- * 16 * SMs + O(nseq) + 2 * SMs * 256 * (D + 2) * 4 bytes (about 40 MB at
- * D = 128 on 152 SMs), sized for the current device and serving that device
- * only.  Its first 256 + 16 * SMs bytes (rounded up to 256; the header and
- * the merge counts) must be zero before its first use, like every header;
- * they stay valid from call to call (counts carry the number of the call
- * that wrote them), so they never need clearing again.
+ * The bf16 path runs one work slot per SM (one CTA); the key tiles of all
+ * (sequence, KV head, query-tile pair) units are split into equal ranges,
+ * one per slot, planned on the device from prefix_len and tree_off.  A unit
+ * cut by a range boundary is merged from fp32 partials in the workspace by
+ * the slot that finishes its piece last.  With the environment variable
+ * JT_ATTN_KERNEL=pair and D = 128, a slot is a cluster of two CTAs on two
+ * SMs sharing each MMA (tcgen05 cta_group::2; one slot per resident pair);
+ * results agree with the single-SM kernel within the bf16 tolerance, and
+ * the variable is read at every call and by jt_workspace_size.  Workspace:
+ * jt_workspace_size(JT_OP_TREE_ATTN, nseq, 0, 0, 0, total_nodes, Hq, Hkv,
+ * D, max_pages, max_tree) = 256 + 16 * slots + O(nseq) + 2 * slots * 256 *
+ * (D + 2) * 4 bytes (about 40 MB at D = 128 on 152 SMs), sized for the
+ * current device and kernel choice and serving that device only.  Its
+ * first 256 + 16 * SMs bytes (rounded up to 256; the header and the merge
+ * counts) must be zero before its first use, like every header; they stay
+ * valid from call to call (counts carry the number of the call that wrote
+ * them, whatever the grid of the calls before), so they never need
+ * clearing again.
  * Node n of sequence b, query head h (KV head h / (Hq/Hkv)) attends to
  * slots 0..L_b-1 and to slot L_b + j for every j in anc(n): never to a
  * sibling or a descendant.  No dense mask is formed.
