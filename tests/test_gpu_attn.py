@@ -119,6 +119,17 @@ def test_bf16_peaky_scores():
     _check_all(*_run(wl, oracle_tree(wl)))
 
 
+def test_bf16_running_max_jumps_late():
+    """q scaled by 8 and the keys of one late prefix page scaled by 20: at that
+    tile the running maximum jumps by far more than 2^32 (log2 units), so both
+    kernels must rescale O there (their lazy thresholds are 2^8 and 2^32)."""
+    wl = _small(15, 2, 32, 8, 128, [1000, 2000], (40, 100), q_mult=8.0)
+    for b in range(wl.nseq):
+        pg = wl.block_table[b, (int(wl.prefix_len[b]) - 40) // 16]
+        wl.k_cache[pg] = wk.f32_to_bf16_bits(wk.bf16_bits_to_f32(wl.k_cache[pg]) * np.float32(20.0))
+    _check_all(*_run(wl, oracle_tree(wl)))
+
+
 def test_bf16_poisoned_pool_is_never_read():
     """Spare pages and page tails past each tree hold NaN; a read outside
     the block table or past the last node would show up in the output."""

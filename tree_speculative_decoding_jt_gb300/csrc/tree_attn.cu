@@ -1112,12 +1112,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // from both CTAs, so a unit's K/V cross HBM and shared memory once while
 // each SM's tensor core does the MMAs of its own 128 rows.  Against the
 // single-SM kernel this halves the shared-memory reads per MMA (the K/V
-// operand is split) and leaves room in TMEM for three S buffers: per CTA
-// S0, S1, S2 (128 columns each) and O (128).  MMAs from one thread run in
-// issue order, and QK(t) may overwrite S(t mod 3) only after PV(t-3) has
-// read P(t-3) from it, so with three buffers QK(j+1) and QK(j+2) are not
-// queued behind PV(j-1): the tensor core scores the next tiles while
-// softmax works on tile j.
+// operand is split) and leaves room in TMEM for double-buffered S: per CTA
+// S0, S1 (128 columns each) and O (128).  MMAs from one thread run in
+// issue order, and QK(t) may overwrite S(t & 1) only after PV(t-2) has
+// read P(t-2) from it.  Softmax releases P(t) without waiting for PV(t-1)
+// (O is rescaled only when a row's maximum grows by more than 2^32, and
+// only then does the softmax wait for that PV), so PV(t) follows PV(t-1)
+// and QK(t+1) in the tensor pipe with no softmax round trip in between.
 //
 // Warp roles (224 threads per CTA):
 //   warps 0-3  softmax + epilogue of this CTA's query tile, one row per
@@ -1126,17 +1127,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 //              (the leader's barriers count both CTAs' bytes);
 //   warp 5     TMEM allocation; in the leader, the single-thread MMA issuer;
 //   warp 6     TMA producer of this CTA's V halves.
-// Issue order per piece: QK(0), QK(1), QK(2), then per tile j: PV(j),
-// QK(j+3) (later, after PV(j+1) or PV(j+2), when its K lands late).  Per
-// tile the eight softmax warps of the pair arrive on the leader's
-// p_full[j mod 3].  Every PV commits one phase of o_done, and every softmax
-// warp waits for PV(t-1) before it releases P(t) (and before rescaling O):
-// that keeps o_done within one phase of each waiter's count, and neither
-// CTA's softmax more than one tile ahead of the other's.
+// Issue order per piece: QK(0), QK(1), then per tile j: PV(j), QK(j+2)
+// (later, after PV(j+1), when its K lands late).  Per tile the eight
+// softmax warps of the pair arrive on the leader's p_full[j & 1]; S(t)
+// needs PV(t-2) issued, so neither CTA's softmax runs more than one tile
+// ahead of the other's.  PV(t) commits a phase of o_done[t & 1]: when a
+// warp waits for PV(t) (a rescale at tile t+1, or the piece's output),
+// PV(t-2) has completed (S(t) has) and PV(t+2) is not issued (it needs
+// this warp's P), so that barrier is within one phase of the wait.
 // ===========================================================================
 constexpr int kPairThreads = 224;
 constexpr int kPairKStages = 6;  // K ring depth (half tiles): a K slot frees at QK, early
 constexpr int kPairVStages = 4;  // V ring depth (half tiles): a V slot frees at PV
+// Lazy rescaling threshold of the pair kernel (log2 units): O is rescaled
+// only when a row's running maximum grows by more than this.  Until then P
+// = exp2(s - m) stays below 2^32 and O and the row sum below ~2^60 times
+// their values: far inside fp32 and bf16 range, with no loss of relative
+// precision.
+constexpr float kPairRescaleLog2 = 32.0f;
 
 struct PairSmem {
     static constexpr int kQChunk = kTileM * 128;  // 128 query rows x 64 dims
@@ -1162,9 +1170,9 @@ struct PairBars {
     uint64_t v_empty[kPairVStages];  // PV of the stage's tile has completed
     uint64_t v_own[kPairVStages];    // this CTA's half of a unit-final V tile has landed
     uint64_t v_last[kPairVStages];   // leader: both halves of a unit-final V tile are zero-filled
-    uint64_t s_full[3];             // S buffer X holds QK of its latest tile
-    uint64_t p_full[3];             // leader: P of the tile in S buffer X, from the pair's 8 softmax warps
-    uint64_t o_done;                // one phase per PV
+    uint64_t s_full[2];             // S buffer X holds QK of its latest tile
+    uint64_t p_full[2];             // leader: P of the tile in S buffer X, from the pair's 8 softmax warps
+    uint64_t o_done[2];             // one phase per PV of a tile t with t & 1 == X
     uint64_t mma_final;             // every MMA of the pair has completed
     uint32_t tmem_base;
     int abort;
@@ -1231,11 +1239,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             mbar_init(&bars->v_own[s], 1);
             mbar_init(&bars->v_last[s], 2);
         }
-        for (int x = 0; x < 3; ++x) {
+        for (int x = 0; x < 2; ++x) {
             mbar_init(&bars->s_full[x], 1);
             mbar_init(&bars->p_full[x], 8);
+            mbar_init(&bars->o_done[x], 1);
         }
-        mbar_init(&bars->o_done, 1);
         mbar_init(&bars->mma_final, 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -1414,31 +1422,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         return false;
                     }
                     tc_fence_after();
-                    issue_qk_pair(tmem + 128 * (t % 3), dq0, dk0 + st * (SL::kKHalf >> 4));
-                    commit_pair_warp(&bars->s_full[t % 3]);
+                    issue_qk_pair(tmem + 128 * (t & 1), dq0, dk0 + st * (SL::kKHalf >> 4));
+                    commit_pair_warp(&bars->s_full[t & 1]);
                     commit_pair_warp(&bars->k_empty[st]);
                     if (++issued == pc.nt) commit_pair_warp(&bars->q_empty);  // the piece's last QK
                     return true;
                 };
-                while (ok && issued < min(3, pc.nt)) qk_next(true);
+                while (ok && issued < min(2, pc.nt)) qk_next(true);
                 for (int j = 0; ok && j < pc.nt; ++j, ++jj) {
-                    const int st = jj % kPairVStages, b = jj % 3;
+                    const int st = jj % kPairVStages, b = jj & 1;
                     const bool unit_final = pc.t0 + j == pc.T - 1;
-                    ok = mbar_wait_warp(&bars->p_full[b], (jj / 3) & 1, p.err, abort);
+                    ok = mbar_wait_warp(&bars->p_full[b], (jj >> 1) & 1, p.err, abort);
                     if (ok)
                         ok = unit_final ? mbar_wait_warp(&bars->v_last[st], vl[st] & 1, p.err, abort)
                                         : mbar_wait_warp(&bars->v_full[st], (jj / kPairVStages) & 1, p.err, abort);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv_pair(tmem + 384, tmem + 128 * b, dv0 + st * (SL::kVHalf >> 4), j > 0);
-                    commit_pair_warp(&bars->o_done);
+                    issue_pv_pair(tmem + 256, tmem + 128 * b, dv0 + st * (SL::kVHalf >> 4), j > 0);
+                    commit_pair_warp(&bars->o_done[b]);
                     commit_pair_warp(&bars->v_empty[st]);
                     if (unit_final) ++vl[st];
-                    // S(j mod 3) is free for QK(j + 3) once PV(j) is issued.
+                    // S(j & 1) is free for QK(j + 2) once PV(j) is issued.
                     // QK(j + 1) must be on its way before P(j + 1) is awaited;
-                    // later QKs go now only if their K has landed, so that a
-                    // late K never holds back the next PV
-                    while (ok && issued < min(j + 4, pc.nt))
+                    // QK(j + 2) goes now only if its K has landed, so that a
+                    // late K never holds back PV(j + 1)
+                    while (ok && issued < min(j + 3, pc.nt))
                         if (!qk_next(issued > j + 1 ? false : true)) break;
                 }
                 ++npc;
@@ -1452,11 +1460,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const int x = static_cast<int>(rank);
         const int r = tid;  // query row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tO = tmem + 384 + lane_off;
+        const uint32_t tO = tmem + 256 + lane_off;
         const float sl2 = p.scale_log2;
         uint8_t* stage = smem + SL::kStage + warp * 4096;
-        const uint32_t lead_p[3] = {cluster_map(&bars->p_full[0], 0), cluster_map(&bars->p_full[1], 0),
-                                    cluster_map(&bars->p_full[2], 0)};
+        const uint32_t lead_p[2] = {cluster_map(&bars->p_full[0], 0), cluster_map(&bars->p_full[1], 0)};
         Walker w;
         w.init(p, bars, work);
         Piece pc;
@@ -1489,9 +1496,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 #endif
             float m_run = -INFINITY, l_run = 0.0f;
             for (int j = 0; j < pc.nt; ++j, ++cnt) {
-                const int b = cnt % 3;
+                const int b = cnt & 1;
                 const uint32_t tS = tmem + 128 * b + lane_off;
-                if (!mbar_wait_warp(&bars->s_full[b], (cnt / 3) & 1, p.err, abort)) {
+                if (!mbar_wait_warp(&bars->s_full[b], (cnt >> 1) & 1, p.err, abort)) {
                     ok = false;
                     break;
                 }
@@ -1505,7 +1512,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     const float mx_s = mx * sl2;
                     bool resc = false;
                     float factor = 1.0f;
-                    if (mx_s > m_run + kRescaleLog2 || m_run == -INFINITY) {
+                    if (mx_s > m_run + kPairRescaleLog2 || m_run == -INFINITY) {
                         const float m_new = fmaxf(m_run, mx_s);
                         if (m_run != -INFINITY) {
                             factor = ex2_approx(m_run - m_new);
@@ -1519,15 +1526,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     // P = exp2(s*scale*log2e - m), written over S (bf16 pairs)
                     const float m_use = (m_run == -INFINITY) ? 0.0f : m_run;
                     l_run += exp_store_srow(sr, tS, sl2, m_use);
-                    if (j > 0) {
-                        // PV(cnt - 1) has completed (awaited below) before O
-                        // is rescaled
-                        if (!mbar_wait_warp(&bars->o_done, (cnt - 1) & 1, p.err, abort)) {
+                    if (__any_sync(0xFFFFFFFFu, resc)) {
+                        // O holds PV(cnt - 1) before it is rescaled
+                        if (!mbar_wait_warp(&bars->o_done[(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, p.err, abort)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        if (__any_sync(0xFFFFFFFFu, resc)) {
+                        {
 #pragma unroll 1
                             for (int q = 0; q < D / 32; ++q) {
                                 uint32_t v[32];
@@ -1542,13 +1548,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     }
                     tmem_wait_st();
                 }
-                // every warp, active or not, sees PV(cnt - 1) complete before
-                // it releases P(cnt) (observed above on an active tile j > 0,
-                // else here)
-                if (cnt > 0 && !(active && j > 0) && !mbar_wait_warp(&bars->o_done, (cnt - 1) & 1, p.err, abort)) {
-                    ok = false;
-                    break;
-                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(lead_p[b]);
@@ -1556,9 +1555,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             if (!ok || !active) continue;
             // epilogue of the piece (after the last piece the combine may be
             // scheduled; it waits for this grid): PV(cnt - 1), the piece's
-            // last, has completed (PV(cnt - 2) was observed above)
+            // last, has completed
             if (w.remaining <= 0) pdl_trigger();
-            if (!mbar_wait_warp(&bars->o_done, (cnt - 1) & 1, p.err, abort)) {
+            if (!mbar_wait_warp(&bars->o_done[(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, p.err, abort)) {
                 ok = false;
                 break;
             }
