@@ -352,10 +352,19 @@ def make_workload(args, seed):
     return wk.make(args.config, seed=seed, overrides={"nseq": args.nseq, "budgets": budgets, "name": name})
 
 
-def attn_kernel(D):
-    """The attention kernel the library picks: the CTA-pair kernel for head
-    dim 128 when JT_ATTN_KERNEL=pair, else the single-SM kernel."""
-    return "pair" if D == 128 and os.environ.get("JT_ATTN_KERNEL") == "pair" else "single"
+def attn_kernel(D, Hq, Hkv, max_tree):
+    """The attention kernel the library picks (its rule, mirrored): for head
+    dim 128 the CTA-pair kernel when every (sequence, KV head) has one
+    query-tile pair at max_tree, else the single-SM kernel; JT_ATTN_KERNEL
+    = pair / single overrides; head dim 64 always runs the single-SM one."""
+    if D != 128:
+        return "single"
+    env = os.environ.get("JT_ATTN_KERNEL")
+    if env in ("pair", "single"):
+        return env
+    npt = 128 // (Hq // Hkv)
+    npairs = (-(-max_tree // npt) + 1) // 2
+    return "pair" if npairs == 1 else "single"
 
 
 def attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, slots):
@@ -745,12 +754,11 @@ def main():
         roof = {"bound": "hbm", "achieved": bytes_a / (attn_mean * 1e-3) / 1e9,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu", c["name"],
-                                       "tree_attn_pair_kernel" if attn_kernel(c["D"]) == "pair"
-                                       else f"tree_attn_tc_kernel<{c['D']}>")
+    kern = attn_kernel(c["D"], c["Hq"], c["Hkv"], max_tree)
+    kname = "tree_attn_pair_kernel" if kern == "pair" else f"tree_attn_tc_kernel<{c['D']}>"
+    roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu", c["name"], kname)
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
-    roof["kernel"] = ("jt_tree_attn_paged (" + ("tree_attn_pair_kernel" if attn_kernel(c["D"]) == "pair"
-                                                 else "tree_attn_tc_kernel") + " + combine in split mode)")
+    roof["kernel"] = f"jt_tree_attn_paged ({kname} + combine in split mode)"
     roof["algorithmic_bytes"] = int(bytes_a)
     roof["algorithmic_flops"] = int(flops_a)
     roof["attn_ms"] = attn_mean
@@ -784,7 +792,6 @@ def main():
     # capped expansion), the attention (one kernel; plus the combine in
     # split mode), the acceptance rules
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    kern = attn_kernel(c["D"])
     split = attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, sms // 2 if kern == "pair" else sms)
     launches_per_step = ((4 if args.adaptive else 2) + (2 if split else 1) + 2 + (1 if args.stochastic else 0))
     if rank == 0:

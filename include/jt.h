@@ -322,11 +322,13 @@ jt_status jt_tree_build_adaptive(const float* draft_logits, const int32_t* root_
  * (sequence, KV head, query-tile pair) units are split into equal ranges,
  * one per slot, planned on the device from prefix_len and tree_off.  A unit
  * cut by a range boundary is merged from fp32 partials in the workspace by
- * the slot that finishes its piece last.  With the environment variable
- * JT_ATTN_KERNEL=pair and D = 128, a slot is a cluster of two CTAs on two
- * SMs sharing each MMA (tcgen05 cta_group::2; one slot per resident pair);
- * results agree with the single-SM kernel within the bf16 tolerance, and
- * the variable is read at every call and by jt_workspace_size.  Workspace:
+ * the slot that finishes its piece last.  For D = 128, when every
+ * (sequence, KV head) has one query-tile pair at max_tree (max_tree <=
+ * 2 * 128 / (Hq/Hkv) nodes), a slot is a cluster of two CTAs on two SMs
+ * sharing each MMA (tcgen05 cta_group::2; one slot per resident pair).
+ * The environment variable JT_ATTN_KERNEL = "pair" or "single" overrides
+ * that choice (read at every call and by jt_workspace_size); both kernels
+ * agree within the bf16 tolerance.  Workspace:
  * jt_workspace_size(JT_OP_TREE_ATTN, nseq, 0, 0, 0, total_nodes, Hq, Hkv,
  * D, max_pages, max_tree) = 256 + 16 * slots + O(nseq) + 2 * slots * 256 *
  * (D + 2) * 4 bytes (about 40 MB at D = 128 on 152 SMs), sized for the

@@ -82,4 +82,15 @@ def test_split_mode_rule_matches_the_workloads():
     assert bench.attn_split_mode(1, 32, 8, 256, 273, sms // 2)     # config 2: 32 units, 2 splits
     assert bench.attn_split_mode(2, 32, 8, 256, 273, sms)           # 64 units: split on 152 slots,
     assert not bench.attn_split_mode(2, 32, 8, 256, 273, sms // 2)  # not on 76
-    assert bench.attn_kernel(128) in ("pair", "single") and bench.attn_kernel(64) == "single"
+
+
+def test_kernel_choice_rule(monkeypatch):
+    """bench.py mirrors the library's choice of attention kernel."""
+    monkeypatch.delenv("JT_ATTN_KERNEL", raising=False)
+    assert bench.attn_kernel(128, 32, 8, 64) == "pair"      # config 4: one query-tile pair per head
+    assert bench.attn_kernel(128, 32, 8, 256) == "single"   # configs 2, 3, 5: four pairs per head
+    assert bench.attn_kernel(64, 32, 8, 64) == "single"     # head dim 64: single-SM kernel only
+    monkeypatch.setenv("JT_ATTN_KERNEL", "single")
+    assert bench.attn_kernel(128, 32, 8, 64) == "single"
+    monkeypatch.setenv("JT_ATTN_KERNEL", "pair")
+    assert bench.attn_kernel(128, 32, 8, 256) == "pair"

@@ -1668,12 +1668,19 @@ static PFN_encodeTiled_t get_encode_fn() {
     return fn;
 }
 
-// Whether D = 128 calls run the CTA-pair kernel: when the environment
-// variable JT_ATTN_KERNEL is "pair"; otherwise the single-SM kernel (which
-// D = 64 always uses).
-static bool pair_kernel_selected() {
+// Whether a D = 128 call runs the CTA-pair kernel.  By default when every
+// (sequence, KV head) has one query-tile pair at max_tree (npairs == 1):
+// then both kernels read each K/V byte once and the pair kernel spends two
+// SMs on each unit.  With several pairs per head the pairs of one head share
+// their K/V through L2, which the single-SM kernel's twice as many work
+// slots keep better (measured on the serving and verify-step batches).  The
+// environment variable JT_ATTN_KERNEL = "pair" or "single" overrides the
+// choice; D = 64 always runs the single-SM kernel.
+static bool pair_kernel_selected(int npairs) {
     const char* v = std::getenv("JT_ATTN_KERNEL");
-    return v && std::strcmp(v, "pair") == 0;
+    if (v && std::strcmp(v, "pair") == 0) return true;
+    if (v && std::strcmp(v, "single") == 0) return false;
+    return npairs == 1;
 }
 
 // Work slots of the CTA-pair kernel on the current device: the clusters of
@@ -1717,7 +1724,7 @@ AttnPlan attn_plan(int nseq, int Hkv, int Hq, int D, int max_tree, int max_pages
     pl.npairs = (pl.mtiles + 1) / 2;
     pl.splits = 0;
     if (dtype == JT_DTYPE_BF16) {
-        pl.pair = (D == 128 && pair_kernel_selected()) ? 1 : 0;
+        pl.pair = (D == 128 && pair_kernel_selected(pl.npairs)) ? 1 : 0;
         // one work slot per SM (single-SM kernel) or per resident CTA pair,
         // every one the same tile count
         const int slots = pl.pair ? pair_work_slots() : device_sm_count();
