@@ -1112,13 +1112,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // from both CTAs, so a unit's K/V cross HBM and shared memory once while
 // each SM's tensor core does the MMAs of its own 128 rows.  Against the
 // single-SM kernel this halves the shared-memory reads per MMA (the K/V
-// operand is split) and leaves room in TMEM for double-buffered S: per CTA
-// S0, S1 (128 columns each) and O (128).  MMAs from one thread run in
-// issue order, and QK(t) may overwrite S(t & 1) only after PV(t-2) has
-// read P(t-2) from it.  Softmax releases P(t) without waiting for PV(t-1)
+// operand is split) and leaves room in TMEM for three S buffers: per CTA
+// S0, S1, S2 (128 columns each) and O (128).  MMAs from one thread run in
+// issue order, and QK(t) may overwrite S(t mod 3) only after PV(t-3) has
+// read P(t-3) from it.  Softmax releases P(t) without waiting for PV(t-1)
 // (O is rescaled only when a row's maximum grows by more than 2^32, and
-// only then does the softmax wait for that PV), so PV(t) follows PV(t-1)
-// and QK(t+1) in the tensor pipe with no softmax round trip in between.
+// only then does the softmax wait for that PV), so the tensor core scores
+// tiles up to three ahead of the softmax and never waits for it in between.
 //
 // Warp roles (224 threads per CTA):
 //   warps 0-3  softmax + epilogue of this CTA's query tile, one row per
@@ -1127,14 +1127,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 //              (the leader's barriers count both CTAs' bytes);
 //   warp 5     TMEM allocation; in the leader, the single-thread MMA issuer;
 //   warp 6     TMA producer of this CTA's V halves.
-// Issue order per piece: QK(0), QK(1), then per tile j: PV(j), QK(j+2)
-// (later, after PV(j+1), when its K lands late).  Per tile the eight
-// softmax warps of the pair arrive on the leader's p_full[j & 1]; S(t)
-// needs PV(t-2) issued, so neither CTA's softmax runs more than one tile
-// ahead of the other's.  PV(t) commits a phase of o_done[t & 1]: when a
-// warp waits for PV(t) (a rescale at tile t+1, or the piece's output),
-// PV(t-2) has completed (S(t) has) and PV(t+2) is not issued (it needs
-// this warp's P), so that barrier is within one phase of the wait.
+// Issue order per piece: QK(0), QK(1), QK(2), then per tile j: PV(j),
+// QK(j+3) (later, when its K lands late).  Per tile the eight softmax
+// warps of the pair arrive on the leader's p_full[j mod 3]; S(t) needs
+// PV(t-3) issued, so neither CTA's softmax runs more than two tiles ahead
+// of the other's.  PV(t) commits a phase of o_done[t mod 3]: when a warp
+// waits for PV(t-1) (a rescale at tile t) or for the piece's last PV,
+// PV(t-4) (resp. the one three before the last) has completed, S(t)
+// having, and the next PV on that barrier is not issued (it needs this
+// warp's P), so that barrier is within one phase of the wait.
 // ===========================================================================
 constexpr int kPairThreads = 224;
 constexpr int kPairKStages = 6;  // K ring depth (half tiles): a K slot frees at QK, early
@@ -1170,9 +1171,9 @@ struct PairBars {
     uint64_t v_empty[kPairVStages];  // PV of the stage's tile has completed
     uint64_t v_own[kPairVStages];    // this CTA's half of a unit-final V tile has landed
     uint64_t v_last[kPairVStages];   // leader: both halves of a unit-final V tile are zero-filled
-    uint64_t s_full[2];             // S buffer X holds QK of its latest tile
-    uint64_t p_full[2];             // leader: P of the tile in S buffer X, from the pair's 8 softmax warps
-    uint64_t o_done[2];             // one phase per PV of a tile t with t & 1 == X
+    uint64_t s_full[3];             // S buffer X holds QK of its latest tile
+    uint64_t p_full[3];             // leader: P of the tile in S buffer X, from the pair's 8 softmax warps
+    uint64_t o_done[3];             // one phase per PV of a tile t with t mod 3 == X
     uint64_t mma_final;             // every MMA of the pair has completed
     uint32_t tmem_base;
     int abort;
@@ -1239,7 +1240,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             mbar_init(&bars->v_own[s], 1);
             mbar_init(&bars->v_last[s], 2);
         }
-        for (int x = 0; x < 2; ++x) {
+        for (int x = 0; x < 3; ++x) {
             mbar_init(&bars->s_full[x], 1);
             mbar_init(&bars->p_full[x], 8);
             mbar_init(&bars->o_done[x], 1);
@@ -1422,31 +1423,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                         return false;
                     }
                     tc_fence_after();
-                    issue_qk_pair(tmem + 128 * (t & 1), dq0, dk0 + st * (SL::kKHalf >> 4));
-                    commit_pair_warp(&bars->s_full[t & 1]);
+                    issue_qk_pair(tmem + 128 * (t % 3), dq0, dk0 + st * (SL::kKHalf >> 4));
+                    commit_pair_warp(&bars->s_full[t % 3]);
                     commit_pair_warp(&bars->k_empty[st]);
                     if (++issued == pc.nt) commit_pair_warp(&bars->q_empty);  // the piece's last QK
                     return true;
                 };
-                while (ok && issued < min(2, pc.nt)) qk_next(true);
+                while (ok && issued < min(3, pc.nt)) qk_next(true);
                 for (int j = 0; ok && j < pc.nt; ++j, ++jj) {
-                    const int st = jj % kPairVStages, b = jj & 1;
+                    const int st = jj % kPairVStages, b = jj % 3;
                     const bool unit_final = pc.t0 + j == pc.T - 1;
-                    ok = mbar_wait_warp(&bars->p_full[b], (jj >> 1) & 1, p.err, abort);
+                    ok = mbar_wait_warp(&bars->p_full[b], (jj / 3) & 1, p.err, abort);
                     if (ok)
                         ok = unit_final ? mbar_wait_warp(&bars->v_last[st], vl[st] & 1, p.err, abort)
                                         : mbar_wait_warp(&bars->v_full[st], (jj / kPairVStages) & 1, p.err, abort);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv_pair(tmem + 256, tmem + 128 * b, dv0 + st * (SL::kVHalf >> 4), j > 0);
+                    issue_pv_pair(tmem + 384, tmem + 128 * b, dv0 + st * (SL::kVHalf >> 4), j > 0);
                     commit_pair_warp(&bars->o_done[b]);
                     commit_pair_warp(&bars->v_empty[st]);
                     if (unit_final) ++vl[st];
-                    // S(j & 1) is free for QK(j + 2) once PV(j) is issued.
+                    // S(j mod 3) is free for QK(j + 3) once PV(j) is issued.
                     // QK(j + 1) must be on its way before P(j + 1) is awaited;
-                    // QK(j + 2) goes now only if its K has landed, so that a
-                    // late K never holds back PV(j + 1)
-                    while (ok && issued < min(j + 3, pc.nt))
+                    // later QKs go now only if their K has landed, so that a
+                    // late K never holds back the next PV
+                    while (ok && issued < min(j + 4, pc.nt))
                         if (!qk_next(issued > j + 1 ? false : true)) break;
                 }
                 ++npc;
@@ -1460,10 +1461,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         const int x = static_cast<int>(rank);
         const int r = tid;  // query row = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tO = tmem + 256 + lane_off;
+        const uint32_t tO = tmem + 384 + lane_off;
         const float sl2 = p.scale_log2;
         uint8_t* stage = smem + SL::kStage + warp * 4096;
-        const uint32_t lead_p[2] = {cluster_map(&bars->p_full[0], 0), cluster_map(&bars->p_full[1], 0)};
+        const uint32_t lead_p[3] = {cluster_map(&bars->p_full[0], 0), cluster_map(&bars->p_full[1], 0),
+                                    cluster_map(&bars->p_full[2], 0)};
         Walker w;
         w.init(p, bars, work);
         Piece pc;
@@ -1496,9 +1498,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
 #endif
             float m_run = -INFINITY, l_run = 0.0f;
             for (int j = 0; j < pc.nt; ++j, ++cnt) {
-                const int b = cnt & 1;
+                const int b = cnt % 3;
                 const uint32_t tS = tmem + 128 * b + lane_off;
-                if (!mbar_wait_warp(&bars->s_full[b], (cnt >> 1) & 1, p.err, abort)) {
+                if (!mbar_wait_warp(&bars->s_full[b], (cnt / 3) & 1, p.err, abort)) {
                     ok = false;
                     break;
                 }
@@ -1528,7 +1530,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     l_run += exp_store_srow(sr, tS, sl2, m_use);
                     if (__any_sync(0xFFFFFFFFu, resc)) {
                         // O holds PV(cnt - 1) before it is rescaled
-                        if (!mbar_wait_warp(&bars->o_done[(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, p.err, abort)) {
+                        if (!mbar_wait_warp(&bars->o_done[(cnt - 1) % 3], ((cnt - 1) / 3) & 1, p.err, abort)) {
                             ok = false;
                             break;
                         }
@@ -1557,7 +1559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             // scheduled; it waits for this grid): PV(cnt - 1), the piece's
             // last, has completed
             if (w.remaining <= 0) pdl_trigger();
-            if (!mbar_wait_warp(&bars->o_done[(cnt - 1) & 1], ((cnt - 1) >> 1) & 1, p.err, abort)) {
+            if (!mbar_wait_warp(&bars->o_done[(cnt - 1) % 3], ((cnt - 1) / 3) & 1, p.err, abort)) {
                 ok = false;
                 break;
             }
