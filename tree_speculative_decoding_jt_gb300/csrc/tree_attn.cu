@@ -17,9 +17,12 @@
 // last node of tile B; ancestors have smaller indices, so no later key is
 // ever visible).  Units are laid end to end in (b, g, mp) order and the
 // T_total key tiles of all units are cut into one equal range of
-// P = ceil(T_total / grid) tiles per CTA, one CTA per SM: every SM gets the
-// same tile count whatever the prefix lengths, so there is no tail wave and
-// no straggler.  A CTA walks the pieces of units in its range; a unit cut
+// P = ceil(T_total / slots) tiles per work slot -- one CTA per SM in the
+// single-SM kernel below, one CTA pair per two SMs in the CTA-pair kernel
+// further down (head dim 128; the host picks it when every (sequence, KV
+// head) has one query-tile pair): every SM gets the same tile count
+// whatever the prefix lengths, so there is no tail wave and no straggler.
+// A slot walks the pieces of units in its range; a unit cut
 // by a range boundary leaves fp32 partials (O, running max, sum) from each
 // CTA that holds a piece of it, and the CTA that finishes its piece last
 // merges them (an atomic count per cut unit, tagged with the call's number
@@ -32,7 +35,7 @@
 // runs in split mode instead: one CTA per (unit, key split), the splits'
 // partials merged by tree_attn_combine_kernel, one warp per query row.
 //
-// Warp roles (320 threads):
+// Single-SM kernel, warp roles (320 threads):
 //   warps 0-3 / 4-7  softmax + epilogue of query tile A / B, one query row
 //                    per thread (TMEM lane);
 //   warp 8           planner, then TMA producer: per piece the Q tiles, then
@@ -1111,14 +1114,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 // every V tile (all 128 keys, dims 64X..64X+63); the MMA reads B's halves
 // from both CTAs, so a unit's K/V cross HBM and shared memory once while
 // each SM's tensor core does the MMAs of its own 128 rows.  Against the
-// single-SM kernel this halves the shared-memory reads per MMA (the K/V
-// operand is split) and leaves room in TMEM for three S buffers: per CTA
-// S0, S1, S2 (128 columns each) and O (128).  MMAs from one thread run in
-// issue order, and QK(t) may overwrite S(t mod 3) only after PV(t-3) has
-// read P(t-3) from it.  Softmax releases P(t) without waiting for PV(t-1)
-// (O is rescaled only when a row's maximum grows by more than 2^32, and
-// only then does the softmax wait for that PV), so the tensor core scores
-// tiles up to three ahead of the softmax and never waits for it in between.
+// single-SM kernel this halves each SM's K/V operand reads per MMA (a
+// quarter of its shared-memory reads) and leaves room in TMEM for three S
+// buffers: per CTA S0, S1, S2 (128 columns each) and O (128).  MMAs from
+// one thread run in issue order, and QK(t) may overwrite S(t mod 3) only
+// after PV(t-3) has read P(t-3) from it.  Softmax releases P(t) without
+// waiting for PV(t-1) (O is rescaled only when a row's maximum grows by
+// more than 2^32, and only then does the softmax wait for that PV), so the
+// tensor core scores tiles up to three ahead of the softmax and never
+// waits for it in between.
 //
 // Warp roles (224 threads per CTA):
 //   warps 0-3  softmax + epilogue of this CTA's query tile, one row per
