@@ -126,7 +126,9 @@ struct Bars {
     int w_b, w_g, w_mp, w_t, w_quota, w_P;
     uint32_t call_id;  // this call's number (+1) on this workspace
     int merge_flag[2];  // per query tile: this CTA finished the last piece of a cut unit
+    uint64_t msync[2];  // per query tile: its four softmax warps meet (merge of a cut unit)
 };
+static_assert(sizeof(Bars) <= 512, "barrier block");
 
 // ---------------------------------------------------------------------------
 // The work plan (shared by the main kernel's roles and the combine)
@@ -364,10 +366,6 @@ struct CutUnit {
     __device__ __forceinline__ int slot(int k) const { return k == 0 ? slot0 : 2 * (c0 + k); }
 };
 
-__device__ __forceinline__ void named_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
 // Stage this warp's 32 rows' 128-byte pieces (slot[8] = this thread's row)
 // through shared memory (16-byte slots XOR-swizzled by row: conflict-free
 // both ways) and store each row's piece as one full line: dst(rr) gives the
@@ -584,11 +582,12 @@ __device__ __forceinline__ uint32_t draw_call_id(unsigned long long* tickets, bo
 // fp32 partial row; when this work slot completes a cut unit, the merge of
 // all its pieces.  O_X is read from TMEM at tO (complete: the caller has
 // waited for the piece's last PV).  The four softmax warps of tile X call
-// this together; bar_id is their named barrier.
-template <int D, typename BarsT>
+// this together; sync4() meets all four (bounded: false when it gives up,
+// the error already raised).
+template <int D, typename BarsT, typename Sync4>
 __device__ __forceinline__ void piece_output(const AttnParams& p, const Piece& pc, BarsT* bars, int work, int x,
                                              int r, int lane, int node, int head, bool valid_row, uint32_t tO,
-                                             uint8_t* stage, float m_run, float l_run, int bar_id) {
+                                             uint8_t* stage, float m_run, float l_run, Sync4&& sync4) {
     const long long rowid = static_cast<long long>(pc.s.off + node) * p.Hq + head;
     const bool partial = pc.slot >= 0;
     const long long prow = (static_cast<long long>(pc.slot) * 2 + x) * kTileM + r;  // partial row
@@ -643,12 +642,12 @@ __device__ __forceinline__ void piece_output(const AttnParams& p, const Piece& p
     if (partial && p.splits == 0) {
         // count this piece done; the CTA that completes the unit
         // merges every piece's partial rows (its own included).  Each
-        // query tile's four warps do this on their own (named barrier
-        // bar_id, count and flag per tile), so neither tile's warps ever
-        // wait for the other's.
+        // query tile's four warps do this on their own (sync4, count and
+        // flag per tile), so neither tile's warps ever wait for the
+        // other's.
         const CutUnit cu(pc.gpos - pc.t0, pc.T, bars->w_P);
         __threadfence();  // this thread's partial rows are visible GPU-wide
-        named_sync(bar_id, 128);
+        if (!sync4()) return;
         if (r == 0) {
             const uint32_t cid = bars->call_id;
             unsigned long long* ctr = p.merge_cnt + 2 * cu.c0 + x;
@@ -662,7 +661,7 @@ __device__ __forceinline__ void piece_output(const AttnParams& p, const Piece& p
             bars->merge_flag[x] = static_cast<int>(nv & 0xFFFFFFFFull) == cu.n;
             __threadfence();  // the other pieces' rows are read after this count
         }
-        named_sync(bar_id, 128);
+        if (!sync4()) return;
         if (bars->merge_flag[x]) {  // uniform over the tile's warps
             // merge this row over the unit's pieces: M = max m_k,
             // O = sum 2^(m_k - M) O_k / sum 2^(m_k - M) l_k.  This
@@ -801,6 +800,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(&bars->s_full[x], 1);
             mbar_init(&bars->p_full[x], 128);
             mbar_init(&bars->o_final[x], 1);
+            mbar_init(&bars->msync[x], 4);
         }
         mbar_init(&bars->mma_final, 1);
         bars->abort = 0;
@@ -1006,6 +1006,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         w.init(p, bars, work);
         Piece pc;
         int cnt = 0, nfin = 0;
+        // the tile's four softmax warps meet (bounded; one phase of msync
+        // per meeting, and no warp can be a meeting ahead of another)
+        uint32_t nsync = 0;
+        auto sync4 = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->msync[x]);
+            return mbar_wait_warp(&bars->msync[x], (nsync++) & 1, p.err, abort);
+        };
         bool ok = true;
         while (ok && w.next(p, pc)) {
             if (x == 1 && (2 * pc.mp + 1) * npt >= pc.s.B) continue;  // tile B absent from this unit
@@ -1089,7 +1097,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             ++nfin;
             tc_fence_after();
-            piece_output<D>(p, pc, bars, work, x, r, lane, node, head, valid_row, tO, stage, m_run, l_run, 1 + x);
+            piece_output<D>(p, pc, bars, work, x, r, lane, node, head, valid_row, tO, stage, m_run, l_run, sync4);
             // O_X has been read (tcgen05.wait::ld above) before this thread
             // arrives on p_full[X] for the next piece's first tile, which is
             // what lets the MMA warp overwrite O_X
@@ -1184,6 +1192,7 @@ struct PairBars {
     int w_b, w_g, w_mp, w_t, w_quota, w_P;
     uint32_t call_id;
     int merge_flag[2];
+    uint64_t msync[2];  // this CTA's four softmax warps meet (merge of a cut unit)
 };
 static_assert(sizeof(PairBars) <= 512, "barrier block");
 
@@ -1249,6 +1258,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             mbar_init(&bars->p_full[x], 8);
             mbar_init(&bars->o_done[x], 1);
         }
+        for (int x = 0; x < 2; ++x) mbar_init(&bars->msync[x], 4);
         mbar_init(&bars->mma_final, 1);
         bars->abort = 0;
         fence_mbar_init();
@@ -1474,6 +1484,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         w.init(p, bars, work);
         Piece pc;
         int cnt = 0;  // tiles of this work slot so far (the pair's global tile count)
+        // the tile's four softmax warps meet (bounded; one phase of msync
+        // per meeting, and no warp can be a meeting ahead of another)
+        uint32_t nsync = 0;
+        auto sync4 = [&]() -> bool {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->msync[x]);
+            return mbar_wait_warp(&bars->msync[x], (nsync++) & 1, p.err, abort);
+        };
         bool ok = true;
         while (ok && w.next(p, pc)) {
             const bool active = (2 * pc.mp + x) * npt < pc.s.B;  // this CTA's query tile exists
@@ -1568,7 +1586,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 break;
             }
             tc_fence_after();
-            piece_output<D>(p, pc, bars, work, x, r, lane, node, head, valid_row, tO, stage, m_run, l_run, 1);
+            piece_output<D>(p, pc, bars, work, x, r, lane, node, head, valid_row, tO, stage, m_run, l_run, sync4);
             // O has been read (tcgen05.wait::ld) before this thread releases
             // P of the next piece's first tile, whose PV overwrites O
         }
