@@ -582,8 +582,8 @@ __device__ __forceinline__ uint32_t draw_call_id(unsigned long long* tickets, bo
 // fp32 partial row; when this work slot completes a cut unit, the merge of
 // all its pieces.  O_X is read from TMEM at tO (complete: the caller has
 // waited for the piece's last PV).  The four softmax warps of tile X call
-// this together; sync4() meets all four (bounded: false when it gives up,
-// the error already raised).
+// this together; sync4(i) is their i-th meeting of this merge (bounded:
+// false when it gives up, the error already raised).
 template <int D, typename BarsT, typename Sync4>
 __device__ __forceinline__ void piece_output(const AttnParams& p, const Piece& pc, BarsT* bars, int work, int x,
                                              int r, int lane, int node, int head, bool valid_row, uint32_t tO,
@@ -647,7 +647,7 @@ __device__ __forceinline__ void piece_output(const AttnParams& p, const Piece& p
         // other's.
         const CutUnit cu(pc.gpos - pc.t0, pc.T, bars->w_P);
         __threadfence();  // this thread's partial rows are visible GPU-wide
-        if (!sync4()) return;
+        if (!sync4(0)) return;
         if (r == 0) {
             const uint32_t cid = bars->call_id;
             unsigned long long* ctr = p.merge_cnt + 2 * cu.c0 + x;
@@ -661,7 +661,7 @@ __device__ __forceinline__ void piece_output(const AttnParams& p, const Piece& p
             bars->merge_flag[x] = static_cast<int>(nv & 0xFFFFFFFFull) == cu.n;
             __threadfence();  // the other pieces' rows are read after this count
         }
-        if (!sync4()) return;
+        if (!sync4(1)) return;
         if (bars->merge_flag[x]) {  // uniform over the tile's warps
             // merge this row over the unit's pieces: M = max m_k,
             // O = sum 2^(m_k - M) O_k / sum 2^(m_k - M) l_k.  This
@@ -1007,12 +1007,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         Piece pc;
         int cnt = 0, nfin = 0;
         // the tile's four softmax warps meet (bounded; one phase of msync
-        // per meeting, and no warp can be a meeting ahead of another)
-        uint32_t nsync = 0;
-        auto sync4 = [&]() -> bool {
+        // per meeting, and no warp can be a meeting ahead of another).  A
+        // merge meets exactly twice, so meeting i of it completes a phase
+        // of parity i.
+        auto sync4 = [&](int i) -> bool {
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->msync[x]);
-            return mbar_wait_warp(&bars->msync[x], (nsync++) & 1, p.err, abort);
+            return mbar_wait_warp(&bars->msync[x], static_cast<uint32_t>(i), p.err, abort);
         };
         bool ok = true;
         while (ok && w.next(p, pc)) {
@@ -1485,12 +1486,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         Piece pc;
         int cnt = 0;  // tiles of this work slot so far (the pair's global tile count)
         // the tile's four softmax warps meet (bounded; one phase of msync
-        // per meeting, and no warp can be a meeting ahead of another)
-        uint32_t nsync = 0;
-        auto sync4 = [&]() -> bool {
+        // per meeting, and no warp can be a meeting ahead of another).  A
+        // merge meets exactly twice, so meeting i of it completes a phase
+        // of parity i.
+        auto sync4 = [&](int i) -> bool {
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->msync[x]);
-            return mbar_wait_warp(&bars->msync[x], (nsync++) & 1, p.err, abort);
+            return mbar_wait_warp(&bars->msync[x], static_cast<uint32_t>(i), p.err, abort);
         };
         bool ok = true;
         while (ok && w.next(p, pc)) {
