@@ -756,9 +756,11 @@ def main():
     roof["frac"] = roof["achieved"] / roof["peak"]
     kern = attn_kernel(c["D"], c["Hq"], c["Hkv"], max_tree)
     kname = "tree_attn_pair_kernel" if kern == "pair" else f"tree_attn_tc_kernel<{c['D']}>"
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    split = attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, sms // 2 if kern == "pair" else sms)
     roof["traffic"] = profiled_traffic("tree_speculative_decoding_jt_gb300/csrc/tree_attn.cu", c["name"], kname)
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json burst)" if peak_src == "measured" else "fallback"
-    roof["kernel"] = f"jt_tree_attn_paged ({kname} + combine in split mode)"
+    roof["kernel"] = f"jt_tree_attn_paged ({kname}" + (" + tree_attn_combine_kernel, split mode)" if split else ")")
     roof["algorithmic_bytes"] = int(bytes_a)
     roof["algorithmic_flops"] = int(flops_a)
     roof["attn_ms"] = attn_mean
@@ -791,8 +793,6 @@ def main():
     # with the row merge; the adaptive build: partials, row merge, policy,
     # capped expansion), the attention (one kernel; plus the combine in
     # split mode), the acceptance rules
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    split = attn_split_mode(nseq, Hq, Hkv, max_tree, max_pages, sms // 2 if kern == "pair" else sms)
     launches_per_step = ((4 if args.adaptive else 2) + (2 if split else 1) + 2 + (1 if args.stochastic else 0))
     if rank == 0:
         line = {
