@@ -61,3 +61,15 @@ def test_checks_variant_builds_and_exports_every_symbol():
     raw.jt_tree_topw.restype = ctypes.c_int
     assert raw.jt_tree_topw(None, ctypes.c_int64(1), ctypes.c_int64(10), 2, None, None, None, None,
                             ctypes.c_size_t(0), None) == -1
+
+
+def test_package_exports_the_status_codes():
+    """The package root re-exports the jt_status codes of include/jt.h
+    (JtError.status is compared with them)."""
+    import tree_speculative_decoding_jt_gb300 as jt
+    assert (jt.JT_OK, jt.JT_ERR_INVALID, jt.JT_ERR_UNSUPPORTED, jt.JT_ERR_CUDA, jt.JT_ERR_TIMEOUT,
+            jt.JT_ERR_WORKSPACE) == (0, -1, -2, -3, -4, -5)
+    hdr = open(os.path.join(ROOT, "include", "jt.h")).read()
+    for name, val in (("JT_ERR_INVALID", -1), ("JT_ERR_UNSUPPORTED", -2), ("JT_ERR_CUDA", -3),
+                      ("JT_ERR_TIMEOUT", -4), ("JT_ERR_WORKSPACE", -5)):
+        assert f"{name} = {val}" in hdr
