@@ -370,6 +370,15 @@ __global__ void __launch_bounds__(kTopwThreads)
             }
         }
     }
+#ifdef JT_CHECKS
+    {   // a NaN logit poisons the sum (the clamps above would hide it), so the
+        // row's lse is NaN and the expansion's check reports it
+        bool bad = false;
+#pragma unroll
+        for (int i = 0; i < PER; ++i) bad |= (x[i] != x[i]);
+        if (bad) acc_hi = __int_as_float(0x7FC00000);
+    }
+#endif
     pdl_trigger();  // the row merge may be scheduled; it waits for this grid's writes
     const ffloat Sw = warp_sum_ff(ff_norm(acc_hi, acc_lo));
     ffloat Tw;
